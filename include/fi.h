@@ -1,0 +1,235 @@
+/*
+ * fi.h - C ABI of the GB300 paged-KV attention library (libfi.so).
+ *
+ * Batched attention over a paged KV cache for LLM serving: prefill,
+ * single-row decode and multi-token speculative verify, computing
+ * softmax(Q K^T * sm_scale + mask) V with fp32 accumulation and a per-row
+ * log-sum-exp, plus split-KV partial states merged by their log-sum-exp.
+ *
+ * The operation is the one described by three pull requests of the
+ * AMD-Ecosystem FlashInfer fork, cited below by key:
+ *   [P1] "Route non-causal windowed prefill to AITER's masked kernel" (#339)
+ *   [P2] "Support speculative-decode verify on ROCm, and stop auto routing
+ *         short-query prefill to AITER" (#362)
+ *   [P3] "Refuse attention inputs the ROCm kernels would compute wrongly" (#399)
+ *
+ * Definition (per request b, query row i in [0, Lq_b), query head h,
+ * g = num_qo_heads / num_kv_heads, kv head h / g):
+ *   Lk_b  = (kv_indptr[b+1] - kv_indptr[b] - 1) * page_size + last_page_len[b]
+ *           (0 when the request has no page) - from the page metadata, never
+ *           from a caller-supplied length [P2 "Review notes"];
+ *   key j lives in page kv_indices[kv_indptr[b] + j / page_size], slot
+ *           j % page_size;
+ *   valid(i, j) = (!causal || j <= i + Lk - Lq)                [P2 "Summary"]
+ *              && (window_left < 0 || j + Lq + window_left >= Lk + i)
+ *              - a left-only window anchored bottom-right and applied with
+ *                or without causal [P1 "Why window_size_right stays -1"];
+ *                all compares are signed [P1 "What changed"];
+ *   s_j = sm_scale * <q[i,h,:], k[j,h/g,:]>;
+ *   lse = ln sum_{valid j} exp(s_j)      (natural log; -inf when no key is valid)
+ *   o   = sum_{valid j} exp(s_j - lse) v[j,h/g,:]   (0 when no key is valid).
+ *
+ * Conventions for every entry point:
+ *   - All tensor data pointers are DEVICE pointers owned by the caller; the
+ *     library never frees them. Host arrays are read during the call only.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Launches are asynchronous on it; run calls never synchronise
+ *     the host and never allocate, so they can be captured in a CUDA graph.
+ *   - Strides are in elements. The last dimension of every tensor must have
+ *     stride 1; a strided last dim is refused, never copied [P3 "Strided
+ *     layouts", "Architecture / design notes"].
+ *   - Errors are return codes; nothing aborts or traps. fi_last_error() gives
+ *     a thread-local message naming the field, the expected value and the
+ *     value given [P3 "Plan-vs-run shapes"].
+ */
+#ifndef FI_H_
+#define FI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fi_status {
+  FI_OK = 0,
+  FI_ERR_INVALID_ARG = 1,          /* null pointer, bad rank, negative size, ... */
+  FI_ERR_STRIDED_LAST_DIM = 2,     /* an input whose last dim has stride != 1 */
+  FI_ERR_NONCONTIGUOUS_OUTPUT = 3, /* out / lse / merge outputs not packed */
+  FI_ERR_GQA_INDIVISIBLE = 4,      /* num_kv_heads == 0 or Hq % Hk != 0 */
+  FI_ERR_PLAN_MISMATCH = 5,        /* run() tensors disagree with plan() */
+  FI_ERR_NOT_PLANNED = 6,          /* run() before a successful plan() */
+  FI_ERR_KV_SHORTER_THAN_Q = 7,    /* causal with Lk_b < Lq_b (from metadata) */
+  FI_ERR_CAPACITY = 8,             /* workspace too small / graph-frozen shape */
+  FI_ERR_UNSUPPORTED = 9,          /* head_dim, dtype or group size not built */
+  FI_ERR_CUDA = 10                 /* a CUDA runtime call failed */
+} fi_status;
+
+typedef enum fi_dtype { FI_F16 = 0, FI_BF16 = 1, FI_F32 = 2, FI_I32 = 3 } fi_dtype;
+
+/* A strided view of caller-owned device memory. Unused trailing entries of
+ * shape/stride are ignored. */
+typedef struct fi_tensor {
+  void* data;
+  fi_dtype dtype;
+  int32_t ndim; /* 1..4 */
+  int64_t shape[4];
+  int64_t stride[4]; /* elements */
+} fi_tensor;
+
+typedef struct fi_plan_s* fi_plan_t;
+
+/* Read-back of a plan's host-side metadata (for tests and diagnostics). */
+typedef struct fi_plan_info {
+  int32_t batch;
+  int32_t total_rows;     /* T = qo_indptr[batch] */
+  int32_t kernel;         /* 0 decode, 1 prefill M=16, 2 prefill M=64, 3 prefill M=128 */
+  int32_t tile_rows;      /* packed (query row x head-in-group) rows per tile */
+  int32_t num_items;      /* work items (request, kv head, q tile, kv chunk) */
+  int32_t num_partials;   /* partial (o, lse) slots used for split-KV */
+  int32_t num_merge_rows; /* query tokens whose partials are merged */
+  int32_t max_chunks;     /* most KV chunks any tile was split into */
+  int32_t grid;           /* CTAs launched by run() */
+  int32_t graph_mode;
+} fi_plan_info;
+
+/*
+ * Bytes of device workspace a plan needs for the given capacities.
+ * max_kv_chunks bounds how many split-KV chunks one query tile may be cut
+ * into (the planner never exceeds what the workspace holds).
+ */
+size_t fi_workspace_bytes(int32_t max_batch, int32_t max_total_rows, int32_t num_qo_heads,
+                          int32_t head_dim, int32_t max_kv_chunks);
+
+/*
+ * Create a plan object bound to a caller-owned device workspace.
+ *   workspace       device buffer, 256-byte aligned, or NULL for a host-only
+ *                   plan (validation and planning without a GPU; run()
+ *                   refuses it).
+ *   enable_graph_capture  non-zero: run() launches a grid that does not depend
+ *                   on the batch, the kernel choice is frozen by the first
+ *                   plan, and later plans may not exceed max_batch or
+ *                   max_total_rows [P2 "Architecture / design notes"].
+ * The library allocates only the host plan object and a pinned host staging
+ * buffer here. Returns FI_ERR_CAPACITY if workspace_bytes cannot hold the
+ * metadata for max_batch / max_total_rows.
+ */
+fi_status fi_plan_create(fi_plan_t* plan, void* workspace, size_t workspace_bytes,
+                         int32_t enable_graph_capture, int32_t max_batch,
+                         int32_t max_total_rows);
+
+/*
+ * Plan one batch ([P2 "What changed"], [P3 "Plan-vs-run shapes"]).
+ *   qo_indptr      host int32 [batch+1], non-decreasing from 0. Must be NULL
+ *                  when q_len_per_req >= 1: the planner then uses
+ *                  qo_indptr[b] = q_len_per_req * b (the verify adapter of
+ *                  [P2 "What changed"]).
+ *   kv_indptr      host int32 [batch+1], page offsets into kv_indices.
+ *   last_page_len  host int32 [batch]; in [1, page_size] for a request with
+ *                  pages (ignored for a request with none).
+ *   page_size      tokens per page, >= 1.
+ *   num_qo_heads, num_kv_heads  Hq % Hk must be 0 and Hk > 0 [P3 "GQA head
+ *                  divisibility"].
+ *   head_dim       64 or 128.
+ *   causal         bottom-right causal mask when non-zero.
+ *   window_left    -1 (no window) or >= 0; values >= Lk act as -1.
+ *   dtype          FI_F16 or FI_BF16 (q, K, V and out share it).
+ *   q_len_per_req  0 plans a prefill (fi_batch_prefill_paged); 1 plans a
+ *                  decode and > 1 a speculative verify with that many draft
+ *                  rows per request (fi_batch_decode_paged; verify forces the
+ *                  causal mask) [P2 "What changed"].
+ *   force_kv_chunks 0 lets the planner split KV; > 0 cuts every query tile's
+ *                  full key range [0, Lk) into exactly that many chunks.
+ *   stream         the metadata upload is enqueued on it.
+ * Validates everything before changing any state: a refused plan leaves the
+ * previous plan usable [P2 "Review notes"], [P3 "Plan-vs-run shapes"]. Host
+ * arrays are deep-copied [P3 "AITER decode LSE fallback"]. Refusals:
+ * FI_ERR_GQA_INDIVISIBLE, FI_ERR_KV_SHORTER_THAN_Q (causal and Lk_b < Lq_b,
+ * including Lk_b < q_len_per_req), FI_ERR_CAPACITY (workspace, or a graph-mode
+ * plan beyond its capacities or changing a frozen shape), FI_ERR_UNSUPPORTED,
+ * FI_ERR_INVALID_ARG.
+ */
+fi_status fi_plan(fi_plan_t plan, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                  const int32_t* last_page_len, int32_t batch, int32_t page_size,
+                  int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t causal, int32_t window_left, fi_dtype dtype,
+                  int32_t q_len_per_req, int32_t force_kv_chunks, void* stream);
+
+/*
+ * Batched prefill over the paged cache, for a plan made with q_len_per_req 0.
+ *   q           [T', Hq, d], T' >= planned T (graph callers may pad; rows past T
+ *               are neither read nor written), any token/head strides.
+ *   k_cache, v_cache  [num_pages, page_size, Hk, d] (NHD), any page/token/head
+ *               strides; 16-byte aligned rows.
+ *   kv_indices  int32 [>= kv_indptr[batch]], contiguous.
+ *   sm_scale    score scale (usually 1/sqrt(d)).
+ *   out         [T', Hq, d] packed, dtype of q. Rows < T are written.
+ *   lse         [T', Hq] fp32 packed, or NULL.
+ * Shape, head, head_dim, page_size and dtype must match the plan
+ * (FI_ERR_PLAN_MISMATCH names the field); FI_ERR_NOT_PLANNED before a plan.
+ */
+fi_status fi_batch_prefill_paged(fi_plan_t plan, const fi_tensor* q, const fi_tensor* k_cache,
+                                 const fi_tensor* v_cache, const fi_tensor* kv_indices,
+                                 float sm_scale, fi_tensor* out, fi_tensor* lse, void* stream);
+
+/*
+ * Batched decode (q_len_per_req == 1) or speculative verify
+ * (q_len_per_req > 1, causal) for a plan made with that q_len_per_req.
+ * q is [batch * q_len_per_req (or more), Hq, d]; the other arguments are as
+ * for fi_batch_prefill_paged.
+ */
+fi_status fi_batch_decode_paged(fi_plan_t plan, const fi_tensor* q, const fi_tensor* k_cache,
+                                const fi_tensor* v_cache, const fi_tensor* kv_indices,
+                                float sm_scale, fi_tensor* out, fi_tensor* lse, void* stream);
+
+/*
+ * Merge two attention states by their log-sum-exp [P3 "Graph-mode
+ * partial_state merge"]:
+ *   m = max(s_a, s_b), s = m + ln(exp(s_a - m) + exp(s_b - m)),
+ *   v = exp(s_a - s) v_a + exp(s_b - s) v_b;  both -inf gives v = 0, s = -inf.
+ *   v_a, v_b, v_out  [rows, H, d], one dtype of FI_F16 / FI_BF16 / FI_F32;
+ *                    v_out packed; v_out may be v_a (in place, element-wise).
+ *   s_a, s_b, s_out  [rows, H] fp32 natural-log LSE; s_out packed, may be s_a.
+ *   num_rows_dev     optional device int32: only rows < *num_rows_dev are
+ *                    touched, so a captured graph re-planned to fewer rows
+ *                    does not write past its output. NULL = all rows.
+ */
+fi_status fi_merge_state(const fi_tensor* v_a, const fi_tensor* s_a, const fi_tensor* v_b,
+                         const fi_tensor* s_b, fi_tensor* v_out, fi_tensor* s_out,
+                         const int32_t* num_rows_dev, void* stream);
+
+/*
+ * Variable-length merge: row r merges states merge_indptr[r] ..
+ * merge_indptr[r+1]-1 of v [n, H, d] (fp32) / s [n, H] (fp32) into
+ * v_out [rows, H, d] (F16/BF16/F32, packed) and s_out [rows, H] (fp32,
+ * packed, or NULL). merge_indptr_dev is a device int32 [rows+1]; a row with
+ * no state gets v = 0, s = -inf. num_rows_dev as for fi_merge_state.
+ */
+fi_status fi_merge_states(const fi_tensor* v, const fi_tensor* s, const int32_t* merge_indptr_dev,
+                          int32_t rows, fi_tensor* v_out, fi_tensor* s_out,
+                          const int32_t* num_rows_dev, void* stream);
+
+/* Copy a plan's host metadata out (any pointer may be NULL):
+ *   items [num_items * 8] int32: per work item {request, kv_head, first packed
+ *         row, packed rows, kv_begin, kv_end, chunk (-1 = written directly),
+ *         partial base};
+ *   merge_indptr [total_rows + 1]: partial slots of each query token. */
+fi_status fi_plan_get_info(fi_plan_t plan, fi_plan_info* info, int32_t* items,
+                           int32_t items_capacity, int32_t* merge_indptr,
+                           int32_t merge_capacity);
+
+/* Copy the plan's device-side metadata back to the host (synchronises the
+ * stream): the same layout as fi_plan_get_info's arrays. For tests. */
+fi_status fi_plan_read_device(fi_plan_t plan, int32_t* items, int32_t items_capacity,
+                              int32_t* merge_indptr, int32_t merge_capacity, void* stream);
+
+void fi_plan_destroy(fi_plan_t plan);
+const char* fi_last_error(void);
+const char* fi_status_str(fi_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FI_H_ */

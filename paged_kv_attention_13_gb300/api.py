@@ -1,0 +1,212 @@
+"""Python binding of libfi with the C ABI's names (argument marshalling only).
+
+Every computation happens in libfi's CUDA kernels; this module turns torch
+tensors into ``fi_tensor`` descriptors, passes the current CUDA stream, and
+raises ``FiError`` with the library's message on any non-OK status.
+"""
+import ctypes
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import FiPlanInfo, FiTensor
+
+_DTYPES = {torch.float16: _lib.FI_F16, torch.bfloat16: _lib.FI_BF16,
+           torch.float32: _lib.FI_F32, torch.int32: _lib.FI_I32}
+
+KERNEL_NAMES = {0: "decode", 1: "prefill_m16", 2: "prefill_m64", 3: "prefill_m128"}
+
+
+class FiError(RuntimeError):
+    """A refusal or failure reported by libfi."""
+
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.status_name = _lib.STATUS_NAMES.get(status, str(status))
+        super().__init__("%s: %s" % (self.status_name, message))
+
+
+def _check(status: int):
+    if status != _lib.FI_OK:
+        msg = _lib.load().fi_last_error().decode(errors="replace")
+        raise FiError(status, msg)
+
+
+def tensor_desc(t: torch.Tensor) -> FiTensor:
+    """fi_tensor view of a torch tensor (no copy; strides in elements)."""
+    if t.dim() < 1 or t.dim() > 4:
+        raise ValueError("fi_tensor supports ranks 1..4, got %d" % t.dim())
+    if t.dtype not in _DTYPES:
+        raise ValueError("unsupported dtype %s" % t.dtype)
+    d = FiTensor()
+    d.data = t.data_ptr()
+    d.dtype = _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _host_i32(x):
+    if x is None:
+        return None, None
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().numpy()
+    a = np.ascontiguousarray(np.asarray(x), dtype=np.int32)
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _stream_handle(stream):
+    if stream is None:
+        if torch.cuda.is_available() and torch.cuda.is_initialized():
+            return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return ctypes.c_void_p(0)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def workspace_bytes(max_batch: int, max_total_rows: int, num_qo_heads: int, head_dim: int,
+                    max_kv_chunks: int) -> int:
+    return int(_lib.load().fi_workspace_bytes(max_batch, max_total_rows, num_qo_heads, head_dim,
+                                              max_kv_chunks))
+
+
+class Plan:
+    """An ``fi_plan_t`` bound to a caller-owned device workspace.
+
+    ``workspace`` is a CUDA uint8 tensor (kept alive by the plan) or None for a
+    host-only plan (validation and planning without a GPU).
+    """
+
+    def __init__(self, workspace=None, enable_graph_capture=False, max_batch=0, max_total_rows=0):
+        lib = _lib.load()
+        self._lib = lib
+        self.workspace = workspace
+        ptr = ctypes.c_void_p()
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        _check(lib.fi_plan_create(ctypes.byref(ptr), ws_ptr, ws_bytes, int(bool(enable_graph_capture)),
+                                  int(max_batch), int(max_total_rows)))
+        self._h = ptr
+        self.q_len_per_req = None
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.fi_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self):
+        if not self._h:
+            raise RuntimeError("plan is closed")
+        return self._h
+
+    def plan(self, qo_indptr, kv_indptr, last_page_len, page_size, num_qo_heads, num_kv_heads,
+             head_dim, causal=False, window_left=-1, dtype=torch.bfloat16, q_len_per_req=0,
+             force_kv_chunks=0, stream=None):
+        """fi_plan: host int32 metadata (tensors, arrays or lists)."""
+        qo, qo_p = _host_i32(qo_indptr)
+        kv, kv_p = _host_i32(kv_indptr)
+        last, last_p = _host_i32(last_page_len)
+        batch = len(kv) - 1 if kv is not None else 0
+        _check(self._lib.fi_plan(self.handle, qo_p, kv_p, last_p, batch, int(page_size),
+                                 int(num_qo_heads), int(num_kv_heads), int(head_dim),
+                                 int(bool(causal)), int(window_left), _DTYPES[dtype],
+                                 int(q_len_per_req), int(force_kv_chunks), _stream_handle(stream)))
+        self.q_len_per_req = q_len_per_req
+        return self
+
+    def info(self, with_arrays=False):
+        inf = FiPlanInfo()
+        _check(self._lib.fi_plan_get_info(self.handle, ctypes.byref(inf), None, 0, None, 0))
+        out = {n: getattr(inf, n) for n, _ in FiPlanInfo._fields_}
+        out["kernel_name"] = KERNEL_NAMES.get(out["kernel"], "?")
+        if with_arrays:
+            items = np.zeros(max(out["num_items"], 1) * 8, np.int32)
+            merge = np.zeros(out["total_rows"] + 1, np.int32)
+            _check(self._lib.fi_plan_get_info(
+                self.handle, None, items.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                items.size, merge.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), merge.size))
+            out["items"] = items[: out["num_items"] * 8].reshape(-1, 8)
+            out["merge_indptr"] = merge
+        return out
+
+    def read_device(self, stream=None):
+        inf = self.info()
+        items = np.zeros(max(inf["num_items"], 1) * 8, np.int32)
+        merge = np.zeros(inf["total_rows"] + 1, np.int32)
+        _check(self._lib.fi_plan_read_device(
+            self.handle, items.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), items.size,
+            merge.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), merge.size,
+            _stream_handle(stream)))
+        return items[: inf["num_items"] * 8].reshape(-1, 8), merge
+
+
+def fi_plan(plan: Plan, *args, **kwargs) -> Plan:
+    return plan.plan(*args, **kwargs)
+
+
+def _run(fn, plan, q, k_cache, v_cache, kv_indices, sm_scale, out, lse, return_lse, stream):
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    qd, kd, vd, idd, od = (tensor_desc(q), tensor_desc(k_cache), tensor_desc(v_cache),
+                           tensor_desc(kv_indices), tensor_desc(out))
+    ld = tensor_desc(lse) if lse is not None else None
+    _check(fn(plan.handle, ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd), ctypes.byref(idd),
+              ctypes.c_float(sm_scale), ctypes.byref(od), ctypes.byref(ld) if ld is not None else None,
+              _stream_handle(stream)))
+    return out, lse
+
+
+def fi_batch_prefill_paged(plan, q, k_cache, v_cache, kv_indices, sm_scale, out=None, lse=None,
+                           return_lse=True, stream=None):
+    """Batched paged prefill; returns (out, lse)."""
+    return _run(_lib.load().fi_batch_prefill_paged, plan, q, k_cache, v_cache, kv_indices,
+                sm_scale, out, lse, return_lse, stream)
+
+
+def fi_batch_decode_paged(plan, q, k_cache, v_cache, kv_indices, sm_scale, out=None, lse=None,
+                          return_lse=True, stream=None):
+    """Batched paged decode / speculative verify; returns (out, lse)."""
+    return _run(_lib.load().fi_batch_decode_paged, plan, q, k_cache, v_cache, kv_indices,
+                sm_scale, out, lse, return_lse, stream)
+
+
+def fi_merge_state(v_a, s_a, v_b, s_b, v_out=None, s_out=None, num_rows_dev=None, stream=None):
+    """Merge two attention states by LSE; returns (v_out, s_out)."""
+    if v_out is None:
+        v_out = torch.empty(v_a.shape, dtype=v_a.dtype, device=v_a.device)
+    if s_out is None:
+        s_out = torch.empty(s_a.shape, dtype=torch.float32, device=s_a.device)
+    descs = [tensor_desc(t) for t in (v_a, s_a, v_b, s_b, v_out, s_out)]
+    _check(_lib.load().fi_merge_state(*[ctypes.byref(d) for d in descs],
+                                      num_rows_dev.data_ptr() if num_rows_dev is not None else None,
+                                      _stream_handle(stream)))
+    return v_out, s_out
+
+
+def fi_merge_states(v, s, merge_indptr, rows, v_out=None, s_out=None, out_dtype=torch.float32,
+                    num_rows_dev=None, return_lse=True, stream=None):
+    """Variable-length merge: row r merges states merge_indptr[r]..[r+1]-1."""
+    if v_out is None:
+        v_out = torch.empty((rows,) + tuple(v.shape[1:]), dtype=out_dtype, device=v.device)
+    if s_out is None and return_lse:
+        s_out = torch.empty((rows, v.shape[1]), dtype=torch.float32, device=v.device)
+    vd, sd, vod = tensor_desc(v), tensor_desc(s), tensor_desc(v_out)
+    sod = tensor_desc(s_out) if s_out is not None else None
+    _check(_lib.load().fi_merge_states(
+        ctypes.byref(vd), ctypes.byref(sd), merge_indptr.data_ptr(), int(rows), ctypes.byref(vod),
+        ctypes.byref(sod) if sod is not None else None,
+        num_rows_dev.data_ptr() if num_rows_dev is not None else None, _stream_handle(stream)))
+    return v_out, s_out

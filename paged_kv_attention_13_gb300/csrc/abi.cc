@@ -1,0 +1,863 @@
+// C ABI of libfi: argument validation, the host planner, the metadata upload
+// and the run() launches. Page citations use the keys of include/fi.h:
+//   [P1] "Route non-causal windowed prefill to AITER's masked kernel" (#339)
+//   [P2] "Support speculative-decode verify on ROCm, and stop auto routing
+//         short-query prefill to AITER" (#362)
+//   [P3] "Refuse attention inputs the ROCm kernels would compute wrongly" (#399)
+#include "../../include/fi.h"
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "fi_internal.h"
+
+using fi::WorkItem;
+using fi::WsHeader;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+fi_status fail(fi_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+fi_status ok() {
+  g_last_error.clear();
+  return FI_OK;
+}
+
+constexpr int64_t kAlign = 256;
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// Everything a committed plan knows (host copy; the device copy is uploaded).
+struct PlanState {
+  int32_t batch = 0, total_rows = 0, page_size = 0, hq = 0, hk = 0, d = 0;
+  int32_t causal = 0, window_left = -1, dtype = 0, q_len_per_req = 0, group = 1;
+  int32_t kernel = 0, tile_rows = 0, grid = 0, max_chunks = 1, n_partials = 0;
+  int32_t kv_indices_len = 0;
+  std::vector<int32_t> qo_indptr, kv_indptr, kv_len, merge_indptr, merge_rows;
+  std::vector<WorkItem> items;
+  WsHeader hdr{};
+  int64_t meta_bytes = 0;   // header + metadata arrays (uploaded)
+  int64_t total_bytes = 0;  // + partial buffers
+};
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace
+
+struct fi_plan_s {
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  bool host_only = true;
+  bool graph = false;
+  int32_t max_batch = 0, max_total_rows = 0;
+  int num_sms = 152;
+  void* staging = nullptr;  // pinned host buffer for the metadata upload
+  size_t staging_bytes = 0;
+  cudaEvent_t upload_done = nullptr;
+  bool upload_pending = false;
+  bool planned = false;
+  PlanState st;
+  // shape frozen by the first plan of a graph-mode plan object
+  bool frozen = false;
+  int32_t fz_kernel = 0, fz_qlpr = 0, fz_hq = 0, fz_hk = 0, fz_d = 0, fz_dtype = 0, fz_page = 0;
+};
+
+extern "C" const char* fi_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" const char* fi_status_str(fi_status s) {
+  switch (s) {
+    case FI_OK: return "FI_OK";
+    case FI_ERR_INVALID_ARG: return "FI_ERR_INVALID_ARG";
+    case FI_ERR_STRIDED_LAST_DIM: return "FI_ERR_STRIDED_LAST_DIM";
+    case FI_ERR_NONCONTIGUOUS_OUTPUT: return "FI_ERR_NONCONTIGUOUS_OUTPUT";
+    case FI_ERR_GQA_INDIVISIBLE: return "FI_ERR_GQA_INDIVISIBLE";
+    case FI_ERR_PLAN_MISMATCH: return "FI_ERR_PLAN_MISMATCH";
+    case FI_ERR_NOT_PLANNED: return "FI_ERR_NOT_PLANNED";
+    case FI_ERR_KV_SHORTER_THAN_Q: return "FI_ERR_KV_SHORTER_THAN_Q";
+    case FI_ERR_CAPACITY: return "FI_ERR_CAPACITY";
+    case FI_ERR_UNSUPPORTED: return "FI_ERR_UNSUPPORTED";
+    case FI_ERR_CUDA: return "FI_ERR_CUDA";
+  }
+  return "FI_ERR_UNKNOWN";
+}
+
+namespace {
+
+// Metadata bytes for a batch (header + int arrays + items), 256-aligned.
+int64_t meta_bytes_for(int64_t batch, int64_t rows, int64_t n_merge, int64_t n_items) {
+  int64_t off = sizeof(WsHeader);
+  off = align_up(off + 4 * (batch + 1), 16);  // qo_indptr
+  off = align_up(off + 4 * (batch + 1), 16);  // kv_indptr
+  off = align_up(off + 4 * batch, 16);        // kv_len
+  off = align_up(off + 4 * (rows + 1), 16);   // merge_indptr
+  off = align_up(off + 4 * n_merge, 32);      // merge_rows
+  off += 32 * n_items;                        // items
+  return align_up(off, kAlign);
+}
+
+int64_t partial_bytes_for(int64_t n_partials, int64_t hq, int64_t d) {
+  return align_up(4 * n_partials * hq, kAlign) + align_up(4 * n_partials * hq * d, kAlign);
+}
+
+}  // namespace
+
+extern "C" size_t fi_workspace_bytes(int32_t max_batch, int32_t max_total_rows,
+                                     int32_t num_qo_heads, int32_t head_dim,
+                                     int32_t max_kv_chunks) {
+  if (max_batch < 0 || max_total_rows < 0 || num_qo_heads <= 0 || head_dim <= 0) return 0;
+  int64_t chunks = std::max<int32_t>(max_kv_chunks, 1);
+  int64_t rows = max_total_rows;
+  // every tile holds >= 1 token, so tiles <= rows; items <= tiles * chunks * heads
+  int64_t items = std::max<int64_t>(rows, 1) * chunks * num_qo_heads;
+  int64_t partials = chunks > 1 ? rows * chunks : 0;
+  return static_cast<size_t>(meta_bytes_for(max_batch, rows, rows, items) +
+                             partial_bytes_for(partials, num_qo_heads, head_dim));
+}
+
+extern "C" fi_status fi_plan_create(fi_plan_t* out, void* workspace, size_t workspace_bytes,
+                                    int32_t enable_graph_capture, int32_t max_batch,
+                                    int32_t max_total_rows) {
+  if (!out) return fail(FI_ERR_INVALID_ARG, "plan: output pointer is NULL");
+  *out = nullptr;
+  if (max_batch < 0 || max_total_rows < 0)
+    return fail(FI_ERR_INVALID_ARG, "plan_create: max_batch=%d max_total_rows=%d must be >= 0",
+                max_batch, max_total_rows);
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
+    return fail(FI_ERR_INVALID_ARG, "plan_create: workspace must be 256-byte aligned");
+  if (workspace && enable_graph_capture &&
+      static_cast<int64_t>(workspace_bytes) < meta_bytes_for(max_batch, max_total_rows, 0, 0))
+    return fail(FI_ERR_CAPACITY, "plan_create: workspace_bytes=%zu cannot hold the metadata of "
+                "max_batch=%d max_total_rows=%d", workspace_bytes, max_batch, max_total_rows);
+  fi_plan_s* p = new (std::nothrow) fi_plan_s();
+  if (!p) return fail(FI_ERR_INVALID_ARG, "plan_create: out of host memory");
+  p->ws = workspace;
+  p->ws_bytes = workspace_bytes;
+  p->host_only = (workspace == nullptr);
+  p->graph = enable_graph_capture != 0;
+  p->max_batch = max_batch;
+  p->max_total_rows = max_total_rows;
+  if (!p->host_only) {
+    int n = device_sm_count();
+    if (n <= 0) {
+      delete p;
+      return fail(FI_ERR_CUDA, "plan_create: no CUDA device (%s)",
+                  cudaGetErrorString(cudaGetLastError()));
+    }
+    p->num_sms = n;
+    if (cudaEventCreateWithFlags(&p->upload_done, cudaEventDisableTiming) != cudaSuccess) {
+      delete p;
+      return fail(FI_ERR_CUDA, "plan_create: cudaEventCreate failed");
+    }
+  }
+  *out = p;
+  return ok();
+}
+
+extern "C" void fi_plan_destroy(fi_plan_t p) {
+  if (!p) return;
+  if (p->upload_pending && p->upload_done) cudaEventSynchronize(p->upload_done);
+  if (p->upload_done) cudaEventDestroy(p->upload_done);
+  if (p->staging) cudaFreeHost(p->staging);
+  delete p;
+}
+
+namespace {
+
+bool group_has_decode_kernel(int g) { return g == 1 || g == 2 || g == 4; }
+
+int choose_kernel(int32_t q_len_per_req, int32_t g, int64_t max_rows_per_req) {
+  if (q_len_per_req == 1 && group_has_decode_kernel(g)) return fi::kDecode;
+  if (max_rows_per_req <= 16 && g <= 16) return fi::kPrefillM16;
+  if (g <= 64) return fi::kPrefillM64;
+  return -1;
+}
+
+int tile_rows_of(int kernel, int g) {
+  switch (kernel) {
+    case fi::kDecode: return g;
+    case fi::kPrefillM16: return (16 / g) * g;
+    case fi::kPrefillM64: return (64 / g) * g;
+    case fi::kPrefillM128: return (128 / g) * g;
+  }
+  return 0;
+}
+
+struct Tile {
+  int32_t b, row0, rows, lo, hi, lk;
+  int32_t first_token;  // global token index of the tile's first query row
+  int32_t n_tokens;
+};
+
+// Build a complete plan into `ns` without touching the plan object.
+fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
+                     const int32_t* last_page_len_h, int32_t batch, int32_t page_size,
+                     int32_t hq, int32_t hk, int32_t d, int32_t causal, int32_t window_left,
+                     fi_dtype dtype, int32_t q_len_per_req, int32_t force_kv_chunks,
+                     PlanState& ns) {
+  // ---- argument validation, before anything is written [P2 "Review notes"]
+  if (batch < 0) return fail(FI_ERR_INVALID_ARG, "plan: batch=%d must be >= 0", batch);
+  if (batch > 0 && (!kv_indptr_h || !last_page_len_h))
+    return fail(FI_ERR_INVALID_ARG, "plan: kv_indptr and last_page_len must be non-NULL");
+  if (page_size < 1) return fail(FI_ERR_INVALID_ARG, "plan: page_size=%d must be >= 1", page_size);
+  // [P3 "GQA head divisibility"]: refuse zero kv heads and a group that does not divide
+  if (hk <= 0 || hq <= 0 || hq % hk != 0)
+    return fail(FI_ERR_GQA_INDIVISIBLE,
+                "plan: num_qo_heads=%d is not a multiple of num_kv_heads=%d", hq, hk);
+  if (d != 64 && d != 128)
+    return fail(FI_ERR_UNSUPPORTED, "plan: head_dim=%d (built: 64, 128)", d);
+  if (dtype != FI_F16 && dtype != FI_BF16)
+    return fail(FI_ERR_UNSUPPORTED, "plan: dtype=%d (built: FI_F16, FI_BF16)", (int)dtype);
+  if (window_left < -1)
+    return fail(FI_ERR_INVALID_ARG, "plan: window_left=%d must be -1 or >= 0", window_left);
+  if (q_len_per_req < 0)
+    return fail(FI_ERR_INVALID_ARG, "plan: q_len_per_req=%d must be >= 0", q_len_per_req);
+  if (force_kv_chunks < 0 || force_kv_chunks > 4096)
+    return fail(FI_ERR_INVALID_ARG, "plan: force_kv_chunks=%d must be in [0, 4096]",
+                force_kv_chunks);
+  if (q_len_per_req >= 1 && qo_indptr_h)
+    return fail(FI_ERR_INVALID_ARG, "plan: qo_indptr must be NULL when q_len_per_req=%d >= 1 "
+                "(it is q_len_per_req * b)", q_len_per_req);
+  if (q_len_per_req == 0 && batch > 0 && !qo_indptr_h)
+    return fail(FI_ERR_INVALID_ARG, "plan: qo_indptr is NULL for a prefill plan");
+  // the verify adapter makes the mask causal [P2 "What changed"]
+  const int32_t eff_causal = (q_len_per_req > 1) ? 1 : (causal ? 1 : 0);
+  const int32_t g = hq / hk;
+
+  ns = PlanState();
+  ns.batch = batch; ns.page_size = page_size; ns.hq = hq; ns.hk = hk; ns.d = d;
+  ns.causal = eff_causal; ns.window_left = window_left; ns.dtype = dtype;
+  ns.q_len_per_req = q_len_per_req; ns.group = g;
+  ns.qo_indptr.resize(batch + 1);
+  ns.kv_indptr.resize(batch + 1);
+  ns.kv_len.resize(batch);
+  int64_t qacc = 0;
+  ns.qo_indptr[0] = 0;
+  for (int32_t b = 0; b <= batch; ++b) {
+    int64_t v = (q_len_per_req >= 1) ? int64_t(q_len_per_req) * b
+                                      : (qo_indptr_h ? int64_t(qo_indptr_h[b]) : 0);
+    if (b == 0 && v != 0) return fail(FI_ERR_INVALID_ARG, "plan: qo_indptr[0]=%lld must be 0", (long long)v);
+    if (v < qacc) return fail(FI_ERR_INVALID_ARG, "plan: qo_indptr decreases at b=%d", b);
+    if (v > INT32_MAX) return fail(FI_ERR_INVALID_ARG, "plan: total query rows overflow int32");
+    qacc = v;
+    ns.qo_indptr[b] = static_cast<int32_t>(v);
+  }
+  ns.total_rows = ns.qo_indptr[batch];
+  int64_t max_rows_per_req = 0;
+  for (int32_t b = 0; b <= batch; ++b) {
+    int32_t v = kv_indptr_h ? kv_indptr_h[b] : 0;
+    if (b == 0 && v != 0) return fail(FI_ERR_INVALID_ARG, "plan: kv_indptr[0]=%d must be 0", v);
+    if (b > 0 && v < ns.kv_indptr[b - 1])
+      return fail(FI_ERR_INVALID_ARG, "plan: kv_indptr decreases at b=%d", b);
+    ns.kv_indptr[b] = v;
+  }
+  ns.kv_indices_len = ns.kv_indptr[batch];
+  for (int32_t b = 0; b < batch; ++b) {
+    // [P2 "Review notes"]: kv_len from the page metadata (paged_kv_t::get_length)
+    int64_t pages = int64_t(ns.kv_indptr[b + 1]) - ns.kv_indptr[b];
+    int64_t lk = 0;
+    if (pages > 0) {
+      int32_t last = last_page_len_h[b];
+      if (last < 1 || last > page_size)
+        return fail(FI_ERR_INVALID_ARG, "plan: last_page_len[%d]=%d outside [1, page_size=%d]",
+                    b, last, page_size);
+      lk = (pages - 1) * page_size + last;
+    }
+    if (lk > INT32_MAX / 2) return fail(FI_ERR_INVALID_ARG, "plan: kv_len of request %d too long", b);
+    int64_t lq = int64_t(ns.qo_indptr[b + 1]) - ns.qo_indptr[b];
+    // [P2 "Review notes"]: a causal request whose KV is shorter than its query
+    // rows would be masked against a range shorter than the query; refuse it.
+    if (eff_causal && lk < lq)
+      return fail(FI_ERR_KV_SHORTER_THAN_Q,
+                  "plan: request %d has kv_len=%lld (from kv_indptr/last_page_len) < qo_len=%lld "
+                  "under the causal mask", b, (long long)lk, (long long)lq);
+    ns.kv_len[b] = static_cast<int32_t>(lk);
+    max_rows_per_req = std::max<int64_t>(max_rows_per_req, lq * g);
+  }
+
+  // ---- graph-mode capacities and frozen shape [P2 "Architecture / design notes"]
+  if (P.graph) {
+    if (batch > P.max_batch)
+      return fail(FI_ERR_CAPACITY, "plan: batch=%d exceeds the graph capacity max_batch=%d",
+                  batch, P.max_batch);
+    if (ns.total_rows > P.max_total_rows)
+      return fail(FI_ERR_CAPACITY, "plan: total rows=%d exceed the graph capacity "
+                  "max_total_rows=%d", ns.total_rows, P.max_total_rows);
+    // the kernel cannot follow per-batch lengths once captured: bound them
+    max_rows_per_req = (q_len_per_req >= 1) ? int64_t(q_len_per_req) * g
+                                             : int64_t(P.max_total_rows) * g;
+  }
+  ns.kernel = choose_kernel(q_len_per_req, g, max_rows_per_req);
+  if (ns.kernel < 0)
+    return fail(FI_ERR_UNSUPPORTED, "plan: GQA group %d is larger than the widest tile", g);
+  if (P.graph && P.frozen) {
+    const char* field = nullptr;
+    int32_t want = 0, got = 0;
+    if (q_len_per_req != P.fz_qlpr) { field = "q_len_per_req"; want = P.fz_qlpr; got = q_len_per_req; }
+    else if (hq != P.fz_hq) { field = "num_qo_heads"; want = P.fz_hq; got = hq; }
+    else if (hk != P.fz_hk) { field = "num_kv_heads"; want = P.fz_hk; got = hk; }
+    else if (d != P.fz_d) { field = "head_dim"; want = P.fz_d; got = d; }
+    else if (dtype != P.fz_dtype) { field = "dtype"; want = P.fz_dtype; got = dtype; }
+    else if (page_size != P.fz_page) { field = "page_size"; want = P.fz_page; got = page_size; }
+    else if (ns.kernel != P.fz_kernel) { field = "kernel"; want = P.fz_kernel; got = ns.kernel; }
+    if (field)
+      return fail(FI_ERR_CAPACITY, "plan: %s is frozen at %d by the first graph-mode plan, got %d",
+                  field, want, got);
+  }
+  ns.tile_rows = tile_rows_of(ns.kernel, g);
+
+  // ---- tiles and their live key ranges
+  std::vector<Tile> tiles;
+  int64_t total_len = 0, max_len = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int64_t lq = int64_t(ns.qo_indptr[b + 1]) - ns.qo_indptr[b];
+    const int64_t lk = ns.kv_len[b];
+    for (int64_t row0 = 0; row0 < lq * g; row0 += ns.tile_rows) {
+      const int64_t rows = std::min<int64_t>(ns.tile_rows, lq * g - row0);
+      const int64_t i0 = row0 / g, i1 = (row0 + rows) / g - 1;
+      int64_t hi = eff_causal ? std::min<int64_t>(lk, i1 + lk - lq + 1) : lk;
+      int64_t lo = window_left >= 0 ? std::max<int64_t>(0, lk - lq + i0 - window_left) : 0;
+      hi = std::max<int64_t>(hi, 0);
+      if (lo > hi) lo = hi;
+      Tile t{b, int32_t(row0), int32_t(rows), int32_t(lo), int32_t(hi), int32_t(lk),
+             int32_t(ns.qo_indptr[b] + i0), int32_t(i1 - i0 + 1)};
+      tiles.push_back(t);
+      total_len += hi - lo;
+      max_len = std::max<int64_t>(max_len, hi - lo);
+    }
+  }
+
+  // ---- KV split
+  const int ctas_per_sm = std::max(1, fi::kernel_ctas_per_sm(ns.kernel, d, g, dtype == FI_BF16));
+  const int64_t grid_cap = int64_t(P.num_sms) * ctas_per_sm;
+  const int64_t avail = P.host_only ? INT64_MAX / 4 : int64_t(P.ws_bytes);
+  auto count_for = [&](int64_t chunk_len, int64_t* n_items, int64_t* n_partials) {
+    int64_t items = 0, partials = 0;
+    for (const Tile& t : tiles) {
+      int64_t n = 1;
+      if (force_kv_chunks > 0) n = force_kv_chunks;
+      else if (chunk_len > 0 && t.hi - t.lo > chunk_len) n = (t.hi - t.lo + chunk_len - 1) / chunk_len;
+      items += n * hk;
+      if (n > 1) partials += n * t.n_tokens;
+    }
+    *n_items = items;
+    *n_partials = partials;
+  };
+  auto fits = [&](int64_t n_items, int64_t n_partials, int64_t n_merge) {
+    return meta_bytes_for(batch, ns.total_rows, n_merge, n_items) +
+               partial_bytes_for(n_partials, hq, d) <= avail;
+  };
+  int64_t chunk_len = 0;  // 0 = no split
+  if (force_kv_chunks == 0 && !tiles.empty()) {
+    const int64_t min_chunk = 256;
+    const int64_t units = int64_t(tiles.size()) * hk;
+    // split when the tiles alone cannot keep every SM busy and balanced:
+    // aim at ~4 items per resident CTA, no chunk shorter than min_chunk keys
+    int64_t want = (total_len * hk + 4 * grid_cap - 1) / (4 * grid_cap);
+    want = std::max<int64_t>(min_chunk, (want + 63) / 64 * 64);
+    if (max_len > want && units < 4 * grid_cap * 4) chunk_len = want;
+    // grow the chunks until the partial states fit the workspace
+    while (chunk_len > 0) {
+      int64_t ni, np;
+      count_for(chunk_len, &ni, &np);
+      if (fits(ni, np, ns.total_rows)) break;
+      chunk_len *= 2;
+      if (chunk_len >= max_len) chunk_len = 0;
+    }
+  }
+  {
+    int64_t ni, np;
+    count_for(chunk_len, &ni, &np);
+    if (ni > INT32_MAX / 2 || np > INT32_MAX / 2)
+      return fail(FI_ERR_CAPACITY, "plan: %lld work items exceed the planner's range", (long long)ni);
+    if (!fits(ni, np, ns.total_rows))
+      return fail(FI_ERR_CAPACITY, "plan: workspace_bytes=%zu < %lld needed for %lld items and "
+                  "%lld partial states", P.ws_bytes,
+                  (long long)(meta_bytes_for(batch, ns.total_rows, ns.total_rows, ni) +
+                              partial_bytes_for(np, hq, d)),
+                  (long long)ni, (long long)np);
+  }
+
+  // ---- work items, partial slots and the merge index
+  ns.merge_indptr.assign(ns.total_rows + 1, 0);
+  std::vector<int32_t> merge_count(ns.total_rows, 0);
+  struct Costed { int64_t cost; WorkItem it; };
+  std::vector<Costed> costed;
+  int32_t partial_cursor = 0;
+  int32_t max_chunks = 1;
+  for (const Tile& t : tiles) {
+    int64_t n = 1;
+    if (force_kv_chunks > 0) n = force_kv_chunks;
+    else if (chunk_len > 0 && t.hi - t.lo > chunk_len) n = (t.hi - t.lo + chunk_len - 1) / chunk_len;
+    max_chunks = std::max<int32_t>(max_chunks, int32_t(n));
+    const int32_t base = (n > 1) ? partial_cursor : -1;
+    if (n > 1) {
+      partial_cursor += int32_t(n) * t.n_tokens;
+      for (int32_t k = 0; k < t.n_tokens; ++k) merge_count[t.first_token + k] = int32_t(n);
+    }
+    for (int64_t c = 0; c < n; ++c) {
+      int64_t kb, ke;
+      if (force_kv_chunks > 0) {  // even cut of the full key range [0, Lk)
+        kb = int64_t(t.lk) * c / n;
+        ke = int64_t(t.lk) * (c + 1) / n;
+      } else if (n > 1) {         // chunk_len cut of the live range
+        kb = t.lo + c * chunk_len;
+        ke = std::min<int64_t>(t.hi, kb + chunk_len);
+      } else {
+        kb = t.lo;
+        ke = t.hi;
+      }
+      const int64_t live = std::max<int64_t>(0, std::min<int64_t>(ke, t.hi) - std::max<int64_t>(kb, t.lo));
+      for (int32_t h = 0; h < hk; ++h) {
+        WorkItem it;
+        it.b = t.b; it.kv_head = h; it.row0 = t.row0;
+        it.kv_begin = int32_t(kb); it.kv_end = int32_t(ke);
+        it.chunk = (n > 1) ? int32_t(c) : -1;
+        it.num_chunks = int32_t(n);
+        it.partial_base = base;
+        costed.push_back({live * t.rows + 64, it});
+      }
+    }
+  }
+  // longest first, so a persistent grid striding over the list stays balanced
+  std::stable_sort(costed.begin(), costed.end(),
+                   [](const Costed& a, const Costed& b) { return a.cost > b.cost; });
+  ns.items.reserve(costed.size());
+  for (const Costed& c : costed) ns.items.push_back(c.it);
+  for (int32_t t = 0; t < ns.total_rows; ++t) {
+    ns.merge_indptr[t + 1] = ns.merge_indptr[t] + merge_count[t];
+    if (merge_count[t] > 1) ns.merge_rows.push_back(t);
+  }
+  ns.n_partials = partial_cursor;
+  ns.max_chunks = max_chunks;
+  const int64_t n_items = int64_t(ns.items.size());
+  ns.grid = int32_t(P.graph ? grid_cap : std::min<int64_t>(n_items, grid_cap));
+
+  // ---- device layout
+  WsHeader& h = ns.hdr;
+  std::memset(&h, 0, sizeof h);
+  h.n_items = int32_t(n_items);
+  h.n_merge_rows = int32_t(ns.merge_rows.size());
+  h.total_rows = ns.total_rows;
+  h.batch = batch;
+  h.group = g;
+  h.causal = eff_causal;
+  h.window_left = window_left;
+  h.tile_rows = ns.tile_rows;
+  h.num_qo_heads = hq;
+  h.head_dim = d;
+  int64_t off = sizeof(WsHeader);
+  h.off_qo_indptr = off; off = align_up(off + 4 * (batch + 1), 16);
+  h.off_kv_indptr = off; off = align_up(off + 4 * (batch + 1), 16);
+  h.off_kv_len = off; off = align_up(off + 4 * batch, 16);
+  h.off_merge_indptr = off; off = align_up(off + 4 * (ns.total_rows + 1), 16);
+  h.off_merge_rows = off; off = align_up(off + 4 * int64_t(ns.merge_rows.size()), 32);
+  h.off_items = off; off += 32 * n_items;
+  ns.meta_bytes = align_up(off, kAlign);
+  h.off_tmp_lse = ns.meta_bytes;
+  h.off_tmp_o = ns.meta_bytes + align_up(4 * int64_t(ns.n_partials) * hq, kAlign);
+  ns.total_bytes = ns.meta_bytes + partial_bytes_for(ns.n_partials, hq, d);
+  return FI_OK;
+}
+
+void write_staging(const PlanState& s, uint8_t* dst) {
+  std::memset(dst, 0, s.meta_bytes);
+  std::memcpy(dst, &s.hdr, sizeof(WsHeader));
+  auto put = [&](int64_t off, const void* src, size_t n) {
+    if (n) std::memcpy(dst + off, src, n);
+  };
+  put(s.hdr.off_qo_indptr, s.qo_indptr.data(), 4 * s.qo_indptr.size());
+  put(s.hdr.off_kv_indptr, s.kv_indptr.data(), 4 * s.kv_indptr.size());
+  put(s.hdr.off_kv_len, s.kv_len.data(), 4 * s.kv_len.size());
+  put(s.hdr.off_merge_indptr, s.merge_indptr.data(), 4 * s.merge_indptr.size());
+  put(s.hdr.off_merge_rows, s.merge_rows.data(), 4 * s.merge_rows.size());
+  put(s.hdr.off_items, s.items.data(), sizeof(WorkItem) * s.items.size());
+}
+
+}  // namespace
+
+extern "C" fi_status fi_plan(fi_plan_t p, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                             const int32_t* last_page_len, int32_t batch, int32_t page_size,
+                             int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t causal, int32_t window_left, fi_dtype dtype,
+                             int32_t q_len_per_req, int32_t force_kv_chunks, void* stream) {
+  if (!p) return fail(FI_ERR_INVALID_ARG, "plan: plan is NULL");
+  PlanState ns;
+  fi_status st = build_plan(*p, qo_indptr, kv_indptr, last_page_len, batch, page_size,
+                            num_qo_heads, num_kv_heads, head_dim, causal, window_left, dtype,
+                            q_len_per_req, force_kv_chunks, ns);
+  if (st != FI_OK) return st;  // the previous plan stays usable
+  if (!p->host_only) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the previous upload must have left the pinned buffer before it is reused
+    if (p->upload_pending) {
+      if (cudaEventSynchronize(p->upload_done) != cudaSuccess) {
+        p->planned = false;
+        return fail(FI_ERR_CUDA, "plan: waiting for the previous upload failed");
+      }
+      p->upload_pending = false;
+    }
+    if (p->staging_bytes < size_t(ns.meta_bytes)) {
+      if (p->staging) cudaFreeHost(p->staging);
+      p->staging = nullptr;
+      p->staging_bytes = 0;
+      size_t want = size_t(align_up(ns.meta_bytes * 5 / 4 + 4096, 4096));
+      if (cudaHostAlloc(&p->staging, want, cudaHostAllocDefault) != cudaSuccess) {
+        p->staging = nullptr;
+        p->planned = false;
+        return fail(FI_ERR_CUDA, "plan: cudaHostAlloc(%zu) failed", want);
+      }
+      p->staging_bytes = want;
+    }
+    write_staging(ns, static_cast<uint8_t*>(p->staging));
+    // from here the device copy changes: a failure leaves run() refusing
+    cudaError_t e = cudaMemcpyAsync(p->ws, p->staging, size_t(ns.meta_bytes),
+                                    cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaEventRecord(p->upload_done, s);
+    if (e != cudaSuccess) {
+      p->planned = false;
+      return fail(FI_ERR_CUDA, "plan: metadata upload failed: %s", cudaGetErrorString(e));
+    }
+    p->upload_pending = true;
+  }
+  if (p->graph && !p->frozen) {
+    p->frozen = true;
+    p->fz_kernel = ns.kernel; p->fz_qlpr = ns.q_len_per_req; p->fz_hq = ns.hq;
+    p->fz_hk = ns.hk; p->fz_d = ns.d; p->fz_dtype = ns.dtype; p->fz_page = ns.page_size;
+  }
+  p->st = std::move(ns);
+  p->planned = true;
+  return ok();
+}
+
+extern "C" fi_status fi_plan_get_info(fi_plan_t p, fi_plan_info* info, int32_t* items,
+                                      int32_t items_capacity, int32_t* merge_indptr,
+                                      int32_t merge_capacity) {
+  if (!p) return fail(FI_ERR_INVALID_ARG, "plan_get_info: plan is NULL");
+  if (!p->planned) return fail(FI_ERR_NOT_PLANNED, "plan_get_info: call fi_plan() first");
+  const PlanState& s = p->st;
+  if (info) {
+    info->batch = s.batch;
+    info->total_rows = s.total_rows;
+    info->kernel = s.kernel;
+    info->tile_rows = s.tile_rows;
+    info->num_items = int32_t(s.items.size());
+    info->num_partials = s.n_partials;
+    info->num_merge_rows = int32_t(s.merge_rows.size());
+    info->max_chunks = s.max_chunks;
+    info->grid = s.grid;
+    info->graph_mode = p->graph ? 1 : 0;
+  }
+  if (items) {
+    if (items_capacity < int32_t(s.items.size() * 8))
+      return fail(FI_ERR_CAPACITY, "plan_get_info: items_capacity=%d < %d", items_capacity,
+                  int32_t(s.items.size() * 8));
+    std::memcpy(items, s.items.data(), s.items.size() * sizeof(WorkItem));
+  }
+  if (merge_indptr) {
+    if (merge_capacity < int32_t(s.merge_indptr.size()))
+      return fail(FI_ERR_CAPACITY, "plan_get_info: merge_capacity=%d < %d", merge_capacity,
+                  int32_t(s.merge_indptr.size()));
+    std::memcpy(merge_indptr, s.merge_indptr.data(), s.merge_indptr.size() * 4);
+  }
+  return ok();
+}
+
+extern "C" fi_status fi_plan_read_device(fi_plan_t p, int32_t* items, int32_t items_capacity,
+                                         int32_t* merge_indptr, int32_t merge_capacity,
+                                         void* stream) {
+  if (!p) return fail(FI_ERR_INVALID_ARG, "plan_read_device: plan is NULL");
+  if (!p->planned) return fail(FI_ERR_NOT_PLANNED, "plan_read_device: call fi_plan() first");
+  if (p->host_only) return fail(FI_ERR_INVALID_ARG, "plan_read_device: host-only plan");
+  const PlanState& s = p->st;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::vector<uint8_t> buf(size_t(s.meta_bytes));
+  cudaError_t e = cudaMemcpyAsync(buf.data(), p->ws, buf.size(), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess)
+    return fail(FI_ERR_CUDA, "plan_read_device: %s", cudaGetErrorString(e));
+  WsHeader h;
+  std::memcpy(&h, buf.data(), sizeof h);
+  if (items) {
+    if (items_capacity < h.n_items * 8) return fail(FI_ERR_CAPACITY, "plan_read_device: items");
+    std::memcpy(items, buf.data() + h.off_items, size_t(h.n_items) * sizeof(WorkItem));
+  }
+  if (merge_indptr) {
+    if (merge_capacity < h.total_rows + 1) return fail(FI_ERR_CAPACITY, "plan_read_device: merge");
+    std::memcpy(merge_indptr, buf.data() + h.off_merge_indptr, size_t(h.total_rows + 1) * 4);
+  }
+  return ok();
+}
+
+// ------------------------------------------------------------------ run()
+namespace {
+
+const char* dtype_name(int d) {
+  switch (d) {
+    case FI_F16: return "f16";
+    case FI_BF16: return "bf16";
+    case FI_F32: return "f32";
+    case FI_I32: return "i32";
+  }
+  return "?";
+}
+
+fi_status check_tensor(const fi_tensor* t, const char* name, int ndim) {
+  if (!t || !t->data) return fail(FI_ERR_INVALID_ARG, "run: %s is NULL", name);
+  if (t->ndim != ndim)
+    return fail(FI_ERR_PLAN_MISMATCH, "run: %s rank: expected %d, got %d", name, ndim, t->ndim);
+  for (int i = 0; i < ndim; ++i)
+    if (t->shape[i] < 0) return fail(FI_ERR_INVALID_ARG, "run: %s shape[%d] < 0", name, i);
+  // [P3 "Strided layouts"]: a strided last dim is refused, not copied
+  if (t->shape[ndim - 1] > 1 && t->stride[ndim - 1] != 1)
+    return fail(FI_ERR_STRIDED_LAST_DIM, "run: %s has stride(-1)=%lld, expected 1", name,
+                (long long)t->stride[ndim - 1]);
+  return FI_OK;
+}
+
+fi_status check_dim(const char* tname, const char* field, int64_t planned, int64_t got) {
+  return fail(FI_ERR_PLAN_MISMATCH, "run: %s %s: planned %lld, got %lld", tname, field,
+              (long long)planned, (long long)got);
+}
+
+fi_status check_packed(const fi_tensor* t, const char* name) {
+  int64_t expect = 1;
+  for (int i = t->ndim - 1; i >= 0; --i) {
+    if (t->shape[i] > 1 && t->stride[i] != expect)
+      return fail(FI_ERR_NONCONTIGUOUS_OUTPUT, "run: %s is not packed (stride[%d]=%lld, "
+                  "expected %lld)", name, i, (long long)t->stride[i], (long long)expect);
+    expect *= t->shape[i];
+  }
+  return FI_OK;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
+
+fi_status run_common(fi_plan_t p, bool decode_api, const fi_tensor* q, const fi_tensor* k,
+                     const fi_tensor* v, const fi_tensor* kv_indices, float sm_scale,
+                     fi_tensor* out, fi_tensor* lse, void* stream) {
+  const char* api = decode_api ? "batch_decode_paged" : "batch_prefill_paged";
+  if (!p) return fail(FI_ERR_INVALID_ARG, "%s: plan is NULL", api);
+  // [P3 "Plan-vs-run shapes"]: a half-planned object refuses run()
+  if (!p->planned) return fail(FI_ERR_NOT_PLANNED, "%s: call fi_plan() first", api);
+  const PlanState& s = p->st;
+  if (decode_api && s.q_len_per_req < 1)
+    return fail(FI_ERR_PLAN_MISMATCH, "%s: q_len_per_req: planned %d (a prefill plan), "
+                "expected >= 1", api, s.q_len_per_req);
+  if (!decode_api && s.q_len_per_req != 0)
+    return fail(FI_ERR_PLAN_MISMATCH, "%s: q_len_per_req: planned %d (a decode plan), "
+                "expected 0", api, s.q_len_per_req);
+  fi_status st;
+  if ((st = check_tensor(q, "q", 3)) != FI_OK) return st;
+  if ((st = check_tensor(k, "k_cache", 4)) != FI_OK) return st;
+  if ((st = check_tensor(v, "v_cache", 4)) != FI_OK) return st;
+  if ((st = check_tensor(kv_indices, "kv_indices", 1)) != FI_OK) return st;
+  if ((st = check_tensor(out, "out", 3)) != FI_OK) return st;
+  if (lse && (st = check_tensor(lse, "lse", 2)) != FI_OK) return st;
+  // [P3 "Plan-vs-run shapes"]: heads, head dims, page size, token minimums
+  if (q->shape[0] < s.total_rows) return check_dim("q", "rows (minimum)", s.total_rows, q->shape[0]);
+  if (q->shape[1] != s.hq) return check_dim("q", "num_qo_heads", s.hq, q->shape[1]);
+  if (q->shape[2] != s.d) return check_dim("q", "head_dim", s.d, q->shape[2]);
+  for (const fi_tensor* c : {k, v}) {
+    const char* n = (c == k) ? "k_cache" : "v_cache";
+    if (c->shape[1] != s.page_size) return check_dim(n, "page_size", s.page_size, c->shape[1]);
+    if (c->shape[2] != s.hk) return check_dim(n, "num_kv_heads", s.hk, c->shape[2]);
+    if (c->shape[3] != s.d) return check_dim(n, "head_dim", s.d, c->shape[3]);
+    if (c->dtype != s.dtype)
+      return fail(FI_ERR_PLAN_MISMATCH, "run: %s dtype: planned %s, got %s", n,
+                  dtype_name(s.dtype), dtype_name(c->dtype));
+  }
+  if (k->shape[0] != v->shape[0])
+    return fail(FI_ERR_INVALID_ARG, "run: k_cache has %lld pages, v_cache %lld",
+                (long long)k->shape[0], (long long)v->shape[0]);
+  if (q->dtype != s.dtype)
+    return fail(FI_ERR_PLAN_MISMATCH, "run: q dtype: planned %s, got %s", dtype_name(s.dtype),
+                dtype_name(q->dtype));
+  if (out->dtype != s.dtype)
+    return fail(FI_ERR_PLAN_MISMATCH, "run: out dtype: planned %s, got %s",
+                dtype_name(s.dtype), dtype_name(out->dtype));
+  if (kv_indices->dtype != FI_I32)
+    return fail(FI_ERR_INVALID_ARG, "run: kv_indices must be int32");
+  if (kv_indices->shape[0] < s.kv_indices_len)
+    return check_dim("kv_indices", "length (minimum)", s.kv_indices_len, kv_indices->shape[0]);
+  if (out->shape[0] < s.total_rows)
+    return check_dim("out", "rows (minimum)", s.total_rows, out->shape[0]);
+  if (out->shape[1] != s.hq) return check_dim("out", "num_qo_heads", s.hq, out->shape[1]);
+  if (out->shape[2] != s.d) return check_dim("out", "head_dim", s.d, out->shape[2]);
+  // [P3 "Strided layouts"]: out and lse must be packed
+  if ((st = check_packed(out, "out")) != FI_OK) return st;
+  if (lse) {
+    if (lse->dtype != FI_F32) return fail(FI_ERR_INVALID_ARG, "run: lse must be fp32");
+    if (lse->shape[0] < s.total_rows)
+      return check_dim("lse", "rows (minimum)", s.total_rows, lse->shape[0]);
+    if (lse->shape[1] != s.hq) return check_dim("lse", "num_qo_heads", s.hq, lse->shape[1]);
+    if ((st = check_packed(lse, "lse")) != FI_OK) return st;
+  }
+  // 16-byte vector loads of every row
+  if (!aligned16(q->data) || !aligned16(k->data) || !aligned16(v->data) || !aligned16(out->data) ||
+      q->stride[0] % 8 || q->stride[1] % 8 || k->stride[0] % 8 || k->stride[1] % 8 ||
+      k->stride[2] % 8 || v->stride[0] % 8 || v->stride[1] % 8 || v->stride[2] % 8)
+    return fail(FI_ERR_UNSUPPORTED, "run: q/k/v/out rows must start on 16-byte boundaries "
+                "(strides multiples of 8 elements)");
+
+  // everything above is host-side validation; a host-only plan stops here
+  if (p->host_only) return fail(FI_ERR_INVALID_ARG, "%s: plan has no device workspace", api);
+
+  fi::AttnParams ap;
+  ap.q = q->data; ap.q_stride_tok = q->stride[0]; ap.q_stride_head = q->stride[1];
+  ap.k = k->data; ap.k_stride_page = k->stride[0]; ap.k_stride_tok = k->stride[1];
+  ap.k_stride_head = k->stride[2];
+  ap.v = v->data; ap.v_stride_page = v->stride[0]; ap.v_stride_tok = v->stride[1];
+  ap.v_stride_head = v->stride[2];
+  ap.kv_indices = static_cast<const int32_t*>(kv_indices->data);
+  ap.out = out->data;
+  ap.lse = lse ? static_cast<float*>(lse->data) : nullptr;
+  ap.ws = p->ws;
+  ap.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  ap.num_qo_heads = s.hq;
+  ap.num_kv_heads = s.hk;
+  ap.page_size = s.page_size;
+  ap.page_shift = -1;
+  for (int sh = 0; sh < 31; ++sh)
+    if ((1 << sh) == s.page_size) ap.page_shift = sh;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const bool bf16 = s.dtype == FI_BF16;
+  const bool any_work = p->graph || !s.items.empty();
+  if (any_work) {
+    cudaError_t e;
+    if (s.kernel == fi::kDecode) e = fi::launch_decode(ap, s.d, s.group, bf16, s.grid, cs);
+    else if (s.kernel == fi::kPrefillM128) e = fi::launch_prefill_tc(ap, s.d, bf16, s.grid, cs);
+    else e = fi::launch_prefill_mma(ap, s.d, s.kernel, bf16, s.grid, cs);
+    if (e != cudaSuccess)
+      return fail(FI_ERR_CUDA, "%s: attention launch failed: %s", api, cudaGetErrorString(e));
+  }
+  if (p->graph || !s.merge_rows.empty()) {
+    int merge_grid = p->graph ? p->num_sms * 4
+                              : int(std::min<int64_t>(p->num_sms * 4,
+                                                      (int64_t(s.merge_rows.size()) * s.hq + 7) / 8));
+    cudaError_t e = fi::launch_merge_workspace(p->ws, out->data, ap.lse, s.hq, s.d, bf16,
+                                               std::max(merge_grid, 1), cs);
+    if (e != cudaSuccess)
+      return fail(FI_ERR_CUDA, "%s: merge launch failed: %s", api, cudaGetErrorString(e));
+  }
+  return ok();
+}
+
+}  // namespace
+
+extern "C" fi_status fi_batch_prefill_paged(fi_plan_t p, const fi_tensor* q, const fi_tensor* k,
+                                            const fi_tensor* v, const fi_tensor* kv_indices,
+                                            float sm_scale, fi_tensor* out, fi_tensor* lse,
+                                            void* stream) {
+  return run_common(p, false, q, k, v, kv_indices, sm_scale, out, lse, stream);
+}
+
+extern "C" fi_status fi_batch_decode_paged(fi_plan_t p, const fi_tensor* q, const fi_tensor* k,
+                                           const fi_tensor* v, const fi_tensor* kv_indices,
+                                           float sm_scale, fi_tensor* out, fi_tensor* lse,
+                                           void* stream) {
+  return run_common(p, true, q, k, v, kv_indices, sm_scale, out, lse, stream);
+}
+
+// ------------------------------------------------------------------ merges
+extern "C" fi_status fi_merge_state(const fi_tensor* va, const fi_tensor* sa, const fi_tensor* vb,
+                                    const fi_tensor* sb, fi_tensor* vo, fi_tensor* so,
+                                    const int32_t* num_rows_dev, void* stream) {
+  fi_status st;
+  if ((st = check_tensor(va, "v_a", 3)) != FI_OK) return st;
+  if ((st = check_tensor(vb, "v_b", 3)) != FI_OK) return st;
+  if ((st = check_tensor(vo, "v_out", 3)) != FI_OK) return st;
+  if ((st = check_tensor(sa, "s_a", 2)) != FI_OK) return st;
+  if ((st = check_tensor(sb, "s_b", 2)) != FI_OK) return st;
+  if ((st = check_tensor(so, "s_out", 2)) != FI_OK) return st;
+  for (const fi_tensor* t : {vb, static_cast<const fi_tensor*>(vo)})
+    for (int i = 0; i < 3; ++i)
+      if (t->shape[i] != va->shape[i])
+        return fail(FI_ERR_INVALID_ARG, "merge_state: v shapes differ at dim %d (%lld vs %lld)", i,
+                    (long long)t->shape[i], (long long)va->shape[i]);
+  for (const fi_tensor* t : {sa, sb, static_cast<const fi_tensor*>(so)})
+    if (t->shape[0] != va->shape[0] || t->shape[1] != va->shape[1])
+      return fail(FI_ERR_INVALID_ARG, "merge_state: s must be [rows, heads] of v");
+  if (va->dtype != vb->dtype || va->dtype != vo->dtype || va->dtype == FI_I32)
+    return fail(FI_ERR_INVALID_ARG, "merge_state: v_a, v_b, v_out must share one float dtype");
+  if (sa->dtype != FI_F32 || sb->dtype != FI_F32 || so->dtype != FI_F32)
+    return fail(FI_ERR_INVALID_ARG, "merge_state: s must be fp32");
+  if ((st = check_packed(vo, "v_out")) != FI_OK) return st;
+  if ((st = check_packed(so, "s_out")) != FI_OK) return st;
+  if (sa->shape[1] > 1 && (sa->stride[1] != 1 || sb->stride[1] != 1))
+    return fail(FI_ERR_STRIDED_LAST_DIM, "merge_state: s head stride must be 1");
+  if (va->shape[0] > INT32_MAX || va->shape[1] > 65535 || va->shape[2] > 1024)
+    return fail(FI_ERR_UNSUPPORTED, "merge_state: shape too large");
+  fi::MergeTwoParams mp;
+  mp.va = va->data; mp.vb = vb->data; mp.vo = vo->data;
+  mp.sa = static_cast<const float*>(sa->data);
+  mp.sb = static_cast<const float*>(sb->data);
+  mp.so = static_cast<float*>(so->data);
+  mp.va_sr = va->stride[0]; mp.va_sh = va->stride[1];
+  mp.vb_sr = vb->stride[0]; mp.vb_sh = vb->stride[1];
+  mp.sa_sr = sa->stride[0]; mp.sb_sr = sb->stride[0];
+  mp.rows = int32_t(va->shape[0]); mp.heads = int32_t(va->shape[1]);
+  mp.head_dim = int32_t(va->shape[2]); mp.dtype = va->dtype;
+  mp.num_rows_dev = num_rows_dev;
+  if (mp.rows == 0 && !num_rows_dev) return ok();
+  cudaError_t e = fi::launch_merge_two(mp, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FI_ERR_CUDA, "merge_state: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+extern "C" fi_status fi_merge_states(const fi_tensor* v, const fi_tensor* s,
+                                     const int32_t* merge_indptr_dev, int32_t rows,
+                                     fi_tensor* v_out, fi_tensor* s_out,
+                                     const int32_t* num_rows_dev, void* stream) {
+  fi_status st;
+  if ((st = check_tensor(v, "v", 3)) != FI_OK) return st;
+  if ((st = check_tensor(s, "s", 2)) != FI_OK) return st;
+  if ((st = check_tensor(v_out, "v_out", 3)) != FI_OK) return st;
+  if (s_out && (st = check_tensor(s_out, "s_out", 2)) != FI_OK) return st;
+  if (!merge_indptr_dev) return fail(FI_ERR_INVALID_ARG, "merge_states: merge_indptr is NULL");
+  if (rows < 0) return fail(FI_ERR_INVALID_ARG, "merge_states: rows=%d < 0", rows);
+  if (v->dtype != FI_F32 || s->dtype != FI_F32)
+    return fail(FI_ERR_INVALID_ARG, "merge_states: partial v and s must be fp32");
+  if ((st = check_packed(v, "v")) != FI_OK) return st;
+  if ((st = check_packed(s, "s")) != FI_OK) return st;
+  if ((st = check_packed(v_out, "v_out")) != FI_OK) return st;
+  if (v_out->shape[0] < rows || v_out->shape[1] != v->shape[1] || v_out->shape[2] != v->shape[2])
+    return fail(FI_ERR_INVALID_ARG, "merge_states: v_out must be [>= rows, H, d] of v");
+  if (s->shape[0] != v->shape[0] || s->shape[1] != v->shape[1])
+    return fail(FI_ERR_INVALID_ARG, "merge_states: s must be [n, H] of v");
+  if (s_out) {
+    if (s_out->dtype != FI_F32) return fail(FI_ERR_INVALID_ARG, "merge_states: s_out must be fp32");
+    if ((st = check_packed(s_out, "s_out")) != FI_OK) return st;
+    if (s_out->shape[0] < rows || s_out->shape[1] != v->shape[1])
+      return fail(FI_ERR_INVALID_ARG, "merge_states: s_out must be [>= rows, H]");
+  }
+  if (v_out->dtype == FI_I32) return fail(FI_ERR_INVALID_ARG, "merge_states: v_out dtype");
+  if (v->shape[2] % 4 != 0 || v->shape[2] > 1024)
+    return fail(FI_ERR_UNSUPPORTED, "merge_states: head_dim must be a multiple of 4, <= 1024");
+  if (rows == 0 && !num_rows_dev) return ok();
+  cudaError_t e = fi::launch_merge_states(
+      static_cast<const float*>(v->data), static_cast<const float*>(s->data), merge_indptr_dev,
+      rows, int(v->shape[1]), int(v->shape[2]), v_out->data, v_out->dtype,
+      s_out ? static_cast<float*>(s_out->data) : nullptr, num_rows_dev,
+      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FI_ERR_CUDA, "merge_states: %s", cudaGetErrorString(e));
+  return ok();
+}

@@ -1,0 +1,113 @@
+// Shared host/device definitions of libfi: the workspace layout written by
+// the planner and read by the kernels, and the kernel launch parameters.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace fi {
+
+// One unit of work: a tile of packed query rows (query row x head in the GQA
+// group) of one request and one kv head, against one chunk of its keys.
+struct alignas(32) WorkItem {
+  int32_t b;             // request
+  int32_t kv_head;
+  int32_t row0;          // first packed row (query row * group + head in group)
+  int32_t kv_begin;      // this chunk's key range [kv_begin, kv_end) before masking
+  int32_t kv_end;
+  int32_t chunk;         // -1: the tile has one chunk and writes out/lse directly
+  int32_t num_chunks;    // chunks of this tile
+  int32_t partial_base;  // partial slot of the tile's first token, chunk 0
+};
+static_assert(sizeof(WorkItem) == 32, "work item is eight int32");
+
+// Device workspace header (the first bytes of the caller's workspace). The
+// kernels read every offset from here, so a re-plan that moves arrays is seen
+// by a captured graph on its next replay.
+struct alignas(128) WsHeader {
+  int32_t n_items;
+  int32_t n_merge_rows;  // tokens whose partial states get merged
+  int32_t total_rows;    // T
+  int32_t batch;
+  int32_t group;         // Hq / Hk
+  int32_t causal;
+  int32_t window_left;
+  int32_t tile_rows;     // packed rows per tile
+  int32_t num_qo_heads;
+  int32_t head_dim;
+  int32_t pad0, pad1;
+  int64_t off_qo_indptr;     // int32 [batch+1]
+  int64_t off_kv_indptr;     // int32 [batch+1]
+  int64_t off_kv_len;        // int32 [batch]
+  int64_t off_merge_indptr;  // int32 [T+1]
+  int64_t off_merge_rows;    // int32 [n_merge_rows]
+  int64_t off_items;         // WorkItem [n_items]
+  int64_t off_tmp_lse;       // float [partials, Hq]
+  int64_t off_tmp_o;         // float [partials, Hq, d]
+};
+static_assert(sizeof(WsHeader) == 128, "header is 128 bytes");
+
+template <typename T>
+__host__ __device__ inline T* ws_ptr(const void* ws, int64_t off) {
+  return reinterpret_cast<T*>(reinterpret_cast<uintptr_t>(ws) + static_cast<uintptr_t>(off));
+}
+
+// Everything a run() kernel needs besides the workspace.
+struct AttnParams {
+  const void* q;
+  int64_t q_stride_tok, q_stride_head;
+  const void* k;
+  int64_t k_stride_page, k_stride_tok, k_stride_head;
+  const void* v;
+  int64_t v_stride_page, v_stride_tok, v_stride_head;
+  const int32_t* kv_indices;
+  void* out;        // packed [T, Hq, d]
+  float* lse;       // packed [T, Hq] or null
+  const void* ws;   // workspace base (WsHeader first)
+  float sm_scale_log2;  // sm_scale * log2(e)
+  int32_t num_qo_heads;
+  int32_t num_kv_heads;
+  int32_t page_size;
+  int32_t page_shift;   // log2(page_size) when it is a power of two, else -1
+};
+
+enum KernelId : int32_t {
+  kDecode = 0,
+  kPrefillM16 = 1,
+  kPrefillM64 = 2,
+  kPrefillM128 = 3,
+};
+
+// Launchers (defined in the .cu files). Each returns cudaGetLastError().
+cudaError_t launch_decode(const AttnParams& p, int head_dim, int group, bool bf16, int grid,
+                          cudaStream_t stream);
+cudaError_t launch_prefill_mma(const AttnParams& p, int head_dim, int kernel, bool bf16,
+                               int grid, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const AttnParams& p, int head_dim, bool bf16, int grid,
+                              cudaStream_t stream);
+// Merge the workspace partials of a plan into out / lse.
+cudaError_t launch_merge_workspace(const void* ws, void* out, float* lse, int num_heads,
+                                   int head_dim, bool bf16, int grid, cudaStream_t stream);
+// Variable-length merge over caller tensors.
+cudaError_t launch_merge_states(const float* v, const float* s, const int32_t* merge_indptr,
+                                int32_t rows, int num_heads, int head_dim, void* v_out,
+                                int out_dtype, float* s_out, const int32_t* num_rows_dev,
+                                cudaStream_t stream);
+// Two-state merge over caller tensors (all packed except the inputs' strides
+// which are [rows, H, d] / [rows, H] element strides).
+struct MergeTwoParams {
+  const void* va; const void* vb; void* vo;
+  const float* sa; const float* sb; float* so;
+  int64_t va_sr, va_sh, vb_sr, vb_sh;  // row / head strides of v_a, v_b
+  int64_t sa_sr, sb_sr;                // row strides of s_a, s_b (head stride 1)
+  int32_t rows, heads, head_dim, dtype;
+  const int32_t* num_rows_dev;
+};
+cudaError_t launch_merge_two(const MergeTwoParams& p, cudaStream_t stream);
+
+// Occupancy of each run kernel (CTAs per SM), for persistent grid sizing.
+int kernel_ctas_per_sm(int kernel, int head_dim, int group, bool bf16);
+
+}  // namespace fi

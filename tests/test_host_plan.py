@@ -1,0 +1,247 @@
+"""Host-side logic of libfi, on the CPU through the C ABI with host-only plans:
+refusals, plan transactionality, graph-mode capacity and frozen shapes, and
+exact-cover properties of the work list. No GPU is touched."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_attention_13_gb300 as fi
+import workloads
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_attention_13_gb300 import build
+    build.build()
+
+
+def _plan(**kw):
+    return fi.Plan(None, **kw)
+
+
+def _status(exc):
+    return exc.value.status_name
+
+
+# --------------------------------------------------------------- refusals
+def test_gqa_indivisible_and_zero_kv_heads_refused():
+    p = _plan()
+    for hq, hk in [(12, 8), (4, 8), (8, 0)]:
+        with pytest.raises(fi.FiError) as e:
+            p.plan([0, 4], [0, 1], [4], 16, hq, hk, 128)
+        assert _status(e) == "FI_ERR_GQA_INDIVISIBLE"
+
+
+def test_unsupported_head_dim_and_dtype():
+    p = _plan()
+    with pytest.raises(fi.FiError) as e:
+        p.plan([0, 4], [0, 1], [4], 16, 8, 2, 96)
+    assert _status(e) == "FI_ERR_UNSUPPORTED"
+    with pytest.raises(fi.FiError) as e:
+        p.plan([0, 4], [0, 1], [4], 16, 8, 2, 128, dtype=torch.float32)
+    assert _status(e) == "FI_ERR_UNSUPPORTED"
+
+
+def test_kv_shorter_than_q_under_causal_refused_from_metadata():
+    p = _plan()
+    with pytest.raises(fi.FiError) as e:  # Lk = 3 < Lq = 5
+        p.plan([0, 5], [0, 1], [3], 16, 8, 2, 128, causal=True)
+    assert _status(e) == "FI_ERR_KV_SHORTER_THAN_Q"
+    assert "kv_len=3" in str(e.value) and "qo_len=5" in str(e.value)
+    # non-causal accepts it
+    p.plan([0, 5], [0, 1], [3], 16, 8, 2, 128, causal=False)
+    # verify: the page metadata says 16 tokens, the draft is 32 rows
+    with pytest.raises(fi.FiError) as e:
+        p.plan(None, [0, 1], [16], 16, 8, 2, 128, q_len_per_req=32)
+    assert _status(e) == "FI_ERR_KV_SHORTER_THAN_Q"
+
+
+def test_bad_metadata_refused():
+    p = _plan()
+    cases = [
+        dict(qo=[0, 4], kv=[0, 1], last=[17]),   # last_page_len > page_size
+        dict(qo=[0, 4], kv=[0, 1], last=[0]),    # last_page_len 0 with a page
+        dict(qo=[1, 4], kv=[0, 1], last=[4]),    # qo_indptr[0] != 0
+        dict(qo=[0, 4, 3], kv=[0, 1, 2], last=[4, 4]),  # qo_indptr decreasing
+        dict(qo=[0, 4, 5], kv=[0, 2, 1], last=[4, 4]),  # kv_indptr decreasing
+    ]
+    for c in cases:
+        with pytest.raises(fi.FiError) as e:
+            p.plan(c["qo"], c["kv"], c["last"], 16, 8, 2, 128)
+        assert _status(e) == "FI_ERR_INVALID_ARG", c
+    with pytest.raises(fi.FiError) as e:
+        p.plan([0, 4], [0, 1], [4], 16, 8, 2, 128, window_left=-2)
+    assert _status(e) == "FI_ERR_INVALID_ARG"
+    with pytest.raises(fi.FiError) as e:  # decode plans derive qo_indptr themselves
+        p.plan([0, 1], [0, 1], [4], 16, 8, 2, 128, q_len_per_req=1)
+    assert _status(e) == "FI_ERR_INVALID_ARG"
+
+
+def test_rejected_plan_leaves_previous_plan_usable():
+    p = _plan()
+    p.plan([0, 3, 10], [0, 2, 5], [7, 16], 16, 8, 2, 128, causal=True)
+    before = p.info(with_arrays=True)
+    # a *different* page table that is refused: nothing may change
+    with pytest.raises(fi.FiError):
+        p.plan([0, 30, 40], [0, 1, 2], [16, 16], 16, 8, 2, 128, causal=True)
+    after = p.info(with_arrays=True)
+    for k in ("batch", "total_rows", "num_items"):
+        assert before[k] == after[k]
+    assert np.array_equal(before["items"], after["items"])
+
+
+def test_run_before_plan_and_run_refusals():
+    lib = fi.load()
+    p = _plan()
+    T, Hq, Hk, d, P = 9, 8, 2, 128, 16
+    q = torch.zeros((T, Hq, d), dtype=torch.bfloat16)
+    k = torch.zeros((4, P, Hk, d), dtype=torch.bfloat16)
+    v = torch.zeros_like(k)
+    idx = torch.zeros(4, dtype=torch.int32)
+    out = torch.zeros_like(q)
+    lse = torch.zeros((T, Hq), dtype=torch.float32)
+
+    def run(qq=q, kk=k, vv=v, ii=idx, oo=out, ll=lse, decode=False):
+        f = fi.fi_batch_decode_paged if decode else fi.fi_batch_prefill_paged
+        with pytest.raises(fi.FiError) as e:
+            f(p, qq, kk, vv, ii, 0.1, out=oo, lse=ll)
+        return _status(e), str(e.value)
+
+    assert run()[0] == "FI_ERR_NOT_PLANNED"
+    p.plan([0, 4, 9], [0, 2, 4], [5, 16], P, Hq, Hk, d, causal=True)
+    # strided last dim refused, never copied
+    wide = torch.zeros((T, Hq, 2 * d), dtype=torch.bfloat16)
+    assert run(qq=wide[..., ::2])[0] == "FI_ERR_STRIDED_LAST_DIM"
+    kw = torch.zeros((4, P, Hk, 2 * d), dtype=torch.bfloat16)
+    assert run(kk=kw[..., ::2])[0] == "FI_ERR_STRIDED_LAST_DIM"
+    # plan-vs-run mismatches name the field, the planned and the given value
+    st, msg = run(qq=torch.zeros((T, 4, d), dtype=torch.bfloat16))
+    assert st == "FI_ERR_PLAN_MISMATCH" and "num_qo_heads" in msg and "8" in msg and "4" in msg
+    st, msg = run(kk=torch.zeros((4, 8, Hk, d), dtype=torch.bfloat16))
+    assert st == "FI_ERR_PLAN_MISMATCH" and "page_size" in msg
+    st, msg = run(qq=torch.zeros((T - 1, Hq, d), dtype=torch.bfloat16))
+    assert st == "FI_ERR_PLAN_MISMATCH" and "rows" in msg
+    st, msg = run(qq=torch.zeros((1, T, Hq, d), dtype=torch.bfloat16))
+    assert st == "FI_ERR_PLAN_MISMATCH" and "rank" in msg
+    st, _ = run(qq=q.half())
+    assert st == "FI_ERR_PLAN_MISMATCH"
+    st, _ = run(decode=True)  # a prefill plan run through the decode entry point
+    assert st == "FI_ERR_PLAN_MISMATCH"
+    # outputs must be packed
+    obig = torch.zeros((T, Hq + 1, d), dtype=torch.bfloat16)
+    assert run(oo=obig[:, :Hq])[0] == "FI_ERR_NONCONTIGUOUS_OUTPUT"
+    lbig = torch.zeros((T, 2 * Hq), dtype=torch.float32)
+    assert run(ll=lbig[:, ::2])[0] == "FI_ERR_STRIDED_LAST_DIM"
+    # kv_indices shorter than the plan's page count
+    assert run(ii=idx[:3])[0] == "FI_ERR_PLAN_MISMATCH"
+    # a valid run on a host-only plan stops before any launch
+    st, msg = run()
+    assert st == "FI_ERR_INVALID_ARG" and "workspace" in msg
+    # q padded with extra rows is accepted up to the launch
+    st, msg = run(qq=torch.zeros((T + 5, Hq, d), dtype=torch.bfloat16),
+                  oo=torch.zeros((T + 5, Hq, d), dtype=torch.bfloat16),
+                  ll=torch.zeros((T + 5, Hq), dtype=torch.float32))
+    assert st == "FI_ERR_INVALID_ARG" and "workspace" in msg
+
+
+def test_graph_mode_capacity_and_frozen_shape():
+    p = _plan(enable_graph_capture=True, max_batch=4, max_total_rows=16)
+    p.plan(None, [0, 1, 2], [8, 9], 16, 32, 8, 128, q_len_per_req=4)
+    assert p.info()["graph_mode"] == 1
+    with pytest.raises(fi.FiError) as e:  # batch beyond capacity
+        p.plan(None, [0, 1, 2, 3, 4, 5], [8, 9, 10, 11, 12], 16, 32, 8, 128, q_len_per_req=4)
+    assert _status(e) == "FI_ERR_CAPACITY"
+    with pytest.raises(fi.FiError) as e:  # draft length frozen, both directions
+        p.plan(None, [0, 1, 2], [8, 9], 16, 32, 8, 128, q_len_per_req=1)
+    assert _status(e) == "FI_ERR_CAPACITY" and "q_len_per_req" in str(e.value)
+    with pytest.raises(fi.FiError) as e:
+        p.plan(None, [0, 1, 2], [8, 9], 16, 64, 8, 128, q_len_per_req=4)
+    assert _status(e) == "FI_ERR_CAPACITY"
+    p.plan(None, [0, 3, 4], [8, 9], 16, 32, 8, 128, q_len_per_req=4)  # same shape: fine
+
+
+def _check_cover(p, pb, causal, wl, forced):
+    info = p.info(with_arrays=True)
+    items = info["items"]
+    g = pb.num_qo_heads // pb.num_kv_heads
+    tile = info["tile_rows"]
+    assert tile % g == 0 and tile >= g
+    qo = pb.qo_indptr.numpy()
+    # every (request, packed row, kv head) is covered by exactly one tile
+    seen = {}
+    for it in items:
+        b, hk, row0, kb, ke, chunk, nch, base = (int(x) for x in it)
+        seen.setdefault((b, hk, row0), set()).add((chunk, kb, ke, nch, base))
+    for b in range(len(qo) - 1):
+        lq = qo[b + 1] - qo[b]
+        lk = pb.kv_lens[b]
+        rows = list(range(0, lq * g, tile))
+        for hk in range(pb.num_kv_heads):
+            for row0 in rows:
+                chunks = sorted(seen.pop((b, hk, row0)))
+                nch = chunks[0][2 + 1]
+                assert all(c[3] == nch for c in chunks) and len(chunks) == nch
+                if nch == 1:
+                    assert chunks[0][0] == -1
+                else:
+                    assert [c[0] for c in chunks] == list(range(nch))
+                # chunks partition one contiguous key range
+                spans = [(c[1], c[2]) for c in chunks]
+                for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+                    assert a1 == b0
+                if forced:
+                    assert spans[0][0] == 0 and spans[-1][1] == lk
+                else:
+                    n_rows = min(tile, lq * g - row0)
+                    i0, i1 = row0 // g, (row0 + n_rows) // g - 1
+                    hi = min(lk, i1 + lk - lq + 1) if causal else lk
+                    lo = max(0, lk - lq + i0 - wl) if wl >= 0 else 0
+                    lo = min(lo, hi)
+                    assert spans[0][0] == lo and spans[-1][1] == hi
+    assert not seen, "items for rows that do not exist: %s" % list(seen)[:3]
+    # merge index: tokens of split tiles own num_chunks partial slots
+    merge = info["merge_indptr"]
+    assert merge[0] == 0 and np.all(np.diff(merge) >= 0)
+    assert merge[-1] == info["num_partials"]
+    assert info["num_merge_rows"] == int(np.sum(np.diff(merge) > 1))
+    for it in items:
+        if it[5] >= 0:
+            b, row0, nch, base = int(it[0]), int(it[2]), int(it[6]), int(it[7])
+            t = qo[b] + row0 // g
+            assert merge[t] == base and merge[t + 1] - merge[t] == nch
+
+
+@pytest.mark.parametrize("forced", [0, 5])
+@pytest.mark.parametrize("causal,wl", [(True, -1), (True, 100), (False, 33), (False, -1)])
+def test_work_list_is_an_exact_cover(forced, causal, wl):
+    pb = workloads.batch_prefill(batch=6, q_lo=1, q_hi=300, prefix_lo=0, prefix_hi=900,
+                                 num_qo_heads=12, num_kv_heads=4, head_dim=64)
+    p = _plan()
+    p.plan(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, 16, 12, 4, 64, causal=causal,
+           window_left=wl, force_kv_chunks=forced)
+    _check_cover(p, pb, causal, wl, forced)
+
+
+def test_decode_split_cover_and_long_context_split():
+    pb = workloads.batch_decode(batch=64)
+    p = _plan()
+    p.plan(None, pb.kv_indptr, pb.last_page_len, 16, 32, 8, 128, q_len_per_req=1)
+    info = p.info()
+    assert info["kernel_name"] == "decode"
+    _check_cover(p, pb, True, -1, 0)
+    pb = workloads.long_context()
+    for forced in (0, 8, 32):
+        p.plan(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, 16, 64, 8, 128, causal=True,
+               force_kv_chunks=forced)
+        _check_cover(p, pb, True, -1, forced)
+        if forced:
+            assert p.info()["max_chunks"] == forced
+
+
+def test_workspace_bytes_grows_with_chunks():
+    a = fi.workspace_bytes(64, 64, 32, 128, 1)
+    b = fi.workspace_bytes(64, 64, 32, 128, 32)
+    assert 0 < a < b
+    assert b >= 64 * 32 * 32 * 129 * 4
