@@ -1,0 +1,491 @@
+"""Benchmark of the paged-KV attention path on one GB300 (or N replicas).
+
+Headline workload: batch decode, batch 64, one query row per request, kv_len
+uniform in [512, 8192], 32 q / 8 kv heads, head_dim 128, bf16, page 16 (pages
+scattered by a seeded permutation), window -1, with LSE. A step is one
+run() of the planned batch (the decode kernel and the split-KV merge); the
+plan is made once, as a graph-replayed serving step would. ``value`` is KV
+GB/s (algorithmic bytes: each live K/V row once, plus q, o, lse and the page
+indices) with every input resident in HBM; ``e2e`` repeats the step through
+the public API with host buffers: plan + host-to-device copy of q and the
+page table + run + device-to-host copy of o and lse, every step.
+
+The other workloads (prefill, verify, long-context split-KV, the 64x256
+paged prefill) are timed the same way and reported under ``workloads``.
+
+``--impl reference`` times the CPU oracle (the plain fp64 definition) on the
+host cores on a bounded sample of the same workload and prints the same line
+with ``"impl": "reference"``.
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "prefill/verify TFLOPS and decode KV GB/s on 1 GB300, % of tensor/HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+
+
+# ------------------------------------------------------------------ accounting
+def valid_counts(lq, lk, causal, wl):
+    """Valid keys per query row under the bottom-right causal mask and the
+    left-only window (closed form of the mask, for FLOP accounting)."""
+    i = np.arange(lq, dtype=np.int64)
+    hi = np.minimum(lk - 1, i + lk - lq) if causal else np.full(lq, lk - 1)
+    lo = np.maximum(0, lk - lq + i - wl) if wl >= 0 else np.zeros(lq, np.int64)
+    return np.maximum(0, hi - lo + 1)
+
+
+def accounting(pb, causal, wl):
+    """(masked FLOPs, algorithmic bytes) of one run over the batch."""
+    d, Hq, Hk = pb.head_dim, pb.num_qo_heads, pb.num_kv_heads
+    es = 2
+    flops = 0
+    kv_rows = 0
+    pages = 0
+    for lq, lk in zip(pb.q_lens, pb.kv_lens):
+        if lq == 0 or lk == 0:
+            continue
+        cnt = valid_counts(lq, lk, causal, wl)
+        flops += 4 * d * Hq * int(cnt.sum())
+        # distinct live keys: union of the rows' ranges [lo_i, hi_i]
+        i = np.arange(lq)
+        hi = np.minimum(lk - 1, i + lk - lq) if causal else np.full(lq, lk - 1)
+        lo = np.maximum(0, lk - lq + i - wl) if wl >= 0 else np.zeros(lq, np.int64)
+        live = np.zeros(lk, bool)
+        for a, b in zip(lo, hi):
+            if b >= a:
+                live[a:b + 1] = True
+        n_live = int(live.sum())
+        kv_rows += n_live
+        pages += len({j // pb.page_size for j in np.nonzero(live)[0]}) if n_live < lk else \
+            (lk + pb.page_size - 1) // pb.page_size
+    T = sum(pb.q_lens)
+    byts = kv_rows * Hk * d * 2 * es + T * Hq * d * es * 2 + T * Hq * 4 + 4 * pages
+    return flops, byts
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            pk = json.load(open(path))
+            hbm = pk.get("hbm_gbs") or pk.get("hbm_GBs") or pk.get("hbm")
+            bf = pk.get("bf16_tflops")
+            bfs = pk.get("bf16_tflops_sustained") or bf
+            if hbm and bf:
+                return float(hbm), float(bf), float(bfs), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", "fi_clocks_%d_%d.csv" % (os.getpid(), index))
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+class Runner:
+    """One planned workload resident on the device."""
+
+    def __init__(self, pb, causal, wl, mode, dev, force_kv_chunks=0, ws=None):
+        import paged_kv_attention_13_gb300 as fi
+        self.fi = fi
+        self.pb, self.causal, self.wl, self.mode = pb, causal, wl, mode
+        self.dev = dev
+        self.q = pb.q.to(dev)
+        self.k = pb.k_cache.to(dev)
+        self.v = pb.v_cache.to(dev)
+        self.idx = pb.kv_indices.to(dev)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=dev)
+        self.ws = ws if ws is not None else torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.plan = fi.Plan(self.ws)
+        self.force = force_kv_chunks
+        self.do_plan()
+        self.flops, self.bytes = accounting(pb, causal or mode == "verify", wl)
+
+    def do_plan(self):
+        pb = self.pb
+        dt = workloads.TORCH_DTYPE[pb.dtype]
+        if self.mode == "prefill":
+            self.plan.plan(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, pb.page_size,
+                           pb.num_qo_heads, pb.num_kv_heads, pb.head_dim, causal=self.causal,
+                           window_left=self.wl, dtype=dt, force_kv_chunks=self.force)
+        else:
+            qlpr = 1 if self.mode == "decode" else pb.extra["q_len_per_req"]
+            self.plan.plan(None, pb.kv_indptr, pb.last_page_len, pb.page_size, pb.num_qo_heads,
+                           pb.num_kv_heads, pb.head_dim, causal=self.causal, window_left=self.wl,
+                           dtype=dt, q_len_per_req=qlpr, force_kv_chunks=self.force)
+        self.info = self.plan.info()
+
+    def run(self):
+        f = self.fi.fi_batch_prefill_paged if self.mode == "prefill" else self.fi.fi_batch_decode_paged
+        f(self.plan, self.q, self.k, self.v, self.idx, self.pb.sm_scale, out=self.out, lse=self.lse)
+
+    def launches_per_step(self):
+        return 1 + (1 if self.info["num_merge_rows"] > 0 else 0)
+
+    def time(self, steps, warmup, flush=False):
+        """Mean and median device time of one run (CUDA events on the
+        launching stream); with ``flush`` a 256 MB buffer is rewritten before
+        every run so the inputs start out of L2."""
+        buf = torch.empty(256 << 20, dtype=torch.uint8, device=self.dev) if flush else None
+        for _ in range(warmup):
+            self.run()
+        torch.cuda.synchronize()
+        s = torch.cuda.current_stream()
+        st = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        en = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            if buf is not None:
+                buf.fill_(i & 0xFF)
+            st[i].record(s)
+            self.run()
+            en[i].record(s)
+        torch.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in zip(st, en)]
+        return float(np.mean(ms)), float(np.median(ms))
+
+    def time_e2e(self, steps, warmup):
+        """plan + H2D(q, page table) + run + D2H(o, lse), host buffers pinned."""
+        pb = self.pb
+        q_h = pb.q.pin_memory()
+        idx_h = pb.kv_indices.pin_memory()
+        out_h = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        lse_h = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+        meta = 4 * (len(pb.kv_indptr) + len(pb.last_page_len) + len(pb.qo_indptr))
+
+        def step():
+            self.do_plan()
+            self.q.copy_(q_h, non_blocking=True)
+            self.idx.copy_(idx_h, non_blocking=True)
+            self.run()
+            out_h.copy_(self.out, non_blocking=True)
+            lse_h.copy_(self.lse, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(warmup):
+            step()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            step()
+        dt = (time.perf_counter() - t0) / steps
+        h2d = q_h.numel() * q_h.element_size() + idx_h.numel() * 4 + meta
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+        return dt * 1e3, h2d, d2h
+
+
+def traffic_from_profile(kernel_file, name):
+    """Per-launch DRAM bytes from the committed ncu summary, if the kernel
+    source is unchanged since it was taken (else None)."""
+    path = os.path.join(ROOT, "profiles", name)
+    src = os.path.join(ROOT, "paged_kv_attention_13_gb300", "csrc", kernel_file)
+    if not os.path.exists(path) or not os.path.exists(src):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_sha256_16") != digest:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def cpu_oracle_sample(pb, causal, wl, budget_s=12.0, seed=1):
+    """Time the oracle on a bounded row sample; scale to a full-batch time."""
+    from oracle.reference import attention_rows
+    T = int(pb.qo_indptr[-1])
+    H = pb.num_qo_heads
+    rng = np.random.default_rng(seed)
+    args = pb.oracle_args()
+    done_rows, t_used = 0, 0.0
+    n = 8
+    while t_used < budget_s and done_rows < T * H:
+        toks = rng.integers(0, T, size=n)
+        heads = rng.integers(0, H, size=n)
+        t0 = time.perf_counter()
+        attention_rows(*args, causal, wl, pb.sm_scale, toks, heads, dtype=pb.dtype)
+        t_used += time.perf_counter() - t0
+        done_rows += n
+        n = min(n * 2, 512)
+    full_s = t_used / done_rows * (T * H)
+    return full_s, done_rows, t_used
+
+
+def run_ours(args):
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    hbm_peak, bf16_peak, bf16_sus, peak_kind = peaks()
+
+    # ---- headline: batch decode
+    pb = workloads.batch_decode()
+    ws = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    r = Runner(pb, False, -1, "decode", dev, ws=ws)
+    for _ in range(args.warmup):
+        r.run()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms_mean, ms_med = r.time(args.steps, args.warmup)
+    if world > 1:
+        dist.barrier()
+    t = torch.tensor([ms_mean], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_step = float(t.item())
+    value = world * r.bytes / (ms_step * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = r.time_e2e(max(3, args.steps // 2), 2)
+    e2e_value = world * r.bytes / (e2e_ms * 1e-3) / 1e9
+    achieved = r.bytes / (ms_step * 1e-3) / 1e9
+    traffic = traffic_from_profile("decode.cu", "decode_kernel_batch64.txt")
+    roof = {"bound": "hbm", "kernel": "decode_kernel (+ split-KV merge, timed together)",
+            "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
+            "frac_of_nominal_8000": round(achieved / 8000.0, 4),
+            "algorithmic_bytes_per_launch": r.bytes,
+            "traffic": traffic}
+    launches = r.launches_per_step() * args.steps
+    clocks = clk.summary()
+
+    extra = {}
+    if rank == 0 and not args.headline_only:
+        extra = other_workloads(args, dev, ws, hbm_peak, bf16_peak)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        full_s, rows, used = cpu_oracle_sample(pb, False, -1, budget_s=args.cpu_budget)
+        cpu = {"value": round(r.bytes / full_s / 1e9, 6), "unit": "GB/s", "cores": 1,
+               "kind": "oracle",
+               "sample": "%d random (token, head) rows of the decode batch (%.1f s of fp64 CPU "
+                         "work), scaled to the full batch's %d rows" % (rows, used, 64 * 32)}
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic (seeded N(0,1) q/k/v, seeded page permutation)",
+                "config": {"workload": "batch decode: batch 64, q_len 1, kv_len U[512,8192], "
+                                       "32 q / 8 kv heads, head_dim 128, bf16, page 16, "
+                                       "window -1, lse",
+                           "total_kv_tokens": int(sum(pb.kv_lens)),
+                           "l2": "inputs larger than L2 (KV cache %.2f GB > 129 MB)" % (
+                               2 * sum(pb.kv_lens) * 8 * 128 * 2 / 1e9),
+                           "plan": {k: r.info[k] for k in ("kernel_name", "num_items", "grid",
+                                                            "max_chunks", "num_merge_rows")},
+                           "parallelism": "replicas" if world > 1 else "single GPU"},
+                "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
+                        "ms_per_step": round(e2e_ms, 4),
+                        "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                        "note": "plan + H2D(q, page table, indptrs) + run + D2H(o, lse); "
+                                "the KV cache stays resident"},
+                "gpu_launches": launches, "clocks": clocks, "roofline": roof,
+                "cpu_baseline": cpu, "workloads": extra}
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def other_workloads(args, dev, ws, hbm_peak, bf16_peak):
+    res = {}
+    steps = max(3, min(args.steps, 10))
+
+    def one(name, pb, causal, wl, mode, force=0, bound="hbm"):
+        r = Runner(pb, causal, wl, mode, dev, force_kv_chunks=force, ws=ws)
+        ms, med = r.time(steps, 3, flush=r.bytes < (512 << 20))
+        tf = r.flops / (ms * 1e-3) / 1e12
+        gbs = r.bytes / (ms * 1e-3) / 1e9
+        ent = {"ms": round(ms, 4), "TFLOPS": round(tf, 2), "GB/s": round(gbs, 1),
+               "kernel": r.info["kernel_name"], "items": r.info["num_items"],
+               "chunks": r.info["max_chunks"]}
+        if bound == "tensor":
+            ent["frac_of_bf16_peak"] = round(tf / bf16_peak, 4)
+        else:
+            ent["frac_of_hbm"] = round(gbs / hbm_peak, 4)
+        res[name] = ent
+        del r
+
+    pb = workloads.speculative_verify(batch=32)
+    one("verify_b32", pb, True, -1, "verify")
+    pb = workloads.speculative_verify(batch=4)
+    one("verify_b4", pb, True, -1, "verify")
+    for P in (16, 1024):
+        pb = workloads.batch_prefill(page_size=P)
+        one("prefill_p%d_causal" % P, pb, True, -1, "prefill", bound="tensor")
+        if P == 16:
+            one("prefill_p16_noncausal", pb, False, -1, "prefill", bound="tensor")
+            one("prefill_p16_causal_wl127", pb, True, 127, "prefill")
+    pb = workloads.long_context()
+    one("longctx_causal_split", pb, True, -1, "prefill")
+    one("longctx_causal_force32", pb, True, -1, "prefill", force=32)
+    one("longctx_causal_wl127", pb, True, 127, "prefill")
+    pb = workloads.pr1_reference()
+    one("pr1_64x256_causal", pb, True, -1, "prefill")
+    return res
+
+
+def run_reference(args):
+    """The CPU oracle as it stands, on the host cores, same metric and unit."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle.build import build_oracle
+    build_oracle()
+    pb = workloads.batch_decode()
+    _, byts = accounting(pb, False, -1)
+    per_step_budget = max(1.0, args.cpu_budget / max(1, args.steps + args.warmup))
+    times = []
+    for i in range(args.warmup + args.steps):
+        full_s, rows, used = cpu_oracle_sample(pb, False, -1, budget_s=per_step_budget, seed=i)
+        if i >= args.warmup:
+            times.append(full_s)
+    full_s = float(np.mean(times))
+    value = byts / full_s / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(full_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "batch decode: batch 64, q_len 1, kv_len U[512,8192], 32 q / "
+                                   "8 kv heads, head_dim 128, bf16, page 16, window -1, lse"},
+            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "each step: random (token, head) rows for ~%.1f s of fp64 "
+                                       "CPU work, scaled to the batch's 2048 rows" % per_step_budget},
+            "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line))
+
+
+PROFILE_CASES = {
+    # name: (batch factory, causal, window_left, mode)
+    "decode_b16": (lambda: workloads.batch_decode(batch=16), False, -1, "decode"),
+    "decode_b64": (lambda: workloads.batch_decode(), False, -1, "decode"),
+    "verify_b32": (lambda: workloads.speculative_verify(batch=32), True, -1, "verify"),
+    "prefill_p16_causal": (lambda: workloads.batch_prefill(page_size=16), True, -1, "prefill"),
+    "prefill_b4_causal": (lambda: workloads.batch_prefill(page_size=16, batch=4), True, -1, "prefill"),
+    "longctx_causal": (lambda: workloads.long_context(), True, -1, "prefill"),
+}
+
+
+def run_case(args):
+    """One workload alone (for profiler captures): warm-up, then timed runs."""
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    make, causal, wl, mode = PROFILE_CASES[args.case]
+    pb = make()
+    r = Runner(pb, causal, wl, mode, dev)
+    ms, med = r.time(args.steps, args.warmup)
+    print(json.dumps({"case": args.case, "ms_mean": round(ms, 4), "ms_median": round(med, 4),
+                      "GB/s": round(r.bytes / (ms * 1e-3) / 1e9, 1),
+                      "TFLOPS": round(r.flops / (ms * 1e-3) / 1e12, 2), "plan": r.info}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--case", default=None, choices=sorted(PROFILE_CASES))
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -184,10 +184,13 @@ namespace {
 
 bool group_has_decode_kernel(int g) { return g == 1 || g == 2 || g == 4; }
 
-int choose_kernel(int32_t q_len_per_req, int32_t g, int64_t max_rows_per_req) {
+int choose_kernel(int32_t q_len_per_req, int32_t g, int64_t max_rows_per_req, int32_t d,
+                  int32_t page_size) {
   if (q_len_per_req == 1 && group_has_decode_kernel(g)) return fi::kDecode;
   if (max_rows_per_req <= 16 && g <= 16) return fi::kPrefillM16;
+  if (max_rows_per_req > 64 && fi::prefill_tc_supports(d, page_size, g)) return fi::kPrefillM128;
   if (g <= 64) return fi::kPrefillM64;
+  if (fi::prefill_tc_supports(d, page_size, g)) return fi::kPrefillM128;
   return -1;
 }
 
@@ -305,7 +308,7 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
     max_rows_per_req = (q_len_per_req >= 1) ? int64_t(q_len_per_req) * g
                                              : int64_t(P.max_total_rows) * g;
   }
-  ns.kernel = choose_kernel(q_len_per_req, g, max_rows_per_req);
+  ns.kernel = choose_kernel(q_len_per_req, g, max_rows_per_req, d, page_size);
   if (ns.kernel < 0)
     return fail(FI_ERR_UNSUPPORTED, "plan: GQA group %d is larger than the widest tile", g);
   if (P.graph && P.frozen) {
@@ -744,7 +747,9 @@ fi_status run_common(fi_plan_t p, bool decode_api, const fi_tensor* q, const fi_
   if (any_work) {
     cudaError_t e;
     if (s.kernel == fi::kDecode) e = fi::launch_decode(ap, s.d, s.group, bf16, s.grid, cs);
-    else if (s.kernel == fi::kPrefillM128) e = fi::launch_prefill_tc(ap, s.d, bf16, s.grid, cs);
+    else if (s.kernel == fi::kPrefillM128)
+      e = fi::launch_prefill_tc(ap, s.d, s.group, s.tile_rows, q->shape[0], k->shape[0], bf16,
+                                s.grid, cs);
     else e = fi::launch_prefill_mma(ap, s.d, s.kernel, bf16, s.grid, cs);
     if (e != cudaSuccess)
       return fail(FI_ERR_CUDA, "%s: attention launch failed: %s", api, cudaGetErrorString(e));

@@ -1,12 +1,15 @@
 // Decode kernel: one query row per request against its paged KV, all G query
 // heads of one kv head together (GQA). Bandwidth-bound: every K/V byte is
-// read exactly once, with 16-byte coalesced loads straight into registers,
+// read exactly once, with 16-byte coalesced cp.async gathers,
 // scores reduced with warp shuffles, and an online softmax kept in fp32.
 //
-// Work item = (request, kv head, key chunk). A CTA of 4 warps walks the
-// chunk's live keys in blocks of U warp-steps; each warp-step covers
-// 32 / (D/8) keys, each key's D/8 lanes holding 8 head-dim elements. At the
-// end the four warps' (max, sum, o) states are merged in shared memory.
+// Work item = (request, kv head, key chunk). A CTA of 4 warps streams the
+// chunk's live keys through a 4-stage cp.async ring in shared memory (32 keys
+// of K and V per stage, gathered page by page, zero-filled past the end), so
+// three stages of loads stay in flight while one is consumed. Each warp takes
+// 8 keys of a stage; a warp step covers 32 / (D/8) keys, each key's D/8 lanes
+// holding 8 head-dim elements. At the end the four warps' (max, sum, o)
+// states are merged in shared memory.
 //
 // Mask for one query row (Lq = 1) [P1 "Why window_size_right stays -1"],
 // [P2 "Summary"]: causal keeps every key j <= Lk - 1; the window keeps
@@ -20,17 +23,29 @@ namespace fi {
 namespace {
 
 constexpr int kDecodeThreads = 128;
+constexpr int kDecodeStages = 4;   // cp.async ring depth
+constexpr int kDecodeKT = 32;      // keys per stage
+
+template <int D>
+constexpr int decode_smem_bytes() {
+  return kDecodeStages * kDecodeKT * D * 2 * 2;  // K and V rings, 16-bit elements
+}
 
 template <int D, int G, bool BF16>
-__global__ void __launch_bounds__(kDecodeThreads, (G >= 4) ? 3 : 4) decode_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kDecodeThreads, 3) decode_kernel(const AttnParams p) {
   using DT = Dt<BF16>;
   using T = typename DT::T;
-  constexpr int LPK = D / 8;          // lanes per key
-  constexpr int KPS = 32 / LPK;       // keys per warp step
-  constexpr int U = (G <= 2) ? 8 : 4;  // warp steps per block
-  constexpr int KPB = KPS * U;        // keys per warp block
+  constexpr int LPK = D / 8;                 // lanes per key
+  constexpr int KPS = 32 / LPK;              // keys per warp step
   constexpr int NWARP = kDecodeThreads / 32;
+  constexpr int KPW = kDecodeKT / NWARP;     // keys per warp per stage
+  constexpr int STEPS = KPW / KPS;           // warp steps per stage
+  constexpr int CH = D / 8;                  // 16-byte chunks per row
+  constexpr int STAGE = kDecodeKT * D;       // elements per stage
 
+  extern __shared__ __align__(128) uint8_t dsmem[];
+  T* sK = reinterpret_cast<T*>(dsmem);
+  T* sV = sK + kDecodeStages * STAGE;
   __shared__ float sm_m[NWARP][G];
   __shared__ float sm_l[NWARP][G];
   __shared__ __align__(16) float sm_o[NWARP][G][D];
@@ -46,8 +61,9 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 4) ? 3 : 4) decode_kerne
   const int window_left = hdr->window_left;
   const int Hq = p.num_qo_heads;
 
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
   const int kg = lane / LPK;   // key within the warp step
   const int dl = lane % LPK;   // 8-element slice of the head dim
 
@@ -56,9 +72,40 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 4) ? 3 : 4) decode_kerne
     const int b = it.b, hk = it.kv_head;
     const int lk = kv_len[b];
     const int token = qo_indptr[b];
-    int lo = it.kv_begin, hi = min(it.kv_end, lk);
+    int lo = it.kv_begin;
+    const int hi = min(it.kv_end, lk);
     if (window_left >= 0) lo = max(lo, lk - 1 - window_left);
     lo = max(lo, 0);
+    const int n_tiles = hi > lo ? (hi - lo + kDecodeKT - 1) / kDecodeKT : 0;
+
+    const int32_t* pages = p.kv_indices + kv_indptr[b];
+    const T* kbase = static_cast<const T*>(p.k) + int64_t(hk) * p.k_stride_head;
+    const T* vbase = static_cast<const T*>(p.v) + int64_t(hk) * p.v_stride_head;
+    // gather one stage of K and V rows (16-byte cp.async, zero-fill past hi)
+    auto issue = [&](int tile, int stage) {
+      const int kt = lo + tile * kDecodeKT;
+      for (int idx = tid; idx < kDecodeKT * CH; idx += kDecodeThreads) {
+        const int key = idx / CH, c = idx % CH;
+        const int j = kt + key;
+        const T* ks = static_cast<const T*>(p.k);
+        const T* vs = static_cast<const T*>(p.v);
+        int bytes = 0;
+        if (j < hi) {
+          ks = kbase + kv_row_offset(pages, j, p.page_size, p.page_shift, p.k_stride_page,
+                                     p.k_stride_tok) + c * 8;
+          vs = vbase + kv_row_offset(pages, j, p.page_size, p.page_shift, p.v_stride_page,
+                                     p.v_stride_tok) + c * 8;
+          bytes = 16;
+        }
+        cp_async16(smem_u32(sK + stage * STAGE + key * D + c * 8), ks, bytes);
+        cp_async16(smem_u32(sV + stage * STAGE + key * D + c * 8), vs, bytes);
+      }
+    };
+#pragma unroll
+    for (int s = 0; s < kDecodeStages - 1; ++s) {
+      if (s < n_tiles) issue(s, s);
+      cp_async_commit();
+    }
 
     // q slice of every head in the group, pre-scaled into the log2 domain
     float qf[G][8];
@@ -74,7 +121,6 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 4) ? 3 : 4) decode_kerne
         qf[h][2 * e + 1] = DT::hi(wv[e]) * p.sm_scale_log2;
       }
     }
-
     float m[G], l[G], o[G][8];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -84,32 +130,24 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 4) ? 3 : 4) decode_kerne
       for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
     }
 
-    const int32_t* pages = p.kv_indices + kv_indptr[b];
-    const T* kbase = static_cast<const T*>(p.k) + int64_t(hk) * p.k_stride_head + dl * 8;
-    const T* vbase = static_cast<const T*>(p.v) + int64_t(hk) * p.v_stride_head + dl * 8;
-
-    for (int base = lo + warp * KPB; base < hi; base += NWARP * KPB) {
-      uint4 kr[U], vr[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int j = base + u * KPS + kg;
-        if (j < hi) {
-          const int64_t ko = kv_row_offset(pages, j, p.page_size, p.page_shift, p.k_stride_page,
-                                           p.k_stride_tok);
-          const int64_t vo = kv_row_offset(pages, j, p.page_size, p.page_shift, p.v_stride_page,
-                                           p.v_stride_tok);
-          kr[u] = ld_stream16(kbase + ko);
-          vr[u] = ld_stream16(vbase + vo);
-        } else {
-          kr[u] = make_uint4(0, 0, 0, 0);
-          vr[u] = make_uint4(0, 0, 0, 0);
-        }
+    for (int tile = 0; tile < n_tiles; ++tile) {
+      cp_async_wait<kDecodeStages - 2>();
+      __syncthreads();
+      {
+        const int nt = tile + kDecodeStages - 1;
+        if (nt < n_tiles) issue(nt, nt % kDecodeStages);
+        cp_async_commit();
       }
-      // scores s[u][h] (log2 domain), identical on the LPK lanes of a key
-      float s[U][G];
+      const int st = tile % kDecodeStages;
+      const int kt = lo + tile * kDecodeKT;
+      const T* cK = sK + st * STAGE;
+      const T* cV = sV + st * STAGE;
+      float s[STEPS][G];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const uint32_t wv[4] = {kr[u].x, kr[u].y, kr[u].z, kr[u].w};
+      for (int u = 0; u < STEPS; ++u) {
+        const int key = warp * KPW + u * KPS + kg;
+        const uint4 kr = *reinterpret_cast<const uint4*>(cK + key * D + dl * 8);
+        const uint32_t wv[4] = {kr.x, kr.y, kr.z, kr.w};
         float kf[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -127,16 +165,15 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 4) ? 3 : 4) decode_kerne
 #pragma unroll
       for (int off = LPK / 2; off >= 1; off >>= 1)
 #pragma unroll
-        for (int u = 0; u < U; ++u)
+        for (int u = 0; u < STEPS; ++u)
 #pragma unroll
           for (int h = 0; h < G; ++h) s[u][h] += __shfl_xor_sync(0xffffffffu, s[u][h], off);
-      // block max per head over the warp's keys
       float mx[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) mx[h] = neg_inf();
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const bool in = (base + u * KPS + kg) < hi;
+      for (int u = 0; u < STEPS; ++u) {
+        const bool in = (kt + warp * KPW + u * KPS + kg) < hi;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           if (!in) s[u][h] = neg_inf();
@@ -160,8 +197,10 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 4) ? 3 : 4) decode_kerne
         for (int e = 0; e < 8; ++e) o[h][e] *= corr;
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const uint32_t wv[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
+      for (int u = 0; u < STEPS; ++u) {
+        const int key = warp * KPW + u * KPS + kg;
+        const uint4 vr = *reinterpret_cast<const uint4*>(cV + key * D + dl * 8);
+        const uint32_t wv[4] = {vr.x, vr.y, vr.z, vr.w};
         float vf[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -177,6 +216,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 4) ? 3 : 4) decode_kerne
         }
       }
     }
+    cp_async_wait<0>();
 
     // the warp's key groups share m; sum their l and o
 #pragma unroll
@@ -208,7 +248,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 4) ? 3 : 4) decode_kerne
     // merge the warps and write: direct to out/lse, or to a partial slot
     const bool direct = it.chunk < 0;
     const int slot = direct ? 0 : it.partial_base + it.chunk;
-    for (int idx = threadIdx.x; idx < G * (D / 4); idx += kDecodeThreads) {
+    for (int idx = tid; idx < G * (D / 4); idx += kDecodeThreads) {
       const int h = idx / (D / 4);
       const int c = (idx % (D / 4)) * 4;
       float M = neg_inf();
@@ -250,15 +290,25 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 4) ? 3 : 4) decode_kerne
   }
 }
 
+template <int D, int G, bool BF16>
+cudaError_t launch_dg(const AttnParams& p, int grid, cudaStream_t s) {
+  auto k = decode_kernel<D, G, BF16>;
+  // once per process, before any capture (no attribute call inside a captured run)
+  static cudaError_t attr =
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, decode_smem_bytes<D>());
+  if (attr != cudaSuccess) return attr;
+  k<<<grid, kDecodeThreads, decode_smem_bytes<D>(), s>>>(p);
+  return cudaGetLastError();
+}
+
 template <int D, bool BF16>
 cudaError_t launch_d(const AttnParams& p, int group, int grid, cudaStream_t s) {
   switch (group) {
-    case 1: decode_kernel<D, 1, BF16><<<grid, kDecodeThreads, 0, s>>>(p); break;
-    case 2: decode_kernel<D, 2, BF16><<<grid, kDecodeThreads, 0, s>>>(p); break;
-    case 4: decode_kernel<D, 4, BF16><<<grid, kDecodeThreads, 0, s>>>(p); break;
+    case 1: return launch_dg<D, 1, BF16>(p, grid, s);
+    case 2: return launch_dg<D, 2, BF16>(p, grid, s);
+    case 4: return launch_dg<D, 4, BF16>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace

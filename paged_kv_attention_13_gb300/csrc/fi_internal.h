@@ -37,7 +37,8 @@ struct alignas(128) WsHeader {
   int32_t tile_rows;     // packed rows per tile
   int32_t num_qo_heads;
   int32_t head_dim;
-  int32_t pad0, pad1;
+  int32_t err_flag;      // set by a kernel whose bounded wait expired
+  int32_t pad1;
   int64_t off_qo_indptr;     // int32 [batch+1]
   int64_t off_kv_indptr;     // int32 [batch+1]
   int64_t off_kv_len;        // int32 [batch]
@@ -85,8 +86,11 @@ cudaError_t launch_decode(const AttnParams& p, int head_dim, int group, bool bf1
                           cudaStream_t stream);
 cudaError_t launch_prefill_mma(const AttnParams& p, int head_dim, int kernel, bool bf16,
                                int grid, cudaStream_t stream);
-cudaError_t launch_prefill_tc(const AttnParams& p, int head_dim, bool bf16, int grid,
+cudaError_t launch_prefill_tc(const AttnParams& p, int head_dim, int group, int tile_rows,
+                              int64_t q_rows, int64_t num_pages, bool bf16, int grid,
                               cudaStream_t stream);
+// Whether the tensor-memory prefill kernel handles this shape.
+bool prefill_tc_supports(int head_dim, int page_size, int group);
 // Merge the workspace partials of a plan into out / lse.
 cudaError_t launch_merge_workspace(const void* ws, void* out, float* lse, int num_heads,
                                    int head_dim, bool bf16, int grid, cudaStream_t stream);

@@ -362,7 +362,7 @@ cudaError_t launch_prefill_mma(const AttnParams& p, int head_dim, int kernel, bo
 int kernel_ctas_per_sm(int kernel, int head_dim, int group, bool bf16) {
   (void)bf16;
   switch (kernel) {
-    case kDecode: return group >= 4 ? 3 : 4;
+    case kDecode: return 3;
     case kPrefillM16: return head_dim == 128 ? 3 : 6;
     case kPrefillM64: return head_dim == 128 ? 2 : 4;
     case kPrefillM128: return 1;
@@ -370,8 +370,5 @@ int kernel_ctas_per_sm(int kernel, int head_dim, int group, bool bf16) {
   return 1;
 }
 
-cudaError_t launch_prefill_tc(const AttnParams&, int, bool, int, cudaStream_t) {
-  return cudaErrorNotSupported;
-}
 
 }  // namespace fi

@@ -1,0 +1,641 @@
+// Prefill kernel on the 5th-generation tensor cores: TMA page gathers into
+// 128B-swizzled shared memory, tcgen05.mma with the S and O accumulators in
+// tensor memory, one thread per query row for the online softmax.
+//
+// Tile: 128 packed rows (query row x head in the GQA group, all heads of one
+// kv head) by 128 keys, head_dim 128, bf16 or fp16 in, fp32 accumulate.
+//
+// Roles inside one CTA (256 threads, one CTA per SM, persistent over the work
+// items of the plan):
+//   warp 0      TMA producer: Q tile (3-D map over [tokens, heads, dim]) and,
+//               per 128-key tile, one box per page of K and of V (4-D maps over
+//               [pages, slot, kv head, dim]) straight from the paged cache;
+//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM (double-buffered),
+//               then O += P V with P read from shared memory;
+//   warps 4-7   softmax: each thread owns one row of S (its TMEM lane), masks
+//               boundary tiles, keeps the running max / sum in registers,
+//               rescales O in TMEM only when the max grows by more than 2^8,
+//               writes P (bf16/fp16) to shared memory, and runs the epilogue.
+// Every mbarrier wait is bounded in time; on expiry the CTA records an error
+// in the workspace header, stops issuing work, waits for its own copies in
+// flight, frees its tensor memory and exits.
+//
+// Mask ("Route non-causal windowed prefill to AITER's masked kernel" (#339),
+// "Why window_size_right stays -1"; "Support speculative-decode verify on
+// ROCm ..." (#362), "Summary"): key j of query row i is kept when
+// (!causal || j <= i + Lk - Lq) && (wl < 0 || j + Lq + wl >= Lk + i). Tiles
+// outside the tile's live key range are never loaded; the per-element test
+// runs on tiles that straddle a bound only.
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace fi {
+namespace {
+
+constexpr int kTcThreads = 256;
+constexpr int kBlk = 128 * 128;       // 128 rows x 128 bytes: one 64-column swizzled block
+constexpr int kTile = 2 * kBlk;       // 128 x 128 16-bit elements
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTile;  // 2 stages
+constexpr int kOffV = kOffK + 2 * kTile;
+constexpr int kOffP = kOffV + 2 * kTile;
+constexpr int kOffBar = kOffP + kTile;
+constexpr int kSmemTc = kOffBar + 256 + 1024;  // barriers + 1 KB alignment slack
+
+// barrier slots
+constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KVFULL = 2, B_KVEMPTY = 4, B_SFULL = 6, B_SFREE = 8,
+              B_PFULL = 10, B_ODONE = 11, B_OFREE = 12, B_FINAL = 13, N_BARS = 14;
+
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete; false on timeout or abort.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start, leading and stride
+// byte offsets in 16-byte units, version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);
+  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+  d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, A/B fp16 or bf16, A
+// K-major, B K-major (S = Q K^T) or MN-major (O += P V), M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool b_mn_major, int M, int N) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((b_mn_major ? 1u : 0u) << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+struct ItemGeom {
+  int b, hk, token0, lq, lk, n_rows, i0, kv_lo, kv_hi, t_start, n_tiles;
+  int chunk, num_chunks, partial_base, row0;
+};
+
+__device__ __forceinline__ ItemGeom item_geom(const WorkItem& it, const int32_t* qo_indptr,
+                                              const int32_t* kv_len, int g, int tile_rows,
+                                              int causal, int wl) {
+  ItemGeom G;
+  G.b = it.b; G.hk = it.kv_head; G.row0 = it.row0;
+  G.token0 = qo_indptr[it.b];
+  G.lq = qo_indptr[it.b + 1] - G.token0;
+  G.lk = kv_len[it.b];
+  G.n_rows = min(tile_rows, G.lq * g - it.row0);
+  G.i0 = it.row0 / g;
+  const int i1 = (it.row0 + G.n_rows) / g - 1;
+  const int hi_t = causal ? min(G.lk, i1 + G.lk - G.lq + 1) : G.lk;
+  const int lo_t = wl >= 0 ? max(0, G.lk - G.lq + G.i0 - wl) : 0;
+  G.kv_lo = max(it.kv_begin, lo_t);
+  G.kv_hi = min(it.kv_end, hi_t);
+  G.t_start = (G.kv_lo / 128) * 128;
+  G.n_tiles = G.kv_lo < G.kv_hi ? (G.kv_hi - G.t_start + 127) / 128 : 0;
+  G.chunk = it.chunk; G.num_chunks = it.num_chunks; G.partial_base = it.partial_base;
+  return G;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tq,
+                      const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                      int kv_box_rows) {
+  using DT = Dt<BF16>;
+  using T = typename DT::T;
+  extern __shared__ uint8_t smem_raw[];
+  uint32_t sbase = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (sbase & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  sbase += pad;
+  const uint32_t bar0 = sbase + kOffBar;
+  auto BAR = [&](int i) { return bar0 + 8u * uint32_t(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * N_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * N_BARS + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
+  const int n_items = hdr->n_items;
+  const WorkItem* items = ws_ptr<const WorkItem>(p.ws, hdr->off_items);
+  const int32_t* qo_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_qo_indptr);
+  const int32_t* kv_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_kv_indptr);
+  const int32_t* kv_len = ws_ptr<const int32_t>(p.ws, hdr->off_kv_len);
+  float* tmp_lse = ws_ptr<float>(p.ws, hdr->off_tmp_lse);
+  float* tmp_o = ws_ptr<float>(p.ws, hdr->off_tmp_o);
+  const int g = hdr->group;
+  const int causal = hdr->causal;
+  const int wl = hdr->window_left;
+  const int tile_rows = hdr->tile_rows;
+  const int Hq = p.num_qo_heads;
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(B_QFULL), 1);
+    mbar_init(BAR(B_QEMPTY), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(BAR(B_KVFULL + s), 1);
+      mbar_init(BAR(B_KVEMPTY + s), 1);
+      mbar_init(BAR(B_SFULL + s), 1);
+      mbar_init(BAR(B_SFREE + s), 128);
+    }
+    mbar_init(BAR(B_PFULL), 128);
+    mbar_init(BAR(B_ODONE), 1);
+    mbar_init(BAR(B_OFREE), 128);
+    mbar_init(BAR(B_FINAL), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // K/V stages start zeroed so rows no copy has written yet hold finite values
+  for (int i = threadIdx.x; i < (4 * kTile) / 16; i += kTcThreads)
+    reinterpret_cast<uint4*>(smem + kOffK)[i] = make_uint4(0, 0, 0, 0);
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                     smem_u32(tmem_slot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int gt = 0, qc = 0;
+      bool kv_armed[2] = {false, false};
+      uint32_t kv_par[2] = {0, 0};
+      bool q_armed = false;
+      uint32_t q_par = 0;
+      for (int w = blockIdx.x; w < n_items && !*abort_flag; w += gridDim.x) {
+        const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
+        if (G.n_tiles == 0) continue;
+        if (qc > 0 && !mbar_wait(BAR(B_QEMPTY), (qc - 1) & 1, abort_flag)) break;
+        const uint32_t qbytes = 2u * uint32_t(tile_rows) * 128u;
+        mbar_expect_tx(BAR(B_QFULL), qbytes);
+        q_armed = true;
+        q_par = qc & 1;
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sbase + kOffQ + h * kBlk, &tq, BAR(B_QFULL), h * 64, G.hk * g,
+                      G.token0 + G.i0);
+        ++qc;
+        const int32_t* pages = p.kv_indices + kv_indptr[G.b];
+        const int n_pages = kv_indptr[G.b + 1] - kv_indptr[G.b];
+        for (int t = 0; t < G.n_tiles && !*abort_flag; ++t, ++gt) {
+          const int st = gt & 1;
+          if (gt >= 2 && !mbar_wait(BAR(B_KVEMPTY + st), ((gt >> 1) - 1) & 1, abort_flag)) break;
+          const int t0 = G.t_start + t * 128;
+          const int pf = t0 / p.page_size;
+          const int npg = 128 / kv_box_rows;  // pages (boxes) per tile
+          int nvalid = 0;
+          for (int q = 0; q < npg; ++q)
+            if (pf + q < n_pages) ++nvalid;
+          mbar_expect_tx(BAR(B_KVFULL + st), uint32_t(nvalid) * uint32_t(kv_box_rows) * 128u * 4u);
+          kv_armed[st] = true;
+          kv_par[st] = (gt >> 1) & 1;
+          const int slot0 = (kv_box_rows == 128) ? (t0 % p.page_size) : 0;
+          for (int q = 0; q < npg; ++q) {
+            if (pf + q >= n_pages) break;
+            const int page = __ldg(pages + pf + q);
+            const uint32_t roff = uint32_t(q * kv_box_rows) * 128u;
+            for (int h = 0; h < 2; ++h) {
+              tma_load_4d(sbase + kOffK + st * kTile + h * kBlk + roff, &tk, BAR(B_KVFULL + st),
+                          h * 64, G.hk, slot0, page);
+              tma_load_4d(sbase + kOffV + st * kTile + h * kBlk + roff, &tv, BAR(B_KVFULL + st),
+                          h * 64, G.hk, slot0, page);
+            }
+          }
+        }
+      }
+      // before exit: every copy this thread started has landed
+      if (q_armed) mbar_wait(BAR(B_QFULL), q_par, abort_flag);
+      for (int s = 0; s < 2; ++s)
+        if (kv_armed[s]) {
+          volatile int dummy = 0;  // these waits ignore the abort flag but keep the time bound
+          mbar_wait(BAR(B_KVFULL + s), kv_par[s], &dummy);
+        }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f16(BF16, false, 128, 128);
+      constexpr uint32_t kIdO = idesc_f16(BF16, true, 128, 128);
+      const uint32_t tS = tmem, tO = tmem + 256;
+      int gt = 0, qc = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
+        if (G.n_tiles == 0) continue;
+        if (!mbar_wait(BAR(B_QFULL), qc & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        for (int t = 0; t <= G.n_tiles && ok; ++t) {
+          if (t < G.n_tiles) {
+            const int g1 = gt + t, st = g1 & 1;
+            if (!mbar_wait(BAR(B_KVFULL + st), (g1 >> 1) & 1, abort_flag)) { ok = false; break; }
+            if (g1 >= 2 && !mbar_wait(BAR(B_SFREE + st), ((g1 >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t koff = uint32_t(kk >> 2) * kBlk + uint32_t(kk & 3) * 32u;
+              const uint64_t ad = sdesc_sw128(sbase + kOffQ + koff, 16, 1024);
+              const uint64_t bd = sdesc_sw128(sbase + kOffK + st * kTile + koff, 16, 1024);
+              tc_mma(tS + uint32_t(st) * 128u, ad, bd, kIdS, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(BAR(B_SFULL + st));
+            if (t == G.n_tiles - 1) tc_commit(BAR(B_QEMPTY));
+          }
+          if (t >= 1) {
+            const int g0 = gt + t - 1, st0 = g0 & 1;
+            if (t == 1 && qc > 0 && !mbar_wait(BAR(B_OFREE), (qc - 1) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_PFULL), g0 & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t aoff = uint32_t(kk >> 2) * kBlk + uint32_t(kk & 3) * 32u;
+              const uint64_t ad = sdesc_sw128(sbase + kOffP + aoff, 16, 1024);
+              const uint64_t bd = sdesc_sw128(sbase + kOffV + st0 * kTile + uint32_t(kk) * 2048u,
+                                              kBlk, 1024);
+              tc_mma(tO, ad, bd, kIdO, (t > 1 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(BAR(B_ODONE));
+            tc_commit(BAR(B_KVEMPTY + st0));
+          }
+        }
+        gt += G.n_tiles;
+        ++qc;
+      }
+      // every MMA this thread issued has completed before tensor memory is freed
+      tc_commit(BAR(B_FINAL));
+      volatile int no_abort = 0;
+      mbar_wait(BAR(B_FINAL), 0, &no_abort);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int sw = warp - 4;               // TMEM lane quadrant
+    const int r = sw * 32 + lane;          // packed row of this thread
+    const uint32_t lane_addr = uint32_t(sw * 32) << 16;
+    const uint32_t tS = tmem + lane_addr, tO = tmem + lane_addr + 256;
+    int gt = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
+      const bool row_ok = r < G.n_rows;
+      const int pr = G.row0 + r;
+      const int qi = pr / g;
+      const int tok = G.token0 + qi;
+      const int head = G.hk * g + pr % g;
+      // this row's live keys: [jmin, jmax]
+      int jmin = G.kv_lo, jmax = G.kv_hi - 1;
+      if (wl >= 0) jmin = max(jmin, G.lk - G.lq + qi - wl);
+      if (causal) jmax = min(jmax, qi + G.lk - G.lq);
+      const int i1 = (G.row0 + G.n_rows) / g - 1;
+      float m_run = neg_inf(), l_run = 0.f;
+      for (int t = 0; t < G.n_tiles; ++t) {
+        const int g1 = gt + t, st = g1 & 1;
+        const int t0 = G.t_start + t * 128;
+        if (!mbar_wait(BAR(B_SFULL + st), (g1 >> 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + uint32_t(st) * 128u + uint32_t(c) * 32u, sr[c]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(BAR(B_SFREE + st));
+        const bool need_mask = (t0 < G.kv_lo) || (t0 + 128 > G.kv_hi) ||
+                               (causal && t0 + 127 > G.i0 + G.lk - G.lq) ||
+                               (wl >= 0 && t0 < G.lk - G.lq + i1 - wl);
+        float mx = neg_inf();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float x = __uint_as_float(sr[c][e]) * p.sm_scale_log2;
+            if (need_mask) {
+              const int j = t0 + c * 32 + e;
+              if (j < jmin || j > jmax) x = neg_inf();
+            }
+            sr[c][e] = __float_as_uint(x);
+            mx = fmaxf(mx, x);
+          }
+        float m_new = m_run;
+        if (mx > m_run + 8.f || (m_run == neg_inf() && mx != neg_inf())) m_new = mx;
+        const float corr = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
+        const float mu = (m_new == neg_inf()) ? 0.f : m_new;
+        float psum = 0.f;
+        uint32_t pk[4][16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2(__uint_as_float(sr[c][2 * e]) - mu);
+            const float p1 = ex2(__uint_as_float(sr[c][2 * e + 1]) - mu);
+            psum += p0 + p1;
+            pk[c][e] = DT::pack(p0, p1);
+          }
+        l_run = l_run * corr + psum;
+        m_run = m_new;
+        if (t > 0) {
+          // the previous P V product has finished: O may be rescaled, P rewritten
+          if (!mbar_wait(BAR(B_ODONE), (g1 - 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t ov[32];
+              tmem_ld32(tO + uint32_t(c) * 32u, ov);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
+              tmem_st32(tO + uint32_t(c) * 32u, ov);
+            }
+            tmem_wait_st();
+          }
+        }
+        if (t0 + 128 > G.lk) {
+          // rows of V past the request's last key may hold anything: zero them
+          if (!mbar_wait(BAR(B_KVFULL + st), (g1 >> 1) & 1, abort_flag)) { ok = false; break; }
+          if (t0 + r >= G.lk) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint4* row = reinterpret_cast<uint4*>(smem + kOffV + st * kTile + h * kBlk + r * 128);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) row[q] = make_uint4(0, 0, 0, 0);
+            }
+          }
+        }
+        // P row r, 128-byte swizzled, two 64-key blocks
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int blk = c >> 3, cc = c & 7;
+          uint4* dst = reinterpret_cast<uint4*>(smem + kOffP + blk * kBlk + r * 128 +
+                                                ((cc ^ (r & 7)) << 4));
+          *dst = make_uint4(pk[c >> 2][(c & 3) * 4 + 0], pk[c >> 2][(c & 3) * 4 + 1],
+                            pk[c >> 2][(c & 3) * 4 + 2], pk[c >> 2][(c & 3) * 4 + 3]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        mbar_arrive(BAR(B_PFULL));
+      }
+      if (!ok) break;
+      // epilogue
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float lse = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : neg_inf();
+      const bool direct = G.chunk < 0;
+      const int slot = direct ? 0 : G.partial_base + (qi - G.i0) * G.num_chunks + G.chunk;
+      if (G.n_tiles > 0) {
+        const int g_last = gt + G.n_tiles - 1;
+        if (!mbar_wait(BAR(B_ODONE), g_last & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tO + uint32_t(c) * 32u, ov);
+          tmem_wait_ld();
+          if (row_ok) {
+            if (direct) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) +
+                                                    (int64_t(tok) * Hq + head) * 128 + c * 32);
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(
+                    DT::pack(__uint_as_float(ov[8 * q + 0]) * inv, __uint_as_float(ov[8 * q + 1]) * inv),
+                    DT::pack(__uint_as_float(ov[8 * q + 2]) * inv, __uint_as_float(ov[8 * q + 3]) * inv),
+                    DT::pack(__uint_as_float(ov[8 * q + 4]) * inv, __uint_as_float(ov[8 * q + 5]) * inv),
+                    DT::pack(__uint_as_float(ov[8 * q + 6]) * inv, __uint_as_float(ov[8 * q + 7]) * inv));
+            } else {
+              float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * 128 + c * 32);
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(__uint_as_float(ov[4 * q]) * inv, __uint_as_float(ov[4 * q + 1]) * inv,
+                                     __uint_as_float(ov[4 * q + 2]) * inv, __uint_as_float(ov[4 * q + 3]) * inv);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(BAR(B_OFREE));
+      } else if (row_ok) {
+        if (direct) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (int64_t(tok) * Hq + head) * 128);
+          for (int q = 0; q < 16; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * 128);
+          for (int q = 0; q < 32; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      if (row_ok) {
+        if (direct) {
+          if (p.lse) p.lse[int64_t(tok) * Hq + head] = lse;
+        } else {
+          tmp_lse[int64_t(slot) * Hq + head] = lse;
+        }
+      }
+      gt += G.n_tiles;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0 && *abort_flag) {
+    int* err = const_cast<int*>(&hdr->err_flag);
+    atomicExch(err, 1);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+  }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+bool encode(CUtensorMap* m, bool bf16, int rank, const void* base, const cuuint64_t* dims,
+            const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  cuuint32_t(rank), const_cast<void*>(base), dims, strides_bytes, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool prefill_tc_supports(int head_dim, int page_size, int group) {
+  if (head_dim != 128 || group < 1 || group > 128) return false;
+  if (page_size >= 128) return page_size % 128 == 0;
+  return page_size >= 16 && 128 % page_size == 0;
+}
+
+cudaError_t launch_prefill_tc(const AttnParams& p, int head_dim, int group, int tile_rows,
+                              int64_t q_rows, int64_t num_pages, bool bf16, int grid,
+                              cudaStream_t s) {
+  if (grid <= 0) return cudaSuccess;
+  if (!prefill_tc_supports(head_dim, p.page_size, group)) return cudaErrorInvalidValue;
+  CUtensorMap tq, tk, tv;
+  const int box_rows = p.page_size >= 128 ? 128 : p.page_size;
+  {
+    cuuint64_t dims[3] = {cuuint64_t(head_dim), cuuint64_t(p.num_qo_heads), cuuint64_t(q_rows)};
+    cuuint64_t str[2] = {cuuint64_t(p.q_stride_head) * 2, cuuint64_t(p.q_stride_tok) * 2};
+    cuuint32_t box[3] = {64, cuuint32_t(group), cuuint32_t(tile_rows / group)};
+    if (!encode(&tq, bf16, 3, p.q, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[4] = {cuuint64_t(head_dim), cuuint64_t(p.num_kv_heads),
+                          cuuint64_t(p.page_size), cuuint64_t(num_pages)};
+    cuuint32_t box[4] = {64, 1, cuuint32_t(box_rows), 1};
+    cuuint64_t sk[3] = {cuuint64_t(p.k_stride_head) * 2, cuuint64_t(p.k_stride_tok) * 2,
+                        cuuint64_t(p.k_stride_page) * 2};
+    cuuint64_t sv[3] = {cuuint64_t(p.v_stride_head) * 2, cuuint64_t(p.v_stride_tok) * 2,
+                        cuuint64_t(p.v_stride_page) * 2};
+    if (!encode(&tk, bf16, 4, p.k, dims, sk, box)) return cudaErrorInvalidValue;
+    if (!encode(&tv, bf16, 4, p.v, dims, sv, box)) return cudaErrorInvalidValue;
+  }
+  if (bf16) {
+    static cudaError_t attr = cudaFuncSetAttribute(
+        prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
+    if (attr != cudaSuccess) return attr;
+    prefill_tc_kernel<true><<<grid, kTcThreads, kSmemTc, s>>>(p, tq, tk, tv, box_rows);
+  } else {
+    static cudaError_t attr = cudaFuncSetAttribute(
+        prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
+    if (attr != cudaSuccess) return attr;
+    prefill_tc_kernel<false><<<grid, kTcThreads, kSmemTc, s>>>(p, tq, tk, tv, box_rows);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fi
