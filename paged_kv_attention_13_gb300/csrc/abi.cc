@@ -714,6 +714,9 @@ fi_status run_common(fi_plan_t p, bool decode_api, const fi_tensor* q, const fi_
     if (lse->shape[1] != s.hq) return check_dim("lse", "num_qo_heads", s.hq, lse->shape[1]);
     if ((st = check_packed(lse, "lse")) != FI_OK) return st;
   }
+  if (!(sm_scale > 0.f) || sm_scale > 3.0e38f)
+    return fail(FI_ERR_INVALID_ARG, "%s: sm_scale=%g must be positive and finite", api,
+                double(sm_scale));
   // 16-byte vector loads of every row
   if (!aligned16(q->data) || !aligned16(k->data) || !aligned16(v->data) || !aligned16(out->data) ||
       q->stride[0] % 8 || q->stride[1] % 8 || k->stride[0] % 8 || k->stride[1] % 8 ||

@@ -5,17 +5,18 @@
 // Tile: 128 packed rows (query row x head in the GQA group, all heads of one
 // kv head) by 128 keys, head_dim 128, bf16 or fp16 in, fp32 accumulate.
 //
-// Roles inside one CTA (256 threads, one CTA per SM, persistent over the work
+// Roles inside one CTA (384 threads, one CTA per SM, persistent over the work
 // items of the plan):
 //   warp 0      TMA producer: Q tile (3-D map over [tokens, heads, dim]) and,
 //               per 128-key tile, one box per page of K and of V (4-D maps over
 //               [pages, slot, kv head, dim]) straight from the paged cache;
 //   warp 1      MMA issuer (one thread): S = Q K^T into TMEM (double-buffered),
 //               then O += P V with P read from shared memory;
-//   warps 4-7   softmax: each thread owns one row of S (its TMEM lane), masks
-//               boundary tiles, keeps the running max / sum in registers,
-//               rescales O in TMEM only when the max grows by more than 2^8,
-//               writes P (bf16/fp16) to shared memory, and runs the epilogue.
+//   warps 4-11  softmax, two warpgroups: a thread owns one row of S (its TMEM
+//               lane) and one half of its columns; it masks boundary tiles,
+//               keeps the running max / sum in registers, rescales its half of
+//               O in TMEM only when the max grows by more than 2^8, writes its
+//               half of P (bf16/fp16) to shared memory, and runs the epilogue.
 // Every mbarrier wait is bounded in time; on expiry the CTA records an error
 // in the workspace header, stops issuing work, waits for its own copies in
 // flight, frees its tensor memory and exits.
@@ -33,7 +34,7 @@
 namespace fi {
 namespace {
 
-constexpr int kTcThreads = 256;
+constexpr int kTcThreads = 384;  // 4 control warps + 2 softmax warpgroups
 constexpr int kBlk = 128 * 128;       // 128 rows x 128 bytes: one 64-column swizzled block
 constexpr int kTile = 2 * kBlk;       // 128 x 128 16-bit elements
 constexpr int kOffQ = 0;
@@ -41,11 +42,11 @@ constexpr int kOffK = kOffQ + kTile;  // 2 stages
 constexpr int kOffV = kOffK + 2 * kTile;
 constexpr int kOffP = kOffV + 2 * kTile;
 constexpr int kOffBar = kOffP + kTile;
-constexpr int kSmemTc = kOffBar + 256 + 1024;  // barriers + 1 KB alignment slack
+constexpr int kSmemTc = kOffBar + 256 + 2048 + 1024;  // barriers, row sums, alignment slack
 
 // barrier slots
 constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KVFULL = 2, B_KVEMPTY = 4, B_SFULL = 6, B_SFREE = 8,
-              B_PFULL = 10, B_ODONE = 11, B_OFREE = 12, B_FINAL = 13, N_BARS = 14;
+              B_PFULL = 10, B_ODONE = 11, B_OFREE = 12, B_FINAL = 13, B_LSUM = 14, N_BARS = 15;
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
@@ -248,12 +249,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(BAR(B_KVFULL + s), 1);
       mbar_init(BAR(B_KVEMPTY + s), 1);
       mbar_init(BAR(B_SFULL + s), 1);
-      mbar_init(BAR(B_SFREE + s), 128);
+      mbar_init(BAR(B_SFREE + s), 256);
     }
-    mbar_init(BAR(B_PFULL), 128);
+    mbar_init(BAR(B_PFULL), 256);
     mbar_init(BAR(B_ODONE), 1);
-    mbar_init(BAR(B_OFREE), 128);
+    mbar_init(BAR(B_OFREE), 256);
     mbar_init(BAR(B_FINAL), 1);
+    mbar_init(BAR(B_LSUM), 256);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -274,59 +276,70 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int gt = 0, qc = 0;
-      bool kv_armed[2] = {false, false};
-      uint32_t kv_par[2] = {0, 0};
-      bool q_armed = false;
-      uint32_t q_par = 0;
-      for (int w = blockIdx.x; w < n_items && !*abort_flag; w += gridDim.x) {
-        const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
-        if (G.n_tiles == 0) continue;
-        if (qc > 0 && !mbar_wait(BAR(B_QEMPTY), (qc - 1) & 1, abort_flag)) break;
-        const uint32_t qbytes = 2u * uint32_t(tile_rows) * 128u;
-        mbar_expect_tx(BAR(B_QFULL), qbytes);
-        q_armed = true;
-        q_par = qc & 1;
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(sbase + kOffQ + h * kBlk, &tq, BAR(B_QFULL), h * 64, G.hk * g,
-                      G.token0 + G.i0);
-        ++qc;
-        const int32_t* pages = p.kv_indices + kv_indptr[G.b];
-        const int n_pages = kv_indptr[G.b + 1] - kv_indptr[G.b];
-        for (int t = 0; t < G.n_tiles && !*abort_flag; ++t, ++gt) {
-          const int st = gt & 1;
-          if (gt >= 2 && !mbar_wait(BAR(B_KVEMPTY + st), ((gt >> 1) - 1) & 1, abort_flag)) break;
-          const int t0 = G.t_start + t * 128;
-          const int pf = t0 / p.page_size;
-          const int npg = 128 / kv_box_rows;  // pages (boxes) per tile
-          int nvalid = 0;
-          for (int q = 0; q < npg; ++q)
-            if (pf + q < n_pages) ++nvalid;
-          mbar_expect_tx(BAR(B_KVFULL + st), uint32_t(nvalid) * uint32_t(kv_box_rows) * 128u * 4u);
-          kv_armed[st] = true;
-          kv_par[st] = (gt >> 1) & 1;
+    // Lane 0 owns the barriers; for each tile every lane fetches one page
+    // index (up to 8 pages per tile) and issues that page's boxes.
+    int gt = 0, qc = 0;
+    bool kv_armed[2] = {false, false};
+    uint32_t kv_par[2] = {0, 0};
+    bool q_armed = false;
+    uint32_t q_par = 0;
+    bool ok = true;
+    const int npg = 128 / kv_box_rows;  // pages (boxes) per tile
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
+      if (G.n_tiles == 0) continue;
+      if (lane == 0) {
+        if (qc > 0 && !mbar_wait(BAR(B_QEMPTY), (qc - 1) & 1, abort_flag)) ok = false;
+        if (ok) {
+          mbar_expect_tx(BAR(B_QFULL), 2u * uint32_t(tile_rows) * 128u);
+          q_armed = true;
+          q_par = qc & 1;
+          for (int h = 0; h < 2; ++h)
+            tma_load_3d(sbase + kOffQ + h * kBlk, &tq, BAR(B_QFULL), h * 64, G.hk * g,
+                        G.token0 + G.i0);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ++qc;
+      const int32_t* pages = p.kv_indices + kv_indptr[G.b];
+      const int n_pages = kv_indptr[G.b + 1] - kv_indptr[G.b];
+      for (int t = 0; t < G.n_tiles; ++t, ++gt) {
+        const int st = gt & 1;
+        const int t0 = G.t_start + t * 128;
+        const int pf = t0 / p.page_size;
+        const bool has = lane < npg && pf + lane < n_pages;
+        const int page = has ? __ldg(pages + pf + lane) : 0;
+        const int nvalid = __popc(__ballot_sync(0xffffffffu, has));
+        if (lane == 0) {
+          if (gt >= 2 && !mbar_wait(BAR(B_KVEMPTY + st), ((gt >> 1) - 1) & 1, abort_flag)) ok = false;
+          if (ok) {
+            mbar_expect_tx(BAR(B_KVFULL + st), uint32_t(nvalid) * uint32_t(kv_box_rows) * 128u * 4u);
+            kv_armed[st] = true;
+            kv_par[st] = (gt >> 1) & 1;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (has) {
           const int slot0 = (kv_box_rows == 128) ? (t0 % p.page_size) : 0;
-          for (int q = 0; q < npg; ++q) {
-            if (pf + q >= n_pages) break;
-            const int page = __ldg(pages + pf + q);
-            const uint32_t roff = uint32_t(q * kv_box_rows) * 128u;
-            for (int h = 0; h < 2; ++h) {
-              tma_load_4d(sbase + kOffK + st * kTile + h * kBlk + roff, &tk, BAR(B_KVFULL + st),
-                          h * 64, G.hk, slot0, page);
-              tma_load_4d(sbase + kOffV + st * kTile + h * kBlk + roff, &tv, BAR(B_KVFULL + st),
-                          h * 64, G.hk, slot0, page);
-            }
+          const uint32_t roff = uint32_t(lane * kv_box_rows) * 128u;
+          for (int h = 0; h < 2; ++h) {
+            tma_load_4d(sbase + kOffK + st * kTile + h * kBlk + roff, &tk, BAR(B_KVFULL + st),
+                        h * 64, G.hk, slot0, page);
+            tma_load_4d(sbase + kOffV + st * kTile + h * kBlk + roff, &tv, BAR(B_KVFULL + st),
+                        h * 64, G.hk, slot0, page);
           }
         }
       }
-      // before exit: every copy this thread started has landed
-      if (q_armed) mbar_wait(BAR(B_QFULL), q_par, abort_flag);
+    }
+    // before exit: every copy this warp started has landed (these waits
+    // ignore the abort flag but keep the time bound)
+    if (lane == 0) {
+      volatile int no_abort = 0;
+      if (q_armed) mbar_wait(BAR(B_QFULL), q_par, &no_abort);
       for (int s = 0; s < 2; ++s)
-        if (kv_armed[s]) {
-          volatile int dummy = 0;  // these waits ignore the abort flag but keep the time bound
-          mbar_wait(BAR(B_KVFULL + s), kv_par[s], &dummy);
-        }
+        if (kv_armed[s]) mbar_wait(BAR(B_KVFULL + s), kv_par[s], &no_abort);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -386,10 +399,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
-    const int sw = warp - 4;               // TMEM lane quadrant
+    // Two warpgroups share every row: both read the whole S row (for the row
+    // max, so both take the same rescale decision), each exponentiates, writes
+    // P for and rescales O over its own 64 columns.
+    const int half = (warp - 4) >> 2;      // column half of this warpgroup
+    const int sw = warp & 3;               // TMEM lane quadrant
     const int r = sw * 32 + lane;          // packed row of this thread
     const uint32_t lane_addr = uint32_t(sw * 32) << 16;
-    const uint32_t tS = tmem + lane_addr, tO = tmem + lane_addr + 256;
+    const uint32_t tS = tmem + lane_addr, tO = tmem + lane_addr + 256 + uint32_t(half) * 64u;
+    float* l_share = reinterpret_cast<float*>(smem + kOffBar + 256);  // [2 buffers][2 halves][128]
+    // every wait here is warp-uniform, so a timeout never splits a warp
+    // in front of a .sync.aligned instruction
+    auto wwait = [&](uint32_t bar, uint32_t parity) {
+      const bool okl = mbar_wait(bar, parity, abort_flag);
+      return __all_sync(0xffffffffu, okl);
+    };
+    int xc = 0;  // row-sum exchanges so far
+    const float scale = p.sm_scale_log2;
     int gt = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
@@ -408,54 +434,66 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int t = 0; t < G.n_tiles; ++t) {
         const int g1 = gt + t, st = g1 & 1;
         const int t0 = G.t_start + t * 128;
-        if (!mbar_wait(BAR(B_SFULL + st), (g1 >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!wwait(BAR(B_SFULL + st), (g1 >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sr[4][32];
+        uint32_t sr[4][32];  // [0..1] this half's columns, [2..3] the other half's
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + uint32_t(st) * 128u + uint32_t(c) * 32u, sr[c]);
+        for (int c = 0; c < 2; ++c) {
+          tmem_ld32(tS + uint32_t(st) * 128u + uint32_t(half * 64 + c * 32), sr[c]);
+          tmem_ld32(tS + uint32_t(st) * 128u + uint32_t((1 - half) * 64 + c * 32), sr[2 + c]);
+        }
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(BAR(B_SFREE + st));
         const bool need_mask = (t0 < G.kv_lo) || (t0 + 128 > G.kv_hi) ||
                                (causal && t0 + 127 > G.i0 + G.lk - G.lq) ||
                                (wl >= 0 && t0 < G.lk - G.lq + i1 - wl);
-        float mx = neg_inf();
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int cb = t0 + ((c < 2) ? half : 1 - half) * 64 + (c & 1) * 32;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int j = cb + e;
+              if (j < jmin || j > jmax) sr[c][e] = __float_as_uint(neg_inf());
+            }
+          }
+        }
+        // row max of the raw scores, eight independent chains
+        float mp[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mp[q] = neg_inf();
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float x = __uint_as_float(sr[c][e]) * p.sm_scale_log2;
-            if (need_mask) {
-              const int j = t0 + c * 32 + e;
-              if (j < jmin || j > jmax) x = neg_inf();
-            }
-            sr[c][e] = __float_as_uint(x);
-            mx = fmaxf(mx, x);
-          }
+          for (int e = 0; e < 32; ++e) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(sr[c][e]));
+        const float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                 fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        const float mx = mraw * scale;  // scale > 0, so this is the max of the scaled row
         float m_new = m_run;
-        if (mx > m_run + 8.f || (m_run == neg_inf() && mx != neg_inf())) m_new = mx;
+        if (mx > m_run + 8.f || (m_run == neg_inf() && mraw != neg_inf())) m_new = mx;
         const float corr = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
         const float mu = (m_new == neg_inf()) ? 0.f : m_new;
-        float psum = 0.f;
-        uint32_t pk[4][16];
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[2][16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2(__uint_as_float(sr[c][2 * e]) - mu);
-            const float p1 = ex2(__uint_as_float(sr[c][2 * e + 1]) - mu);
-            psum += p0 + p1;
+            const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * e]), scale, -mu));
+            const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * e + 1]), scale, -mu));
+            ps[e & 3] += p0 + p1;
             pk[c][e] = DT::pack(p0, p1);
           }
-        l_run = l_run * corr + psum;
+        l_run = l_run * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
         m_run = m_new;
         if (t > 0) {
           // the previous P V product has finished: O may be rescaled, P rewritten
-          if (!mbar_wait(BAR(B_ODONE), (g1 - 1) & 1, abort_flag)) { ok = false; break; }
+          if (!wwait(BAR(B_ODONE), (g1 - 1) & 1)) { ok = false; break; }
           tc_fence_after();
           if (__any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
               uint32_t ov[32];
               tmem_ld32(tO + uint32_t(c) * 32u, ov);
               tmem_wait_ld();
@@ -468,48 +506,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (t0 + 128 > G.lk) {
           // rows of V past the request's last key may hold anything: zero them
-          if (!mbar_wait(BAR(B_KVFULL + st), (g1 >> 1) & 1, abort_flag)) { ok = false; break; }
+          if (!wwait(BAR(B_KVFULL + st), (g1 >> 1) & 1)) { ok = false; break; }
           if (t0 + r >= G.lk) {
+            uint4* row = reinterpret_cast<uint4*>(smem + kOffV + st * kTile + half * kBlk + r * 128);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint4* row = reinterpret_cast<uint4*>(smem + kOffV + st * kTile + h * kBlk + r * 128);
-#pragma unroll
-              for (int q = 0; q < 8; ++q) row[q] = make_uint4(0, 0, 0, 0);
-            }
+            for (int q = 0; q < 8; ++q) row[q] = make_uint4(0, 0, 0, 0);
           }
         }
-        // P row r, 128-byte swizzled, two 64-key blocks
+        // P row r, this half's 64 keys: one 128-byte swizzled block
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int blk = c >> 3, cc = c & 7;
-          uint4* dst = reinterpret_cast<uint4*>(smem + kOffP + blk * kBlk + r * 128 +
+        for (int cc = 0; cc < 8; ++cc) {
+          uint4* dst = reinterpret_cast<uint4*>(smem + kOffP + half * kBlk + r * 128 +
                                                 ((cc ^ (r & 7)) << 4));
-          *dst = make_uint4(pk[c >> 2][(c & 3) * 4 + 0], pk[c >> 2][(c & 3) * 4 + 1],
-                            pk[c >> 2][(c & 3) * 4 + 2], pk[c >> 2][(c & 3) * 4 + 3]);
+          *dst = make_uint4(pk[cc >> 2][(cc & 3) * 4 + 0], pk[cc >> 2][(cc & 3) * 4 + 1],
+                            pk[cc >> 2][(cc & 3) * 4 + 2], pk[cc >> 2][(cc & 3) * 4 + 3]);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         mbar_arrive(BAR(B_PFULL));
       }
       if (!ok) break;
-      // epilogue
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const float lse = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : neg_inf();
+      // epilogue: combine the two halves' row sums (double-buffered exchange
+      // through shared memory, ordered by an mbarrier with a bounded wait)
+      float l_tot = l_run;
+      if (G.n_tiles > 0) {
+        float* buf = l_share + (xc & 1) * 256;
+        buf[half * 128 + r] = l_run;
+        mbar_arrive(BAR(B_LSUM));
+        if (!wwait(BAR(B_LSUM), xc & 1)) { ok = false; break; }
+        l_tot += buf[(1 - half) * 128 + r];
+        ++xc;
+      }
+      const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+      const float lse = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : neg_inf();
       const bool direct = G.chunk < 0;
       const int slot = direct ? 0 : G.partial_base + (qi - G.i0) * G.num_chunks + G.chunk;
       if (G.n_tiles > 0) {
         const int g_last = gt + G.n_tiles - 1;
-        if (!mbar_wait(BAR(B_ODONE), g_last & 1, abort_flag)) { ok = false; break; }
+        if (!wwait(BAR(B_ODONE), g_last & 1)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t ov[32];
           tmem_ld32(tO + uint32_t(c) * 32u, ov);
           tmem_wait_ld();
+          const int col = half * 64 + c * 32;
           if (row_ok) {
             if (direct) {
               uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) +
-                                                    (int64_t(tok) * Hq + head) * 128 + c * 32);
+                                                    (int64_t(tok) * Hq + head) * 128 + col);
 #pragma unroll
               for (int q = 0; q < 4; ++q)
                 dst[q] = make_uint4(
@@ -518,7 +563,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     DT::pack(__uint_as_float(ov[8 * q + 4]) * inv, __uint_as_float(ov[8 * q + 5]) * inv),
                     DT::pack(__uint_as_float(ov[8 * q + 6]) * inv, __uint_as_float(ov[8 * q + 7]) * inv));
             } else {
-              float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * 128 + c * 32);
+              float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * 128 + col);
 #pragma unroll
               for (int q = 0; q < 8; ++q)
                 dst[q] = make_float4(__uint_as_float(ov[4 * q]) * inv, __uint_as_float(ov[4 * q + 1]) * inv,
@@ -529,15 +574,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_before();
         mbar_arrive(BAR(B_OFREE));
       } else if (row_ok) {
+        const int col = half * 64;
         if (direct) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (int64_t(tok) * Hq + head) * 128);
-          for (int q = 0; q < 16; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (int64_t(tok) * Hq + head) * 128 + col);
+          for (int q = 0; q < 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);
         } else {
-          float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * 128);
-          for (int q = 0; q < 32; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * 128 + col);
+          for (int q = 0; q < 16; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      if (row_ok) {
+      if (row_ok && half == 0) {
         if (direct) {
           if (p.lse) p.lse[int64_t(tok) * Hq + head] = lse;
         } else {
@@ -547,7 +593,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       gt += G.n_tiles;
     }
   }
-
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
