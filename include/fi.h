@@ -224,6 +224,47 @@ fi_status fi_plan_get_info(fi_plan_t plan, fi_plan_info* info, int32_t* items,
 fi_status fi_plan_read_device(fi_plan_t plan, int32_t* items, int32_t items_capacity,
                               int32_t* merge_indptr, int32_t merge_capacity, void* stream);
 
+/*
+ * Batch decode that allocates nothing (the pages have no counterpart; this is
+ * an addition of this library).
+ *
+ * For callers that cannot allocate device memory when they run attention: a
+ * serving loop that handed all GPU memory to its own pool up front, code that
+ * runs inside another framework's allocator, or a host path where a
+ * cudaMalloc/cudaFree (or a caching allocator's growth) would stall the device.
+ * Instead of a caller workspace it uses one fixed scratch array compiled into
+ * libfi: fi_noalloc_scratch_bytes() bytes (32 MiB) that every GPU which loads
+ * the library holds until the process exits. The call makes no cudaMalloc,
+ * cudaFree or other allocating call; out and lse are the caller's.
+ *
+ *   q            [>= batch, Hq, d] bf16/fp16, one query row per request.
+ *   k_cache, v_cache  [pages, page_size, Hk, d], as for fi_batch_decode_paged.
+ *   kv_indices   int32 device page table; kv_indptr_dev [batch+1] and
+ *                last_page_len_dev [batch] are device int32 arrays, read on the
+ *                device (their values are trusted: they are not checked on the
+ *                host).
+ *   window_left  -1 or >= 0; kv_chunks in [1, 64]: each request's keys are cut
+ *                into that many even chunks whose partial states are merged.
+ *   out, lse     packed [>= batch, Hq, d] / [>= batch, Hq] fp32.
+ * Group size 1, 2 or 4 and head_dim 64 or 128. A batch whose plan and partial
+ * states do not fit the scratch returns FI_ERR_CAPACITY (message from
+ * fi_noalloc_last_error()). The first call on a device looks up the array's
+ * device address once with that device current; make that first call before
+ * any stream capture. Every call rewrites the scratch from scratch, and calls
+ * share it: two calls that overlap on the GPU (different streams, no ordering)
+ * race.
+ */
+fi_status fi_batch_decode_paged_noalloc(const fi_tensor* q, const fi_tensor* k_cache,
+                                        const fi_tensor* v_cache, const fi_tensor* kv_indices,
+                                        const int32_t* kv_indptr_dev,
+                                        const int32_t* last_page_len_dev, int32_t batch,
+                                        int32_t window_left, int32_t kv_chunks, float sm_scale,
+                                        fi_tensor* out, fi_tensor* lse, void* stream);
+/* Size of the fixed scratch array behind fi_batch_decode_paged_noalloc. */
+size_t fi_noalloc_scratch_bytes(void);
+/* Thread-local message of the last refusal of fi_batch_decode_paged_noalloc. */
+const char* fi_noalloc_last_error(void);
+
 void fi_plan_destroy(fi_plan_t plan);
 const char* fi_last_error(void);
 const char* fi_status_str(fi_status status);

@@ -23,6 +23,7 @@ EXPORTED = [
     "fi_workspace_bytes", "fi_plan_create", "fi_plan", "fi_batch_prefill_paged",
     "fi_batch_decode_paged", "fi_merge_state", "fi_merge_states", "fi_plan_get_info",
     "fi_plan_read_device", "fi_plan_destroy", "fi_last_error", "fi_status_str",
+    "fi_batch_decode_paged_noalloc", "fi_noalloc_scratch_bytes", "fi_noalloc_last_error",
 ]
 
 
@@ -79,5 +80,12 @@ def load():
     lib.fi_last_error.argtypes = []
     lib.fi_status_str.restype = ctypes.c_char_p
     lib.fi_status_str.argtypes = [ctypes.c_int]
+    lib.fi_batch_decode_paged_noalloc.restype = ctypes.c_int
+    lib.fi_batch_decode_paged_noalloc.argtypes = [PT, PT, PT, PT, P, P, i32, i32, i32,
+                                                  ctypes.c_float, PT, PT, P]
+    lib.fi_noalloc_scratch_bytes.restype = ctypes.c_size_t
+    lib.fi_noalloc_scratch_bytes.argtypes = []
+    lib.fi_noalloc_last_error.restype = ctypes.c_char_p
+    lib.fi_noalloc_last_error.argtypes = []
     _lib = lib
     return lib

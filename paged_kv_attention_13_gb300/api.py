@@ -210,3 +210,27 @@ def fi_merge_states(v, s, merge_indptr, rows, v_out=None, s_out=None, out_dtype=
         ctypes.byref(sod) if sod is not None else None,
         num_rows_dev.data_ptr() if num_rows_dev is not None else None, _stream_handle(stream)))
     return v_out, s_out
+
+
+def fi_batch_decode_paged_noalloc(q, k_cache, v_cache, kv_indices, kv_indptr, last_page_len,
+                                  sm_scale, window_left=-1, kv_chunks=4, out=None, lse=None,
+                                  stream=None):
+    """Batch decode whose split-KV scratch is a fixed device array inside the
+    library: the call itself allocates no device memory (``out``/``lse`` are
+    allocated here only when not passed). kv_indptr / last_page_len are device
+    int32 tensors; the batch is ``len(kv_indptr) - 1``."""
+    lib = _lib.load()
+    batch = kv_indptr.shape[0] - 1
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    descs = [tensor_desc(t) for t in (q, k_cache, v_cache, kv_indices)]
+    od, ld = tensor_desc(out), tensor_desc(lse)
+    st = lib.fi_batch_decode_paged_noalloc(
+        *[ctypes.byref(d) for d in descs], kv_indptr.data_ptr(), last_page_len.data_ptr(),
+        int(batch), int(window_left), int(kv_chunks), ctypes.c_float(sm_scale), ctypes.byref(od),
+        ctypes.byref(ld), _stream_handle(stream))
+    if st != _lib.FI_OK:
+        raise FiError(st, lib.fi_noalloc_last_error().decode(errors="replace"))
+    return out, lse
