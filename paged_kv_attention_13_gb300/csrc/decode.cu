@@ -107,8 +107,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_kernel(const AttnPar
       cp_async_commit();
     }
 
-    // q slice of every head in the group, pre-scaled into the log2 domain
-    float qf[G][8];
+    // q slice of every head in the group, pre-scaled into the log2 domain,
+    // as pairs for the packed fp32x2 FMA
+    float2 q2[G][4];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const T* qp = static_cast<const T*>(p.q) + int64_t(token) * p.q_stride_tok +
@@ -116,18 +117,42 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_kernel(const AttnPar
       uint4 r = ld_nc16(qp);
       const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        qf[h][2 * e] = DT::lo(wv[e]) * p.sm_scale_log2;
-        qf[h][2 * e + 1] = DT::hi(wv[e]) * p.sm_scale_log2;
+      for (int e = 0; e < 4; ++e)
+        q2[h][e] = make_float2(DT::lo(wv[e]) * p.sm_scale_log2, DT::hi(wv[e]) * p.sm_scale_log2);
+    }
+    // After the reduce-scatter below, this lane holds the score of head
+    // `myh` of its key; the running max / sum of that head live on the lanes
+    // that own it, o (all heads, this lane's 8 dims) lives on every lane.
+    int myh = 0;
+    {
+      int cnt = G;
+#pragma unroll
+      for (int off = LPK / 2; off >= 1; off >>= 1) {
+        if (cnt > 1) {
+          cnt >>= 1;
+          if (lane & off) myh += cnt;
+        }
       }
     }
-    float m[G], l[G], o[G][8];
+    float m_me = neg_inf(), l_me = 0.f;
+    float2 o2[G][4];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o2[h][e] = make_float2(0.f, 0.f);
+    // lane (within this key's lane group) that holds head h's score
+    int src_of[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      m[h] = neg_inf();
-      l[h] = 0.f;
+      int l_in = 0, cnt = G, rem = h;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
+      for (int off = LPK / 2; off >= 1; off >>= 1) {
+        if (cnt > 1) {
+          cnt >>= 1;
+          if (rem >= cnt) { l_in |= off; rem -= cnt; }
+        }
+      }
+      src_of[h] = (lane & ~(LPK - 1)) | l_in;
     }
 
     for (int tile = 0; tile < n_tiles; ++tile) {
@@ -142,105 +167,121 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_kernel(const AttnPar
       const int kt = lo + tile * kDecodeKT;
       const T* cK = sK + st * STAGE;
       const T* cV = sV + st * STAGE;
-      float s[STEPS][G];
+      float s[STEPS];  // this lane's (key, head) score per step
 #pragma unroll
       for (int u = 0; u < STEPS; ++u) {
         const int key = warp * KPW + u * KPS + kg;
         const uint4 kr = *reinterpret_cast<const uint4*>(cK + key * D + dl * 8);
         const uint32_t wv[4] = {kr.x, kr.y, kr.z, kr.w};
-        float kf[8];
+        float2 k2[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          kf[2 * e] = DT::lo(wv[e]);
-          kf[2 * e + 1] = DT::hi(wv[e]);
-        }
+        for (int e = 0; e < 4; ++e) k2[e] = make_float2(DT::lo(wv[e]), DT::hi(wv[e]));
+        float part[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          float acc = 0.f;
+          float2 acc = __fmul2_rn(q2[h][0], k2[0]);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc = fmaf(qf[h][e], kf[e], acc);
-          s[u][h] = acc;
+          for (int e = 1; e < 4; ++e) acc = __ffma2_rn(q2[h][e], k2[e], acc);
+          part[h] = acc.x + acc.y;
         }
+        // reduce-scatter over the key's LPK lanes: halve the heads a lane
+        // keeps at each of the first log2(G) levels, then a plain butterfly
+        int cnt = G;
+#pragma unroll
+        for (int off = LPK / 2; off >= 1; off >>= 1) {
+          if (cnt > 1) {
+            const int half = cnt >> 1;
+            const bool upper = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < half; ++i) {
+              const float send = upper ? part[i] : part[half + i];
+              const float keep = upper ? part[half + i] : part[i];
+              part[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            }
+            cnt = half;
+          } else {
+            part[0] += __shfl_xor_sync(0xffffffffu, part[0], off);
+          }
+        }
+        s[u] = (kt + key < hi) ? part[0] : neg_inf();
       }
+      // stage max of my head over the warp's keys
+      float mx = s[0];
 #pragma unroll
-      for (int off = LPK / 2; off >= 1; off >>= 1)
+      for (int u = 1; u < STEPS; ++u) mx = fmaxf(mx, s[u]);
 #pragma unroll
-        for (int u = 0; u < STEPS; ++u)
-#pragma unroll
-          for (int h = 0; h < G; ++h) s[u][h] += __shfl_xor_sync(0xffffffffu, s[u][h], off);
-      float mx[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) mx[h] = neg_inf();
+      for (int off = LPK; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mn = fmaxf(m_me, mx);
+      const float mu = (mn == neg_inf()) ? 0.f : mn;
+      const float corr_me = ex2(m_me - mu);
+      m_me = mn;
+      float pu[STEPS];
+      float psum = 0.f;
 #pragma unroll
       for (int u = 0; u < STEPS; ++u) {
-        const bool in = (kt + warp * KPW + u * KPS + kg) < hi;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          if (!in) s[u][h] = neg_inf();
-          mx[h] = fmaxf(mx[h], s[u][h]);
-        }
+        pu[u] = ex2(s[u] - mu);
+        psum += pu[u];
       }
-#pragma unroll
-      for (int off = LPK; off < 32; off <<= 1)
-#pragma unroll
-        for (int h = 0; h < G; ++h) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], off));
-      float pm[G];
+      l_me = l_me * corr_me + psum;
+      // rescale o of every head by that head's correction
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const float mn = fmaxf(m[h], mx[h]);
-        const float mu = (mn == neg_inf()) ? 0.f : mn;
-        const float corr = ex2(m[h] - mu);
-        m[h] = mn;
-        pm[h] = mu;
-        l[h] *= corr;
+        const float c = __shfl_sync(0xffffffffu, corr_me, src_of[h]);
+        const float2 c2 = make_float2(c, c);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[h][e] *= corr;
+        for (int e = 0; e < 4; ++e) o2[h][e] = __fmul2_rn(o2[h][e], c2);
       }
 #pragma unroll
       for (int u = 0; u < STEPS; ++u) {
         const int key = warp * KPW + u * KPS + kg;
         const uint4 vr = *reinterpret_cast<const uint4*>(cV + key * D + dl * 8);
         const uint32_t wv[4] = {vr.x, vr.y, vr.z, vr.w};
-        float vf[8];
+        float2 v2[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          vf[2 * e] = DT::lo(wv[e]);
-          vf[2 * e + 1] = DT::hi(wv[e]);
-        }
+        for (int e = 0; e < 4; ++e) v2[e] = make_float2(DT::lo(wv[e]), DT::hi(wv[e]));
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float pr = ex2(s[u][h] - pm[h]);
-          l[h] += pr;
+          const float ph = __shfl_sync(0xffffffffu, pu[u], src_of[h]);
+          const float2 p2 = make_float2(ph, ph);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pr, vf[e], o[h][e]);
+          for (int e = 0; e < 4; ++e) o2[h][e] = __ffma2_rn(p2, v2[e], o2[h][e]);
         }
       }
     }
     cp_async_wait<0>();
 
-    // the warp's key groups share m; sum their l and o
+    // sums over the warp's key groups (they share each head's max)
+    float l_h[G], m_h[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      m_h[h] = __shfl_sync(0xffffffffu, m_me, src_of[h]);
+      l_h[h] = __shfl_sync(0xffffffffu, l_me, src_of[h]);
+    }
 #pragma unroll
     for (int off = LPK; off < 32; off <<= 1) {
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+        l_h[h] += __shfl_xor_sync(0xffffffffu, l_h[h], off);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[h][e] += __shfl_xor_sync(0xffffffffu, o[h][e], off);
+        for (int e = 0; e < 4; ++e) {
+          o2[h][e].x += __shfl_xor_sync(0xffffffffu, o2[h][e].x, off);
+          o2[h][e].y += __shfl_xor_sync(0xffffffffu, o2[h][e].y, off);
+        }
       }
     }
     if (lane == 0) {
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        sm_m[warp][h] = m[h];
-        sm_l[warp][h] = l[h];
+        sm_m[warp][h] = m_h[h];
+        sm_l[warp][h] = l_h[h];
       }
     }
     if (kg == 0) {
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         float4* dst = reinterpret_cast<float4*>(&sm_o[warp][h][dl * 8]);
-        dst[0] = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-        dst[1] = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+        dst[0] = make_float4(o2[h][0].x, o2[h][0].y, o2[h][1].x, o2[h][1].y);
+        dst[1] = make_float4(o2[h][2].x, o2[h][2].y, o2[h][3].x, o2[h][3].y);
       }
     }
     __syncthreads();
