@@ -199,7 +199,7 @@ int tile_rows_of(int kernel, int g) {
     case fi::kDecode: return g;
     case fi::kPrefillM16: return (16 / g) * g;
     case fi::kPrefillM64: return (64 / g) * g;
-    case fi::kPrefillM128: return (128 / g) * g;
+    case fi::kPrefillM128: return 2 * ((128 / g) * g);  // two 128-row Q tiles
   }
   return 0;
 }

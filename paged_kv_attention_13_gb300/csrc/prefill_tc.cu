@@ -1,32 +1,37 @@
 // Prefill kernel on the 5th-generation tensor cores: TMA page gathers into
-// 128B-swizzled shared memory, tcgen05.mma with the S and O accumulators in
-// tensor memory, one thread per query row for the online softmax.
+// 128B-swizzled shared memory, tcgen05.mma with S, P and O in tensor memory,
+// one thread per query row for the online softmax.
 //
-// Tile: 128 packed rows (query row x head in the GQA group, all heads of one
-// kv head) by 128 keys, head_dim 128, bf16 or fp16 in, fp32 accumulate.
+// A work item is two 128-row Q tiles (packed rows: query row x head in the
+// GQA group, all heads of one kv head) against a range of 128-key tiles,
+// head_dim 128, bf16 or fp16 in, fp32 accumulate. Both Q tiles use every K/V
+// tile staged in shared memory.
 //
 // Roles inside one CTA (384 threads, one CTA per SM, persistent over the work
 // items of the plan):
-//   warp 0      TMA producer: Q tile (3-D map over [tokens, heads, dim]) and,
-//               per 128-key tile, one box per page of K and of V (4-D maps over
-//               [pages, slot, kv head, dim]) straight from the paged cache;
-//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM (double-buffered),
-//               then O += P V with P read from shared memory;
-//   warps 4-11  softmax, two warpgroups: a thread owns one row of S (its TMEM
-//               lane) and one half of its columns; it masks boundary tiles,
-//               keeps the running max / sum in registers, rescales its half of
-//               O in TMEM only when the max grows by more than 2^8, writes its
-//               half of P (bf16/fp16) to shared memory, and runs the epilogue.
+//   warp 0      TMA producer: the two Q tiles (3-D map over [tokens, heads,
+//               dim]) and, per key tile, one box per page of K and of V (4-D
+//               maps over [pages, slot, kv head, dim]) straight from the
+//               paged cache, two stages;
+//   warp 1      MMA issuer (one thread): S_x = Q_x K^T into TMEM, then
+//               O_x += P_x V with P_x read from TMEM, alternating the tiles so
+//               the tensor core works on one tile while the other's softmax
+//               runs;
+//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: a thread owns
+//               one row (its TMEM lane), masks boundary tiles, keeps the
+//               running max / sum in registers, rescales O in TMEM only when
+//               the max grows by more than 2^8, writes P over its S columns,
+//               and runs the epilogue.
 // Every mbarrier wait is bounded in time; on expiry the CTA records an error
-// in the workspace header, stops issuing work, waits for its own copies in
-// flight, frees its tensor memory and exits.
+// in the workspace header, stops issuing work, waits for its own copies and
+// MMAs in flight, frees its tensor memory and exits.
 //
 // Mask ("Route non-causal windowed prefill to AITER's masked kernel" (#339),
 // "Why window_size_right stays -1"; "Support speculative-decode verify on
 // ROCm ..." (#362), "Summary"): key j of query row i is kept when
-// (!causal || j <= i + Lk - Lq) && (wl < 0 || j + Lq + wl >= Lk + i). Tiles
-// outside the tile's live key range are never loaded; the per-element test
-// runs on tiles that straddle a bound only.
+// (!causal || j <= i + Lk - Lq) && (wl < 0 || j + Lq + wl >= Lk + i). Key
+// tiles outside the item's live range are never loaded; the per-element
+// test runs on tiles that straddle a bound only.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -37,16 +42,15 @@ namespace {
 constexpr int kTcThreads = 384;  // 4 control warps + 2 softmax warpgroups
 constexpr int kBlk = 128 * 128;       // 128 rows x 128 bytes: one 64-column swizzled block
 constexpr int kTile = 2 * kBlk;       // 128 x 128 16-bit elements
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTile;  // 2 stages
+constexpr int kOffQ = 0;              // Q tiles A and B
+constexpr int kOffK = kOffQ + 2 * kTile;  // 2 stages
 constexpr int kOffV = kOffK + 2 * kTile;
-constexpr int kOffP = kOffV + 2 * kTile;
-constexpr int kOffBar = kOffP + kTile;
-constexpr int kSmemTc = kOffBar + 256 + 2048 + 1024;  // barriers, row sums, alignment slack
+constexpr int kOffBar = kOffV + 2 * kTile;
+constexpr int kSmemTc = kOffBar + 256 + 1024;  // barriers, alignment slack
 
 // barrier slots
-constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KVFULL = 2, B_KVEMPTY = 4, B_SFULL = 6, B_SFREE = 8,
-              B_PFULL = 10, B_ODONE = 11, B_OFREE = 12, B_FINAL = 13, B_LSUM = 14, N_BARS = 15;
+constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KVFULL = 2, B_KVEMPTY = 4, B_SFULL = 6, B_PFULL = 8,
+              B_ODONE = 10, B_OFREE = 12, B_FINAL = 14, N_BARS = 15;
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
@@ -209,6 +213,33 @@ __device__ __forceinline__ ItemGeom item_geom(const WorkItem& it, const int32_t*
   return G;
 }
 
+// 16 packed columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+// O += P V with P (the A operand) read from tensor memory.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Two Q tiles per CTA (A: packed rows [row0, row0+tr), B: the next tr rows)
+// share every K/V tile, which halves the K/V bytes per FLOP. The tensor core
+// alternates between them - S_A(j+1) and PV_B(j) run while softmax A works,
+// PV_A(j+1) and S_B(j+1) while softmax B works - and P is written back into
+// tensor memory over the S columns it came from.
 template <bool BF16>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tq,
@@ -239,7 +270,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int g = hdr->group;
   const int causal = hdr->causal;
   const int wl = hdr->window_left;
-  const int tile_rows = hdr->tile_rows;
+  const int tile_rows = hdr->tile_rows;  // two Q tiles
+  const int tr = tile_rows / 2;          // rows of one Q tile
   const int Hq = p.num_qo_heads;
 
   if (threadIdx.x == 0) {
@@ -249,13 +281,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(BAR(B_KVFULL + s), 1);
       mbar_init(BAR(B_KVEMPTY + s), 1);
       mbar_init(BAR(B_SFULL + s), 1);
-      mbar_init(BAR(B_SFREE + s), 256);
+      mbar_init(BAR(B_PFULL + s), 128);
+      mbar_init(BAR(B_ODONE + s), 1);
+      mbar_init(BAR(B_OFREE + s), 128);
     }
-    mbar_init(BAR(B_PFULL), 256);
-    mbar_init(BAR(B_ODONE), 1);
-    mbar_init(BAR(B_OFREE), 256);
     mbar_init(BAR(B_FINAL), 1);
-    mbar_init(BAR(B_LSUM), 256);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -276,7 +306,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Lane 0 owns the barriers; for each tile every lane fetches one page
+    // Lane 0 owns the barriers; for each K/V tile every lane fetches one page
     // index (up to 8 pages per tile) and issues that page's boxes.
     int gt = 0, qc = 0;
     bool kv_armed[2] = {false, false};
@@ -284,19 +314,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool q_armed = false;
     uint32_t q_par = 0;
     bool ok = true;
-    const int npg = 128 / kv_box_rows;  // pages (boxes) per tile
+    const int npg = 128 / kv_box_rows;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
       if (G.n_tiles == 0) continue;
+      const bool hasB = G.n_rows > tr;
       if (lane == 0) {
         if (qc > 0 && !mbar_wait(BAR(B_QEMPTY), (qc - 1) & 1, abort_flag)) ok = false;
         if (ok) {
-          mbar_expect_tx(BAR(B_QFULL), 2u * uint32_t(tile_rows) * 128u);
+          mbar_expect_tx(BAR(B_QFULL), (hasB ? 2u : 1u) * 2u * uint32_t(tr) * 128u);
           q_armed = true;
           q_par = qc & 1;
-          for (int h = 0; h < 2; ++h)
-            tma_load_3d(sbase + kOffQ + h * kBlk, &tq, BAR(B_QFULL), h * 64, G.hk * g,
-                        G.token0 + G.i0);
+          for (int x = 0; x < (hasB ? 2 : 1); ++x)
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(sbase + kOffQ + x * kTile + h * kBlk, &tq, BAR(B_QFULL), h * 64,
+                          G.hk * g, G.token0 + G.i0 + x * (tr / g));
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -347,49 +379,76 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(BF16, false, 128, 128);
       constexpr uint32_t kIdO = idesc_f16(BF16, true, 128, 128);
-      const uint32_t tS = tmem, tO = tmem + 256;
-      int gt = 0, qc = 0;
+      auto issue_s = [&](int x, int st) {  // S_x = Q_x K^T
+        const uint32_t d = tmem + uint32_t(x) * 128u;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t koff = uint32_t(kk >> 2) * kBlk + uint32_t(kk & 3) * 32u;
+          const uint64_t ad = sdesc_sw128(sbase + kOffQ + x * kTile + koff, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sbase + kOffK + st * kTile + koff, 16, 1024);
+          tc_mma(d, ad, bd, kIdS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(BAR(B_SFULL + x));
+      };
+      auto issue_pv = [&](int x, int st, bool acc) {  // O_x += P_x V
+        const uint32_t d = tmem + 256u + uint32_t(x) * 128u;
+        const uint32_t a = tmem + uint32_t(x) * 128u;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bd = sdesc_sw128(sbase + kOffV + st * kTile + uint32_t(kk) * 2048u, kBlk, 1024);
+          tc_mma_ts(d, a + uint32_t(kk) * 8u, bd, kIdO, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      int gt = 0, qc = 0, cnt[2] = {0, 0}, itc[2] = {0, 0};
       bool ok = true;
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
         const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
         if (G.n_tiles == 0) continue;
+        const bool hasB = G.n_rows > tr;
+        const int n = G.n_tiles;
         if (!mbar_wait(BAR(B_QFULL), qc & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(BAR(B_KVFULL + (gt & 1)), (gt >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        for (int t = 0; t <= G.n_tiles && ok; ++t) {
-          if (t < G.n_tiles) {
-            const int g1 = gt + t, st = g1 & 1;
-            if (!mbar_wait(BAR(B_KVFULL + st), (g1 >> 1) & 1, abort_flag)) { ok = false; break; }
-            if (g1 >= 2 && !mbar_wait(BAR(B_SFREE + st), ((g1 >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+        issue_s(0, gt & 1);
+        if (hasB) issue_s(1, gt & 1);
+        if (n == 1) tc_commit(BAR(B_QEMPTY));
+        for (int j = 0; j < n && ok; ++j) {
+          const int g1 = gt + j, st = g1 & 1, st1 = (g1 + 1) & 1;
+          // ---- tile A
+          if (j == 0 && itc[0] > 0 && !mbar_wait(BAR(B_OFREE), (itc[0] - 1) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(BAR(B_PFULL), (cnt[0] + j) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(0, st, j > 0);
+          if (j == n - 1) tc_commit(BAR(B_ODONE));
+          if (!hasB) tc_commit(BAR(B_KVEMPTY + st));
+          if (j + 1 < n) {
+            if (!mbar_wait(BAR(B_KVFULL + st1), ((g1 + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t koff = uint32_t(kk >> 2) * kBlk + uint32_t(kk & 3) * 32u;
-              const uint64_t ad = sdesc_sw128(sbase + kOffQ + koff, 16, 1024);
-              const uint64_t bd = sdesc_sw128(sbase + kOffK + st * kTile + koff, 16, 1024);
-              tc_mma(tS + uint32_t(st) * 128u, ad, bd, kIdS, kk > 0 ? 1u : 0u);
-            }
-            tc_commit(BAR(B_SFULL + st));
-            if (t == G.n_tiles - 1) tc_commit(BAR(B_QEMPTY));
+            issue_s(0, st1);
+            if (!hasB && j + 1 == n - 1) tc_commit(BAR(B_QEMPTY));
           }
-          if (t >= 1) {
-            const int g0 = gt + t - 1, st0 = g0 & 1;
-            if (t == 1 && qc > 0 && !mbar_wait(BAR(B_OFREE), (qc - 1) & 1, abort_flag)) { ok = false; break; }
-            if (!mbar_wait(BAR(B_PFULL), g0 & 1, abort_flag)) { ok = false; break; }
+          // ---- tile B
+          if (hasB) {
+            if (j == 0 && itc[1] > 0 && !mbar_wait(BAR(B_OFREE + 1), (itc[1] - 1) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_PFULL + 1), (cnt[1] + j) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t aoff = uint32_t(kk >> 2) * kBlk + uint32_t(kk & 3) * 32u;
-              const uint64_t ad = sdesc_sw128(sbase + kOffP + aoff, 16, 1024);
-              const uint64_t bd = sdesc_sw128(sbase + kOffV + st0 * kTile + uint32_t(kk) * 2048u,
-                                              kBlk, 1024);
-              tc_mma(tO, ad, bd, kIdO, (t > 1 || kk > 0) ? 1u : 0u);
+            issue_pv(1, st, j > 0);
+            tc_commit(BAR(B_KVEMPTY + st));
+            if (j == n - 1) tc_commit(BAR(B_ODONE + 1));
+            if (j + 1 < n) {
+              issue_s(1, st1);
+              if (j + 1 == n - 1) tc_commit(BAR(B_QEMPTY));
             }
-            tc_commit(BAR(B_ODONE));
-            tc_commit(BAR(B_KVEMPTY + st0));
           }
         }
-        gt += G.n_tiles;
+        gt += n;
         ++qc;
+        cnt[0] += n;
+        ++itc[0];
+        if (hasB) {
+          cnt[1] += n;
+          ++itc[1];
+        }
       }
       // every MMA this thread issued has completed before tensor memory is freed
       tc_commit(BAR(B_FINAL));
@@ -399,200 +458,192 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
-    // Two warpgroups share every row: both read the whole S row (for the row
-    // max, so both take the same rescale decision), each exponentiates, writes
-    // P for and rescales O over its own 64 columns.
-    const int half = (warp - 4) >> 2;      // column half of this warpgroup
+    const int x = (warp - 4) >> 2;         // Q tile of this warpgroup
     const int sw = warp & 3;               // TMEM lane quadrant
-    const int r = sw * 32 + lane;          // packed row of this thread
+    const int r = sw * 32 + lane;          // row within the Q tile
     const uint32_t lane_addr = uint32_t(sw * 32) << 16;
-    const uint32_t tS = tmem + lane_addr, tO = tmem + lane_addr + 256 + uint32_t(half) * 64u;
-    float* l_share = reinterpret_cast<float*>(smem + kOffBar + 256);  // [2 buffers][2 halves][128]
-    // every wait here is warp-uniform, so a timeout never splits a warp
-    // in front of a .sync.aligned instruction
+    const uint32_t tS = tmem + lane_addr + uint32_t(x) * 128u;
+    const uint32_t tO = tmem + lane_addr + 256u + uint32_t(x) * 128u;
+    const float scale = p.sm_scale_log2;
+    // every wait here is warp-uniform, so a timeout never splits a warp in
+    // front of a .sync.aligned instruction
     auto wwait = [&](uint32_t bar, uint32_t parity) {
       const bool okl = mbar_wait(bar, parity, abort_flag);
       return __all_sync(0xffffffffu, okl);
     };
-    int xc = 0;  // row-sum exchanges so far
-    const float scale = p.sm_scale_log2;
-    int gt = 0;
+    int gt = 0, cnt = 0, itc = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
-      const bool row_ok = r < G.n_rows;
-      const int pr = G.row0 + r;
+      const bool hasB = G.n_rows > tr;
+      const int n = G.n_tiles;
+      const int nx = x == 0 ? min(tr, G.n_rows) : max(0, G.n_rows - tr);  // rows of my tile
+      const bool active = n > 0 && (x == 0 || hasB);
+      const bool row_ok = r < nx;
+      const int pr = G.row0 + x * tr + r;
       const int qi = pr / g;
       const int tok = G.token0 + qi;
       const int head = G.hk * g + pr % g;
+      const bool direct = G.chunk < 0;
+      const int slot = direct ? 0 : G.partial_base + (qi - G.i0) * G.num_chunks + G.chunk;
+      if (!active) {
+        if (n == 0 && row_ok) {  // no live key: o = 0, lse = -inf
+          if (direct) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (int64_t(tok) * Hq + head) * 128);
+            for (int q = 0; q < 16; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+            if (p.lse) p.lse[int64_t(tok) * Hq + head] = neg_inf();
+          } else {
+            float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * 128);
+            for (int q = 0; q < 32; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            tmp_lse[int64_t(slot) * Hq + head] = neg_inf();
+          }
+        }
+        gt += n;
+        continue;
+      }
       // this row's live keys: [jmin, jmax]
       int jmin = G.kv_lo, jmax = G.kv_hi - 1;
       if (wl >= 0) jmin = max(jmin, G.lk - G.lq + qi - wl);
       if (causal) jmax = min(jmax, qi + G.lk - G.lq);
-      const int i1 = (G.row0 + G.n_rows) / g - 1;
+      const int ix0 = (G.row0 + x * tr) / g;              // first / last query row of my tile
+      const int ix1 = (G.row0 + x * tr + nx) / g - 1;
       float m_run = neg_inf(), l_run = 0.f;
-      for (int t = 0; t < G.n_tiles; ++t) {
-        const int g1 = gt + t, st = g1 & 1;
-        const int t0 = G.t_start + t * 128;
-        if (!wwait(BAR(B_SFULL + st), (g1 >> 1) & 1)) { ok = false; break; }
+      for (int j = 0; j < n; ++j) {
+        const int g1 = gt + j, st = g1 & 1;
+        const int t0 = G.t_start + j * 128;
+        if (!wwait(BAR(B_SFULL + x), (cnt + j) & 1)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sr[4][32];  // [0..1] this half's columns, [2..3] the other half's
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          tmem_ld32(tS + uint32_t(st) * 128u + uint32_t(half * 64 + c * 32), sr[c]);
-          tmem_ld32(tS + uint32_t(st) * 128u + uint32_t((1 - half) * 64 + c * 32), sr[2 + c]);
-        }
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(BAR(B_SFREE + st));
         const bool need_mask = (t0 < G.kv_lo) || (t0 + 128 > G.kv_hi) ||
-                               (causal && t0 + 127 > G.i0 + G.lk - G.lq) ||
-                               (wl >= 0 && t0 < G.lk - G.lq + i1 - wl);
-        if (need_mask) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int cb = t0 + ((c < 2) ? half : 1 - half) * 64 + (c & 1) * 32;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int j = cb + e;
-              if (j < jmin || j > jmax) sr[c][e] = __float_as_uint(neg_inf());
-            }
-          }
-        }
-        // row max of the raw scores, eight independent chains
+                               (causal && t0 + 127 > ix0 + G.lk - G.lq) ||
+                               (wl >= 0 && t0 < G.lk - G.lq + ix1 - wl);
+        // pass 1: row max of the raw scores
         float mp[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) mp[q] = neg_inf();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tS + uint32_t(c) * 32u, v);
+          tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(sr[c][e]));
+          for (int e = 0; e < 32; ++e) {
+            float xv = __uint_as_float(v[e]);
+            if (need_mask) {
+              const int jj = t0 + c * 32 + e;
+              if (jj < jmin || jj > jmax) xv = neg_inf();
+            }
+            mp[e & 7] = fmaxf(mp[e & 7], xv);
+          }
+        }
         const float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                                  fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-        const float mx = mraw * scale;  // scale > 0, so this is the max of the scaled row
+        const float mx = mraw * scale;  // scale > 0
         float m_new = m_run;
         if (mx > m_run + 8.f || (m_run == neg_inf() && mraw != neg_inf())) m_new = mx;
         const float corr = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
         const float mu = (m_new == neg_inf()) ? 0.f : m_new;
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[2][16];
+        // O rescale: S_x(j) is complete, so the P V product before it is too
+        if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + uint32_t(c) * 32u, ov);
+            tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * e]), scale, -mu));
-            const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * e + 1]), scale, -mu));
-            ps[e & 3] += p0 + p1;
-            pk[c][e] = DT::pack(p0, p1);
-          }
-        l_run = l_run * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-        m_run = m_new;
-        if (t > 0) {
-          // the previous P V product has finished: O may be rescaled, P rewritten
-          if (!wwait(BAR(B_ODONE), (g1 - 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              uint32_t ov[32];
-              tmem_ld32(tO + uint32_t(c) * 32u, ov);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
-              tmem_st32(tO + uint32_t(c) * 32u, ov);
-            }
-            tmem_wait_st();
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
+            tmem_st32(tO + uint32_t(c) * 32u, ov);
           }
         }
-        if (t0 + 128 > G.lk) {
+        bool zeroed = false;
+        if (x == 0 && t0 + 128 > G.lk) {
           // rows of V past the request's last key may hold anything: zero them
           if (!wwait(BAR(B_KVFULL + st), (g1 >> 1) & 1)) { ok = false; break; }
           if (t0 + r >= G.lk) {
-            uint4* row = reinterpret_cast<uint4*>(smem + kOffV + st * kTile + half * kBlk + r * 128);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) row[q] = make_uint4(0, 0, 0, 0);
-          }
-        }
-        // P row r, this half's 64 keys: one 128-byte swizzled block
+            for (int h = 0; h < 2; ++h) {
+              uint4* row = reinterpret_cast<uint4*>(smem + kOffV + st * kTile + h * kBlk + r * 128);
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint4* dst = reinterpret_cast<uint4*>(smem + kOffP + half * kBlk + r * 128 +
-                                                ((cc ^ (r & 7)) << 4));
-          *dst = make_uint4(pk[cc >> 2][(cc & 3) * 4 + 0], pk[cc >> 2][(cc & 3) * 4 + 1],
-                            pk[cc >> 2][(cc & 3) * 4 + 2], pk[cc >> 2][(cc & 3) * 4 + 3]);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc_fence_before();
-        mbar_arrive(BAR(B_PFULL));
-      }
-      if (!ok) break;
-      // epilogue: combine the two halves' row sums (double-buffered exchange
-      // through shared memory, ordered by an mbarrier with a bounded wait)
-      float l_tot = l_run;
-      if (G.n_tiles > 0) {
-        float* buf = l_share + (xc & 1) * 256;
-        buf[half * 128 + r] = l_run;
-        mbar_arrive(BAR(B_LSUM));
-        if (!wwait(BAR(B_LSUM), xc & 1)) { ok = false; break; }
-        l_tot += buf[(1 - half) * 128 + r];
-        ++xc;
-      }
-      const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-      const float lse = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : neg_inf();
-      const bool direct = G.chunk < 0;
-      const int slot = direct ? 0 : G.partial_base + (qi - G.i0) * G.num_chunks + G.chunk;
-      if (G.n_tiles > 0) {
-        const int g_last = gt + G.n_tiles - 1;
-        if (!wwait(BAR(B_ODONE), g_last & 1)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(tO + uint32_t(c) * 32u, ov);
-          tmem_wait_ld();
-          const int col = half * 64 + c * 32;
-          if (row_ok) {
-            if (direct) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) +
-                                                    (int64_t(tok) * Hq + head) * 128 + col);
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                dst[q] = make_uint4(
-                    DT::pack(__uint_as_float(ov[8 * q + 0]) * inv, __uint_as_float(ov[8 * q + 1]) * inv),
-                    DT::pack(__uint_as_float(ov[8 * q + 2]) * inv, __uint_as_float(ov[8 * q + 3]) * inv),
-                    DT::pack(__uint_as_float(ov[8 * q + 4]) * inv, __uint_as_float(ov[8 * q + 5]) * inv),
-                    DT::pack(__uint_as_float(ov[8 * q + 6]) * inv, __uint_as_float(ov[8 * q + 7]) * inv));
-            } else {
-              float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * 128 + col);
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                dst[q] = make_float4(__uint_as_float(ov[4 * q]) * inv, __uint_as_float(ov[4 * q + 1]) * inv,
-                                     __uint_as_float(ov[4 * q + 2]) * inv, __uint_as_float(ov[4 * q + 3]) * inv);
+              for (int q = 0; q < 8; ++q) row[q] = make_uint4(0, 0, 0, 0);
             }
           }
+          zeroed = true;
         }
+        // pass 2: P = exp2(s * scale - m), packed, back into the S columns
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tS + uint32_t(c) * 32u, v);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float s0 = __uint_as_float(v[2 * e]), s1 = __uint_as_float(v[2 * e + 1]);
+            if (need_mask) {
+              const int jj = t0 + c * 32 + 2 * e;
+              if (jj < jmin || jj > jmax) s0 = neg_inf();
+              if (jj + 1 < jmin || jj + 1 > jmax) s1 = neg_inf();
+            }
+            const float p0 = ex2(fmaf(s0, scale, -mu));
+            const float p1 = ex2(fmaf(s1, scale, -mu));
+            ps[e & 3] += p0 + p1;
+            pk[e] = DT::pack(p0, p1);
+          }
+          tmem_st16(tS + uint32_t(c) * 16u, pk);
+        }
+        tmem_wait_st();
+        l_run = l_run * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+        m_run = m_new;
+        if (zeroed) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
-        mbar_arrive(BAR(B_OFREE));
-      } else if (row_ok) {
-        const int col = half * 64;
-        if (direct) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (int64_t(tok) * Hq + head) * 128 + col);
-          for (int q = 0; q < 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);
-        } else {
-          float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * 128 + col);
-          for (int q = 0; q < 16; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        mbar_arrive(BAR(B_PFULL + x));
+      }
+      if (!ok) break;
+      // epilogue
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float lse = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : neg_inf();
+      if (!wwait(BAR(B_ODONE + x), itc & 1)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tO + uint32_t(c) * 32u, ov);
+        tmem_wait_ld();
+        if (row_ok) {
+          if (direct) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) +
+                                                  (int64_t(tok) * Hq + head) * 128 + c * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(
+                  DT::pack(__uint_as_float(ov[8 * q + 0]) * inv, __uint_as_float(ov[8 * q + 1]) * inv),
+                  DT::pack(__uint_as_float(ov[8 * q + 2]) * inv, __uint_as_float(ov[8 * q + 3]) * inv),
+                  DT::pack(__uint_as_float(ov[8 * q + 4]) * inv, __uint_as_float(ov[8 * q + 5]) * inv),
+                  DT::pack(__uint_as_float(ov[8 * q + 6]) * inv, __uint_as_float(ov[8 * q + 7]) * inv));
+          } else {
+            float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * 128 + c * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(__uint_as_float(ov[4 * q]) * inv, __uint_as_float(ov[4 * q + 1]) * inv,
+                                   __uint_as_float(ov[4 * q + 2]) * inv, __uint_as_float(ov[4 * q + 3]) * inv);
+          }
         }
       }
-      if (row_ok && half == 0) {
+      tc_fence_before();
+      mbar_arrive(BAR(B_OFREE + x));
+      if (row_ok) {
         if (direct) {
           if (p.lse) p.lse[int64_t(tok) * Hq + head] = lse;
         } else {
           tmp_lse[int64_t(slot) * Hq + head] = lse;
         }
       }
-      gt += G.n_tiles;
+      gt += n;
+      cnt += n;
+      ++itc;
     }
   }
+
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -655,7 +706,7 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int head_dim, int group, int 
   {
     cuuint64_t dims[3] = {cuuint64_t(head_dim), cuuint64_t(p.num_qo_heads), cuuint64_t(q_rows)};
     cuuint64_t str[2] = {cuuint64_t(p.q_stride_head) * 2, cuuint64_t(p.q_stride_tok) * 2};
-    cuuint32_t box[3] = {64, cuuint32_t(group), cuuint32_t(tile_rows / group)};
+    cuuint32_t box[3] = {64, cuuint32_t(group), cuuint32_t(tile_rows / 2 / group)};
     if (!encode(&tq, bf16, 3, p.q, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
