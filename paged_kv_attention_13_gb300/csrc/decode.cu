@@ -211,9 +211,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_kernel(const AttnPar
       for (int u = 1; u < STEPS; ++u) mx = fmaxf(mx, s[u]);
 #pragma unroll
       for (int off = LPK; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float mn = fmaxf(m_me, mx);
+      // lazy max: the reference moves only when the stage max exceeds it by
+      // more than 2^8 (p stays <= 256), so o is rarely rescaled
+      float mn = m_me;
+      if (mx > m_me + 8.f || (m_me == neg_inf() && mx != neg_inf())) mn = mx;
+      const float corr_me = (mn == m_me) ? 1.f : ex2(m_me - mn);
       const float mu = (mn == neg_inf()) ? 0.f : mn;
-      const float corr_me = ex2(m_me - mu);
       m_me = mn;
       float pu[STEPS];
       float psum = 0.f;
@@ -224,12 +227,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_kernel(const AttnPar
       }
       l_me = l_me * corr_me + psum;
       // rescale o of every head by that head's correction
+      if (__any_sync(0xffffffffu, corr_me != 1.f)) {
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float c = __shfl_sync(0xffffffffu, corr_me, src_of[h]);
-        const float2 c2 = make_float2(c, c);
+        for (int h = 0; h < G; ++h) {
+          const float c = __shfl_sync(0xffffffffu, corr_me, src_of[h]);
+          const float2 c2 = make_float2(c, c);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o2[h][e] = __fmul2_rn(o2[h][e], c2);
+          for (int e = 0; e < 4; ++e) o2[h][e] = __fmul2_rn(o2[h][e], c2);
+        }
       }
 #pragma unroll
       for (int u = 0; u < STEPS; ++u) {
