@@ -287,6 +287,17 @@ def cpu_oracle_sample(pb, causal, wl, budget_s=12.0, seed=1):
     return full_s, done_rows, t_used
 
 
+def aggregate_ranks(ms_local, bytes_per_rank, world, device):
+    """Whole-job rate of N replicas: the step time is the max over ranks, the
+    bytes are every rank's. Returns (ms_max, GB/s)."""
+    import torch.distributed as dist
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    return ms, world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def run_ours(args):
     import torch.distributed as dist
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -314,11 +325,7 @@ def run_ours(args):
         ms_mean, ms_med = r.time(args.steps, args.warmup)
     if world > 1:
         dist.barrier()
-    t = torch.tensor([ms_mean], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_step = float(t.item())
-    value = world * r.bytes / (ms_step * 1e-3) / 1e9
+    ms_step, value = aggregate_ranks(ms_mean, r.bytes, world, dev)
     e2e_ms, h2d, d2h = r.time_e2e(max(3, args.steps // 2), 2)
     e2e_value = world * r.bytes / (e2e_ms * 1e-3) / 1e9
     achieved = r.bytes / (ms_step * 1e-3) / 1e9
@@ -447,6 +454,8 @@ PROFILE_CASES = {
     "verify_b32": (lambda: workloads.speculative_verify(batch=32), True, -1, "verify"),
     "prefill_p16_causal": (lambda: workloads.batch_prefill(page_size=16), True, -1, "prefill"),
     "prefill_b4_causal": (lambda: workloads.batch_prefill(page_size=16, batch=4), True, -1, "prefill"),
+    "prefill_p1024_causal": (lambda: workloads.batch_prefill(page_size=1024), True, -1, "prefill"),
+    "prefill_p16_noncausal": (lambda: workloads.batch_prefill(page_size=16), False, -1, "prefill"),
     "longctx_causal": (lambda: workloads.long_context(), True, -1, "prefill"),
 }
 

@@ -6,8 +6,9 @@
 // A tile packs query rows and the GQA group: packed row r = query row * g +
 // head in group, all heads of one kv head, so every K/V tile staged in shared
 // memory serves g query heads. K/V rows are gathered page by page straight
-// from the cache with cp.async (16-byte, double-buffered, XOR-swizzled
-// shared memory) - no contiguous copy of the cache is ever made.
+// from the cache with cp.async (16-byte, XOR-swizzled
+// shared memory, a 2-stage ring) - no contiguous copy of the cache is ever
+// made.
 //
 // Mask [P1 "Why window_size_right stays -1"], [P2 "Summary"] for query row i
 // and key j: (!causal || j <= i + Lk - Lq) && (wl < 0 || j + Lq + wl >= Lk + i).
@@ -35,7 +36,8 @@ struct MmaCfg {
   static constexpr int CH = D / 8;         // 16-byte chunks per row
   static constexpr int Q_ELEMS = M * D;
   static constexpr int KV_ELEMS = kN * D;
-  static constexpr int SMEM_BYTES = (Q_ELEMS + 4 * KV_ELEMS) * 2;
+  static constexpr int STAGES = 2;  // cp.async ring depth
+  static constexpr int SMEM_BYTES = (Q_ELEMS + 2 * STAGES * KV_ELEMS) * 2;
 };
 
 // XOR swizzle of 16-byte chunks inside a row (conflict-free ldmatrix)
@@ -48,8 +50,8 @@ __global__ void __launch_bounds__(kThreads) prefill_mma_kernel(const AttnParams 
   using T = typename DT::T;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   T* sQ = reinterpret_cast<T*>(smem_raw);
-  T* sK = sQ + C::Q_ELEMS;            // [2][kN][D]
-  T* sV = sK + 2 * C::KV_ELEMS;       // [2][kN][D]
+  T* sK = sQ + C::Q_ELEMS;                 // [STAGES][kN][D]
+  T* sV = sK + C::STAGES * C::KV_ELEMS;    // [STAGES][kN][D]
 
   const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
   const int n_items = hdr->n_items;
@@ -119,9 +121,13 @@ __global__ void __launch_bounds__(kThreads) prefill_mma_kernel(const AttnParams 
         cp_async16(smem_u32(dv + r * D + swz(r, c) * 8), vs, bytes);
       }
     };
-    if (kv_lo < kv_hi) load_kv(0, kv_lo);
-    cp_async_commit();
-    cp_async_wait<0>();
+    const int n_kt = kv_lo < kv_hi ? (kv_hi - kv_lo + kN - 1) / kN : 0;
+#pragma unroll
+    for (int s = 0; s < C::STAGES - 1; ++s) {
+      if (s < n_kt) load_kv(s, kv_lo + s * kN);
+      cp_async_commit();  // group s (group 0 also carries Q)
+    }
+    cp_async_wait<C::STAGES - 2>();
     __syncthreads();
 
     uint32_t qa[C::KD][4];
@@ -142,13 +148,16 @@ __global__ void __launch_bounds__(kThreads) prefill_mma_kernel(const AttnParams 
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) qi[hr] = (it.row0 + wm * 16 + qr + hr * 8) / g;
 
-    int stage = 0;
-    for (int kt = kv_lo; kt < kv_hi; kt += kN) {
-      const bool more = kt + kN < kv_hi;
-      if (more) load_kv(stage ^ 1, kt + kN);
-      cp_async_commit();
-      if (more) cp_async_wait<1>(); else cp_async_wait<0>();
-      __syncthreads();
+    for (int t = 0; t < n_kt; ++t) {
+      const int kt = kv_lo + t * kN;
+      cp_async_wait<C::STAGES - 2>();  // tile t has landed
+      __syncthreads();                 // and every warp is done with tile t - 1
+      {
+        const int nt = t + C::STAGES - 1;
+        if (nt < n_kt) load_kv(nt % C::STAGES, kv_lo + nt * kN);
+        cp_async_commit();
+      }
+      const int stage = t % C::STAGES;
       const T* cK = sK + stage * C::KV_ELEMS;
       const T* cV = sV + stage * C::KV_ELEMS;
 
@@ -233,9 +242,9 @@ __global__ void __launch_bounds__(kThreads) prefill_mma_kernel(const AttnParams 
           mma16816<BF16>(o[2 * dn + 1], pa, b2, b3);
         }
       }
-      __syncthreads();
-      stage ^= 1;
     }
+    cp_async_wait<0>();
+    __syncthreads();
 
     // row sums across the quad
 #pragma unroll

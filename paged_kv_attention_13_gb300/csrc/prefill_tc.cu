@@ -12,7 +12,7 @@
 //   warp 0      TMA producer: the two Q tiles (3-D map over [tokens, heads,
 //               dim]) and, per key tile, one box per page of K and of V (4-D
 //               maps over [pages, slot, kv head, dim]) straight from the
-//               paged cache, two stages;
+//               paged cache; two K and two V stages, released separately;
 //   warp 1      MMA issuer (one thread): S_x = Q_x K^T into TMEM, then
 //               O_x += P_x V with P_x read from TMEM, alternating the tiles so
 //               the tensor core works on one tile while the other's softmax
@@ -49,8 +49,8 @@ constexpr int kOffBar = kOffV + 2 * kTile;
 constexpr int kSmemTc = kOffBar + 256 + 1024;  // barriers, alignment slack
 
 // barrier slots
-constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KVFULL = 2, B_KVEMPTY = 4, B_SFULL = 6, B_PFULL = 8,
-              B_ODONE = 10, B_OFREE = 12, B_FINAL = 14, N_BARS = 15;
+constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 4, B_VFULL = 6, B_VEMPTY = 8,
+              B_SFULL = 10, B_PFULL = 12, B_ODONE = 14, B_OFREE = 16, B_FINAL = 18, N_BARS = 19;
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
@@ -163,6 +163,46 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld_tied16(uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+        "+r"(r[14]), "+r"(r[15])
+      :
+      : "memory");
+}
+// 8 packed columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+// Wait for outstanding TMEM loads; the registers of `r` are tied to the wait,
+// so no use of them can be scheduled above it.
+__device__ __forceinline__ void tmem_wait_ld_tied(uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+        "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+        "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+        "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+      :
+      : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -278,8 +318,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(BAR(B_QFULL), 1);
     mbar_init(BAR(B_QEMPTY), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(BAR(B_KVFULL + s), 1);
-      mbar_init(BAR(B_KVEMPTY + s), 1);
+      mbar_init(BAR(B_KFULL + s), 1);
+      mbar_init(BAR(B_KEMPTY + s), 1);
+      mbar_init(BAR(B_VFULL + s), 1);
+      mbar_init(BAR(B_VEMPTY + s), 1);
       mbar_init(BAR(B_SFULL + s), 1);
       mbar_init(BAR(B_PFULL + s), 128);
       mbar_init(BAR(B_ODONE + s), 1);
@@ -306,19 +348,58 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Lane 0 owns the barriers; for each K/V tile every lane fetches one page
-    // index (up to 8 pages per tile) and issues that page's boxes.
-    int gt = 0, qc = 0;
-    bool kv_armed[2] = {false, false};
-    uint32_t kv_par[2] = {0, 0};
+    // Lane 0 owns the barriers; for each K or V tile every lane fetches one
+    // page index (up to 8 pages per tile) and issues that page's boxes. K and
+    // V stages are released separately (K after the S products, V after the
+    // P V products), and K is issued one tile ahead of V.
+    int gk = 0, gv = 0, qc = 0;
+    bool armed[2][2] = {{false, false}, {false, false}};
+    uint32_t apar[2][2] = {{0, 0}, {0, 0}};
     bool q_armed = false;
     uint32_t q_par = 0;
     bool ok = true;
     const int npg = 128 / kv_box_rows;
+    const int tiles_per_batch = 32 / npg;  // page indices the warp holds per batch of tiles
+    // issue K (which = 0) or V (which = 1) of tile t, whose page index this
+    // lane holds in `page` (valid when `has`)
+    auto load = [&](int which, const ItemGeom& G, int t, int cntr, bool has, int page,
+                    int nvalid) {
+      const int st = cntr & 1;
+      const int t0 = G.t_start + t * 128;
+      const int full = which ? B_VFULL : B_KFULL, empty = which ? B_VEMPTY : B_KEMPTY;
+      bool okl = true;
+      if (lane == 0) {
+        if (cntr >= 2 && !mbar_wait(BAR(empty + st), ((cntr >> 1) - 1) & 1, abort_flag)) okl = false;
+        if (okl) {
+          mbar_expect_tx(BAR(full + st), uint32_t(nvalid) * uint32_t(kv_box_rows) * 128u * 2u);
+          armed[which][st] = true;
+          apar[which][st] = (cntr >> 1) & 1;
+        }
+      }
+      okl = __shfl_sync(0xffffffffu, okl, 0);
+      if (okl && has) {
+        const int slot0 = (kv_box_rows == 128) ? (t0 % p.page_size) : 0;
+        const uint32_t roff = uint32_t(lane * kv_box_rows) * 128u;
+        const uint32_t dst = sbase + (which ? kOffV : kOffK) + st * kTile + roff;
+        for (int h = 0; h < 2; ++h)
+          tma_load_4d(dst + h * kBlk, which ? &tv : &tk, BAR(full + st), h * 64, G.hk, slot0, page);
+      }
+      return okl;
+    };
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
       if (G.n_tiles == 0) continue;
       const bool hasB = G.n_rows > tr;
+      const int32_t* pages = p.kv_indices + kv_indptr[G.b];
+      const int n_pages = kv_indptr[G.b + 1] - kv_indptr[G.b];
+      // page index of lane L for batch bt: tile bt * tiles_per_batch + L / npg,
+      // its page L % npg (0 when past the request)
+      auto fetch = [&](int bt) {
+        const int t = bt * tiles_per_batch + lane / npg;
+        const int pg = (G.t_start + t * 128) / p.page_size + lane % npg;
+        return (t < G.n_tiles && pg < n_pages && lane < tiles_per_batch * npg) ? __ldg(pages + pg) : 0;
+      };
+      int idx_cur = fetch(0), idx_nxt = fetch(1);
       if (lane == 0) {
         if (qc > 0 && !mbar_wait(BAR(B_QEMPTY), (qc - 1) & 1, abort_flag)) ok = false;
         if (ok) {
@@ -334,35 +415,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ++qc;
-      const int32_t* pages = p.kv_indices + kv_indptr[G.b];
-      const int n_pages = kv_indptr[G.b + 1] - kv_indptr[G.b];
-      for (int t = 0; t < G.n_tiles; ++t, ++gt) {
-        const int st = gt & 1;
-        const int t0 = G.t_start + t * 128;
-        const int pf = t0 / p.page_size;
-        const bool has = lane < npg && pf + lane < n_pages;
-        const int page = has ? __ldg(pages + pf + lane) : 0;
-        const int nvalid = __popc(__ballot_sync(0xffffffffu, has));
-        if (lane == 0) {
-          if (gt >= 2 && !mbar_wait(BAR(B_KVEMPTY + st), ((gt >> 1) - 1) & 1, abort_flag)) ok = false;
-          if (ok) {
-            mbar_expect_tx(BAR(B_KVFULL + st), uint32_t(nvalid) * uint32_t(kv_box_rows) * 128u * 4u);
-            kv_armed[st] = true;
-            kv_par[st] = (gt >> 1) & 1;
+      bool has_prev = false;
+      int page_prev = 0, nvalid_prev = 0;
+      for (int step = 0; step <= G.n_tiles && ok; ++step) {
+        bool has = false;
+        int page = 0, nvalid = 0;
+        if (step < G.n_tiles) {
+          const int bt = step / tiles_per_batch, k = step % tiles_per_batch;
+          if (k == 0 && bt > 0) {  // move to the next batch, prefetch the one after
+            idx_cur = idx_nxt;
+            idx_nxt = fetch(bt + 1);
           }
+          const int pf = (G.t_start + step * 128) / p.page_size;
+          has = lane < npg && pf + lane < n_pages;
+          page = __shfl_sync(0xffffffffu, idx_cur, (k * npg + lane) & 31);
+          nvalid = __popc(__ballot_sync(0xffffffffu, has));
+          ok = load(0, G, step, gk, has, page, nvalid);
+          ++gk;
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        if (has) {
-          const int slot0 = (kv_box_rows == 128) ? (t0 % p.page_size) : 0;
-          const uint32_t roff = uint32_t(lane * kv_box_rows) * 128u;
-          for (int h = 0; h < 2; ++h) {
-            tma_load_4d(sbase + kOffK + st * kTile + h * kBlk + roff, &tk, BAR(B_KVFULL + st),
-                        h * 64, G.hk, slot0, page);
-            tma_load_4d(sbase + kOffV + st * kTile + h * kBlk + roff, &tv, BAR(B_KVFULL + st),
-                        h * 64, G.hk, slot0, page);
-          }
+        if (ok && step >= 1) {
+          ok = load(1, G, step - 1, gv, has_prev, page_prev, nvalid_prev);
+          ++gv;
         }
+        has_prev = has;
+        page_prev = page;
+        nvalid_prev = nvalid;
       }
     }
     // before exit: every copy this warp started has landed (these waits
@@ -370,8 +447,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       volatile int no_abort = 0;
       if (q_armed) mbar_wait(BAR(B_QFULL), q_par, &no_abort);
-      for (int s = 0; s < 2; ++s)
-        if (kv_armed[s]) mbar_wait(BAR(B_KVFULL + s), kv_par[s], &no_abort);
+      for (int which = 0; which < 2; ++which)
+        for (int s = 0; s < 2; ++s)
+          if (armed[which][s])
+            mbar_wait(BAR((which ? B_VFULL : B_KFULL) + s), apar[which][s], &no_abort);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -407,25 +486,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool hasB = G.n_rows > tr;
         const int n = G.n_tiles;
         if (!mbar_wait(BAR(B_QFULL), qc & 1, abort_flag)) { ok = false; break; }
-        if (!mbar_wait(BAR(B_KVFULL + (gt & 1)), (gt >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(BAR(B_KFULL + (gt & 1)), (gt >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         issue_s(0, gt & 1);
         if (hasB) issue_s(1, gt & 1);
+        tc_commit(BAR(B_KEMPTY + (gt & 1)));
         if (n == 1) tc_commit(BAR(B_QEMPTY));
         for (int j = 0; j < n && ok; ++j) {
           const int g1 = gt + j, st = g1 & 1, st1 = (g1 + 1) & 1;
           // ---- tile A
           if (j == 0 && itc[0] > 0 && !mbar_wait(BAR(B_OFREE), (itc[0] - 1) & 1, abort_flag)) { ok = false; break; }
           if (!mbar_wait(BAR(B_PFULL), (cnt[0] + j) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(BAR(B_VFULL + st), (g1 >> 1) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
           issue_pv(0, st, j > 0);
           if (j == n - 1) tc_commit(BAR(B_ODONE));
-          if (!hasB) tc_commit(BAR(B_KVEMPTY + st));
+          if (!hasB) tc_commit(BAR(B_VEMPTY + st));
           if (j + 1 < n) {
-            if (!mbar_wait(BAR(B_KVFULL + st1), ((g1 + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_KFULL + st1), ((g1 + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
             issue_s(0, st1);
-            if (!hasB && j + 1 == n - 1) tc_commit(BAR(B_QEMPTY));
+            if (!hasB) {
+              tc_commit(BAR(B_KEMPTY + st1));
+              if (j + 1 == n - 1) tc_commit(BAR(B_QEMPTY));
+            }
           }
           // ---- tile B
           if (hasB) {
@@ -433,10 +517,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!mbar_wait(BAR(B_PFULL + 1), (cnt[1] + j) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
             issue_pv(1, st, j > 0);
-            tc_commit(BAR(B_KVEMPTY + st));
+            tc_commit(BAR(B_VEMPTY + st));
             if (j == n - 1) tc_commit(BAR(B_ODONE + 1));
             if (j + 1 < n) {
               issue_s(1, st1);
+              tc_commit(BAR(B_KEMPTY + st1));
               if (j + 1 == n - 1) tc_commit(BAR(B_QEMPTY));
             }
           }
@@ -516,23 +601,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool need_mask = (t0 < G.kv_lo) || (t0 + 128 > G.kv_hi) ||
                                (causal && t0 + 127 > ix0 + G.lk - G.lq) ||
                                (wl >= 0 && t0 < G.lk - G.lq + ix1 - wl);
-        // pass 1: row max of the raw scores
+        // pass 1: row max of the raw scores; the next 32 columns load while
+        // the current ones are reduced
         float mp[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) mp[q] = neg_inf();
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tS + uint32_t(c) * 32u, v);
-          tmem_wait_ld();
+        {
+          uint32_t va[16], vb[16];
+          tmem_ld16(tS, va);
+          tmem_wait_ld_tied16(va);
+#pragma unroll 2
+          for (int c = 0; c < 8; ++c) {
+            uint32_t (&cur)[16] = (c & 1) ? vb : va;
+            uint32_t (&nxt)[16] = (c & 1) ? va : vb;
+            if (c + 1 < 8) tmem_ld16(tS + uint32_t(c + 1) * 16u, nxt);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float xv = __uint_as_float(v[e]);
-            if (need_mask) {
-              const int jj = t0 + c * 32 + e;
-              if (jj < jmin || jj > jmax) xv = neg_inf();
+            for (int e = 0; e < 16; ++e) {
+              float xv = __uint_as_float(cur[e]);
+              if (need_mask) {
+                const int jj = t0 + c * 16 + e;
+                if (jj < jmin || jj > jmax) xv = neg_inf();
+              }
+              mp[e & 7] = fmaxf(mp[e & 7], xv);
             }
-            mp[e & 7] = fmaxf(mp[e & 7], xv);
+            if (c + 1 < 8) tmem_wait_ld_tied16(nxt);
           }
         }
         const float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
@@ -557,7 +649,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool zeroed = false;
         if (x == 0 && t0 + 128 > G.lk) {
           // rows of V past the request's last key may hold anything: zero them
-          if (!wwait(BAR(B_KVFULL + st), (g1 >> 1) & 1)) { ok = false; break; }
+          if (!wwait(BAR(B_VFULL + st), (g1 >> 1) & 1)) { ok = false; break; }
           if (t0 + r >= G.lk) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -569,27 +661,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           zeroed = true;
         }
         // pass 2: P = exp2(s * scale - m), packed, back into the S columns
+        // (P chunk c lands on columns already read); loads of 16 columns run
+        // one chunk ahead
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tS + uint32_t(c) * 32u, v);
-          tmem_wait_ld();
-          uint32_t pk[16];
+        {
+          uint32_t va[16], vb[16];
+          tmem_ld16(tS, va);
+          tmem_wait_ld_tied16(va);
+#pragma unroll 2
+          for (int c = 0; c < 8; ++c) {
+            uint32_t (&cur)[16] = (c & 1) ? vb : va;
+            uint32_t (&nxt)[16] = (c & 1) ? va : vb;
+            if (c + 1 < 8) tmem_ld16(tS + uint32_t(c + 1) * 16u, nxt);
+            uint32_t pk[8];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float s0 = __uint_as_float(v[2 * e]), s1 = __uint_as_float(v[2 * e + 1]);
-            if (need_mask) {
-              const int jj = t0 + c * 32 + 2 * e;
-              if (jj < jmin || jj > jmax) s0 = neg_inf();
-              if (jj + 1 < jmin || jj + 1 > jmax) s1 = neg_inf();
+            for (int e = 0; e < 8; ++e) {
+              float s0 = __uint_as_float(cur[2 * e]), s1 = __uint_as_float(cur[2 * e + 1]);
+              if (need_mask) {
+                const int jj = t0 + c * 16 + 2 * e;
+                if (jj < jmin || jj > jmax) s0 = neg_inf();
+                if (jj + 1 < jmin || jj + 1 > jmax) s1 = neg_inf();
+              }
+              const float p0 = ex2(fmaf(s0, scale, -mu));
+              const float p1 = ex2(fmaf(s1, scale, -mu));
+              ps[e & 3] += p0 + p1;
+              pk[e] = DT::pack(p0, p1);
             }
-            const float p0 = ex2(fmaf(s0, scale, -mu));
-            const float p1 = ex2(fmaf(s1, scale, -mu));
-            ps[e & 3] += p0 + p1;
-            pk[e] = DT::pack(p0, p1);
+            tmem_st8(tS + uint32_t(c) * 8u, pk);
+            if (c + 1 < 8) tmem_wait_ld_tied16(nxt);
           }
-          tmem_st16(tS + uint32_t(c) * 16u, pk);
         }
         tmem_wait_st();
         l_run = l_run * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
