@@ -346,6 +346,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Register split: the control warpgroup (producer, MMA issuer, two idle
+  // warps) gives registers to the two softmax warpgroups, which hold a whole
+  // 128-column score row: 128 x 112 + 256 x 192 = 63488 <= 384 x 168 launched.
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // Lane 0 owns the barriers; for each K or V tile every lane fetches one
@@ -541,7 +546,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_wait(BAR(B_FINAL), 0, &no_abort);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
     // ------------------------------------------------------------ softmax + epilogue
     const int x = (warp - 4) >> 2;         // Q tile of this warpgroup
     const int sw = warp & 3;               // TMEM lane quadrant
@@ -601,32 +608,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool need_mask = (t0 < G.kv_lo) || (t0 + 128 > G.kv_hi) ||
                                (causal && t0 + 127 > ix0 + G.lk - G.lq) ||
                                (wl >= 0 && t0 < G.lk - G.lq + ix1 - wl);
-        // pass 1: row max of the raw scores; the next 32 columns load while
-        // the current ones are reduced
+        // the whole 128-column row in registers, one wait for the four loads
+        uint32_t sv[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + uint32_t(c) * 32u, sv[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_wait_ld_tied(sv[c]);
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int jj = t0 + c * 32 + e;
+              if (jj < jmin || jj > jmax) sv[c][e] = __float_as_uint(neg_inf());
+            }
+        }
+        // row max of the raw scores, eight independent chains
         float mp[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) mp[q] = neg_inf();
-        {
-          uint32_t va[16], vb[16];
-          tmem_ld16(tS, va);
-          tmem_wait_ld_tied16(va);
-#pragma unroll 2
-          for (int c = 0; c < 8; ++c) {
-            uint32_t (&cur)[16] = (c & 1) ? vb : va;
-            uint32_t (&nxt)[16] = (c & 1) ? va : vb;
-            if (c + 1 < 8) tmem_ld16(tS + uint32_t(c + 1) * 16u, nxt);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              float xv = __uint_as_float(cur[e]);
-              if (need_mask) {
-                const int jj = t0 + c * 16 + e;
-                if (jj < jmin || jj > jmax) xv = neg_inf();
-              }
-              mp[e & 7] = fmaxf(mp[e & 7], xv);
-            }
-            if (c + 1 < 8) tmem_wait_ld_tied16(nxt);
-          }
-        }
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mp[e & 7] = fmaxf(mp[e & 7], __uint_as_float(sv[c][e]));
         const float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                                  fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
         const float mx = mraw * scale;  // scale > 0
@@ -660,36 +664,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           zeroed = true;
         }
-        // pass 2: P = exp2(s * scale - m), packed, back into the S columns
-        // (P chunk c lands on columns already read); loads of 16 columns run
-        // one chunk ahead
+        // P = exp2(s * scale - m), packed in pairs, over the S columns
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-          uint32_t va[16], vb[16];
-          tmem_ld16(tS, va);
-          tmem_wait_ld_tied16(va);
-#pragma unroll 2
-          for (int c = 0; c < 8; ++c) {
-            uint32_t (&cur)[16] = (c & 1) ? vb : va;
-            uint32_t (&nxt)[16] = (c & 1) ? va : vb;
-            if (c + 1 < 8) tmem_ld16(tS + uint32_t(c + 1) * 16u, nxt);
-            uint32_t pk[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              float s0 = __uint_as_float(cur[2 * e]), s1 = __uint_as_float(cur[2 * e + 1]);
-              if (need_mask) {
-                const int jj = t0 + c * 16 + 2 * e;
-                if (jj < jmin || jj > jmax) s0 = neg_inf();
-                if (jj + 1 < jmin || jj + 1 > jmax) s1 = neg_inf();
-              }
-              const float p0 = ex2(fmaf(s0, scale, -mu));
-              const float p1 = ex2(fmaf(s1, scale, -mu));
-              ps[e & 3] += p0 + p1;
-              pk[e] = DT::pack(p0, p1);
-            }
-            tmem_st8(tS + uint32_t(c) * 8u, pk);
-            if (c + 1 < 8) tmem_wait_ld_tied16(nxt);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2(fmaf(__uint_as_float(sv[c][2 * e]), scale, -mu));
+            const float p1 = ex2(fmaf(__uint_as_float(sv[c][2 * e + 1]), scale, -mu));
+            ps[e & 3] += p0 + p1;
+            pk[e] = DT::pack(p0, p1);
           }
+          tmem_st16(tS + uint32_t(c) * 16u, pk);
         }
         tmem_wait_st();
         l_run = l_run * corr + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
