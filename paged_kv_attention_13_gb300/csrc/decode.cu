@@ -4,9 +4,10 @@
 // scores reduced with warp shuffles, and an online softmax kept in fp32.
 //
 // Work item = (request, kv head, key chunk). A CTA of 4 warps streams the
-// chunk's live keys through a 4-stage cp.async ring in shared memory (32 keys
+// chunk's live keys through a 3-stage cp.async ring in shared memory (32 keys
 // of K and V per stage, gathered page by page, zero-filled past the end), so
-// three stages of loads stay in flight while one is consumed. Each warp takes
+// two stages of loads stay in flight while one is consumed; four CTAs share
+// an SM. Each warp takes
 // 8 keys of a stage; a warp step covers 32 / (D/8) keys, each key's D/8 lanes
 // holding 8 head-dim elements. At the end the four warps' (max, sum, o)
 // states are merged in shared memory.
@@ -23,7 +24,7 @@ namespace fi {
 namespace {
 
 constexpr int kDecodeThreads = 128;
-constexpr int kDecodeStages = 4;   // cp.async ring depth
+constexpr int kDecodeStages = 3;   // cp.async ring depth
 constexpr int kDecodeKT = 32;      // keys per stage
 
 template <int D>
@@ -32,7 +33,7 @@ constexpr int decode_smem_bytes() {
 }
 
 template <int D, int G, bool BF16>
-__global__ void __launch_bounds__(kDecodeThreads, 3) decode_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnParams p) {
   using DT = Dt<BF16>;
   using T = typename DT::T;
   constexpr int LPK = D / 8;                 // lanes per key
@@ -48,7 +49,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_kernel(const AttnPar
   T* sV = sK + kDecodeStages * STAGE;
   __shared__ float sm_m[NWARP][G];
   __shared__ float sm_l[NWARP][G];
-  __shared__ __align__(16) float sm_o[NWARP][G][D];
+  // the warps' o partials reuse the ring once an item's keys are consumed
+  float (*sm_o)[G][D] = reinterpret_cast<float (*)[G][D]>(dsmem);
+  static_assert(NWARP * G * D * 4 <= kDecodeStages * kDecodeKT * D * 2 * 2, "o partials fit the ring");
 
   const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
   const int n_items = hdr->n_items;
@@ -254,6 +257,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_kernel(const AttnPar
       }
     }
     cp_async_wait<0>();
+    __syncthreads();  // every warp is done with the ring before it holds o partials
 
     // sums over the warp's key groups (they share each head's max)
     float l_h[G], m_h[G];
