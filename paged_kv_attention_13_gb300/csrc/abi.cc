@@ -402,8 +402,20 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
   // ---- work items, partial slots and the merge index
   ns.merge_indptr.assign(ns.total_rows + 1, 0);
   std::vector<int32_t> merge_count(ns.total_rows, 0);
-  struct Costed { int64_t cost; WorkItem it; };
-  std::vector<Costed> costed;
+  // Items are made per (tile, chunk) group - one per kv head, all of the same
+  // cost - and the groups are sorted by cost, longest first.
+  struct Group { int64_t cost; WorkItem it; };
+  std::vector<Group> groups;
+  {
+    size_t n_est = 0;
+    for (const Tile& t : tiles) {
+      int64_t n = 1;
+      if (force_kv_chunks > 0) n = force_kv_chunks;
+      else if (chunk_len > 0 && t.hi - t.lo > chunk_len) n = (t.hi - t.lo + chunk_len - 1) / chunk_len;
+      n_est += size_t(n);
+    }
+    groups.reserve(n_est);
+  }
   int32_t partial_cursor = 0;
   int32_t max_chunks = 1;
   for (const Tile& t : tiles) {
@@ -429,22 +441,84 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
         ke = t.hi;
       }
       const int64_t live = std::max<int64_t>(0, std::min<int64_t>(ke, t.hi) - std::max<int64_t>(kb, t.lo));
-      for (int32_t h = 0; h < hk; ++h) {
-        WorkItem it;
-        it.b = t.b; it.kv_head = h; it.row0 = t.row0;
-        it.kv_begin = int32_t(kb); it.kv_end = int32_t(ke);
-        it.chunk = (n > 1) ? int32_t(c) : -1;
-        it.num_chunks = int32_t(n);
-        it.partial_base = base;
-        costed.push_back({live * t.rows + 64, it});
+      Group gr;
+      gr.cost = live * t.rows + 64;
+      gr.it.b = t.b; gr.it.kv_head = 0; gr.it.row0 = t.row0;
+      gr.it.kv_begin = int32_t(kb); gr.it.kv_end = int32_t(ke);
+      gr.it.chunk = (n > 1) ? int32_t(c) : -1;
+      gr.it.num_chunks = int32_t(n);
+      gr.it.partial_base = base;
+      groups.push_back(gr);
+    }
+  }
+  std::stable_sort(groups.begin(), groups.end(),
+                   [](const Group& a, const Group& b) { return a.cost > b.cost; });
+  // Static longest-processing-time schedule for the persistent grid: groups,
+  // longest first, go to the least-loaded bundle of Hk CTAs (one item per CTA
+  // of the bundle; a bundle is one CTA when Hk does not divide the grid),
+  // found with a binary min-heap of bundle loads; CTA c then finds its list at
+  // positions c, c + grid, ... (padded with items whose request is -1, which
+  // every kernel skips).
+  const int64_t n_all = int64_t(groups.size()) * hk;
+  const int64_t G = std::max<int64_t>(1, P.graph ? grid_cap : std::min<int64_t>(n_all, grid_cap));
+  const int32_t bundle = (G % hk == 0) ? hk : 1;
+  const int32_t n_bundles = int32_t(G / bundle);
+  {
+    std::vector<int64_t> load(static_cast<size_t>(n_bundles), 0);
+    std::vector<int32_t> heap(static_cast<size_t>(n_bundles));  // heap-ordered by (load, id)
+    for (int32_t c = 0; c < n_bundles; ++c) heap[size_t(c)] = c;
+    auto less = [&](int32_t a, int32_t b) {
+      return load[size_t(a)] != load[size_t(b)] ? load[size_t(a)] < load[size_t(b)] : a < b;
+    };
+    auto take = [&](int64_t cost) {  // least-loaded bundle gets `cost`
+      const int32_t c = heap[0];
+      load[size_t(c)] += cost;
+      size_t k = 0;
+      const size_t n = size_t(n_bundles);
+      for (;;) {
+        size_t l = 2 * k + 1, r = l + 1, m = k;
+        if (l < n && less(heap[l], heap[m])) m = l;
+        if (r < n && less(heap[r], heap[m])) m = r;
+        if (m == k) break;
+        std::swap(heap[k], heap[m]);
+        k = m;
+      }
+      return c;
+    };
+    std::vector<int32_t> cta_of(static_cast<size_t>(n_all));
+    std::vector<int32_t> count(static_cast<size_t>(G), 0);
+    int64_t i = 0;
+    for (const Group& gr : groups) {
+      if (bundle == hk) {
+        const int32_t c0 = take(gr.cost) * hk;
+        for (int32_t h = 0; h < hk; ++h, ++i) {
+          cta_of[size_t(i)] = c0 + h;
+          count[size_t(c0 + h)]++;
+        }
+      } else {
+        for (int32_t h = 0; h < hk; ++h, ++i) {
+          const int32_t c = take(gr.cost);
+          cta_of[size_t(i)] = c;
+          count[size_t(c)]++;
+        }
+      }
+    }
+    int32_t rounds = 0;
+    for (int32_t c : count) rounds = std::max(rounds, c);
+    WorkItem pad{};
+    pad.b = -1;
+    ns.items.assign(size_t(rounds) * size_t(G), pad);
+    std::vector<int32_t> next(static_cast<size_t>(G), 0);
+    i = 0;
+    for (const Group& gr : groups) {
+      for (int32_t h = 0; h < hk; ++h, ++i) {
+        const int32_t c = cta_of[size_t(i)];
+        WorkItem it = gr.it;
+        it.kv_head = h;
+        ns.items[size_t(next[size_t(c)]++) * size_t(G) + size_t(c)] = it;
       }
     }
   }
-  // longest first, so a persistent grid striding over the list stays balanced
-  std::stable_sort(costed.begin(), costed.end(),
-                   [](const Costed& a, const Costed& b) { return a.cost > b.cost; });
-  ns.items.reserve(costed.size());
-  for (const Costed& c : costed) ns.items.push_back(c.it);
   for (int32_t t = 0; t < ns.total_rows; ++t) {
     ns.merge_indptr[t + 1] = ns.merge_indptr[t] + merge_count[t];
     if (merge_count[t] > 1) ns.merge_rows.push_back(t);
@@ -452,7 +526,7 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
   ns.n_partials = partial_cursor;
   ns.max_chunks = max_chunks;
   const int64_t n_items = int64_t(ns.items.size());
-  ns.grid = int32_t(P.graph ? grid_cap : std::min<int64_t>(n_items, grid_cap));
+  ns.grid = int32_t(n_items == 0 ? 0 : G);
 
   // ---- device layout
   WsHeader& h = ns.hdr;
@@ -478,6 +552,10 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
   h.off_tmp_lse = ns.meta_bytes;
   h.off_tmp_o = ns.meta_bytes + align_up(4 * int64_t(ns.n_partials) * hq, kAlign);
   ns.total_bytes = ns.meta_bytes + partial_bytes_for(ns.n_partials, hq, d);
+  if (!P.host_only && ns.total_bytes > int64_t(P.ws_bytes))
+    return fail(FI_ERR_CAPACITY, "plan: workspace_bytes=%zu < %lld needed for %lld scheduled items "
+                "and %d partial states", P.ws_bytes, (long long)ns.total_bytes,
+                (long long)n_items, ns.n_partials);
   return FI_OK;
 }
 

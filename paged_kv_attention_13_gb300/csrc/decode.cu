@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnPar
 
   for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
     const WorkItem it = items[w];
+    if (it.b < 0) continue;  // schedule padding
     const int b = it.b, hk = it.kv_head;
     const int lk = kv_len[b];
     const int token = qo_indptr[b];

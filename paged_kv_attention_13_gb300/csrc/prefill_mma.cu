@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(kThreads) prefill_mma_kernel(const AttnParams 
 
   for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
     const WorkItem it = items[w];
+    if (it.b < 0) continue;  // schedule padding
     const int b = it.b, hk = it.kv_head;
     const int token0 = qo_indptr[b];
     const int lq = qo_indptr[b + 1] - token0;

@@ -392,6 +392,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       return okl;
     };
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      if (items[w].b < 0) continue;  // schedule padding
       const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
       if (G.n_tiles == 0) continue;
       const bool hasB = G.n_rows > tr;
@@ -486,7 +487,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int gt = 0, qc = 0, cnt[2] = {0, 0}, itc[2] = {0, 0};
       bool ok = true;
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
+        if (items[w].b < 0) continue;  // schedule padding
+      const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
         if (G.n_tiles == 0) continue;
         const bool hasB = G.n_rows > tr;
         const int n = G.n_tiles;
@@ -566,6 +568,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int gt = 0, cnt = 0, itc = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      if (items[w].b < 0) continue;  // schedule padding
       const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
       const bool hasB = G.n_rows > tr;
       const int n = G.n_tiles;
