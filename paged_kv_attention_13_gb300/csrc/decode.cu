@@ -86,23 +86,41 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnPar
     const T* kbase = static_cast<const T*>(p.k) + int64_t(hk) * p.k_stride_head;
     const T* vbase = static_cast<const T*>(p.v) + int64_t(hk) * p.v_stride_head;
     // gather one stage of K and V rows (16-byte cp.async, zero-fill past hi)
+    // Thread t copies 16-byte chunk (t % CH) of rows t / CH + i * (128 / CH) of
+    // every stage: K and V share the page lookup, and everything that does not
+    // depend on the stage is computed once per item.
+    constexpr int ROWS_PER_PASS = kDecodeThreads / CH;
+    constexpr int PASSES = kDecodeKT / ROWS_PER_PASS;
+    const int my_c = tid % CH, my_row = tid / CH;
+    const T* kcol = kbase + my_c * 8;
+    const T* vcol = vbase + my_c * 8;
+    const uint32_t sk0 = smem_u32(sK + my_row * D + my_c * 8);
+    const uint32_t sv0 = smem_u32(sV + my_row * D + my_c * 8);
     auto issue = [&](int tile, int stage) {
-      const int kt = lo + tile * kDecodeKT;
-      for (int idx = tid; idx < kDecodeKT * CH; idx += kDecodeThreads) {
-        const int key = idx / CH, c = idx % CH;
-        const int j = kt + key;
+      const int kt = lo + tile * kDecodeKT + my_row;
+#pragma unroll
+      for (int i = 0; i < PASSES; ++i) {
+        const int j = kt + i * ROWS_PER_PASS;
         const T* ks = static_cast<const T*>(p.k);
         const T* vs = static_cast<const T*>(p.v);
         int bytes = 0;
         if (j < hi) {
-          ks = kbase + kv_row_offset(pages, j, p.page_size, p.page_shift, p.k_stride_page,
-                                     p.k_stride_tok) + c * 8;
-          vs = vbase + kv_row_offset(pages, j, p.page_size, p.page_shift, p.v_stride_page,
-                                     p.v_stride_tok) + c * 8;
+          int32_t pi, slot;
+          if (p.page_shift >= 0) {
+            pi = j >> p.page_shift;
+            slot = j & ((1 << p.page_shift) - 1);
+          } else {
+            pi = j / p.page_size;
+            slot = j - pi * p.page_size;
+          }
+          const int64_t page = __ldg(pages + pi);
+          ks = kcol + page * p.k_stride_page + int64_t(slot) * p.k_stride_tok;
+          vs = vcol + page * p.v_stride_page + int64_t(slot) * p.v_stride_tok;
           bytes = 16;
         }
-        cp_async16(smem_u32(sK + stage * STAGE + key * D + c * 8), ks, bytes);
-        cp_async16(smem_u32(sV + stage * STAGE + key * D + c * 8), vs, bytes);
+        const uint32_t off = uint32_t((stage * STAGE + i * ROWS_PER_PASS * D) * 2);
+        cp_async16(sk0 + off, ks, bytes);
+        cp_async16(sv0 + off, vs, bytes);
       }
     };
 #pragma unroll
@@ -111,19 +129,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnPar
       cp_async_commit();
     }
 
-    // q slice of every head in the group, pre-scaled into the log2 domain,
-    // as pairs for the packed fp32x2 FMA
-    float2 q2[G][4];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const T* qp = static_cast<const T*>(p.q) + int64_t(token) * p.q_stride_tok +
-                    int64_t(hk * G + h) * p.q_stride_head + dl * 8;
-      uint4 r = ld_nc16(qp);
-      const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        q2[h][e] = make_float2(DT::lo(wv[e]) * p.sm_scale_log2, DT::hi(wv[e]) * p.sm_scale_log2);
-    }
     // After the reduce-scatter below, this lane holds the score of head
     // `myh` of its key; the running max / sum of that head live on the lanes
     // that own it, o (all heads, this lane's 8 dims) lives on every lane.
@@ -137,6 +142,22 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnPar
           if (lane & off) myh += cnt;
         }
       }
+    }
+    // q of every head in the group, pre-scaled into the log2 domain, as pairs
+    // for the packed fp32x2 FMA. Slot s holds head (myh ^ s): at each level of
+    // the reduce-scatter a lane then keeps its first half of the slots and
+    // sends the second, with no per-lane selection.
+    float2 q2[G][4];
+#pragma unroll
+    for (int sl = 0; sl < G; ++sl) {
+      const int h = myh ^ sl;
+      const T* qp = static_cast<const T*>(p.q) + int64_t(token) * p.q_stride_tok +
+                    int64_t(hk * G + h) * p.q_stride_head + dl * 8;
+      uint4 r = ld_nc16(qp);
+      const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        q2[sl][e] = make_float2(DT::lo(wv[e]) * p.sm_scale_log2, DT::hi(wv[e]) * p.sm_scale_log2);
     }
     float m_me = neg_inf(), l_me = 0.f;
     float2 o2[G][4];
@@ -169,6 +190,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnPar
       }
       const int st = tile % kDecodeStages;
       const int kt = lo + tile * kDecodeKT;
+      const bool full_tile = kt + kDecodeKT <= hi;
       const T* cK = sK + st * STAGE;
       const T* cV = sV + st * STAGE;
       float s[STEPS];  // this lane's (key, head) score per step
@@ -180,34 +202,31 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnPar
         float2 k2[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) k2[e] = make_float2(DT::lo(wv[e]), DT::hi(wv[e]));
-        float part[G];
+        float part[G];  // slot order: part[s] belongs to head myh ^ s
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float2 acc = __fmul2_rn(q2[h][0], k2[0]);
+        for (int sl = 0; sl < G; ++sl) {
+          float2 acc = __fmul2_rn(q2[sl][0], k2[0]);
 #pragma unroll
-          for (int e = 1; e < 4; ++e) acc = __ffma2_rn(q2[h][e], k2[e], acc);
-          part[h] = acc.x + acc.y;
+          for (int e = 1; e < 4; ++e) acc = __ffma2_rn(q2[sl][e], k2[e], acc);
+          part[sl] = acc.x + acc.y;
         }
-        // reduce-scatter over the key's LPK lanes: halve the heads a lane
-        // keeps at each of the first log2(G) levels, then a plain butterfly
+        // reduce-scatter over the key's LPK lanes: at each of the first
+        // log2(G) levels keep the first half of the slots and add the
+        // partner's second half (which holds the same heads), then a plain
+        // butterfly
         int cnt = G;
 #pragma unroll
         for (int off = LPK / 2; off >= 1; off >>= 1) {
           if (cnt > 1) {
             const int half = cnt >> 1;
-            const bool upper = (lane & off) != 0;
 #pragma unroll
-            for (int i = 0; i < half; ++i) {
-              const float send = upper ? part[i] : part[half + i];
-              const float keep = upper ? part[half + i] : part[i];
-              part[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-            }
+            for (int i = 0; i < half; ++i) part[i] += __shfl_xor_sync(0xffffffffu, part[half + i], off);
             cnt = half;
           } else {
             part[0] += __shfl_xor_sync(0xffffffffu, part[0], off);
           }
         }
-        s[u] = (kt + key < hi) ? part[0] : neg_inf();
+        s[u] = (full_tile || kt + key < hi) ? part[0] : neg_inf();
       }
       // stage max of my head over the warp's keys
       float mx = s[0];
