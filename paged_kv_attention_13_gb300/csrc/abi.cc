@@ -827,7 +827,8 @@ fi_status run_common(fi_plan_t p, bool decode_api, const fi_tensor* q, const fi_
   const bool any_work = p->graph || !s.items.empty();
   if (any_work) {
     cudaError_t e;
-    if (s.kernel == fi::kDecode) e = fi::launch_decode(ap, s.d, s.group, bf16, s.grid, cs);
+    if (s.kernel == fi::kDecode)
+      e = fi::launch_decode(ap, s.d, s.group, bf16, k->shape[0], s.grid, cs);
     else if (s.kernel == fi::kPrefillM128)
       e = fi::launch_prefill_tc(ap, s.d, s.group, s.tile_rows, q->shape[0], k->shape[0], bf16,
                                 s.grid, cs);

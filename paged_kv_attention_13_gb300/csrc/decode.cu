@@ -1,16 +1,26 @@
-// Decode kernel: one query row per request against its paged KV, all G query
+// Decode kernels: one query row per request against its paged KV, all G query
 // heads of one kv head together (GQA). Bandwidth-bound: every K/V byte is
-// read exactly once, with 16-byte coalesced cp.async gathers,
-// scores reduced with warp shuffles, and an online softmax kept in fp32.
+// read exactly once, scores are reduced with warp shuffles, and the online
+// softmax is kept in fp32.
 //
-// Work item = (request, kv head, key chunk). A CTA of 4 warps streams the
-// chunk's live keys through a 3-stage cp.async ring in shared memory (32 keys
-// of K and V per stage, gathered page by page, zero-filled past the end), so
-// two stages of loads stay in flight while one is consumed; four CTAs share
-// an SM. Each warp takes
-// 8 keys of a stage; a warp step covers 32 / (D/8) keys, each key's D/8 lanes
-// holding 8 head-dim elements. At the end the four warps' (max, sum, o)
-// states are merged in shared memory.
+// Work item = (request, kv head, key chunk). The item's live keys stream
+// through a ring of stages in shared memory, each stage a tile of KT keys of
+// K and of V. Consumer warps take KT / warps keys of a stage each: a warp step
+// covers 32 / (D/8) keys, each key's D/8 lanes holding 8 head-dim elements.
+// At the end of an item the warps' (max, sum, o) states are merged in shared
+// memory.
+//
+// Two kernels fill the ring:
+//   decode_tma_kernel  one producer warp issues, per page of a stage, one
+//                      cp.async.bulk.tensor box of K and one of V (4-D maps
+//                      over [pages, slot, kv head, dim]); mbarriers hand the
+//                      stages to the consumer warps and back. The producer
+//                      runs ahead across work items, so the ring stays full
+//                      through item boundaries and the consumers issue no
+//                      load instructions at all.
+//   decode_kernel      every thread gathers 16-byte chunks with cp.async
+//                      (2 stages of 48 keys, four CTAs per SM), used when the
+//                      driver refuses a tensor map for the cache's strides.
 //
 // Mask for one query row (Lq = 1) [P1 "Why window_size_right stays -1"],
 // [P2 "Summary"]: causal keeps every key j <= Lk - 1; the window keeps
@@ -18,136 +28,91 @@
 //   [P1] "Route non-causal windowed prefill to AITER's masked kernel" (#339)
 //   [P2] "Support speculative-decode verify on ROCm, and stop auto routing
 //         short-query prefill to AITER" (#362)
-#include "common.cuh"
+#include "tma.cuh"
 
 namespace fi {
 namespace {
 
-constexpr int kDecodeThreads = 128;
-constexpr int kDecodeStages = 3;   // cp.async ring depth
-constexpr int kDecodeKT = 32;      // keys per stage
+// ------------------------------------------------------------------ geometry
 
-template <int D>
-constexpr int decode_smem_bytes() {
-  return kDecodeStages * kDecodeKT * D * 2 * 2;  // K and V rings, 16-bit elements
+// Live keys [lo, hi) of one work item, visited as tiles of `kt` keys from
+// `start` = lo rounded down to `align` (a power of two); keys below lo in the
+// first tile are masked.
+struct DecodeRange {
+  int lo, hi, start, n_tiles;
+};
+
+__device__ __forceinline__ DecodeRange decode_range(const WorkItem& it, int lk, int window_left,
+                                                    int align, int kt) {
+  DecodeRange r;
+  r.hi = min(it.kv_end, lk);
+  r.lo = it.kv_begin;
+  if (window_left >= 0) r.lo = max(r.lo, lk - 1 - window_left);
+  r.lo = max(r.lo, 0);
+  r.start = r.lo & ~(align - 1);
+  r.n_tiles = r.hi > r.lo ? (r.hi - r.start + kt - 1) / kt : 0;
+  return r;
 }
 
-template <int D, int G, bool BF16>
-__global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnParams p) {
+// ------------------------------------------------------------- warp consumer
+
+// One consumer warp's share of a work item: q of the G heads pre-scaled into
+// the exp2 domain (fp32 pairs for the packed FMA), o of every head on this
+// lane's 8 dims, and the running max / sum of the head whose score this lane
+// holds after the reduce-scatter.
+template <int D, int G, bool BF16, int NWARP, int KT>
+struct DecodeWarp {
   using DT = Dt<BF16>;
   using T = typename DT::T;
-  constexpr int LPK = D / 8;                 // lanes per key
-  constexpr int KPS = 32 / LPK;              // keys per warp step
-  constexpr int NWARP = kDecodeThreads / 32;
-  constexpr int KPW = kDecodeKT / NWARP;     // keys per warp per stage
-  constexpr int STEPS = KPW / KPS;           // warp steps per stage
-  constexpr int CH = D / 8;                  // 16-byte chunks per row
-  constexpr int STAGE = kDecodeKT * D;       // elements per stage
+  static constexpr int LPK = D / 8;          // lanes per key
+  static constexpr int KPS = 32 / LPK;       // keys per warp step
+  static constexpr int KPW = KT / NWARP;     // keys per warp per stage
+  static constexpr int STEPS = KPW / KPS;    // warp steps per stage
+  static_assert(KPW % KPS == 0, "a warp's keys of a stage are whole warp steps");
 
-  extern __shared__ __align__(128) uint8_t dsmem[];
-  T* sK = reinterpret_cast<T*>(dsmem);
-  T* sV = sK + kDecodeStages * STAGE;
-  __shared__ float sm_m[NWARP][G];
-  __shared__ float sm_l[NWARP][G];
-  // the warps' o partials reuse the ring once an item's keys are consumed
-  float (*sm_o)[G][D] = reinterpret_cast<float (*)[G][D]>(dsmem);
-  static_assert(NWARP * G * D * 4 <= kDecodeStages * kDecodeKT * D * 2 * 2, "o partials fit the ring");
+  int warp, lane, kg, dl;
+  int myh;          // head whose score this lane holds after the reduce-scatter
+  int src_of[G];    // lane (within this key's lane group) holding head h's score
+  float2 q2[G][4];  // slot s holds head (myh ^ s)
+  float2 o2[G][4];
+  float m_me, l_me;
 
-  const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
-  const int n_items = hdr->n_items;
-  const WorkItem* items = ws_ptr<const WorkItem>(p.ws, hdr->off_items);
-  const int32_t* qo_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_qo_indptr);
-  const int32_t* kv_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_kv_indptr);
-  const int32_t* kv_len = ws_ptr<const int32_t>(p.ws, hdr->off_kv_len);
-  float* tmp_lse = ws_ptr<float>(p.ws, hdr->off_tmp_lse);
-  float* tmp_o = ws_ptr<float>(p.ws, hdr->off_tmp_o);
-  const int window_left = hdr->window_left;
-  const int Hq = p.num_qo_heads;
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int kg = lane / LPK;   // key within the warp step
-  const int dl = lane % LPK;   // 8-element slice of the head dim
-
-  for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
-    const WorkItem it = items[w];
-    if (it.b < 0) continue;  // schedule padding
-    const int b = it.b, hk = it.kv_head;
-    const int lk = kv_len[b];
-    const int token = qo_indptr[b];
-    int lo = it.kv_begin;
-    const int hi = min(it.kv_end, lk);
-    if (window_left >= 0) lo = max(lo, lk - 1 - window_left);
-    lo = max(lo, 0);
-    const int n_tiles = hi > lo ? (hi - lo + kDecodeKT - 1) / kDecodeKT : 0;
-
-    const int32_t* pages = p.kv_indices + kv_indptr[b];
-    const T* kbase = static_cast<const T*>(p.k) + int64_t(hk) * p.k_stride_head;
-    const T* vbase = static_cast<const T*>(p.v) + int64_t(hk) * p.v_stride_head;
-    // gather one stage of K and V rows (16-byte cp.async, zero-fill past hi)
-    // Thread t copies 16-byte chunk (t % CH) of rows t / CH + i * (128 / CH) of
-    // every stage: K and V share the page lookup, and everything that does not
-    // depend on the stage is computed once per item.
-    constexpr int ROWS_PER_PASS = kDecodeThreads / CH;
-    constexpr int PASSES = kDecodeKT / ROWS_PER_PASS;
-    const int my_c = tid % CH, my_row = tid / CH;
-    const T* kcol = kbase + my_c * 8;
-    const T* vcol = vbase + my_c * 8;
-    const uint32_t sk0 = smem_u32(sK + my_row * D + my_c * 8);
-    const uint32_t sv0 = smem_u32(sV + my_row * D + my_c * 8);
-    auto issue = [&](int tile, int stage) {
-      const int kt = lo + tile * kDecodeKT + my_row;
+  __device__ __forceinline__ void setup(int warp_, int lane_) {
+    warp = warp_;
+    lane = lane_;
+    kg = lane / LPK;
+    dl = lane % LPK;
+    myh = 0;
+    int cnt = G;
 #pragma unroll
-      for (int i = 0; i < PASSES; ++i) {
-        const int j = kt + i * ROWS_PER_PASS;
-        const T* ks = static_cast<const T*>(p.k);
-        const T* vs = static_cast<const T*>(p.v);
-        int bytes = 0;
-        if (j < hi) {
-          int32_t pi, slot;
-          if (p.page_shift >= 0) {
-            pi = j >> p.page_shift;
-            slot = j & ((1 << p.page_shift) - 1);
-          } else {
-            pi = j / p.page_size;
-            slot = j - pi * p.page_size;
-          }
-          const int64_t page = __ldg(pages + pi);
-          ks = kcol + page * p.k_stride_page + int64_t(slot) * p.k_stride_tok;
-          vs = vcol + page * p.v_stride_page + int64_t(slot) * p.v_stride_tok;
-          bytes = 16;
-        }
-        const uint32_t off = uint32_t((stage * STAGE + i * ROWS_PER_PASS * D) * 2);
-        cp_async16(sk0 + off, ks, bytes);
-        cp_async16(sv0 + off, vs, bytes);
+    for (int off = LPK / 2; off >= 1; off >>= 1) {
+      if (cnt > 1) {
+        cnt >>= 1;
+        if (lane & off) myh += cnt;
       }
-    };
-#pragma unroll
-    for (int s = 0; s < kDecodeStages - 1; ++s) {
-      if (s < n_tiles) issue(s, s);
-      cp_async_commit();
     }
-
-    // After the reduce-scatter below, this lane holds the score of head
-    // `myh` of its key; the running max / sum of that head live on the lanes
-    // that own it, o (all heads, this lane's 8 dims) lives on every lane.
-    int myh = 0;
-    {
-      int cnt = G;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      int l_in = 0, c = G, rem = h;
 #pragma unroll
       for (int off = LPK / 2; off >= 1; off >>= 1) {
-        if (cnt > 1) {
-          cnt >>= 1;
-          if (lane & off) myh += cnt;
+        if (c > 1) {
+          c >>= 1;
+          if (rem >= c) {
+            l_in |= off;
+            rem -= c;
+          }
         }
       }
+      src_of[h] = (lane & ~(LPK - 1)) | l_in;
     }
-    // q of every head in the group, pre-scaled into the log2 domain, as pairs
-    // for the packed fp32x2 FMA. Slot s holds head (myh ^ s): at each level of
-    // the reduce-scatter a lane then keeps its first half of the slots and
-    // sends the second, with no per-lane selection.
-    float2 q2[G][4];
+  }
+
+  // Load q of the item's G heads; reset o and the running max / sum. Slot s
+  // holds head (myh ^ s): at each level of the reduce-scatter a lane then
+  // keeps its first half of the slots and sends the second, with no per-lane
+  // selection.
+  __device__ __forceinline__ void begin(const AttnParams& p, int token, int hk) {
 #pragma unroll
     for (int sl = 0; sl < G; ++sl) {
       const int h = myh ^ sl;
@@ -159,126 +124,117 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnPar
       for (int e = 0; e < 4; ++e)
         q2[sl][e] = make_float2(DT::lo(wv[e]) * p.sm_scale_log2, DT::hi(wv[e]) * p.sm_scale_log2);
     }
-    float m_me = neg_inf(), l_me = 0.f;
-    float2 o2[G][4];
+    m_me = neg_inf();
+    l_me = 0.f;
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
       for (int e = 0; e < 4; ++e) o2[h][e] = make_float2(0.f, 0.f);
-    // lane (within this key's lane group) that holds head h's score
-    int src_of[G];
+  }
+
+  // Consume one stage: keys k0 .. k0+KT-1 in rows 0..KT-1 of cK / cV, of
+  // which [lo, hi) are live. Rows outside the live range may hold anything
+  // (a neighbour's page slots): their scores are masked to -inf and their V
+  // rows are read as zero, so no value there reaches o.
+  __device__ __forceinline__ void stage(const T* cK, const T* cV, int k0, int lo, int hi) {
+    const bool full_tile = k0 >= lo && k0 + KT <= hi;
+    float s[STEPS];  // this lane's (key, head) score per step
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      int l_in = 0, cnt = G, rem = h;
+    for (int u = 0; u < STEPS; ++u) {
+      const int key = warp * KPW + u * KPS + kg;
+      const uint4 kr = *reinterpret_cast<const uint4*>(cK + key * D + dl * 8);
+      const uint32_t wv[4] = {kr.x, kr.y, kr.z, kr.w};
+      float2 k2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) k2[e] = make_float2(DT::lo(wv[e]), DT::hi(wv[e]));
+      float part[G];  // slot order: part[s] belongs to head myh ^ s
+#pragma unroll
+      for (int sl = 0; sl < G; ++sl) {
+        float2 acc = __fmul2_rn(q2[sl][0], k2[0]);
+#pragma unroll
+        for (int e = 1; e < 4; ++e) acc = __ffma2_rn(q2[sl][e], k2[e], acc);
+        part[sl] = acc.x + acc.y;
+      }
+      // reduce-scatter over the key's LPK lanes: at each of the first
+      // log2(G) levels keep the first half of the slots and add the
+      // partner's second half (which holds the same heads), then a plain
+      // butterfly
+      int cnt = G;
 #pragma unroll
       for (int off = LPK / 2; off >= 1; off >>= 1) {
         if (cnt > 1) {
-          cnt >>= 1;
-          if (rem >= cnt) { l_in |= off; rem -= cnt; }
+          const int half = cnt >> 1;
+#pragma unroll
+          for (int i = 0; i < half; ++i) part[i] += __shfl_xor_sync(0xffffffffu, part[half + i], off);
+          cnt = half;
+        } else {
+          part[0] += __shfl_xor_sync(0xffffffffu, part[0], off);
         }
       }
-      src_of[h] = (lane & ~(LPK - 1)) | l_in;
+      const int kk = k0 + key;
+      s[u] = (full_tile || (kk >= lo && kk < hi)) ? part[0] : neg_inf();
     }
-
-    for (int tile = 0; tile < n_tiles; ++tile) {
-      cp_async_wait<kDecodeStages - 2>();
-      __syncthreads();
-      {
-        const int nt = tile + kDecodeStages - 1;
-        if (nt < n_tiles) issue(nt, nt % kDecodeStages);
-        cp_async_commit();
-      }
-      const int st = tile % kDecodeStages;
-      const int kt = lo + tile * kDecodeKT;
-      const bool full_tile = kt + kDecodeKT <= hi;
-      const T* cK = sK + st * STAGE;
-      const T* cV = sV + st * STAGE;
-      float s[STEPS];  // this lane's (key, head) score per step
+    // stage max of my head over the warp's keys
+    float mx = s[0];
 #pragma unroll
-      for (int u = 0; u < STEPS; ++u) {
-        const int key = warp * KPW + u * KPS + kg;
-        const uint4 kr = *reinterpret_cast<const uint4*>(cK + key * D + dl * 8);
-        const uint32_t wv[4] = {kr.x, kr.y, kr.z, kr.w};
-        float2 k2[4];
+    for (int u = 1; u < STEPS; ++u) mx = fmaxf(mx, s[u]);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) k2[e] = make_float2(DT::lo(wv[e]), DT::hi(wv[e]));
-        float part[G];  // slot order: part[s] belongs to head myh ^ s
+    for (int off = LPK; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    // lazy max: the reference moves only when the stage max exceeds it by
+    // more than 2^8 (p stays <= 256), so o is rarely rescaled
+    float mn = m_me;
+    if (mx > m_me + 8.f || (m_me == neg_inf() && mx != neg_inf())) mn = mx;
+    const float corr_me = (mn == m_me) ? 1.f : ex2(m_me - mn);
+    const float mu = (mn == neg_inf()) ? 0.f : mn;
+    m_me = mn;
+    float pu[STEPS];
+    float psum = 0.f;
 #pragma unroll
-        for (int sl = 0; sl < G; ++sl) {
-          float2 acc = __fmul2_rn(q2[sl][0], k2[0]);
+    for (int u = 0; u < STEPS; ++u) {
+      pu[u] = ex2(s[u] - mu);
+      psum += pu[u];
+    }
+    l_me = l_me * corr_me + psum;
+    // rescale o of every head by that head's correction
+    if (__any_sync(0xffffffffu, corr_me != 1.f)) {
 #pragma unroll
-          for (int e = 1; e < 4; ++e) acc = __ffma2_rn(q2[sl][e], k2[e], acc);
-          part[sl] = acc.x + acc.y;
-        }
-        // reduce-scatter over the key's LPK lanes: at each of the first
-        // log2(G) levels keep the first half of the slots and add the
-        // partner's second half (which holds the same heads), then a plain
-        // butterfly
-        int cnt = G;
+      for (int h = 0; h < G; ++h) {
+        const float c = __shfl_sync(0xffffffffu, corr_me, src_of[h]);
+        const float2 c2 = make_float2(c, c);
 #pragma unroll
-        for (int off = LPK / 2; off >= 1; off >>= 1) {
-          if (cnt > 1) {
-            const int half = cnt >> 1;
-#pragma unroll
-            for (int i = 0; i < half; ++i) part[i] += __shfl_xor_sync(0xffffffffu, part[half + i], off);
-            cnt = half;
-          } else {
-            part[0] += __shfl_xor_sync(0xffffffffu, part[0], off);
-          }
-        }
-        s[u] = (full_tile || kt + key < hi) ? part[0] : neg_inf();
-      }
-      // stage max of my head over the warp's keys
-      float mx = s[0];
-#pragma unroll
-      for (int u = 1; u < STEPS; ++u) mx = fmaxf(mx, s[u]);
-#pragma unroll
-      for (int off = LPK; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      // lazy max: the reference moves only when the stage max exceeds it by
-      // more than 2^8 (p stays <= 256), so o is rarely rescaled
-      float mn = m_me;
-      if (mx > m_me + 8.f || (m_me == neg_inf() && mx != neg_inf())) mn = mx;
-      const float corr_me = (mn == m_me) ? 1.f : ex2(m_me - mn);
-      const float mu = (mn == neg_inf()) ? 0.f : mn;
-      m_me = mn;
-      float pu[STEPS];
-      float psum = 0.f;
-#pragma unroll
-      for (int u = 0; u < STEPS; ++u) {
-        pu[u] = ex2(s[u] - mu);
-        psum += pu[u];
-      }
-      l_me = l_me * corr_me + psum;
-      // rescale o of every head by that head's correction
-      if (__any_sync(0xffffffffu, corr_me != 1.f)) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float c = __shfl_sync(0xffffffffu, corr_me, src_of[h]);
-          const float2 c2 = make_float2(c, c);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o2[h][e] = __fmul2_rn(o2[h][e], c2);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < STEPS; ++u) {
-        const int key = warp * KPW + u * KPS + kg;
-        const uint4 vr = *reinterpret_cast<const uint4*>(cV + key * D + dl * 8);
-        const uint32_t wv[4] = {vr.x, vr.y, vr.z, vr.w};
-        float2 v2[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) v2[e] = make_float2(DT::lo(wv[e]), DT::hi(wv[e]));
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float ph = __shfl_sync(0xffffffffu, pu[u], src_of[h]);
-          const float2 p2 = make_float2(ph, ph);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o2[h][e] = __ffma2_rn(p2, v2[e], o2[h][e]);
-        }
+        for (int e = 0; e < 4; ++e) o2[h][e] = __fmul2_rn(o2[h][e], c2);
       }
     }
-    cp_async_wait<0>();
-    __syncthreads();  // every warp is done with the ring before it holds o partials
+#pragma unroll
+    for (int u = 0; u < STEPS; ++u) {
+      const int key = warp * KPW + u * KPS + kg;
+      uint4 vr = *reinterpret_cast<const uint4*>(cV + key * D + dl * 8);
+      if (!full_tile) {
+        const int kk = k0 + key;
+        if (kk < lo || kk >= hi) vr = make_uint4(0u, 0u, 0u, 0u);
+      }
+      const uint32_t wv[4] = {vr.x, vr.y, vr.z, vr.w};
+      float2 v2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v2[e] = make_float2(DT::lo(wv[e]), DT::hi(wv[e]));
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float ph = __shfl_sync(0xffffffffu, pu[u], src_of[h]);
+        const float2 p2 = make_float2(ph, ph);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o2[h][e] = __ffma2_rn(p2, v2[e], o2[h][e]);
+      }
+    }
+  }
 
+  // Merge the NWARP warps' states of the item and write o / lse (directly, or
+  // to the item's split-KV partial slot). `sync` is a barrier over the
+  // consumer threads (tid = 0 .. NWARP*32-1); sm_o holds NWARP x G x D
+  // floats. Ends with a barrier, so the shared arrays are free on return.
+  template <class Sync>
+  __device__ __forceinline__ void finish(const AttnParams& p, const WorkItem& it, int token, int tid,
+                                         float* sm_o, float (*sm_m)[G], float (*sm_l)[G],
+                                         Sync sync) {
     // sums over the warp's key groups (they share each head's max)
     float l_h[G], m_h[G];
 #pragma unroll
@@ -308,17 +264,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnPar
     if (kg == 0) {
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        float4* dst = reinterpret_cast<float4*>(&sm_o[warp][h][dl * 8]);
+        float4* dst = reinterpret_cast<float4*>(sm_o + (warp * G + h) * D + dl * 8);
         dst[0] = make_float4(o2[h][0].x, o2[h][0].y, o2[h][1].x, o2[h][1].y);
         dst[1] = make_float4(o2[h][2].x, o2[h][2].y, o2[h][3].x, o2[h][3].y);
       }
     }
-    __syncthreads();
+    sync();
 
-    // merge the warps and write: direct to out/lse, or to a partial slot
+    const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
+    float* tmp_lse = ws_ptr<float>(p.ws, hdr->off_tmp_lse);
+    float* tmp_o = ws_ptr<float>(p.ws, hdr->off_tmp_o);
+    const int Hq = p.num_qo_heads;
+    const int hk = it.kv_head;
     const bool direct = it.chunk < 0;
     const int slot = direct ? 0 : it.partial_base + it.chunk;
-    for (int idx = tid; idx < G * (D / 4); idx += kDecodeThreads) {
+    for (int idx = tid; idx < G * (D / 4); idx += NWARP * 32) {
       const int h = idx / (D / 4);
       const int c = (idx % (D / 4)) * 4;
       float M = neg_inf();
@@ -331,7 +291,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnPar
       for (int wq = 0; wq < NWARP; ++wq) {
         const float sc = ex2(sm_m[wq][h] - Mu);
         den += sc * sm_l[wq][h];
-        const float4 ov = *reinterpret_cast<const float4*>(&sm_o[wq][h][c]);
+        const float4 ov = *reinterpret_cast<const float4*>(sm_o + (wq * G + h) * D + c);
         num.x += sc * ov.x; num.y += sc * ov.y; num.z += sc * ov.z; num.w += sc * ov.w;
       }
       const float inv = den > 0.f ? 1.f / den : 0.f;
@@ -356,14 +316,305 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnPar
         }
       }
     }
-    __syncthreads();
+    sync();
+  }
+};
+
+// ------------------------------------------------------- cp.async kernel
+
+constexpr int kDecodeThreads = 128;
+constexpr int kDecodeStages = 2;   // cp.async ring depth
+constexpr int kDecodeKT = 48;      // keys per stage
+
+template <int D>
+constexpr int decode_smem_bytes() {
+  return kDecodeStages * kDecodeKT * D * 2 * 2;  // K and V rings, 16-bit elements
+}
+
+// Every thread gathers: thread t copies 16-byte chunk (t % (D/8)) of rows
+// t / (D/8) + i * (128 / (D/8)) of every stage, K and V sharing the page
+// lookup, zero-filled past hi. Of the ring shapes that fit four CTAs per SM
+// (2 x 32, 3 x 32, 2 x 48 keys) the widest stage measured fastest: the
+// per-stage cost (wait, barrier, max and rescale) is spread over more keys.
+template <int D, int G, bool BF16>
+__global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnParams p) {
+  using W = DecodeWarp<D, G, BF16, kDecodeThreads / 32, kDecodeKT>;
+  using T = typename W::T;
+  constexpr int CH = D / 8;                  // 16-byte chunks per row
+  constexpr int STAGE = kDecodeKT * D;       // elements per stage
+  constexpr int NWARP = kDecodeThreads / 32;
+
+  extern __shared__ __align__(128) uint8_t dsmem[];
+  T* sK = reinterpret_cast<T*>(dsmem);
+  T* sV = sK + kDecodeStages * STAGE;
+  __shared__ float sm_m[NWARP][G];
+  __shared__ float sm_l[NWARP][G];
+  // the warps' o partials reuse the ring once an item's keys are consumed
+  float* sm_o = reinterpret_cast<float*>(dsmem);
+  static_assert(NWARP * G * D * 4 <= kDecodeStages * kDecodeKT * D * 2 * 2, "o partials fit the ring");
+
+  const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
+  const int n_items = hdr->n_items;
+  const WorkItem* items = ws_ptr<const WorkItem>(p.ws, hdr->off_items);
+  const int32_t* qo_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_qo_indptr);
+  const int32_t* kv_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_kv_indptr);
+  const int32_t* kv_len = ws_ptr<const int32_t>(p.ws, hdr->off_kv_len);
+  const int window_left = hdr->window_left;
+
+  const int tid = threadIdx.x;
+  W wk;
+  wk.setup(tid >> 5, tid & 31);
+
+  for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+    const WorkItem it = items[w];
+    if (it.b < 0) continue;  // schedule padding
+    const int b = it.b, hk = it.kv_head;
+    const int token = qo_indptr[b];
+    const DecodeRange R = decode_range(it, kv_len[b], window_left, 1, kDecodeKT);
+    const int lo = R.lo, hi = R.hi;
+
+    const int32_t* pages = p.kv_indices + kv_indptr[b];
+    const T* kcol = static_cast<const T*>(p.k) + int64_t(hk) * p.k_stride_head + (tid % CH) * 8;
+    const T* vcol = static_cast<const T*>(p.v) + int64_t(hk) * p.v_stride_head + (tid % CH) * 8;
+    constexpr int ROWS_PER_PASS = kDecodeThreads / CH;
+    constexpr int PASSES = kDecodeKT / ROWS_PER_PASS;
+    const int my_row = tid / CH;
+    const uint32_t sk0 = smem_u32(sK + my_row * D + (tid % CH) * 8);
+    const uint32_t sv0 = smem_u32(sV + my_row * D + (tid % CH) * 8);
+    auto issue = [&](int tile, int stage) {
+      const int kt = lo + tile * kDecodeKT + my_row;
+#pragma unroll
+      for (int i = 0; i < PASSES; ++i) {
+        const int j = kt + i * ROWS_PER_PASS;
+        const T* ks = static_cast<const T*>(p.k);
+        const T* vs = static_cast<const T*>(p.v);
+        int bytes = 0;
+        if (j < hi) {
+          int32_t pi, slot;
+          if (p.page_shift >= 0) {
+            pi = j >> p.page_shift;
+            slot = j & ((1 << p.page_shift) - 1);
+          } else {
+            pi = j / p.page_size;
+            slot = j - pi * p.page_size;
+          }
+          const int64_t page = __ldg(pages + pi);
+          ks = kcol + page * p.k_stride_page + int64_t(slot) * p.k_stride_tok;
+          vs = vcol + page * p.v_stride_page + int64_t(slot) * p.v_stride_tok;
+          bytes = 16;
+        }
+        const uint32_t off = uint32_t((stage * STAGE + i * ROWS_PER_PASS * D) * 2);
+        cp_async16(sk0 + off, ks, bytes);
+        cp_async16(sv0 + off, vs, bytes);
+      }
+    };
+#pragma unroll
+    for (int s = 0; s < kDecodeStages - 1; ++s) {
+      if (s < R.n_tiles) issue(s, s);
+      cp_async_commit();
+    }
+    wk.begin(p, token, hk);
+
+    for (int tile = 0; tile < R.n_tiles; ++tile) {
+      cp_async_wait<kDecodeStages - 2>();
+      __syncthreads();
+      {
+        const int nt = tile + kDecodeStages - 1;
+        if (nt < R.n_tiles) issue(nt, nt % kDecodeStages);
+        cp_async_commit();
+      }
+      const int st = tile % kDecodeStages;
+      wk.stage(sK + st * STAGE, sV + st * STAGE, lo + tile * kDecodeKT, lo, hi);
+    }
+    cp_async_wait<0>();
+    __syncthreads();  // every warp is done with the ring before it holds o partials
+    wk.finish(p, it, token, tid, sm_o, sm_m, sm_l, [] { __syncthreads(); });
   }
 }
 
+// ------------------------------------------------------------ TMA kernel
+
+// Ring geometry of the TMA kernel: NCW consumer warps of 8 (D = 128) or 16
+// (D = 64) keys each per stage, NS stages, MINB CTAs per SM.
+template <int D>
+struct TmaCfg {
+  static constexpr int NCW = 4;
+  static constexpr int KT = NCW * 8 * (128 / D);  // keys per stage (a power of two)
+  static constexpr int NS = 4;
+  static constexpr int MINB = 3;
+  static constexpr int THREADS = (NCW + 1) * 32;
+  static constexpr int STAGE = KT * D;             // elements per stage, K or V
+  static constexpr int RING_BYTES = NS * STAGE * 2 * 2;
+  static constexpr int NBAR = 2 * NS;
+  // dynamic shared memory: ring | o partials | per-warp max, sum | barriers
+  template <int G>
+  static constexpr int o_bytes() { return NCW * G * D * 4; }
+  template <int G>
+  static constexpr int ml_bytes() { return 2 * NCW * G * 4; }
+  template <int G>
+  static constexpr int smem_bytes() { return RING_BYTES + o_bytes<G>() + ml_bytes<G>() + NBAR * 8 + 16; }
+  static_assert((KT & (KT - 1)) == 0, "keys per stage is a power of two");
+};
+
 template <int D, int G, bool BF16>
-cudaError_t launch_dg(const AttnParams& p, int grid, cudaStream_t s) {
+__global__ void __launch_bounds__(TmaCfg<D>::THREADS, TmaCfg<D>::MINB)
+    decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv, int box_rows) {
+  using C = TmaCfg<D>;
+  constexpr int NCW = C::NCW, KT = C::KT, NS = C::NS, STAGE = C::STAGE;
+  using W = DecodeWarp<D, G, BF16, NCW, KT>;
+  using T = typename W::T;
+
+  extern __shared__ __align__(128) uint8_t dsmem[];
+  T* sK = reinterpret_cast<T*>(dsmem);
+  T* sV = sK + NS * STAGE;
+  float* sm_o = reinterpret_cast<float*>(dsmem + C::RING_BYTES);
+  float (*sm_m)[G] = reinterpret_cast<float (*)[G]>(dsmem + C::RING_BYTES + C::template o_bytes<G>());
+  float (*sm_l)[G] = sm_m + NCW;
+  uint8_t* bar_base = dsmem + C::RING_BYTES + C::template o_bytes<G>() + C::template ml_bytes<G>();
+  const uint32_t bar0 = smem_u32(bar_base);
+  auto FULL = [&](int s) { return bar0 + 8u * uint32_t(s); };
+  auto EMPTY = [&](int s) { return bar0 + 8u * uint32_t(NS + s); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_base + C::NBAR * 8);
+
+  const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
+  const int n_items = hdr->n_items;
+  const WorkItem* items = ws_ptr<const WorkItem>(p.ws, hdr->off_items);
+  const int32_t* qo_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_qo_indptr);
+  const int32_t* kv_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_kv_indptr);
+  const int32_t* kv_len = ws_ptr<const int32_t>(p.ws, hdr->off_kv_len);
+  const int window_left = hdr->window_left;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(FULL(s), 1);
+      mbar_init(EMPTY(s), NCW);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  // a stage is KT / box_rows boxes of box_rows slots of one page
+  const int n_boxes = KT / box_rows;
+  const uint32_t box_bytes = uint32_t(box_rows) * D * 2;
+
+  if (warp == NCW) {
+    // ------------------------------------------------------------ producer
+    // Stage c of this CTA's sequence goes to slot c % NS; its (c / NS)-th
+    // fill waits for the consumers' release of the previous one.
+    int c = 0;
+    bool ok = true;
+    uint32_t last_par[NS];
+    bool armed[NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+      armed[s] = false;
+      last_par[s] = 0;
+    }
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const WorkItem it = items[w];
+      if (it.b < 0) continue;  // schedule padding
+      const DecodeRange R = decode_range(it, kv_len[it.b], window_left, box_rows, KT);
+      const int32_t* pages = p.kv_indices + kv_indptr[it.b];
+      for (int t = 0; t < R.n_tiles; ++t, ++c) {
+        const int st = c % NS;
+        const uint32_t par = uint32_t(c / NS) & 1u;
+        const int k0 = R.start + t * KT;
+        const int n_live = min(n_boxes, (R.hi - k0 + box_rows - 1) / box_rows);
+        bool okl = true;
+        if (lane == 0) {
+          if (c >= NS) okl = mbar_wait(EMPTY(st), par ^ 1u, abort_flag);
+          if (okl) mbar_expect_tx(FULL(st), uint32_t(n_live) * box_bytes * 2u);
+        }
+        okl = __shfl_sync(0xffffffffu, okl, 0);
+        if (!okl) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int s = 0; s < NS; ++s)
+          if (s == st) {
+            armed[s] = true;
+            last_par[s] = par;
+          }
+        const uint32_t dk = smem_u32(sK + st * STAGE), dv = smem_u32(sV + st * STAGE);
+        for (int i = lane; i < n_live; i += 32) {
+          const int kb = k0 + i * box_rows;
+          int pi, slot;
+          if (p.page_shift >= 0) {
+            pi = kb >> p.page_shift;
+            slot = kb & ((1 << p.page_shift) - 1);
+          } else {
+            pi = kb / p.page_size;
+            slot = kb - pi * p.page_size;
+          }
+          const int page = __ldg(pages + pi);
+          const uint32_t off = uint32_t(i) * box_bytes;
+          tma_load_4d(dk + off, &tk, FULL(st), 0, it.kv_head, slot, page);
+          tma_load_4d(dv + off, &tv, FULL(st), 0, it.kv_head, slot, page);
+        }
+      }
+    }
+    // Drain: the last fill of every slot has landed before the CTA exits
+    // (the consumers waited for all of them unless a wait expired; this wait
+    // ignores the abort flag but keeps its time bound).
+    if (lane == 0) {
+      volatile int no_abort = 0;
+#pragma unroll
+      for (int s = 0; s < NS; ++s)
+        if (armed[s]) mbar_wait(FULL(s), last_par[s], &no_abort);
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    W wk;
+    wk.setup(warp, lane);
+    int c = 0;
+    auto consumer_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory"); };
+    for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+      const WorkItem it = items[w];
+      if (it.b < 0) continue;  // schedule padding
+      const int token = qo_indptr[it.b];
+      const DecodeRange R = decode_range(it, kv_len[it.b], window_left, box_rows, KT);
+      wk.begin(p, token, it.kv_head);
+      for (int t = 0; t < R.n_tiles; ++t, ++c) {
+        const int st = c % NS;
+        // on an expired wait the warp goes on without the data (the abort
+        // flag makes every later wait return at once), so all consumer warps
+        // still meet at the same barriers; the error is reported below
+        mbar_wait(FULL(st), uint32_t(c / NS) & 1u, abort_flag);
+        wk.stage(sK + st * STAGE, sV + st * STAGE, R.start + t * KT, R.lo, R.hi);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(EMPTY(st));
+      }
+      wk.finish(p, it, token, tid, sm_o, sm_m, sm_l, consumer_sync);
+    }
+  }
+  __syncthreads();
+  if (tid == 0 && *abort_flag) {
+    int* err = const_cast<int*>(&hdr->err_flag);
+    atomicExch(err, 1);
+  }
+}
+
+// -------------------------------------------------------------- launchers
+
+template <int D, int G, bool BF16>
+cudaError_t launch_dg(const AttnParams& p, int grid, const CUtensorMap* tk, const CUtensorMap* tv,
+                      int box_rows, cudaStream_t s) {
+  if (tk) {
+    using C = TmaCfg<D>;
+    auto k = decode_tma_kernel<D, G, BF16>;
+    constexpr int smem = C::template smem_bytes<G>();
+    // once per process, before any capture (no attribute call inside a captured run)
+    static cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (attr != cudaSuccess) return attr;
+    k<<<grid, C::THREADS, smem, s>>>(p, *tk, *tv, box_rows);
+    return cudaGetLastError();
+  }
   auto k = decode_kernel<D, G, BF16>;
-  // once per process, before any capture (no attribute call inside a captured run)
   static cudaError_t attr =
       cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, decode_smem_bytes<D>());
   if (attr != cudaSuccess) return attr;
@@ -372,25 +623,54 @@ cudaError_t launch_dg(const AttnParams& p, int grid, cudaStream_t s) {
 }
 
 template <int D, bool BF16>
-cudaError_t launch_d(const AttnParams& p, int group, int grid, cudaStream_t s) {
+cudaError_t launch_d(const AttnParams& p, int group, int grid, const CUtensorMap* tk,
+                     const CUtensorMap* tv, int box_rows, cudaStream_t s) {
   switch (group) {
-    case 1: return launch_dg<D, 1, BF16>(p, grid, s);
-    case 2: return launch_dg<D, 2, BF16>(p, grid, s);
-    case 4: return launch_dg<D, 4, BF16>(p, grid, s);
+    case 1: return launch_dg<D, 1, BF16>(p, grid, tk, tv, box_rows, s);
+    case 2: return launch_dg<D, 2, BF16>(p, grid, tk, tv, box_rows, s);
+    case 4: return launch_dg<D, 4, BF16>(p, grid, tk, tv, box_rows, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
+int gcd_int(int a, int b) {
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
 }  // namespace
 
-cudaError_t launch_decode(const AttnParams& p, int head_dim, int group, bool bf16, int grid,
-                          cudaStream_t stream) {
+int decode_ctas_per_sm(int head_dim) {
+  return head_dim == 64 ? TmaCfg<64>::MINB : TmaCfg<128>::MINB;
+}
+
+cudaError_t launch_decode(const AttnParams& p, int head_dim, int group, bool bf16,
+                          int64_t num_pages, int grid, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
-  if (head_dim == 128) return bf16 ? launch_d<128, true>(p, group, grid, stream)
-                                   : launch_d<128, false>(p, group, grid, stream);
-  if (head_dim == 64) return bf16 ? launch_d<64, true>(p, group, grid, stream)
-                                  : launch_d<64, false>(p, group, grid, stream);
-  return cudaErrorInvalidValue;
+  if (head_dim != 128 && head_dim != 64) return cudaErrorInvalidValue;
+  // Boxes of gcd(page_size, KT) slots never cross a page: every box starts
+  // at a multiple of that size (tiles start at lo rounded down to it).
+  const int kt = head_dim == 128 ? TmaCfg<128>::KT : TmaCfg<64>::KT;
+  const int box_rows = gcd_int(p.page_size, kt);
+  CUtensorMap tk, tv;
+  const bool tma =
+      num_pages > 0 &&
+      encode_paged_kv_map(&tk, bf16, p.k, head_dim, p.num_kv_heads, p.page_size, num_pages,
+                          p.k_stride_head, p.k_stride_tok, p.k_stride_page, head_dim, box_rows,
+                          CU_TENSOR_MAP_SWIZZLE_NONE) &&
+      encode_paged_kv_map(&tv, bf16, p.v, head_dim, p.num_kv_heads, p.page_size, num_pages,
+                          p.v_stride_head, p.v_stride_tok, p.v_stride_page, head_dim, box_rows,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+  const CUtensorMap* mk = tma ? &tk : nullptr;
+  const CUtensorMap* mv = tma ? &tv : nullptr;
+  if (head_dim == 128) return bf16 ? launch_d<128, true>(p, group, grid, mk, mv, box_rows, stream)
+                                   : launch_d<128, false>(p, group, grid, mk, mv, box_rows, stream);
+  return bf16 ? launch_d<64, true>(p, group, grid, mk, mv, box_rows, stream)
+              : launch_d<64, false>(p, group, grid, mk, mv, box_rows, stream);
 }
 
 }  // namespace fi

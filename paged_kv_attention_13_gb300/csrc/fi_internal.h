@@ -82,8 +82,11 @@ enum KernelId : int32_t {
 };
 
 // Launchers (defined in the .cu files). Each returns cudaGetLastError().
-cudaError_t launch_decode(const AttnParams& p, int head_dim, int group, bool bf16, int grid,
-                          cudaStream_t stream);
+// num_pages: pages in the K/V cache tensors (the TMA maps' outer extent).
+cudaError_t launch_decode(const AttnParams& p, int head_dim, int group, bool bf16,
+                          int64_t num_pages, int grid, cudaStream_t stream);
+// CTAs per SM the decode kernel is built for.
+int decode_ctas_per_sm(int head_dim);
 cudaError_t launch_prefill_mma(const AttnParams& p, int head_dim, int kernel, bool bf16,
                                int grid, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const AttnParams& p, int head_dim, int group, int tile_rows,

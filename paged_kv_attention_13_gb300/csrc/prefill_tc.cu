@@ -32,9 +32,7 @@
 // (!causal || j <= i + Lk - Lq) && (wl < 0 || j + Lq + wl >= Lk + i). Key
 // tiles outside the item's live range are never loaded; the per-element
 // test runs on tiles that straddle a bound only.
-#include <cuda.h>
-
-#include "common.cuh"
+#include "tma.cuh"
 
 namespace fi {
 namespace {
@@ -51,69 +49,6 @@ constexpr int kSmemTc = kOffBar + 256 + 1024;  // barriers, alignment slack
 // barrier slots
 constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 4, B_VFULL = 6, B_VEMPTY = 8,
               B_SFULL = 10, B_PFULL = 12, B_ODONE = 14, B_OFREE = 16, B_FINAL = 18, N_BARS = 19;
-
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
-
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Wait for the phase of `parity` to complete; false on timeout or abort.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y, int z, int w) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
-      : "memory");
-}
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -329,7 +264,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(BAR(B_FINAL), 1);
     *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_init_fence();
   }
   // K/V stages start zeroed so rows no copy has written yet hold finite values
   for (int i = threadIdx.x; i < (4 * kTile) / 16; i += kTcThreads)
@@ -746,38 +681,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// against libcuda).
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = []() -> EncodeTiledFn {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    return reinterpret_cast<EncodeTiledFn>(ptr);
-  }();
-  return fn;
-}
-
-bool encode(CUtensorMap* m, bool bf16, int rank, const void* base, const cuuint64_t* dims,
-            const cuuint64_t* strides_bytes, const cuuint32_t* box) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                  cuuint32_t(rank), const_cast<void*>(base), dims, strides_bytes, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 bool prefill_tc_supports(int head_dim, int page_size, int group) {
@@ -797,19 +700,16 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int head_dim, int group, int 
     cuuint64_t dims[3] = {cuuint64_t(head_dim), cuuint64_t(p.num_qo_heads), cuuint64_t(q_rows)};
     cuuint64_t str[2] = {cuuint64_t(p.q_stride_head) * 2, cuuint64_t(p.q_stride_tok) * 2};
     cuuint32_t box[3] = {64, cuuint32_t(group), cuuint32_t(tile_rows / 2 / group)};
-    if (!encode(&tq, bf16, 3, p.q, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_tensor_map(&tq, bf16, 3, p.q, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
   }
-  {
-    cuuint64_t dims[4] = {cuuint64_t(head_dim), cuuint64_t(p.num_kv_heads),
-                          cuuint64_t(p.page_size), cuuint64_t(num_pages)};
-    cuuint32_t box[4] = {64, 1, cuuint32_t(box_rows), 1};
-    cuuint64_t sk[3] = {cuuint64_t(p.k_stride_head) * 2, cuuint64_t(p.k_stride_tok) * 2,
-                        cuuint64_t(p.k_stride_page) * 2};
-    cuuint64_t sv[3] = {cuuint64_t(p.v_stride_head) * 2, cuuint64_t(p.v_stride_tok) * 2,
-                        cuuint64_t(p.v_stride_page) * 2};
-    if (!encode(&tk, bf16, 4, p.k, dims, sk, box)) return cudaErrorInvalidValue;
-    if (!encode(&tv, bf16, 4, p.v, dims, sv, box)) return cudaErrorInvalidValue;
-  }
+  if (!encode_paged_kv_map(&tk, bf16, p.k, head_dim, p.num_kv_heads, p.page_size, num_pages,
+                           p.k_stride_head, p.k_stride_tok, p.k_stride_page, 64, box_rows,
+                           CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_paged_kv_map(&tv, bf16, p.v, head_dim, p.num_kv_heads, p.page_size, num_pages,
+                           p.v_stride_head, p.v_stride_tok, p.v_stride_page, 64, box_rows,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   if (bf16) {
     static cudaError_t attr = cudaFuncSetAttribute(
         prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
