@@ -213,6 +213,8 @@ class Runner:
             self.run()
             en[i].record(s)
         torch.cuda.synchronize()
+        if self.plan.device_error():
+            raise RuntimeError("a kernel gave up an expired bounded wait: timings are not valid")
         ms = [a.elapsed_time(b) for a, b in zip(st, en)]
         return float(np.mean(ms)), float(np.median(ms))
 

@@ -224,6 +224,16 @@ fi_status fi_plan_get_info(fi_plan_t plan, fi_plan_info* info, int32_t* items,
 fi_status fi_plan_read_device(fi_plan_t plan, int32_t* items, int32_t items_capacity,
                               int32_t* merge_indptr, int32_t merge_capacity, void* stream);
 
+/* Read the device error flag of the plan's workspace (synchronises the
+ * stream). A kernel sets it when one of its bounded waits on an mbarrier
+ * expired (2 s): it then gives up the rest of its work, waits (bounded) for
+ * its own copies in flight and exits, so the context stays usable but that
+ * launch's output is not valid. *err_flag receives 0 (no expiry since the
+ * last fi_plan or clear) or 1. clear != 0 resets the flag afterwards. Errors:
+ * FI_ERR_INVALID_ARG (NULL plan or pointer, host-only plan),
+ * FI_ERR_NOT_PLANNED, FI_ERR_CUDA. */
+fi_status fi_plan_device_error(fi_plan_t plan, int32_t* err_flag, int clear, void* stream);
+
 /*
  * Batch decode that allocates nothing (the pages have no counterpart; this is
  * an addition of this library).

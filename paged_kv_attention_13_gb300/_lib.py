@@ -24,6 +24,7 @@ EXPORTED = [
     "fi_batch_decode_paged", "fi_merge_state", "fi_merge_states", "fi_plan_get_info",
     "fi_plan_read_device", "fi_plan_destroy", "fi_last_error", "fi_status_str",
     "fi_batch_decode_paged_noalloc", "fi_noalloc_scratch_bytes", "fi_noalloc_last_error",
+    "fi_plan_device_error",
 ]
 
 
@@ -74,6 +75,8 @@ def load():
     lib.fi_plan_get_info.argtypes = [P, ctypes.POINTER(FiPlanInfo), pi32, i32, pi32, i32]
     lib.fi_plan_read_device.restype = ctypes.c_int
     lib.fi_plan_read_device.argtypes = [P, pi32, i32, pi32, i32, P]
+    lib.fi_plan_device_error.restype = ctypes.c_int
+    lib.fi_plan_device_error.argtypes = [P, pi32, ctypes.c_int, P]
     lib.fi_plan_destroy.restype = None
     lib.fi_plan_destroy.argtypes = [P]
     lib.fi_last_error.restype = ctypes.c_char_p

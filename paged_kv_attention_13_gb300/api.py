@@ -151,6 +151,15 @@ class Plan:
         return items[: inf["num_items"] * 8].reshape(-1, 8), merge
 
 
+    def device_error(self, clear=False, stream=None) -> int:
+        """fi_plan_device_error: 1 when a kernel run on this plan's workspace
+        gave up an expired bounded wait since the last plan / clear, else 0."""
+        v = ctypes.c_int32(0)
+        _check(self._lib.fi_plan_device_error(self.handle, ctypes.byref(v), int(bool(clear)),
+                                              _stream_handle(stream)))
+        return int(v.value)
+
+
 def fi_plan(plan: Plan, *args, **kwargs) -> Plan:
     return plan.plan(*args, **kwargs)
 

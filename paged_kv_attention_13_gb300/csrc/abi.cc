@@ -10,6 +10,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <cstddef>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -685,6 +686,22 @@ extern "C" fi_status fi_plan_read_device(fi_plan_t p, int32_t* items, int32_t it
     if (merge_capacity < h.total_rows + 1) return fail(FI_ERR_CAPACITY, "plan_read_device: merge");
     std::memcpy(merge_indptr, buf.data() + h.off_merge_indptr, size_t(h.total_rows + 1) * 4);
   }
+  return ok();
+}
+
+extern "C" fi_status fi_plan_device_error(fi_plan_t p, int32_t* err_flag, int clear,
+                                          void* stream) {
+  if (!p || !err_flag) return fail(FI_ERR_INVALID_ARG, "plan_device_error: NULL argument");
+  if (!p->planned) return fail(FI_ERR_NOT_PLANNED, "plan_device_error: call fi_plan() first");
+  if (p->host_only) return fail(FI_ERR_INVALID_ARG, "plan_device_error: host-only plan");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* flag = static_cast<uint8_t*>(p->ws) + offsetof(WsHeader, err_flag);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, flag, sizeof v, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(flag, 0, sizeof v, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail(FI_ERR_CUDA, "plan_device_error: %s", cudaGetErrorString(e));
+  *err_flag = v;
   return ok();
 }
 

@@ -132,6 +132,25 @@ struct DecodeWarp {
       for (int e = 0; e < 4; ++e) o2[h][e] = make_float2(0.f, 0.f);
   }
 
+  // Same as begin(), with q of the G heads staged in shared memory as
+  // [G][D] (head h of the group at row h).
+  __device__ __forceinline__ void begin_smem(const T* qs, float sm_scale_log2) {
+#pragma unroll
+    for (int sl = 0; sl < G; ++sl) {
+      const uint4 r = *reinterpret_cast<const uint4*>(qs + (myh ^ sl) * D + dl * 8);
+      const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        q2[sl][e] = make_float2(DT::lo(wv[e]) * sm_scale_log2, DT::hi(wv[e]) * sm_scale_log2);
+    }
+    m_me = neg_inf();
+    l_me = 0.f;
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o2[h][e] = make_float2(0.f, 0.f);
+  }
+
   // Consume one stage: keys k0 .. k0+KT-1 in rows 0..KT-1 of cK / cV, of
   // which [lo, hi) are live. Rows outside the live range may hold anything
   // (a neighbour's page slots): their scores are masked to -inf and their V
@@ -232,7 +251,8 @@ struct DecodeWarp {
   // consumer threads (tid = 0 .. NWARP*32-1); sm_o holds NWARP x G x D
   // floats. Ends with a barrier, so the shared arrays are free on return.
   template <class Sync>
-  __device__ __forceinline__ void finish(const AttnParams& p, const WorkItem& it, int token, int tid,
+  __device__ __forceinline__ void finish(const AttnParams& p, int token, int hk, int chunk,
+                                         int partial_base, float* tmp_o, float* tmp_lse, int tid,
                                          float* sm_o, float (*sm_m)[G], float (*sm_l)[G],
                                          Sync sync) {
     // sums over the warp's key groups (they share each head's max)
@@ -271,13 +291,9 @@ struct DecodeWarp {
     }
     sync();
 
-    const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
-    float* tmp_lse = ws_ptr<float>(p.ws, hdr->off_tmp_lse);
-    float* tmp_o = ws_ptr<float>(p.ws, hdr->off_tmp_o);
     const int Hq = p.num_qo_heads;
-    const int hk = it.kv_head;
-    const bool direct = it.chunk < 0;
-    const int slot = direct ? 0 : it.partial_base + it.chunk;
+    const bool direct = chunk < 0;
+    const int slot = direct ? 0 : partial_base + chunk;
     for (int idx = tid; idx < G * (D / 4); idx += NWARP * 32) {
       const int h = idx / (D / 4);
       const int c = (idx % (D / 4)) * 4;
@@ -359,6 +375,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnPar
   const int32_t* qo_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_qo_indptr);
   const int32_t* kv_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_kv_indptr);
   const int32_t* kv_len = ws_ptr<const int32_t>(p.ws, hdr->off_kv_len);
+  float* tmp_lse = ws_ptr<float>(p.ws, hdr->off_tmp_lse);
+  float* tmp_o = ws_ptr<float>(p.ws, hdr->off_tmp_o);
   const int window_left = hdr->window_left;
 
   const int tid = threadIdx.x;
@@ -428,32 +446,45 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnPar
     }
     cp_async_wait<0>();
     __syncthreads();  // every warp is done with the ring before it holds o partials
-    wk.finish(p, it, token, tid, sm_o, sm_m, sm_l, [] { __syncthreads(); });
+    wk.finish(p, token, hk, it.chunk, it.partial_base, tmp_o, tmp_lse, tid, sm_o, sm_m, sm_l,
+              [] { __syncthreads(); });
   }
 }
 
 // ------------------------------------------------------------ TMA kernel
 
-// Ring geometry of the TMA kernel: NCW consumer warps of 8 (D = 128) or 16
-// (D = 64) keys each per stage, NS stages, MINB CTAs per SM.
+// Ring geometry of the TMA kernel: NCW consumer warps of KPW keys each per
+// stage (D = 128; twice as many keys at D = 64, so a stage is always the same
+// bytes), NS stages, MINB CTAs per SM. Among the shapes that fit three CTAs
+// per SM, 2 stages of 64 keys measured fastest.
 template <int D>
 struct TmaCfg {
   static constexpr int NCW = 4;
-  static constexpr int KT = NCW * 8 * (128 / D);  // keys per stage (a power of two)
-  static constexpr int NS = 4;
+  static constexpr int KPW = 16;
+  static constexpr int KT = NCW * KPW * (128 / D);  // keys per stage (a power of two)
+  static constexpr int NS = 2;
   static constexpr int MINB = 3;
   static constexpr int THREADS = (NCW + 1) * 32;
   static constexpr int STAGE = KT * D;             // elements per stage, K or V
   static constexpr int RING_BYTES = NS * STAGE * 2 * 2;
-  static constexpr int NBAR = 2 * NS;
-  // dynamic shared memory: ring | o partials | per-warp max, sum | barriers
-  template <int G>
-  static constexpr int o_bytes() { return NCW * G * D * 4; }
-  template <int G>
-  static constexpr int ml_bytes() { return 2 * NCW * G * 4; }
-  template <int G>
-  static constexpr int smem_bytes() { return RING_BYTES + o_bytes<G>() + ml_bytes<G>() + NBAR * 8 + 16; }
+  static constexpr int NBAR = 2 * NS + 1;          // full, empty per slot; merge
+  // dynamic shared memory: K/V ring | o partials | per-warp max, sum |
+  // q per slot | stage header per slot | barriers, abort flag
+  template <int G> static constexpr int o_off() { return RING_BYTES; }
+  template <int G> static constexpr int ml_off() { return o_off<G>() + NCW * G * D * 4; }
+  template <int G> static constexpr int q_off() { return ml_off<G>() + 2 * NCW * G * 4; }
+  template <int G> static constexpr int hdr_off() { return q_off<G>() + NS * G * D * 2; }
+  template <int G> static constexpr int bar_off() { return hdr_off<G>() + NS * 32; }
+  template <int G> static constexpr int smem_bytes() { return bar_off<G>() + NBAR * 8 + 16; }
   static_assert((KT & (KT - 1)) == 0, "keys per stage is a power of two");
+  static_assert(MINB * (smem_bytes<4>() + 1024) <= 233472, "MINB CTAs fit one SM's shared memory");
+};
+
+// Stage header, written by the producer before it arms the stage's barrier.
+enum : int32_t { kStFirst = 1, kStLast = 2, kStEnd = 4, kStNoKeys = 8 };
+struct alignas(16) StageHdr {
+  int32_t flags, k0, lo, hi;                      // this stage
+  int32_t token, kv_head, chunk, partial_base;    // its work item
 };
 
 template <int D, int G, bool BF16>
@@ -468,23 +499,19 @@ __global__ void __launch_bounds__(TmaCfg<D>::THREADS, TmaCfg<D>::MINB)
   extern __shared__ __align__(128) uint8_t dsmem[];
   T* sK = reinterpret_cast<T*>(dsmem);
   T* sV = sK + NS * STAGE;
-  float* sm_o = reinterpret_cast<float*>(dsmem + C::RING_BYTES);
-  float (*sm_m)[G] = reinterpret_cast<float (*)[G]>(dsmem + C::RING_BYTES + C::template o_bytes<G>());
+  float* sm_o = reinterpret_cast<float*>(dsmem + C::template o_off<G>());
+  float (*sm_m)[G] = reinterpret_cast<float (*)[G]>(dsmem + C::template ml_off<G>());
   float (*sm_l)[G] = sm_m + NCW;
-  uint8_t* bar_base = dsmem + C::RING_BYTES + C::template o_bytes<G>() + C::template ml_bytes<G>();
-  const uint32_t bar0 = smem_u32(bar_base);
+  T* sQ = reinterpret_cast<T*>(dsmem + C::template q_off<G>());  // [NS][G][D]
+  StageHdr* sH = reinterpret_cast<StageHdr*>(dsmem + C::template hdr_off<G>());
+  const uint32_t bar0 = smem_u32(dsmem + C::template bar_off<G>());
   auto FULL = [&](int s) { return bar0 + 8u * uint32_t(s); };
   auto EMPTY = [&](int s) { return bar0 + 8u * uint32_t(NS + s); };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_base + C::NBAR * 8);
+  const uint32_t MERGE = bar0 + 8u * uint32_t(2 * NS);
+  volatile int* abort_flag =
+      reinterpret_cast<volatile int*>(dsmem + C::template bar_off<G>() + C::NBAR * 8);
 
   const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
-  const int n_items = hdr->n_items;
-  const WorkItem* items = ws_ptr<const WorkItem>(p.ws, hdr->off_items);
-  const int32_t* qo_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_qo_indptr);
-  const int32_t* kv_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_kv_indptr);
-  const int32_t* kv_len = ws_ptr<const int32_t>(p.ws, hdr->off_kv_len);
-  const int window_left = hdr->window_left;
-
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -492,19 +519,27 @@ __global__ void __launch_bounds__(TmaCfg<D>::THREADS, TmaCfg<D>::MINB)
       mbar_init(FULL(s), 1);
       mbar_init(EMPTY(s), NCW);
     }
+    mbar_init(MERGE, NCW * 32);
     *abort_flag = 0;
     mbar_init_fence();
   }
   __syncthreads();
 
-  // a stage is KT / box_rows boxes of box_rows slots of one page
-  const int n_boxes = KT / box_rows;
-  const uint32_t box_bytes = uint32_t(box_rows) * D * 2;
-
   if (warp == NCW) {
     // ------------------------------------------------------------ producer
     // Stage c of this CTA's sequence goes to slot c % NS; its (c / NS)-th
-    // fill waits for the consumers' release of the previous one.
+    // fill waits for the consumers' release of the previous one. Everything
+    // a stage needs from global memory (the item's metadata, the page
+    // indices) is loaded before that wait, so a full ring hides it.
+    const int n_items = hdr->n_items;
+    const WorkItem* items = ws_ptr<const WorkItem>(p.ws, hdr->off_items);
+    const int32_t* qo_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_qo_indptr);
+    const int32_t* kv_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_kv_indptr);
+    const int32_t* kv_len = ws_ptr<const int32_t>(p.ws, hdr->off_kv_len);
+    const int window_left = hdr->window_left;
+    const int n_boxes = KT / box_rows;  // a stage is n_boxes boxes of box_rows slots of one page
+    const uint32_t box_bytes = uint32_t(box_rows) * D * 2;
+    constexpr int BPL = (KT + 31) / 32;  // boxes per lane, at most
     int c = 0;
     bool ok = true;
     uint32_t last_par[NS];
@@ -514,49 +549,99 @@ __global__ void __launch_bounds__(TmaCfg<D>::THREADS, TmaCfg<D>::MINB)
       armed[s] = false;
       last_par[s] = 0;
     }
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const WorkItem it = items[w];
-      if (it.b < 0) continue;  // schedule padding
-      const DecodeRange R = decode_range(it, kv_len[it.b], window_left, box_rows, KT);
-      const int32_t* pages = p.kv_indices + kv_indptr[it.b];
-      for (int t = 0; t < R.n_tiles; ++t, ++c) {
-        const int st = c % NS;
-        const uint32_t par = uint32_t(c / NS) & 1u;
-        const int k0 = R.start + t * KT;
-        const int n_live = min(n_boxes, (R.hi - k0 + box_rows - 1) / box_rows);
-        bool okl = true;
-        if (lane == 0) {
-          if (c >= NS) okl = mbar_wait(EMPTY(st), par ^ 1u, abort_flag);
-          if (okl) mbar_expect_tx(FULL(st), uint32_t(n_live) * box_bytes * 2u);
+    // claim slot st for stage c: wait for its release, then write the header
+    // and arm its barrier for `bytes` (lane 0); false once the CTA aborts.
+    // Every armed phase is recorded (the end-of-work stage too), so the drain
+    // below waits on each slot's latest phase.
+    auto claim = [&](int st, uint32_t par, const StageHdr& h, uint32_t bytes) {
+      bool okl = true;
+      if (lane == 0) {
+        if (c >= NS) okl = mbar_wait(EMPTY(st), par ^ 1u, abort_flag);
+        if (okl) {
+          sH[st] = h;
+          mbar_expect_tx(FULL(st), bytes);
         }
-        okl = __shfl_sync(0xffffffffu, okl, 0);
-        if (!okl) {
-          ok = false;
-          break;
-        }
+      }
+      okl = __shfl_sync(0xffffffffu, okl, 0) != 0;
+      if (okl) {
 #pragma unroll
         for (int s = 0; s < NS; ++s)
           if (s == st) {
             armed[s] = true;
             last_par[s] = par;
           }
-        const uint32_t dk = smem_u32(sK + st * STAGE), dv = smem_u32(sV + st * STAGE);
-        for (int i = lane; i < n_live; i += 32) {
-          const int kb = k0 + i * box_rows;
-          int pi, slot;
-          if (p.page_shift >= 0) {
-            pi = kb >> p.page_shift;
-            slot = kb & ((1 << p.page_shift) - 1);
-          } else {
-            pi = kb / p.page_size;
-            slot = kb - pi * p.page_size;
+      }
+      return okl;
+    };
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const WorkItem it = items[w];
+      if (it.b < 0) continue;  // schedule padding
+      const int token = qo_indptr[it.b];
+      const DecodeRange R = decode_range(it, kv_len[it.b], window_left, box_rows, KT);
+      const int32_t* pages = p.kv_indices + kv_indptr[it.b];
+      const T* qsrc = static_cast<const T*>(p.q) + int64_t(token) * p.q_stride_tok +
+                      int64_t(it.kv_head * G) * p.q_stride_head;
+      const int n_st = max(R.n_tiles, 1);  // an item without keys still writes its output
+      for (int t = 0; t < n_st; ++t, ++c) {
+        const int st = c % NS;
+        const uint32_t par = uint32_t(c / NS) & 1u;
+        const int k0 = R.start + t * KT;
+        const int n_live = R.n_tiles ? min(n_boxes, (R.hi - k0 + box_rows - 1) / box_rows) : 0;
+        int page[BPL], slot[BPL];
+#pragma unroll
+        for (int j = 0; j < BPL; ++j) {
+          const int i = lane + 32 * j;
+          page[j] = 0;
+          slot[j] = 0;
+          if (i < n_live) {
+            const int kb = k0 + i * box_rows;
+            int pi;
+            if (p.page_shift >= 0) {
+              pi = kb >> p.page_shift;
+              slot[j] = kb & ((1 << p.page_shift) - 1);
+            } else {
+              pi = kb / p.page_size;
+              slot[j] = kb - pi * p.page_size;
+            }
+            page[j] = __ldg(pages + pi);
           }
-          const int page = __ldg(pages + pi);
-          const uint32_t off = uint32_t(i) * box_bytes;
-          tma_load_4d(dk + off, &tk, FULL(st), 0, it.kv_head, slot, page);
-          tma_load_4d(dv + off, &tv, FULL(st), 0, it.kv_head, slot, page);
+        }
+        StageHdr h;
+        h.flags = (t == 0 ? kStFirst : 0) | (t == n_st - 1 ? kStLast : 0) |
+                  (R.n_tiles ? 0 : kStNoKeys);
+        h.k0 = k0;
+        h.lo = R.lo;
+        h.hi = R.hi;
+        h.token = token;
+        h.kv_head = it.kv_head;
+        h.chunk = it.chunk;
+        h.partial_base = it.partial_base;
+        const uint32_t qbytes = t == 0 ? uint32_t(G * D * 2) : 0u;
+        if (!claim(st, par, h, uint32_t(n_live) * box_bytes * 2u + qbytes)) {
+          ok = false;
+          break;
+        }
+        if (t == 0 && lane < G)
+          bulk_load(smem_u32(sQ + (st * G + lane) * D), qsrc + int64_t(lane) * p.q_stride_head,
+                    uint32_t(D * 2), FULL(st));
+        const uint32_t dk = smem_u32(sK + st * STAGE), dv = smem_u32(sV + st * STAGE);
+#pragma unroll
+        for (int j = 0; j < BPL; ++j) {
+          const int i = lane + 32 * j;
+          if (i < n_live) {
+            const uint32_t off = uint32_t(i) * box_bytes;
+            tma_load_4d(dk + off, &tk, FULL(st), 0, it.kv_head, slot[j], page[j]);
+            tma_load_4d(dv + off, &tv, FULL(st), 0, it.kv_head, slot[j], page[j]);
+          }
         }
       }
+    }
+    if (ok) {
+      // end of work: a header-only stage tells the consumers to stop
+      StageHdr h = {};
+      h.flags = kStEnd;
+      const int st = c % NS;
+      if (!claim(st, uint32_t(c / NS) & 1u, h, 0u)) ok = false;
     }
     // Drain: the last fill of every slot has landed before the CTA exits
     // (the consumers waited for all of them unless a wait expired; this wait
@@ -565,31 +650,38 @@ __global__ void __launch_bounds__(TmaCfg<D>::THREADS, TmaCfg<D>::MINB)
       volatile int no_abort = 0;
 #pragma unroll
       for (int s = 0; s < NS; ++s)
-        if (armed[s]) mbar_wait(FULL(s), last_par[s], &no_abort);
+        if (armed[s] && !mbar_wait(FULL(s), last_par[s], &no_abort)) *abort_flag = 1;
     }
   } else {
     // ------------------------------------------------------------ consumers
+    // Consumers read nothing from global memory: each stage's header says
+    // which keys it holds and where the item's output goes, and an item's
+    // first stage brings its q.
+    float* tmp_lse = ws_ptr<float>(p.ws, hdr->off_tmp_lse);
+    float* tmp_o = ws_ptr<float>(p.ws, hdr->off_tmp_o);
     W wk;
     wk.setup(warp, lane);
-    int c = 0;
-    auto consumer_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory"); };
-    for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
-      const WorkItem it = items[w];
-      if (it.b < 0) continue;  // schedule padding
-      const int token = qo_indptr[it.b];
-      const DecodeRange R = decode_range(it, kv_len[it.b], window_left, box_rows, KT);
-      wk.begin(p, token, it.kv_head);
-      for (int t = 0; t < R.n_tiles; ++t, ++c) {
-        const int st = c % NS;
-        // on an expired wait the warp goes on without the data (the abort
-        // flag makes every later wait return at once), so all consumer warps
-        // still meet at the same barriers; the error is reported below
-        mbar_wait(FULL(st), uint32_t(c / NS) & 1u, abort_flag);
-        wk.stage(sK + st * STAGE, sV + st * STAGE, R.start + t * KT, R.lo, R.hi);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(EMPTY(st));
-      }
-      wk.finish(p, it, token, tid, sm_o, sm_m, sm_l, consumer_sync);
+    uint32_t n_sync = 0;
+    // barrier over the consumer threads, bounded like every other wait
+    auto consumer_sync = [&] {
+      mbar_arrive(MERGE);
+      mbar_wait(MERGE, n_sync & 1u, abort_flag);
+      ++n_sync;
+    };
+    for (int c = 0;; ++c) {
+      const int st = c % NS;
+      // an expired wait ends the warp's work (the abort flag then makes
+      // every other wait return at once); the error is reported below
+      if (!mbar_wait(FULL(st), uint32_t(c / NS) & 1u, abort_flag)) break;
+      const StageHdr h = sH[st];
+      if (h.flags & kStEnd) break;
+      if (h.flags & kStFirst) wk.begin_smem(sQ + st * G * D, p.sm_scale_log2);
+      if (!(h.flags & kStNoKeys)) wk.stage(sK + st * STAGE, sV + st * STAGE, h.k0, h.lo, h.hi);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(EMPTY(st));
+      if (h.flags & kStLast)
+        wk.finish(p, h.token, h.kv_head, h.chunk, h.partial_base, tmp_o, tmp_lse, tid, sm_o,
+                  sm_m, sm_l, consumer_sync);
     }
   }
   __syncthreads();

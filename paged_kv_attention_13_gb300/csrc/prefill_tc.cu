@@ -392,6 +392,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int s = 0; s < 2; ++s)
           if (armed[which][s])
             mbar_wait(BAR((which ? B_VFULL : B_KFULL) + s), apar[which][s], &no_abort);
+      if (no_abort) *abort_flag = 1;  // an expired drain wait is reported too
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -480,7 +481,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // every MMA this thread issued has completed before tensor memory is freed
       tc_commit(BAR(B_FINAL));
       volatile int no_abort = 0;
-      mbar_wait(BAR(B_FINAL), 0, &no_abort);
+      if (!mbar_wait(BAR(B_FINAL), 0, &no_abort)) *abort_flag = 1;
     }
     __syncwarp();
   }

@@ -46,6 +46,7 @@ def run_gpu(pb, causal, window_left, mode="prefill", force_kv_chunks=0, ws=None,
                   dtype=TD[pb.dtype], q_len_per_req=qlpr, force_kv_chunks=force_kv_chunks)
         out, lse = fi.fi_batch_decode_paged(plan, q, k, v, idx, pb.sm_scale)
     torch.cuda.synchronize()
+    assert plan.device_error() == 0, "a kernel gave up an expired bounded wait"
     return out, lse, plan
 
 
