@@ -331,8 +331,8 @@ def run_ours(args):
     e2e_ms, h2d, d2h = r.time_e2e(max(3, args.steps // 2), 2)
     e2e_value = world * r.bytes / (e2e_ms * 1e-3) / 1e9
     achieved = r.bytes / (ms_step * 1e-3) / 1e9
-    traffic = traffic_from_profile("decode.cu", "decode_kernel_batch64.txt")
-    roof = {"bound": "hbm", "kernel": "decode_kernel (+ split-KV merge, timed together)",
+    traffic = traffic_from_profile("decode.cu", "decode_tma_kernel_batch64.txt")
+    roof = {"bound": "hbm", "kernel": "decode_tma_kernel (+ split-KV merge, timed together)",
             "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
             "frac_of_nominal_8000": round(achieved / 8000.0, 4),

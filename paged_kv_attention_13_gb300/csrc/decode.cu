@@ -10,17 +10,15 @@
 // At the end of an item the warps' (max, sum, o) states are merged in shared
 // memory.
 //
-// Two kernels fill the ring:
-//   decode_tma_kernel  one producer warp issues, per page of a stage, one
-//                      cp.async.bulk.tensor box of K and one of V (4-D maps
-//                      over [pages, slot, kv head, dim]); mbarriers hand the
-//                      stages to the consumer warps and back. The producer
-//                      runs ahead across work items, so the ring stays full
-//                      through item boundaries and the consumers issue no
-//                      load instructions at all.
-//   decode_kernel      every thread gathers 16-byte chunks with cp.async
-//                      (2 stages of 48 keys, four CTAs per SM), used when the
-//                      driver refuses a tensor map for the cache's strides.
+// One producer warp fills the ring: per page of a stage it issues one
+// cp.async.bulk.tensor box of K and one of V (4-D maps over [pages, slot,
+// kv head, dim]), and for an item's first stage q by plain bulk copy;
+// mbarriers hand the stages to the consumer warps and back. The producer
+// runs ahead across work items, so the ring stays full through item
+// boundaries, and the consumer warps issue no load instructions at all.
+// (A version in which every thread gathered 16-byte chunks with cp.async
+// reached 4870 GB/s at best on the batch-64 decode, against 5750 for this
+// one, and was slower at page size 1 too.)
 //
 // Mask for one query row (Lq = 1) [P1 "Why window_size_right stays -1"],
 // [P2 "Summary"]: causal keeps every key j <= Lk - 1; the window keeps
@@ -336,121 +334,6 @@ struct DecodeWarp {
   }
 };
 
-// ------------------------------------------------------- cp.async kernel
-
-constexpr int kDecodeThreads = 128;
-constexpr int kDecodeStages = 2;   // cp.async ring depth
-constexpr int kDecodeKT = 48;      // keys per stage
-
-template <int D>
-constexpr int decode_smem_bytes() {
-  return kDecodeStages * kDecodeKT * D * 2 * 2;  // K and V rings, 16-bit elements
-}
-
-// Every thread gathers: thread t copies 16-byte chunk (t % (D/8)) of rows
-// t / (D/8) + i * (128 / (D/8)) of every stage, K and V sharing the page
-// lookup, zero-filled past hi. Of the ring shapes that fit four CTAs per SM
-// (2 x 32, 3 x 32, 2 x 48 keys) the widest stage measured fastest: the
-// per-stage cost (wait, barrier, max and rescale) is spread over more keys.
-template <int D, int G, bool BF16>
-__global__ void __launch_bounds__(kDecodeThreads, 4) decode_kernel(const AttnParams p) {
-  using W = DecodeWarp<D, G, BF16, kDecodeThreads / 32, kDecodeKT>;
-  using T = typename W::T;
-  constexpr int CH = D / 8;                  // 16-byte chunks per row
-  constexpr int STAGE = kDecodeKT * D;       // elements per stage
-  constexpr int NWARP = kDecodeThreads / 32;
-
-  extern __shared__ __align__(128) uint8_t dsmem[];
-  T* sK = reinterpret_cast<T*>(dsmem);
-  T* sV = sK + kDecodeStages * STAGE;
-  __shared__ float sm_m[NWARP][G];
-  __shared__ float sm_l[NWARP][G];
-  // the warps' o partials reuse the ring once an item's keys are consumed
-  float* sm_o = reinterpret_cast<float*>(dsmem);
-  static_assert(NWARP * G * D * 4 <= kDecodeStages * kDecodeKT * D * 2 * 2, "o partials fit the ring");
-
-  const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
-  const int n_items = hdr->n_items;
-  const WorkItem* items = ws_ptr<const WorkItem>(p.ws, hdr->off_items);
-  const int32_t* qo_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_qo_indptr);
-  const int32_t* kv_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_kv_indptr);
-  const int32_t* kv_len = ws_ptr<const int32_t>(p.ws, hdr->off_kv_len);
-  float* tmp_lse = ws_ptr<float>(p.ws, hdr->off_tmp_lse);
-  float* tmp_o = ws_ptr<float>(p.ws, hdr->off_tmp_o);
-  const int window_left = hdr->window_left;
-
-  const int tid = threadIdx.x;
-  W wk;
-  wk.setup(tid >> 5, tid & 31);
-
-  for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
-    const WorkItem it = items[w];
-    if (it.b < 0) continue;  // schedule padding
-    const int b = it.b, hk = it.kv_head;
-    const int token = qo_indptr[b];
-    const DecodeRange R = decode_range(it, kv_len[b], window_left, 1, kDecodeKT);
-    const int lo = R.lo, hi = R.hi;
-
-    const int32_t* pages = p.kv_indices + kv_indptr[b];
-    const T* kcol = static_cast<const T*>(p.k) + int64_t(hk) * p.k_stride_head + (tid % CH) * 8;
-    const T* vcol = static_cast<const T*>(p.v) + int64_t(hk) * p.v_stride_head + (tid % CH) * 8;
-    constexpr int ROWS_PER_PASS = kDecodeThreads / CH;
-    constexpr int PASSES = kDecodeKT / ROWS_PER_PASS;
-    const int my_row = tid / CH;
-    const uint32_t sk0 = smem_u32(sK + my_row * D + (tid % CH) * 8);
-    const uint32_t sv0 = smem_u32(sV + my_row * D + (tid % CH) * 8);
-    auto issue = [&](int tile, int stage) {
-      const int kt = lo + tile * kDecodeKT + my_row;
-#pragma unroll
-      for (int i = 0; i < PASSES; ++i) {
-        const int j = kt + i * ROWS_PER_PASS;
-        const T* ks = static_cast<const T*>(p.k);
-        const T* vs = static_cast<const T*>(p.v);
-        int bytes = 0;
-        if (j < hi) {
-          int32_t pi, slot;
-          if (p.page_shift >= 0) {
-            pi = j >> p.page_shift;
-            slot = j & ((1 << p.page_shift) - 1);
-          } else {
-            pi = j / p.page_size;
-            slot = j - pi * p.page_size;
-          }
-          const int64_t page = __ldg(pages + pi);
-          ks = kcol + page * p.k_stride_page + int64_t(slot) * p.k_stride_tok;
-          vs = vcol + page * p.v_stride_page + int64_t(slot) * p.v_stride_tok;
-          bytes = 16;
-        }
-        const uint32_t off = uint32_t((stage * STAGE + i * ROWS_PER_PASS * D) * 2);
-        cp_async16(sk0 + off, ks, bytes);
-        cp_async16(sv0 + off, vs, bytes);
-      }
-    };
-#pragma unroll
-    for (int s = 0; s < kDecodeStages - 1; ++s) {
-      if (s < R.n_tiles) issue(s, s);
-      cp_async_commit();
-    }
-    wk.begin(p, token, hk);
-
-    for (int tile = 0; tile < R.n_tiles; ++tile) {
-      cp_async_wait<kDecodeStages - 2>();
-      __syncthreads();
-      {
-        const int nt = tile + kDecodeStages - 1;
-        if (nt < R.n_tiles) issue(nt, nt % kDecodeStages);
-        cp_async_commit();
-      }
-      const int st = tile % kDecodeStages;
-      wk.stage(sK + st * STAGE, sV + st * STAGE, lo + tile * kDecodeKT, lo, hi);
-    }
-    cp_async_wait<0>();
-    __syncthreads();  // every warp is done with the ring before it holds o partials
-    wk.finish(p, token, hk, it.chunk, it.partial_base, tmp_o, tmp_lse, tid, sm_o, sm_m, sm_l,
-              [] { __syncthreads(); });
-  }
-}
-
 // ------------------------------------------------------------ TMA kernel
 
 // Ring geometry of the TMA kernel: NCW consumer warps of KPW keys each per
@@ -694,29 +577,21 @@ __global__ void __launch_bounds__(TmaCfg<D>::THREADS, TmaCfg<D>::MINB)
 // -------------------------------------------------------------- launchers
 
 template <int D, int G, bool BF16>
-cudaError_t launch_dg(const AttnParams& p, int grid, const CUtensorMap* tk, const CUtensorMap* tv,
+cudaError_t launch_dg(const AttnParams& p, int grid, const CUtensorMap& tk, const CUtensorMap& tv,
                       int box_rows, cudaStream_t s) {
-  if (tk) {
-    using C = TmaCfg<D>;
-    auto k = decode_tma_kernel<D, G, BF16>;
-    constexpr int smem = C::template smem_bytes<G>();
-    // once per process, before any capture (no attribute call inside a captured run)
-    static cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (attr != cudaSuccess) return attr;
-    k<<<grid, C::THREADS, smem, s>>>(p, *tk, *tv, box_rows);
-    return cudaGetLastError();
-  }
-  auto k = decode_kernel<D, G, BF16>;
-  static cudaError_t attr =
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, decode_smem_bytes<D>());
+  using C = TmaCfg<D>;
+  auto k = decode_tma_kernel<D, G, BF16>;
+  constexpr int smem = C::template smem_bytes<G>();
+  // once per process, before any capture (no attribute call inside a captured run)
+  static cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (attr != cudaSuccess) return attr;
-  k<<<grid, kDecodeThreads, decode_smem_bytes<D>(), s>>>(p);
+  k<<<grid, C::THREADS, smem, s>>>(p, tk, tv, box_rows);
   return cudaGetLastError();
 }
 
 template <int D, bool BF16>
-cudaError_t launch_d(const AttnParams& p, int group, int grid, const CUtensorMap* tk,
-                     const CUtensorMap* tv, int box_rows, cudaStream_t s) {
+cudaError_t launch_d(const AttnParams& p, int group, int grid, const CUtensorMap& tk,
+                     const CUtensorMap& tv, int box_rows, cudaStream_t s) {
   switch (group) {
     case 1: return launch_dg<D, 1, BF16>(p, grid, tk, tv, box_rows, s);
     case 2: return launch_dg<D, 2, BF16>(p, grid, tk, tv, box_rows, s);
@@ -749,20 +624,18 @@ cudaError_t launch_decode(const AttnParams& p, int head_dim, int group, bool bf1
   const int kt = head_dim == 128 ? TmaCfg<128>::KT : TmaCfg<64>::KT;
   const int box_rows = gcd_int(p.page_size, kt);
   CUtensorMap tk, tv;
-  const bool tma =
-      num_pages > 0 &&
-      encode_paged_kv_map(&tk, bf16, p.k, head_dim, p.num_kv_heads, p.page_size, num_pages,
-                          p.k_stride_head, p.k_stride_tok, p.k_stride_page, head_dim, box_rows,
-                          CU_TENSOR_MAP_SWIZZLE_NONE) &&
-      encode_paged_kv_map(&tv, bf16, p.v, head_dim, p.num_kv_heads, p.page_size, num_pages,
-                          p.v_stride_head, p.v_stride_tok, p.v_stride_page, head_dim, box_rows,
-                          CU_TENSOR_MAP_SWIZZLE_NONE);
-  const CUtensorMap* mk = tma ? &tk : nullptr;
-  const CUtensorMap* mv = tma ? &tv : nullptr;
-  if (head_dim == 128) return bf16 ? launch_d<128, true>(p, group, grid, mk, mv, box_rows, stream)
-                                   : launch_d<128, false>(p, group, grid, mk, mv, box_rows, stream);
-  return bf16 ? launch_d<64, true>(p, group, grid, mk, mv, box_rows, stream)
-              : launch_d<64, false>(p, group, grid, mk, mv, box_rows, stream);
+  if (num_pages <= 0 ||
+      !encode_paged_kv_map(&tk, bf16, p.k, head_dim, p.num_kv_heads, p.page_size, num_pages,
+                           p.k_stride_head, p.k_stride_tok, p.k_stride_page, head_dim, box_rows,
+                           CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_paged_kv_map(&tv, bf16, p.v, head_dim, p.num_kv_heads, p.page_size, num_pages,
+                           p.v_stride_head, p.v_stride_tok, p.v_stride_page, head_dim, box_rows,
+                           CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  if (head_dim == 128) return bf16 ? launch_d<128, true>(p, group, grid, tk, tv, box_rows, stream)
+                                   : launch_d<128, false>(p, group, grid, tk, tv, box_rows, stream);
+  return bf16 ? launch_d<64, true>(p, group, grid, tk, tv, box_rows, stream)
+              : launch_d<64, false>(p, group, grid, tk, tv, box_rows, stream);
 }
 
 }  // namespace fi
