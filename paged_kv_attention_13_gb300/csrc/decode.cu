@@ -26,6 +26,8 @@
 //   [P1] "Route non-causal windowed prefill to AITER's masked kernel" (#339)
 //   [P2] "Support speculative-decode verify on ROCm, and stop auto routing
 //         short-query prefill to AITER" (#362)
+#include <type_traits>
+
 #include "tma.cuh"
 
 namespace fi {
@@ -52,6 +54,61 @@ __device__ __forceinline__ DecodeRange decode_range(const WorkItem& it, int lk, 
   return r;
 }
 
+// Merge the NWARP consumer warps' states of one work item and write o / lse:
+// directly, or to the item's split-KV partial slot. sm_o holds the warps'
+// unnormalised o as [NWARP][G][D] floats; sm_m / sm_l their per-head running
+// max (log2 domain) and sum.
+template <int D, int G, bool BF16, int NWARP>
+__device__ __forceinline__ void decode_merge_write(const AttnParams& p, int token, int hk, int chunk,
+                                                   int partial_base, float* tmp_o, float* tmp_lse,
+                                                   int tid, const float* sm_o,
+                                                   const float (*sm_m)[G],
+                                                   const float (*sm_l)[G]) {
+  using DT = Dt<BF16>;
+  using T = typename DT::T;
+  const int Hq = p.num_qo_heads;
+  const bool direct = chunk < 0;
+  const int slot = direct ? 0 : partial_base + chunk;
+  for (int idx = tid; idx < G * (D / 4); idx += NWARP * 32) {
+    const int h = idx / (D / 4);
+    const int c = (idx % (D / 4)) * 4;
+    float M = neg_inf();
+#pragma unroll
+    for (int wq = 0; wq < NWARP; ++wq) M = fmaxf(M, sm_m[wq][h]);
+    const float Mu = (M == neg_inf()) ? 0.f : M;
+    float den = 0.f;
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int wq = 0; wq < NWARP; ++wq) {
+      const float sc = ex2(sm_m[wq][h] - Mu);
+      den += sc * sm_l[wq][h];
+      const float4 ov = *reinterpret_cast<const float4*>(sm_o + (wq * G + h) * D + c);
+      num.x += sc * ov.x; num.y += sc * ov.y; num.z += sc * ov.z; num.w += sc * ov.w;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const int head = hk * G + h;
+    if (direct) {
+      T* op = static_cast<T*>(p.out) + (int64_t(token) * Hq + head) * D + c;
+      uint2 pk;
+      pk.x = DT::pack(num.x * inv, num.y * inv);
+      pk.y = DT::pack(num.z * inv, num.w * inv);
+      *reinterpret_cast<uint2*>(op) = pk;
+    } else {
+      float* op = tmp_o + (int64_t(slot) * Hq + head) * D + c;
+      *reinterpret_cast<float4*>(op) =
+          make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
+    }
+    if (c == 0) {
+      const float lse = den > 0.f ? (M + __log2f(den)) * kLn2 : neg_inf();
+      if (direct) {
+        if (p.lse) p.lse[int64_t(token) * Hq + head] = lse;
+      } else {
+        tmp_lse[int64_t(slot) * Hq + head] = lse;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------- warp consumer
 
 // One consumer warp's share of a work item: q of the G heads pre-scaled into
@@ -67,6 +124,7 @@ struct DecodeWarp {
   static constexpr int KPW = KT / NWARP;     // keys per warp per stage
   static constexpr int STEPS = KPW / KPS;    // warp steps per stage
   static_assert(KPW % KPS == 0, "a warp's keys of a stage are whole warp steps");
+  static constexpr bool kSwizzled = false;  // reads K/V stages as plain [KT][D] rows
 
   int warp, lane, kg, dl;
   int myh;          // head whose score this lane holds after the reduce-scatter
@@ -153,7 +211,7 @@ struct DecodeWarp {
   // which [lo, hi) are live. Rows outside the live range may hold anything
   // (a neighbour's page slots): their scores are masked to -inf and their V
   // rows are read as zero, so no value there reaches o.
-  __device__ __forceinline__ void stage(const T* cK, const T* cV, int k0, int lo, int hi) {
+  __device__ __forceinline__ void stage(T* cK, T* cV, int k0, int lo, int hi) {
     const bool full_tile = k0 >= lo && k0 + KT <= hi;
     float s[STEPS];  // this lane's (key, head) score per step
 #pragma unroll
@@ -288,48 +346,178 @@ struct DecodeWarp {
       }
     }
     sync();
+    decode_merge_write<D, G, BF16, NWARP>(p, token, hk, chunk, partial_base, tmp_o, tmp_lse, tid,
+                                           sm_o, sm_m, sm_l);
+    sync();
+  }
+};
 
-    const int Hq = p.num_qo_heads;
-    const bool direct = chunk < 0;
-    const int slot = direct ? 0 : partial_base + chunk;
-    for (int idx = tid; idx < G * (D / 4); idx += NWARP * 32) {
-      const int h = idx / (D / 4);
-      const int c = (idx % (D / 4)) * 4;
-      float M = neg_inf();
+// A consumer warp on the warp-level tensor cores. The GQA group is a dense
+// contraction: S = Q K^T with Q the G heads' rows (padded to the 16 rows of
+// mma.m16n8k16) against the warp's KPW keys, then O += P V. K and V stages
+// are 128B-swizzled 64-column halves written by TMA, so ldmatrix reads them
+// without bank conflicts. The fragment row of lane l is head l / 4 (rows
+// G..15 are zero padding); its running max / sum live in the lane's quad.
+// Per stage a warp issues about 80 instructions for its 16 keys, against
+// about 900 for the shuffle-reduction consumer above.
+template <int D, int G, bool BF16, int NWARP, int KT>
+struct DecodeMmaWarp {
+  using DT = Dt<BF16>;
+  using T = typename DT::T;
+  static constexpr int KPW = KT / NWARP;  // keys per warp per stage
+  static constexpr int NT = KPW / 8;      // n8 score tiles per warp
+  static constexpr int KD = D / 16;       // k16 steps over the head dim
+  static constexpr int HALF = KT * 128;   // bytes of one 64-column half of a stage
+  static_assert(KPW % 16 == 0, "a warp's keys are whole k16 steps of P V");
+  static_assert(G <= 8, "the group fits the live fragment rows");
+  static constexpr bool kSwizzled = true;
+
+  int warp, lane, qr, qc;
+  uint32_t qa0[KD], qa2[KD];  // A fragment, row qr: columns kd*16 + qc*2 (+8)
+  float o[D / 8][4];          // rows qr (live for qr < G) and qr + 8 (padding)
+  float m_me, l_me, scale;
+
+  // byte offset of 16-byte chunk c of row r in a swizzled stage
+  __device__ __forceinline__ static uint32_t swz(int r, int c) {
+    return uint32_t((c >> 3) * HALF + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+  }
+
+  __device__ __forceinline__ void setup(int warp_, int lane_) {
+    warp = warp_;
+    lane = lane_;
+    qr = lane >> 2;
+    qc = lane & 3;
+  }
+
+  // q of the G heads staged in shared memory as [G][D]
+  __device__ __forceinline__ void begin_smem(const T* qs, float sm_scale_log2) {
 #pragma unroll
-      for (int wq = 0; wq < NWARP; ++wq) M = fmaxf(M, sm_m[wq][h]);
-      const float Mu = (M == neg_inf()) ? 0.f : M;
-      float den = 0.f;
-      float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int wq = 0; wq < NWARP; ++wq) {
-        const float sc = ex2(sm_m[wq][h] - Mu);
-        den += sc * sm_l[wq][h];
-        const float4 ov = *reinterpret_cast<const float4*>(sm_o + (wq * G + h) * D + c);
-        num.x += sc * ov.x; num.y += sc * ov.y; num.z += sc * ov.z; num.w += sc * ov.w;
-      }
-      const float inv = den > 0.f ? 1.f / den : 0.f;
-      const int head = hk * G + h;
-      if (direct) {
-        T* op = static_cast<T*>(p.out) + (int64_t(token) * Hq + head) * D + c;
-        uint2 pk;
-        pk.x = DT::pack(num.x * inv, num.y * inv);
-        pk.y = DT::pack(num.z * inv, num.w * inv);
-        *reinterpret_cast<uint2*>(op) = pk;
-      } else {
-        float* op = tmp_o + (int64_t(slot) * Hq + head) * D + c;
-        *reinterpret_cast<float4*>(op) =
-            make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
-      }
-      if (c == 0) {
-        const float lse = den > 0.f ? (M + __log2f(den)) * kLn2 : neg_inf();
-        if (direct) {
-          if (p.lse) p.lse[int64_t(token) * Hq + head] = lse;
-        } else {
-          tmp_lse[int64_t(slot) * Hq + head] = lse;
-        }
+    for (int kd = 0; kd < KD; ++kd) {
+      qa0[kd] = 0u;
+      qa2[kd] = 0u;
+      if (qr < G) {
+        qa0[kd] = *reinterpret_cast<const uint32_t*>(qs + qr * D + kd * 16 + qc * 2);
+        qa2[kd] = *reinterpret_cast<const uint32_t*>(qs + qr * D + kd * 16 + 8 + qc * 2);
       }
     }
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    m_me = neg_inf();
+    l_me = 0.f;
+    scale = sm_scale_log2;
+  }
+
+  // Consume one stage (keys k0 .. k0+KT-1, live [lo, hi)). In a stage that
+  // is not entirely live the warp first zeroes its V rows outside the range:
+  // they may hold anything (a neighbour's slots), and 0 * NaN would reach o.
+  __device__ __forceinline__ void stage(T* cK, T* cV, int k0, int lo, int hi) {
+    const uint32_t sk = smem_u32(cK), sv = smem_u32(cV);
+    const int kb = warp * KPW;  // this warp's first key in the stage
+    const bool full_tile = k0 >= lo && k0 + KT <= hi;
+    if (!full_tile) {
+      // lane l zeroes chunks l, l+32, ... of the warp's dead rows
+      for (int idx = lane; idx < KPW * (D / 8); idx += 32) {
+        const int r = kb + idx / (D / 8), c = idx % (D / 8);
+        const int kk = k0 + r;
+        if (kk < lo || kk >= hi)
+          *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(cV) + swz(r, c)) =
+              make_uint4(0u, 0u, 0u, 0u);
+      }
+      // these generic-proxy writes are ordered before the slot's next TMA fill
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+    }
+    float s[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+    for (int kd = 0; kd < KD; ++kd) {
+      const uint32_t a[4] = {qa0[kd], 0u, qa2[kd], 0u};
+#pragma unroll
+      for (int nt = 0; nt < NT; nt += 2) {
+        const int r = kb + nt * 8 + (lane & 7) + (lane >> 4) * 8;
+        const int c = kd * 2 + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(sk + swz(r, c), b0, b1, b2, b3);
+        mma16816<BF16>(s[nt], a, b0, b1);
+        mma16816<BF16>(s[nt + 1], a, b2, b3);
+      }
+    }
+    // row qr's scores: s[nt][e], key kb + nt*8 + qc*2 + e (e < 2)
+    float mx = neg_inf();
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float x = s[nt][e] * scale;
+        if (!full_tile) {
+          const int kk = k0 + kb + nt * 8 + qc * 2 + e;
+          if (kk < lo || kk >= hi) x = neg_inf();
+        }
+        s[nt][e] = x;
+        mx = fmaxf(mx, x);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    // lazy max, as in the shuffle consumer
+    float mn = m_me;
+    if (mx > m_me + 8.f || (m_me == neg_inf() && mx != neg_inf())) mn = mx;
+    const float corr = (mn == m_me) ? 1.f : ex2(m_me - mn);
+    const float mu = (mn == neg_inf()) ? 0.f : mn;
+    m_me = mn;
+    float psum = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        s[nt][e] = ex2(s[nt][e] - mu);
+        psum += s[nt][e];
+      }
+    l_me = l_me * corr + psum;
+    if (__any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        o[i][0] *= corr;
+        o[i][1] *= corr;
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < KPW / 16; ++kk) {
+      const uint32_t pa[4] = {DT::pack(s[2 * kk][0], s[2 * kk][1]), 0u,
+                              DT::pack(s[2 * kk + 1][0], s[2 * kk + 1][1]), 0u};
+#pragma unroll
+      for (int dn = 0; dn < D / 16; ++dn) {
+        const int r = kb + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int c = dn * 2 + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(sv + swz(r, c), b0, b1, b2, b3);
+        mma16816<BF16>(o[2 * dn], pa, b0, b1);
+        mma16816<BF16>(o[2 * dn + 1], pa, b2, b3);
+      }
+    }
+  }
+
+  template <class Sync>
+  __device__ __forceinline__ void finish(const AttnParams& p, int token, int hk, int chunk,
+                                         int partial_base, float* tmp_o, float* tmp_lse, int tid,
+                                         float* sm_o, float (*sm_m)[G], float (*sm_l)[G],
+                                         Sync sync) {
+    float l = l_me;
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (qr < G) {
+      if (qc == 0) {
+        sm_m[warp][qr] = m_me;
+        sm_l[warp][qr] = l;
+      }
+      float* dst = sm_o + (warp * G + qr) * D + qc * 2;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i)
+        *reinterpret_cast<float2*>(dst + i * 8) = make_float2(o[i][0], o[i][1]);
+    }
+    sync();
+    decode_merge_write<D, G, BF16, NWARP>(p, token, hk, chunk, partial_base, tmp_o, tmp_lse, tid,
+                                           sm_o, sm_m, sm_l);
     sync();
   }
 };
@@ -370,16 +558,26 @@ struct alignas(16) StageHdr {
   int32_t token, kv_head, chunk, partial_base;    // its work item
 };
 
-template <int D, int G, bool BF16>
+// MMA selects the tensor-core consumer (stages 128B-swizzled, 64-column
+// boxes; needs boxes of at least 8 slots, i.e. whole 1024-byte swizzle
+// atoms), else the shuffle-reduction consumer (plain rows).
+template <int D, int G, bool BF16, bool MMA>
 __global__ void __launch_bounds__(TmaCfg<D>::THREADS, TmaCfg<D>::MINB)
     decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, int box_rows) {
   using C = TmaCfg<D>;
   constexpr int NCW = C::NCW, KT = C::KT, NS = C::NS, STAGE = C::STAGE;
-  using W = DecodeWarp<D, G, BF16, NCW, KT>;
+  using W = typename std::conditional<MMA, DecodeMmaWarp<D, G, BF16, NCW, KT>,
+                                      DecodeWarp<D, G, BF16, NCW, KT>>::type;
   using T = typename W::T;
 
-  extern __shared__ __align__(128) uint8_t dsmem[];
+  extern __shared__ __align__(1024) uint8_t dsmem[];
+  if (MMA && (smem_u32(dsmem) & 1023u) != 0) {
+    // the swizzle pattern is anchored to 1024-byte boundaries: report and
+    // skip the work rather than compute with a shifted pattern
+    if (threadIdx.x == 0) atomicExch(&const_cast<WsHeader*>(static_cast<const WsHeader*>(p.ws))->err_flag, 1);
+    return;
+  }
   T* sK = reinterpret_cast<T*>(dsmem);
   T* sV = sK + NS * STAGE;
   float* sm_o = reinterpret_cast<float*>(dsmem + C::template o_off<G>());
@@ -512,9 +710,19 @@ __global__ void __launch_bounds__(TmaCfg<D>::THREADS, TmaCfg<D>::MINB)
         for (int j = 0; j < BPL; ++j) {
           const int i = lane + 32 * j;
           if (i < n_live) {
-            const uint32_t off = uint32_t(i) * box_bytes;
-            tma_load_4d(dk + off, &tk, FULL(st), 0, it.kv_head, slot[j], page[j]);
-            tma_load_4d(dv + off, &tv, FULL(st), 0, it.kv_head, slot[j], page[j]);
+            if constexpr (W::kSwizzled) {
+              // one box per 64-column half; half h of the stage at h * KT * 128
+              const uint32_t off = uint32_t(i * box_rows) * 128u;
+#pragma unroll
+              for (int h = 0; h < D / 64; ++h) {
+                tma_load_4d(dk + h * KT * 128 + off, &tk, FULL(st), h * 64, it.kv_head, slot[j], page[j]);
+                tma_load_4d(dv + h * KT * 128 + off, &tv, FULL(st), h * 64, it.kv_head, slot[j], page[j]);
+              }
+            } else {
+              const uint32_t off = uint32_t(i) * box_bytes;
+              tma_load_4d(dk + off, &tk, FULL(st), 0, it.kv_head, slot[j], page[j]);
+              tma_load_4d(dv + off, &tv, FULL(st), 0, it.kv_head, slot[j], page[j]);
+            }
           }
         }
       }
@@ -576,11 +784,11 @@ __global__ void __launch_bounds__(TmaCfg<D>::THREADS, TmaCfg<D>::MINB)
 
 // -------------------------------------------------------------- launchers
 
-template <int D, int G, bool BF16>
+template <int D, int G, bool BF16, bool MMA>
 cudaError_t launch_dg(const AttnParams& p, int grid, const CUtensorMap& tk, const CUtensorMap& tv,
                       int box_rows, cudaStream_t s) {
   using C = TmaCfg<D>;
-  auto k = decode_tma_kernel<D, G, BF16>;
+  auto k = decode_tma_kernel<D, G, BF16, MMA>;
   constexpr int smem = C::template smem_bytes<G>();
   // once per process, before any capture (no attribute call inside a captured run)
   static cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -589,15 +797,22 @@ cudaError_t launch_dg(const AttnParams& p, int grid, const CUtensorMap& tk, cons
   return cudaGetLastError();
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool MMA>
 cudaError_t launch_d(const AttnParams& p, int group, int grid, const CUtensorMap& tk,
                      const CUtensorMap& tv, int box_rows, cudaStream_t s) {
   switch (group) {
-    case 1: return launch_dg<D, 1, BF16>(p, grid, tk, tv, box_rows, s);
-    case 2: return launch_dg<D, 2, BF16>(p, grid, tk, tv, box_rows, s);
-    case 4: return launch_dg<D, 4, BF16>(p, grid, tk, tv, box_rows, s);
+    case 1: return launch_dg<D, 1, BF16, MMA>(p, grid, tk, tv, box_rows, s);
+    case 2: return launch_dg<D, 2, BF16, MMA>(p, grid, tk, tv, box_rows, s);
+    case 4: return launch_dg<D, 4, BF16, MMA>(p, grid, tk, tv, box_rows, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_dm(const AttnParams& p, int group, int grid, const CUtensorMap& tk,
+                      const CUtensorMap& tv, int box_rows, bool mma, cudaStream_t s) {
+  return mma ? launch_d<D, BF16, true>(p, group, grid, tk, tv, box_rows, s)
+             : launch_d<D, BF16, false>(p, group, grid, tk, tv, box_rows, s);
 }
 
 int gcd_int(int a, int b) {
@@ -623,19 +838,25 @@ cudaError_t launch_decode(const AttnParams& p, int head_dim, int group, bool bf1
   // at a multiple of that size (tiles start at lo rounded down to it).
   const int kt = head_dim == 128 ? TmaCfg<128>::KT : TmaCfg<64>::KT;
   const int box_rows = gcd_int(p.page_size, kt);
+  // Tensor-core consumer when a box spans whole swizzle atoms (8 slots of
+  // 128 bytes per 64-column half); shuffle consumer for smaller boxes.
+  const bool mma = box_rows >= 8;
+  const int box_cols = mma ? 64 : head_dim;
+  const CUtensorMapSwizzle swz = mma ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUtensorMap tk, tv;
   if (num_pages <= 0 ||
       !encode_paged_kv_map(&tk, bf16, p.k, head_dim, p.num_kv_heads, p.page_size, num_pages,
-                           p.k_stride_head, p.k_stride_tok, p.k_stride_page, head_dim, box_rows,
-                           CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                           p.k_stride_head, p.k_stride_tok, p.k_stride_page, box_cols, box_rows,
+                           swz) ||
       !encode_paged_kv_map(&tv, bf16, p.v, head_dim, p.num_kv_heads, p.page_size, num_pages,
-                           p.v_stride_head, p.v_stride_tok, p.v_stride_page, head_dim, box_rows,
-                           CU_TENSOR_MAP_SWIZZLE_NONE))
+                           p.v_stride_head, p.v_stride_tok, p.v_stride_page, box_cols, box_rows,
+                           swz))
     return cudaErrorInvalidValue;
-  if (head_dim == 128) return bf16 ? launch_d<128, true>(p, group, grid, tk, tv, box_rows, stream)
-                                   : launch_d<128, false>(p, group, grid, tk, tv, box_rows, stream);
-  return bf16 ? launch_d<64, true>(p, group, grid, tk, tv, box_rows, stream)
-              : launch_d<64, false>(p, group, grid, tk, tv, box_rows, stream);
+  if (head_dim == 128)
+    return bf16 ? launch_dm<128, true>(p, group, grid, tk, tv, box_rows, mma, stream)
+                : launch_dm<128, false>(p, group, grid, tk, tv, box_rows, mma, stream);
+  return bf16 ? launch_dm<64, true>(p, group, grid, tk, tv, box_rows, mma, stream)
+              : launch_dm<64, false>(p, group, grid, tk, tv, box_rows, mma, stream);
 }
 
 }  // namespace fi
