@@ -183,11 +183,13 @@ extern "C" void fi_plan_destroy(fi_plan_t p) {
 
 namespace {
 
-bool group_has_decode_kernel(int g) { return g == 1 || g == 2 || g == 4; }
-
+// The short-query kernel (kDecode) takes every request of at most 16 packed
+// rows on its tensor-core consumer when the group and page size allow, and
+// decode on its CUDA-core consumer otherwise (groups 1, 2, 4).
 int choose_kernel(int32_t q_len_per_req, int32_t g, int64_t max_rows_per_req, int32_t d,
                   int32_t page_size) {
-  if (q_len_per_req == 1 && group_has_decode_kernel(g)) return fi::kDecode;
+  if (max_rows_per_req <= 16 && fi::decode_mma_supports(d, page_size, g)) return fi::kDecode;
+  if (q_len_per_req == 1 && fi::decode_shuffle_supports(d, g)) return fi::kDecode;
   if (max_rows_per_req <= 16 && g <= 16) return fi::kPrefillM16;
   if (max_rows_per_req > 64 && fi::prefill_tc_supports(d, page_size, g)) return fi::kPrefillM128;
   if (g <= 64) return fi::kPrefillM64;
@@ -195,9 +197,13 @@ int choose_kernel(int32_t q_len_per_req, int32_t g, int64_t max_rows_per_req, in
   return -1;
 }
 
-int tile_rows_of(int kernel, int g) {
+int tile_rows_of(int kernel, int g, int64_t max_rows_per_req, int32_t d, int32_t page_size) {
   switch (kernel) {
-    case fi::kDecode: return g;
+    case fi::kDecode:
+      // tensor-core consumer: one row half (8 rows) when every request fits,
+      // else two; CUDA-core consumer: the G heads of one token
+      if (!fi::decode_mma_supports(d, page_size, g)) return g;
+      return (max_rows_per_req <= 8 && g <= 8) ? (8 / g) * g : (16 / g) * g;
     case fi::kPrefillM16: return (16 / g) * g;
     case fi::kPrefillM64: return (64 / g) * g;
     case fi::kPrefillM128: return 2 * ((128 / g) * g);  // two 128-row Q tiles
@@ -326,7 +332,7 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
       return fail(FI_ERR_CAPACITY, "plan: %s is frozen at %d by the first graph-mode plan, got %d",
                   field, want, got);
   }
-  ns.tile_rows = tile_rows_of(ns.kernel, g);
+  ns.tile_rows = tile_rows_of(ns.kernel, g, max_rows_per_req, d, page_size);
 
   // ---- tiles and their live key ranges
   std::vector<Tile> tiles;
@@ -350,7 +356,8 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
   }
 
   // ---- KV split
-  const int ctas_per_sm = std::max(1, fi::kernel_ctas_per_sm(ns.kernel, d, g, dtype == FI_BF16));
+  const int ctas_per_sm =
+      std::max(1, fi::kernel_ctas_per_sm(ns.kernel, d, g, dtype == FI_BF16, page_size));
   const int64_t grid_cap = int64_t(P.num_sms) * ctas_per_sm;
   const int64_t avail = P.host_only ? INT64_MAX / 4 : int64_t(P.ws_bytes);
   auto count_for = [&](int64_t chunk_len, int64_t* n_items, int64_t* n_partials) {
@@ -374,8 +381,10 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
     const int64_t min_chunk = 256;
     const int64_t units = int64_t(tiles.size()) * hk;
     // split when the tiles alone cannot keep every SM busy and balanced:
-    // aim at ~4 items per resident CTA, no chunk shorter than min_chunk keys
-    int64_t want = (total_len * hk + 4 * grid_cap - 1) / (4 * grid_cap);
+    // aim at ~2 items per resident CTA (measured against 4 and 8: fewer,
+    // longer items win on decode and verify once the longest-first schedule
+    // balances them), no chunk shorter than min_chunk keys
+    int64_t want = (total_len * hk + 2 * grid_cap - 1) / (2 * grid_cap);
     want = std::max<int64_t>(min_chunk, (want + 63) / 64 * 64);
     if (max_len > want && units < 4 * grid_cap * 4) chunk_len = want;
     // grow the chunks until the partial states fit the workspace
@@ -845,7 +854,7 @@ fi_status run_common(fi_plan_t p, bool decode_api, const fi_tensor* q, const fi_
   if (any_work) {
     cudaError_t e;
     if (s.kernel == fi::kDecode)
-      e = fi::launch_decode(ap, s.d, s.group, bf16, k->shape[0], s.grid, cs);
+      e = fi::launch_decode(ap, s.d, s.group, bf16, k->shape[0], s.tile_rows, s.grid, cs);
     else if (s.kernel == fi::kPrefillM128)
       e = fi::launch_prefill_tc(ap, s.d, s.group, s.tile_rows, q->shape[0], k->shape[0], bf16,
                                 s.grid, cs);

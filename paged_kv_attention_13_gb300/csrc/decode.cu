@@ -1,28 +1,35 @@
-// Decode kernels: one query row per request against its paged KV, all G query
-// heads of one kv head together (GQA). Bandwidth-bound: every K/V byte is
-// read exactly once, scores are reduced with warp shuffles, and the online
-// softmax is kept in fp32.
+// Short-query attention kernels (decode, speculative verify, and any request
+// of at most 16 packed rows: query row x head of the GQA group), against
+// the paged KV. Bandwidth-bound: every K/V byte is read exactly once, the
+// online softmax is kept in fp32.
 //
-// Work item = (request, kv head, key chunk). The item's live keys stream
-// through a ring of stages in shared memory, each stage a tile of KT keys of
-// K and of V. Consumer warps take KT / warps keys of a stage each: a warp step
-// covers 32 / (D/8) keys, each key's D/8 lanes holding 8 head-dim elements.
-// At the end of an item the warps' (max, sum, o) states are merged in shared
-// memory.
+// Work item = (request tile, kv head, key chunk). One producer warp streams
+// the item's live keys through a ring of stages in shared memory: per page
+// of a stage it issues one cp.async.bulk.tensor box of K and one of V (4-D
+// maps over [pages, slot, kv head, dim]), and for an item's first stage its
+// q rows by plain bulk copy into a q buffer. mbarriers hand the stages to the
+// consumer warps and back; each stage carries a 64-byte header with the
+// item's geometry, so consumer warps read no global memory before they write
+// the output. The producer runs ahead across work items, so the ring stays
+// full through item boundaries.
 //
-// One producer warp fills the ring: per page of a stage it issues one
-// cp.async.bulk.tensor box of K and one of V (4-D maps over [pages, slot,
-// kv head, dim]), and for an item's first stage q by plain bulk copy;
-// mbarriers hand the stages to the consumer warps and back. The producer
-// runs ahead across work items, so the ring stays full through item
-// boundaries, and the consumer warps issue no load instructions at all.
-// (A version in which every thread gathered 16-byte chunks with cp.async
-// reached 4870 GB/s at best on the batch-64 decode, against 5750 for this
-// one, and was slower at page size 1 too.)
+// Two consumers:
+//   DecodeMmaWarp  the GQA contraction on the warp-level tensor cores:
+//                  S = Q K^T with the item's packed rows (padded to the 16
+//                  rows of mma.m16n8k16), then O += P V. Stages are 64-column
+//                  halves in 128B swizzle, so ldmatrix reads them without bank
+//                  conflicts; needs boxes of at least 8 slots.
+//   DecodeWarp     CUDA cores, for decode with smaller boxes (page sizes
+//                  1, 2, 4): 16 lanes per key, a shuffle reduce-scatter of
+//                  the G heads' dot products.
+// At the end of an item the consumer warps' (max, sum, o) states are merged
+// in shared memory, in rounds of 8 rows.
 //
-// Mask for one query row (Lq = 1) [P1 "Why window_size_right stays -1"],
-// [P2 "Summary"]: causal keeps every key j <= Lk - 1; the window keeps
-// j >= Lk - 1 - window_left. So decode needs only a key range.
+// Mask [P1 "Why window_size_right stays -1"], [P2 "Summary"]: key j of
+// query row i is kept when (!causal || j <= i + Lk - Lq) &&
+// (wl < 0 || j + Lq + wl >= Lk + i). Stages outside the item's live range
+// are never loaded; the per-element test runs only on stages that straddle
+// a bound.
 //   [P1] "Route non-causal windowed prefill to AITER's masked kernel" (#339)
 //   [P2] "Support speculative-decode verify on ROCm, and stop auto routing
 //         short-query prefill to AITER" (#362)
@@ -33,88 +40,84 @@
 namespace fi {
 namespace {
 
-// ------------------------------------------------------------------ geometry
+constexpr int kMaxRows = 16;  // packed rows per item
 
-// Live keys [lo, hi) of one work item, visited as tiles of `kt` keys from
-// `start` = lo rounded down to `align` (a power of two); keys below lo in the
-// first tile are masked.
-struct DecodeRange {
-  int lo, hi, start, n_tiles;
+// Header of one stage, written by the producer before it arms the stage's
+// barrier. Keys [lo, hi) are live for some row of the item, keys
+// [lo_full, hi_full) for every row; diff = Lk - Lq of the request.
+enum : int32_t { kStFirst = 1, kStLast = 2, kStEnd = 4, kStNoKeys = 8 };
+struct alignas(16) StageHdr {
+  int32_t flags, k0, lo, hi;
+  int32_t lo_full, hi_full, token0, kv_head;  // token0: global token of query row i0
+  int32_t row0, n_rows, diff, chunk;          // first packed row, rows, Lk - Lq, chunk (-1: direct)
+  int32_t num_chunks, partial_base, i0, pad;
 };
 
-__device__ __forceinline__ DecodeRange decode_range(const WorkItem& it, int lk, int window_left,
-                                                    int align, int kt) {
-  DecodeRange r;
-  r.hi = min(it.kv_end, lk);
-  r.lo = it.kv_begin;
-  if (window_left >= 0) r.lo = max(r.lo, lk - 1 - window_left);
-  r.lo = max(r.lo, 0);
-  r.start = r.lo & ~(align - 1);
-  r.n_tiles = r.hi > r.lo ? (r.hi - r.start + kt - 1) / kt : 0;
-  return r;
-}
-
-// Merge the NWARP consumer warps' states of one work item and write o / lse:
-// directly, or to the item's split-KV partial slot. sm_o holds the warps'
-// unnormalised o as [NWARP][G][D] floats; sm_m / sm_l their per-head running
-// max (log2 domain) and sum.
-template <int D, int G, bool BF16, int NWARP>
-__device__ __forceinline__ void decode_merge_write(const AttnParams& p, int token, int hk, int chunk,
-                                                   int partial_base, float* tmp_o, float* tmp_lse,
-                                                   int tid, const float* sm_o,
-                                                   const float (*sm_m)[G],
-                                                   const float (*sm_l)[G]) {
+// Write rows [r0, r0 + 8) of an item: sm_o holds those rows' o summed over
+// the consumer warps (in MB partial sums of 8 rows each, added here in a
+// fixed order), each warp's share already scaled to the row's common max;
+// sm_m / sm_l hold each warp's row max (log2 domain) and sum.
+template <int D, int G, bool BF16, int NWARP, int MB>
+__device__ __forceinline__ void write_rows(const AttnParams& p, const StageHdr& h, int r0,
+                                           float* tmp_o, float* tmp_lse, int tid, float* sm_o,
+                                           float (*sm_m)[kMaxRows], float (*sm_l)[kMaxRows]) {
   using DT = Dt<BF16>;
   using T = typename DT::T;
   const int Hq = p.num_qo_heads;
-  const bool direct = chunk < 0;
-  const int slot = direct ? 0 : partial_base + chunk;
-  for (int idx = tid; idx < G * (D / 4); idx += NWARP * 32) {
-    const int h = idx / (D / 4);
+  for (int idx = tid; idx < 8 * (D / 4); idx += NWARP * 32) {
+    const int rl = idx / (D / 4);
     const int c = (idx % (D / 4)) * 4;
+    const int r = r0 + rl;
+    if (r >= h.n_rows) continue;
+    float4 num = *reinterpret_cast<const float4*>(sm_o + rl * D + c);
+    if (MB == 2) {  // (warps 0 + 1) + (warps 2 + 3)
+      const float4 b = *reinterpret_cast<const float4*>(sm_o + (8 + rl) * D + c);
+      num.x += b.x; num.y += b.y; num.z += b.z; num.w += b.w;
+    }
     float M = neg_inf();
 #pragma unroll
-    for (int wq = 0; wq < NWARP; ++wq) M = fmaxf(M, sm_m[wq][h]);
+    for (int w = 0; w < NWARP; ++w) M = fmaxf(M, sm_m[w][r]);
     const float Mu = (M == neg_inf()) ? 0.f : M;
     float den = 0.f;
-    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int wq = 0; wq < NWARP; ++wq) {
-      const float sc = ex2(sm_m[wq][h] - Mu);
-      den += sc * sm_l[wq][h];
-      const float4 ov = *reinterpret_cast<const float4*>(sm_o + (wq * G + h) * D + c);
-      num.x += sc * ov.x; num.y += sc * ov.y; num.z += sc * ov.z; num.w += sc * ov.w;
-    }
+    for (int w = 0; w < NWARP; ++w) den += ex2(sm_m[w][r] - Mu) * sm_l[w][r];
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    const int head = hk * G + h;
-    if (direct) {
-      T* op = static_cast<T*>(p.out) + (int64_t(token) * Hq + head) * D + c;
+    const float lse = den > 0.f ? (M + __log2f(den)) * kLn2 : neg_inf();
+    const int pr = h.row0 + r;
+    const int ti = pr / G - h.i0;  // query row within the tile
+    const int head = h.kv_head * G + pr % G;
+    if (h.chunk < 0) {
+      T* op = static_cast<T*>(p.out) + (int64_t(h.token0 + ti) * Hq + head) * D + c;
       uint2 pk;
       pk.x = DT::pack(num.x * inv, num.y * inv);
       pk.y = DT::pack(num.z * inv, num.w * inv);
       *reinterpret_cast<uint2*>(op) = pk;
+      if (c == 0 && p.lse) p.lse[int64_t(h.token0 + ti) * Hq + head] = lse;
     } else {
-      float* op = tmp_o + (int64_t(slot) * Hq + head) * D + c;
-      *reinterpret_cast<float4*>(op) =
+      const int slot = h.partial_base + ti * h.num_chunks + h.chunk;
+      *reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * D + c) =
           make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
-    }
-    if (c == 0) {
-      const float lse = den > 0.f ? (M + __log2f(den)) * kLn2 : neg_inf();
-      if (direct) {
-        if (p.lse) p.lse[int64_t(token) * Hq + head] = lse;
-      } else {
-        tmp_lse[int64_t(slot) * Hq + head] = lse;
-      }
+      if (c == 0) tmp_lse[int64_t(slot) * Hq + head] = lse;
     }
   }
 }
 
-// ------------------------------------------------------------- warp consumer
+// Common max of row r over the warps (0 when every warp's max is -inf).
+template <int NWARP>
+__device__ __forceinline__ float row_max(float (*sm_m)[kMaxRows], int r) {
+  float M = neg_inf();
+#pragma unroll
+  for (int w = 0; w < NWARP; ++w) M = fmaxf(M, sm_m[w][r]);
+  return (M == neg_inf()) ? 0.f : M;
+}
 
-// One consumer warp's share of a work item: q of the G heads pre-scaled into
-// the exp2 domain (fp32 pairs for the packed FMA), o of every head on this
-// lane's 8 dims, and the running max / sum of the head whose score this lane
-// holds after the reduce-scatter.
+// ------------------------------------------------------- shuffle consumer
+
+// One consumer warp on CUDA cores, decode only (the item's rows are the G
+// heads of one query token): q of the G heads pre-scaled into the exp2
+// domain (fp32 pairs for the packed FMA), o of every head on this lane's 8
+// dims, and the running max / sum of the head whose score this lane holds
+// after the reduce-scatter.
 template <int D, int G, bool BF16, int NWARP, int KT>
 struct DecodeWarp {
   using DT = Dt<BF16>;
@@ -123,7 +126,9 @@ struct DecodeWarp {
   static constexpr int KPS = 32 / LPK;       // keys per warp step
   static constexpr int KPW = KT / NWARP;     // keys per warp per stage
   static constexpr int STEPS = KPW / KPS;    // warp steps per stage
+  static constexpr int ROUNDS = 1;           // G <= 8 rows: one merge round
   static_assert(KPW % KPS == 0, "a warp's keys of a stage are whole warp steps");
+  static_assert(G <= 8, "one merge round");
   static constexpr bool kSwizzled = false;  // reads K/V stages as plain [KT][D] rows
 
   int warp, lane, kg, dl;
@@ -132,6 +137,7 @@ struct DecodeWarp {
   float2 q2[G][4];  // slot s holds head (myh ^ s)
   float2 o2[G][4];
   float m_me, l_me;
+  float m_h[G];     // per-head max and sum of the warp (after publish)
 
   __device__ __forceinline__ void setup(int warp_, int lane_) {
     warp = warp_;
@@ -164,33 +170,12 @@ struct DecodeWarp {
     }
   }
 
-  // Load q of the item's G heads; reset o and the running max / sum. Slot s
-  // holds head (myh ^ s): at each level of the reduce-scatter a lane then
-  // keeps its first half of the slots and sends the second, with no per-lane
-  // selection.
-  __device__ __forceinline__ void begin(const AttnParams& p, int token, int hk) {
-#pragma unroll
-    for (int sl = 0; sl < G; ++sl) {
-      const int h = myh ^ sl;
-      const T* qp = static_cast<const T*>(p.q) + int64_t(token) * p.q_stride_tok +
-                    int64_t(hk * G + h) * p.q_stride_head + dl * 8;
-      uint4 r = ld_nc16(qp);
-      const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        q2[sl][e] = make_float2(DT::lo(wv[e]) * p.sm_scale_log2, DT::hi(wv[e]) * p.sm_scale_log2);
-    }
-    m_me = neg_inf();
-    l_me = 0.f;
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o2[h][e] = make_float2(0.f, 0.f);
-  }
-
-  // Same as begin(), with q of the G heads staged in shared memory as
-  // [G][D] (head h of the group at row h).
-  __device__ __forceinline__ void begin_smem(const T* qs, float sm_scale_log2) {
+  // q of the G heads staged in shared memory as rows 0..G-1 of [16][D].
+  // Slot s holds head (myh ^ s): at each level of the reduce-scatter a lane
+  // then keeps its first half of the slots and sends the second, with no
+  // per-lane selection.
+  __device__ __forceinline__ void begin(const T* qs, int n_rows, float sm_scale_log2) {
+    (void)n_rows;
 #pragma unroll
     for (int sl = 0; sl < G; ++sl) {
       const uint4 r = *reinterpret_cast<const uint4*>(qs + (myh ^ sl) * D + dl * 8);
@@ -207,11 +192,17 @@ struct DecodeWarp {
       for (int e = 0; e < 4; ++e) o2[h][e] = make_float2(0.f, 0.f);
   }
 
+  __device__ __forceinline__ void stage(T* cK, T* cV, const StageHdr& h, int causal, int wl) {
+    (void)causal;
+    (void)wl;
+    stage_keys(cK, cV, h.k0, h.lo, h.hi);
+  }
+
   // Consume one stage: keys k0 .. k0+KT-1 in rows 0..KT-1 of cK / cV, of
   // which [lo, hi) are live. Rows outside the live range may hold anything
   // (a neighbour's page slots): their scores are masked to -inf and their V
   // rows are read as zero, so no value there reaches o.
-  __device__ __forceinline__ void stage(T* cK, T* cV, int k0, int lo, int hi) {
+  __device__ __forceinline__ void stage_keys(T* cK, T* cV, int k0, int lo, int hi) {
     const bool full_tile = k0 >= lo && k0 + KT <= hi;
     float s[STEPS];  // this lane's (key, head) score per step
 #pragma unroll
@@ -302,17 +293,9 @@ struct DecodeWarp {
     }
   }
 
-  // Merge the NWARP warps' states of the item and write o / lse (directly, or
-  // to the item's split-KV partial slot). `sync` is a barrier over the
-  // consumer threads (tid = 0 .. NWARP*32-1); sm_o holds NWARP x G x D
-  // floats. Ends with a barrier, so the shared arrays are free on return.
-  template <class Sync>
-  __device__ __forceinline__ void finish(const AttnParams& p, int token, int hk, int chunk,
-                                         int partial_base, float* tmp_o, float* tmp_lse, int tid,
-                                         float* sm_o, float (*sm_m)[G], float (*sm_l)[G],
-                                         Sync sync) {
-    // sums over the warp's key groups (they share each head's max)
-    float l_h[G], m_h[G];
+  // Reduce the warp's key groups and publish each head's max / sum.
+  __device__ __forceinline__ void publish_ml(float (*sm_m)[kMaxRows], float (*sm_l)[kMaxRows]) {
+    float l_h[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       m_h[h] = __shfl_sync(0xffffffffu, m_me, src_of[h]);
@@ -337,30 +320,43 @@ struct DecodeWarp {
         sm_l[warp][h] = l_h[h];
       }
     }
-    if (kg == 0) {
+  }
+
+  // Store (first) or add this warp's o, scaled to each head's common max,
+  // into sm_o (rows = heads); the warps take turns in a fixed order. The
+  // lanes of key group 0 hold the warp's sums.
+  __device__ __forceinline__ void add_o(int round, int n_rows, bool first, float* sm_o,
+                                        float (*sm_m)[kMaxRows]) {
+    (void)round;
+    (void)n_rows;
+    if (kg != 0) return;
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float4* dst = reinterpret_cast<float4*>(sm_o + (warp * G + h) * D + dl * 8);
-        dst[0] = make_float4(o2[h][0].x, o2[h][0].y, o2[h][1].x, o2[h][1].y);
-        dst[1] = make_float4(o2[h][2].x, o2[h][2].y, o2[h][3].x, o2[h][3].y);
+    for (int h = 0; h < G; ++h) {
+      const float sc = ex2(m_h[h] - row_max<NWARP>(sm_m, h));
+      float4* dst = reinterpret_cast<float4*>(sm_o + h * D + dl * 8);
+      float4 v0 = make_float4(o2[h][0].x * sc, o2[h][0].y * sc, o2[h][1].x * sc, o2[h][1].y * sc);
+      float4 v1 = make_float4(o2[h][2].x * sc, o2[h][2].y * sc, o2[h][3].x * sc, o2[h][3].y * sc);
+      if (!first) {
+        const float4 a0 = dst[0], a1 = dst[1];
+        v0.x += a0.x; v0.y += a0.y; v0.z += a0.z; v0.w += a0.w;
+        v1.x += a1.x; v1.y += a1.y; v1.z += a1.z; v1.w += a1.w;
       }
+      dst[0] = v0;
+      dst[1] = v1;
     }
-    sync();
-    decode_merge_write<D, G, BF16, NWARP>(p, token, hk, chunk, partial_base, tmp_o, tmp_lse, tid,
-                                           sm_o, sm_m, sm_l);
-    sync();
   }
 };
 
-// A consumer warp on the warp-level tensor cores. The GQA group is a dense
-// contraction: S = Q K^T with Q the G heads' rows (padded to the 16 rows of
-// mma.m16n8k16) against the warp's KPW keys, then O += P V. K and V stages
-// are 128B-swizzled 64-column halves written by TMA, so ldmatrix reads them
-// without bank conflicts. The fragment row of lane l is head l / 4 (rows
-// G..15 are zero padding); its running max / sum live in the lane's quad.
-// Per stage a warp issues about 80 instructions for its 16 keys, against
-// about 900 for the shuffle-reduction consumer above.
-template <int D, int G, bool BF16, int NWARP, int KT>
+// ------------------------------------------------------- tensor-core consumer
+
+// One consumer warp on the warp-level tensor cores. The GQA group is a dense
+// contraction: S = Q K^T with the item's packed rows (query row x head,
+// padded to 16) against the warp's KPW keys of a stage, then O += P V. RH
+// fragment row halves are live: 1 when the items have at most 8 rows (decode
+// with G <= 8), else 2. Lane l holds rows l / 4 and l / 4 + 8; its running
+// max / sum live in the lane's quad. About 80 instructions per warp-stage
+// for 16 keys, against about 900 for the shuffle consumer.
+template <int D, int G, bool BF16, int NWARP, int KT, int RH>
 struct DecodeMmaWarp {
   using DT = Dt<BF16>;
   using T = typename DT::T;
@@ -368,14 +364,16 @@ struct DecodeMmaWarp {
   static constexpr int NT = KPW / 8;      // n8 score tiles per warp
   static constexpr int KD = D / 16;       // k16 steps over the head dim
   static constexpr int HALF = KT * 128;   // bytes of one 64-column half of a stage
+  static constexpr int ROUNDS = RH;
   static_assert(KPW % 16 == 0, "a warp's keys are whole k16 steps of P V");
-  static_assert(G <= 8, "the group fits the live fragment rows");
+  static_assert(RH == 1 || RH == 2, "one or two live row halves");
   static constexpr bool kSwizzled = true;
 
   int warp, lane, qr, qc;
-  uint32_t qa0[KD], qa2[KD];  // A fragment, row qr: columns kd*16 + qc*2 (+8)
-  float o[D / 8][4];          // rows qr (live for qr < G) and qr + 8 (padding)
-  float m_me, l_me, scale;
+  uint32_t qa[KD][4];   // A fragments (rows qr, qr + 8; the padding rows are zero)
+  float o[D / 8][4];    // rows qr (o[.][0..1]) and qr + 8 (o[.][2..3])
+  float m[RH], l[RH];   // running max / sum of rows qr (+ 8)
+  float scale;
 
   // byte offset of 16-byte chunk c of row r in a swizzled stage
   __device__ __forceinline__ static uint32_t swz(int r, int c) {
@@ -389,37 +387,46 @@ struct DecodeMmaWarp {
     qc = lane & 3;
   }
 
-  // q of the G heads staged in shared memory as [G][D]
-  __device__ __forceinline__ void begin_smem(const T* qs, float sm_scale_log2) {
+  // q of the item's rows staged in shared memory as [16][D]
+  __device__ __forceinline__ void begin(const T* qs, int n_rows, float sm_scale_log2) {
 #pragma unroll
     for (int kd = 0; kd < KD; ++kd) {
-      qa0[kd] = 0u;
-      qa2[kd] = 0u;
-      if (qr < G) {
-        qa0[kd] = *reinterpret_cast<const uint32_t*>(qs + qr * D + kd * 16 + qc * 2);
-        qa2[kd] = *reinterpret_cast<const uint32_t*>(qs + qr * D + kd * 16 + 8 + qc * 2);
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int r = qr + 8 * hr;
+        uint32_t lo = 0u, hi = 0u;
+        if (hr < RH && r < n_rows) {
+          lo = *reinterpret_cast<const uint32_t*>(qs + r * D + kd * 16 + qc * 2);
+          hi = *reinterpret_cast<const uint32_t*>(qs + r * D + kd * 16 + 8 + qc * 2);
+        }
+        qa[kd][hr] = lo;
+        qa[kd][2 + hr] = hi;
       }
     }
 #pragma unroll
     for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    m_me = neg_inf();
-    l_me = 0.f;
+#pragma unroll
+    for (int hr = 0; hr < RH; ++hr) {
+      m[hr] = neg_inf();
+      l[hr] = 0.f;
+    }
     scale = sm_scale_log2;
   }
 
-  // Consume one stage (keys k0 .. k0+KT-1, live [lo, hi)). In a stage that
-  // is not entirely live the warp first zeroes its V rows outside the range:
-  // they may hold anything (a neighbour's slots), and 0 * NaN would reach o.
-  __device__ __forceinline__ void stage(T* cK, T* cV, int k0, int lo, int hi) {
+  // Consume one stage (keys h.k0 .. + KT). Where the stage is not inside
+  // every row's range the per-element mask runs; where it is not inside the
+  // item's live range the warp first zeroes its V rows outside it (they may
+  // hold anything, a neighbour's slots, and 0 * NaN would reach o).
+  __device__ __forceinline__ void stage(T* cK, T* cV, const StageHdr& h, int causal, int wl) {
     const uint32_t sk = smem_u32(cK), sv = smem_u32(cV);
     const int kb = warp * KPW;  // this warp's first key in the stage
-    const bool full_tile = k0 >= lo && k0 + KT <= hi;
-    if (!full_tile) {
+    const int k0 = h.k0;
+    if (!(k0 >= h.lo && k0 + KT <= h.hi)) {
       // lane l zeroes chunks l, l+32, ... of the warp's dead rows
       for (int idx = lane; idx < KPW * (D / 8); idx += 32) {
         const int r = kb + idx / (D / 8), c = idx % (D / 8);
         const int kk = k0 + r;
-        if (kk < lo || kk >= hi)
+        if (kk < h.lo || kk >= h.hi)
           *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(cV) + swz(r, c)) =
               make_uint4(0u, 0u, 0u, 0u);
       }
@@ -427,64 +434,80 @@ struct DecodeMmaWarp {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
     }
+    const bool full_tile = k0 >= h.lo_full && k0 + KT <= h.hi_full;
     float s[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
     for (int kd = 0; kd < KD; ++kd) {
-      const uint32_t a[4] = {qa0[kd], 0u, qa2[kd], 0u};
 #pragma unroll
       for (int nt = 0; nt < NT; nt += 2) {
         const int r = kb + nt * 8 + (lane & 7) + (lane >> 4) * 8;
         const int c = kd * 2 + ((lane >> 3) & 1);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(sk + swz(r, c), b0, b1, b2, b3);
-        mma16816<BF16>(s[nt], a, b0, b1);
-        mma16816<BF16>(s[nt + 1], a, b2, b3);
+        mma16816<BF16>(s[nt], qa[kd], b0, b1);
+        mma16816<BF16>(s[nt + 1], qa[kd], b2, b3);
       }
     }
-    // row qr's scores: s[nt][e], key kb + nt*8 + qc*2 + e (e < 2)
-    float mx = neg_inf();
+    // s[nt][2*hr + e]: row qr + 8*hr, key kb + nt*8 + qc*2 + e
+    float corr[RH];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int hr = 0; hr < RH; ++hr) {
+      const int r = qr + 8 * hr;
+      const int i = (h.row0 + r) / G;  // query row of the request
+      float mx = neg_inf();
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float x = s[nt][e] * scale;
-        if (!full_tile) {
-          const int kk = k0 + kb + nt * 8 + qc * 2 + e;
-          if (kk < lo || kk >= hi) x = neg_inf();
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float x = s[nt][2 * hr + e] * scale;
+          if (!full_tile) {
+            const int kk = k0 + kb + nt * 8 + qc * 2 + e;
+            bool ok = r < h.n_rows && kk >= h.lo && kk < h.hi;
+            if (causal && kk > i + h.diff) ok = false;
+            if (wl >= 0 && kk + wl < h.diff + i) ok = false;
+            if (!ok) x = neg_inf();
+          }
+          s[nt][2 * hr + e] = x;
+          mx = fmaxf(mx, x);
         }
-        s[nt][e] = x;
-        mx = fmaxf(mx, x);
-      }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    // lazy max, as in the shuffle consumer
-    float mn = m_me;
-    if (mx > m_me + 8.f || (m_me == neg_inf() && mx != neg_inf())) mn = mx;
-    const float corr = (mn == m_me) ? 1.f : ex2(m_me - mn);
-    const float mu = (mn == neg_inf()) ? 0.f : mn;
-    m_me = mn;
-    float psum = 0.f;
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      // lazy max: moves only when the stage max exceeds it by more than 2^8
+      float mn = m[hr];
+      if (mx > m[hr] + 8.f || (m[hr] == neg_inf() && mx != neg_inf())) mn = mx;
+      corr[hr] = (mn == m[hr]) ? 1.f : ex2(m[hr] - mn);
+      const float mu = (mn == neg_inf()) ? 0.f : mn;
+      m[hr] = mn;
+      float psum = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        s[nt][e] = ex2(s[nt][e] - mu);
-        psum += s[nt][e];
-      }
-    l_me = l_me * corr + psum;
-    if (__any_sync(0xffffffffu, corr != 1.f)) {
+        for (int e = 0; e < 2; ++e) {
+          s[nt][2 * hr + e] = ex2(s[nt][2 * hr + e] - mu);
+          psum += s[nt][2 * hr + e];
+        }
+      l[hr] = l[hr] * corr[hr] + psum;
+    }
+    bool any = corr[0] != 1.f;
+    if (RH == 2) any = any || corr[RH - 1] != 1.f;
+    if (__any_sync(0xffffffffu, any)) {
 #pragma unroll
-      for (int i = 0; i < D / 8; ++i) {
-        o[i][0] *= corr;
-        o[i][1] *= corr;
-      }
+      for (int i = 0; i < D / 8; ++i)
+#pragma unroll
+        for (int hr = 0; hr < RH; ++hr) {
+          o[i][2 * hr] *= corr[hr];
+          o[i][2 * hr + 1] *= corr[hr];
+        }
     }
 #pragma unroll
     for (int kk = 0; kk < KPW / 16; ++kk) {
-      const uint32_t pa[4] = {DT::pack(s[2 * kk][0], s[2 * kk][1]), 0u,
-                              DT::pack(s[2 * kk + 1][0], s[2 * kk + 1][1]), 0u};
+      uint32_t pa[4];
+      pa[0] = DT::pack(s[2 * kk][0], s[2 * kk][1]);
+      pa[2] = DT::pack(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      pa[1] = RH == 2 ? DT::pack(s[2 * kk][2], s[2 * kk][3]) : 0u;
+      pa[3] = RH == 2 ? DT::pack(s[2 * kk + 1][2], s[2 * kk + 1][3]) : 0u;
 #pragma unroll
       for (int dn = 0; dn < D / 16; ++dn) {
         const int r = kb + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -497,102 +520,302 @@ struct DecodeMmaWarp {
     }
   }
 
-  template <class Sync>
-  __device__ __forceinline__ void finish(const AttnParams& p, int token, int hk, int chunk,
-                                         int partial_base, float* tmp_o, float* tmp_lse, int tid,
-                                         float* sm_o, float (*sm_m)[G], float (*sm_l)[G],
-                                         Sync sync) {
-    float l = l_me;
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    if (qr < G) {
-      if (qc == 0) {
-        sm_m[warp][qr] = m_me;
-        sm_l[warp][qr] = l;
-      }
-      float* dst = sm_o + (warp * G + qr) * D + qc * 2;
+  __device__ __forceinline__ void publish_ml(float (*sm_m)[kMaxRows], float (*sm_l)[kMaxRows]) {
 #pragma unroll
-      for (int i = 0; i < D / 8; ++i)
-        *reinterpret_cast<float2*>(dst + i * 8) = make_float2(o[i][0], o[i][1]);
+    for (int hr = 0; hr < RH; ++hr) {
+      float lr = l[hr];
+      lr += __shfl_xor_sync(0xffffffffu, lr, 1);
+      lr += __shfl_xor_sync(0xffffffffu, lr, 2);
+      if (qc == 0) {
+        sm_m[warp][qr + 8 * hr] = m[hr];
+        sm_l[warp][qr + 8 * hr] = lr;
+      }
     }
-    sync();
-    decode_merge_write<D, G, BF16, NWARP>(p, token, hk, chunk, partial_base, tmp_o, tmp_lse, tid,
-                                           sm_o, sm_m, sm_l);
-    sync();
+  }
+
+  // Store (first) or add this warp's o of rows [8*round, 8*round + 8),
+  // scaled to each row's common max, into sm_o (8 rows). The warps take
+  // turns in a fixed order, so the sum is the same on every run.
+  __device__ __forceinline__ void add_o(int round, int n_rows, bool first, float* sm_o,
+                                        float (*sm_m)[kMaxRows]) {
+#pragma unroll
+    for (int hr = 0; hr < RH; ++hr) {
+      if (hr != round) continue;
+      const int r = qr + 8 * hr;
+      if (r >= n_rows) continue;
+      const float sc = ex2(m[hr] - row_max<NWARP>(sm_m, r));
+      float2* dst = reinterpret_cast<float2*>(sm_o + qr * D + qc * 2);
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        float2 v = make_float2(o[i][2 * hr] * sc, o[i][2 * hr + 1] * sc);
+        if (!first) {
+          const float2 a = dst[i * 4];
+          v.x += a.x;
+          v.y += a.y;
+        }
+        dst[i * 4] = v;
+      }
+    }
   }
 };
 
 // ------------------------------------------------------------ TMA kernel
 
-// Ring geometry of the TMA kernel: NCW consumer warps of KPW keys each per
-// stage (D = 128; twice as many keys at D = 64, so a stage is always the same
-// bytes), NS stages, MINB CTAs per SM. Among the shapes that fit three CTAs
-// per SM, 2 stages of 64 keys measured fastest.
-template <int D>
+// Ring geometry: NCW consumer warps of KPW keys each per stage (D = 128;
+// twice as many keys at D = 64, so a stage is always the same bytes), NS
+// stages, MINB CTAs per SM. Measured on the batch-64 decode (page 16): the
+// tensor-core consumer is fastest with 3 stages at 2 CTAs per SM (6300
+// GB/s; 2 stages at 3 CTAs per SM: 5930, and it spills), the CUDA-core
+// consumer with 2 stages at 3 CTAs per SM (5760; 3 stages at 2 CTAs: 5045).
+template <int D, bool MMA>
 struct TmaCfg {
   static constexpr int NCW = 4;
   static constexpr int KPW = 16;
   static constexpr int KT = NCW * KPW * (128 / D);  // keys per stage (a power of two)
-  static constexpr int NS = 2;
-  static constexpr int MINB = 3;
+  static constexpr int NS = MMA ? 3 : 2;
+  static constexpr int MINB = MMA ? 2 : 3;
   static constexpr int THREADS = (NCW + 1) * 32;
   static constexpr int STAGE = KT * D;             // elements per stage, K or V
   static constexpr int RING_BYTES = NS * STAGE * 2 * 2;
-  static constexpr int NBAR = 2 * NS + 1;          // full, empty per slot; merge
-  // dynamic shared memory: K/V ring | o partials | per-warp max, sum |
-  // q per slot | stage header per slot | barriers, abort flag
-  template <int G> static constexpr int o_off() { return RING_BYTES; }
-  template <int G> static constexpr int ml_off() { return o_off<G>() + NCW * G * D * 4; }
-  template <int G> static constexpr int q_off() { return ml_off<G>() + 2 * NCW * G * 4; }
-  template <int G> static constexpr int hdr_off() { return q_off<G>() + NS * G * D * 2; }
-  template <int G> static constexpr int bar_off() { return hdr_off<G>() + NS * 32; }
-  template <int G> static constexpr int smem_bytes() { return bar_off<G>() + NBAR * 8 + 16; }
+  static constexpr int NBAR = 2 * NS + 2;          // full, empty per slot; q free; merge
+  // dynamic shared memory: K/V ring | merge rows | per-warp row max, sum |
+  // q rows | stage headers | barriers, abort flag
+  // merge buffers of 8 rows: two (a pairwise merge, 3 barriers per round)
+  // where shared memory allows, else one (warps take turns, 5 barriers)
+  static constexpr int MB = MMA ? 2 : 1;
+  static_assert(!MMA || NCW == 4, "the pairwise merge pairs four warps");
+  static constexpr int O_OFF = RING_BYTES;
+  static constexpr int ML_OFF = O_OFF + MB * 8 * D * 4;
+  static constexpr int Q_OFF = ML_OFF + 2 * NCW * kMaxRows * 4;
+  static constexpr int HDR_OFF = Q_OFF + kMaxRows * D * 2;
+  static constexpr int BAR_OFF = HDR_OFF + NS * int(sizeof(StageHdr));
+  static constexpr int SMEM = BAR_OFF + NBAR * 8 + 16;
   static_assert((KT & (KT - 1)) == 0, "keys per stage is a power of two");
-  static_assert(MINB * (smem_bytes<4>() + 1024) <= 233472, "MINB CTAs fit one SM's shared memory");
+  static_assert(MINB * (SMEM + 1024) <= 233472, "MINB CTAs fit one SM's shared memory");
 };
 
-// Stage header, written by the producer before it arms the stage's barrier.
-enum : int32_t { kStFirst = 1, kStLast = 2, kStEnd = 4, kStNoKeys = 8 };
-struct alignas(16) StageHdr {
-  int32_t flags, k0, lo, hi;                      // this stage
-  int32_t token, kv_head, chunk, partial_base;    // its work item
-};
+// The producer warp of decode_tma_kernel (see there). Kept out of line, so
+// its registers are allocated apart from the consumer warps' path.
+template <int D, int G, bool BF16, bool MMA, class W>
+__device__ __noinline__ void decode_producer(const AttnParams& p, const CUtensorMap* tkp,
+                                             const CUtensorMap* tvp, int box_rows, uint8_t* dsmem,
+                                             int lane, int causal, int window_left,
+                                             volatile int* abort_flag) {
+  using C = TmaCfg<D, MMA>;
+  constexpr int NCW = C::NCW, KT = C::KT, NS = C::NS, STAGE = C::STAGE;
+  using T = typename W::T;
+  const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
+  T* sK = reinterpret_cast<T*>(dsmem);
+  T* sV = sK + NS * STAGE;
+  T* sQ = reinterpret_cast<T*>(dsmem + C::Q_OFF);
+  StageHdr* sH = reinterpret_cast<StageHdr*>(dsmem + C::HDR_OFF);
+  const uint32_t bar0 = smem_u32(dsmem + C::BAR_OFF);
+  auto FULL = [&](int s) { return bar0 + 8u * uint32_t(s); };
+  auto EMPTY = [&](int s) { return bar0 + 8u * uint32_t(NS + s); };
+  const uint32_t QFREE = bar0 + 8u * uint32_t(2 * NS);
+  (void)NCW;
+  // ------------------------------------------------------------ producer
+  // Stage c of this CTA's sequence goes to slot c % NS; its (c / NS)-th
+  // fill waits for the consumers' release of the previous one. The q
+  // buffer of item n waits for the consumers' release of item n - 1's q.
+  // Everything a stage needs from global memory (the item's metadata, the
+  // page indices) is loaded before those waits, so a full ring hides it.
+  const int n_items = hdr->n_items;
+  const WorkItem* items = ws_ptr<const WorkItem>(p.ws, hdr->off_items);
+  const int32_t* qo_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_qo_indptr);
+  const int32_t* kv_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_kv_indptr);
+  const int32_t* kv_len = ws_ptr<const int32_t>(p.ws, hdr->off_kv_len);
+  const int tile_rows = hdr->tile_rows;
+  const int n_boxes = KT / box_rows;  // a stage is n_boxes boxes of box_rows slots of one page
+  const uint32_t box_bytes = uint32_t(box_rows) * D * 2;
+  constexpr int BPL = (KT + 31) / 32;  // boxes per lane, at most
+  int c = 0, n_item = 0;
+  bool ok = true;
+  uint32_t last_par[NS];
+  bool armed[NS];
+#pragma unroll
+  for (int s = 0; s < NS; ++s) {
+    armed[s] = false;
+    last_par[s] = 0;
+  }
+  // claim slot st for stage c (and, for an item's first stage, the q
+  // buffer): wait for their release, then write the header and arm the
+  // slot's barrier for `bytes` (lane 0); false once the CTA aborts. Every
+  // armed phase is recorded (the end-of-work stage too), so the drain below
+  // waits on each slot's latest phase.
+  auto claim = [&](int st, uint32_t par, const StageHdr& h, uint32_t bytes, bool first) {
+    bool okl = true;
+    if (lane == 0) {
+      if (c >= NS) okl = mbar_wait(EMPTY(st), par ^ 1u, abort_flag);
+      if (okl && first && n_item > 0)
+        okl = mbar_wait(QFREE, uint32_t(n_item - 1) & 1u, abort_flag);
+      if (okl) {
+        sH[st] = h;
+        mbar_expect_tx(FULL(st), bytes);
+      }
+    }
+    okl = __shfl_sync(0xffffffffu, okl, 0) != 0;
+    if (okl) {
+#pragma unroll
+      for (int s = 0; s < NS; ++s)
+        if (s == st) {
+          armed[s] = true;
+          last_par[s] = par;
+        }
+    }
+    return okl;
+  };
+  for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+    const WorkItem it = items[w];
+    if (it.b < 0) continue;  // schedule padding
+    // item geometry: packed rows [row0, row0 + n_rows) = query rows
+    // i0..i1 of request b, and the key ranges their masks leave
+    const int tok_b = qo_indptr[it.b];
+    const int lq = qo_indptr[it.b + 1] - tok_b;
+    const int lk = kv_len[it.b];
+    const int n_rows = min(tile_rows, lq * G - it.row0);
+    const int i0 = it.row0 / G, i1 = (it.row0 + n_rows) / G - 1;
+    const int diff = lk - lq;
+    const int hi_t = causal ? min(lk, i1 + diff + 1) : lk;
+    const int lo_t = window_left >= 0 ? max(0, diff + i0 - window_left) : 0;
+    const int lo = max(it.kv_begin, lo_t), hi = min(it.kv_end, hi_t);
+    StageHdr h;
+    h.lo = lo;
+    h.hi = hi;
+    h.lo_full = max(lo, window_left >= 0 ? diff + i1 - window_left : 0);
+    h.hi_full = min(hi, causal ? i0 + diff + 1 : hi);
+    h.token0 = tok_b + i0;
+    h.kv_head = it.kv_head;
+    h.row0 = it.row0;
+    h.n_rows = n_rows;
+    h.diff = diff;
+    h.chunk = it.chunk;
+    h.num_chunks = it.num_chunks;
+    h.partial_base = it.partial_base;
+    h.i0 = i0;
+    h.pad = 0;
+    const int start = lo & ~(box_rows - 1);
+    const int n_tiles = hi > lo ? (hi - start + KT - 1) / KT : 0;
+    const int32_t* pages = p.kv_indices + kv_indptr[it.b];
+    const int n_st = max(n_tiles, 1);  // an item without keys still writes its output
+    for (int t = 0; t < n_st; ++t, ++c) {
+      const int st = c % NS;
+      const uint32_t par = uint32_t(c / NS) & 1u;
+      const int k0 = start + t * KT;
+      const int n_live = n_tiles ? min(n_boxes, (hi - k0 + box_rows - 1) / box_rows) : 0;
+      int page[BPL], slot[BPL];
+#pragma unroll
+      for (int j = 0; j < BPL; ++j) {
+        const int i = lane + 32 * j;
+        page[j] = 0;
+        slot[j] = 0;
+        if (i < n_live) {
+          const int kb = k0 + i * box_rows;
+          int pi;
+          if (p.page_shift >= 0) {
+            pi = kb >> p.page_shift;
+            slot[j] = kb & ((1 << p.page_shift) - 1);
+          } else {
+            pi = kb / p.page_size;
+            slot[j] = kb - pi * p.page_size;
+          }
+          page[j] = __ldg(pages + pi);
+        }
+      }
+      h.flags = (t == 0 ? kStFirst : 0) | (t == n_st - 1 ? kStLast : 0) |
+                (n_tiles ? 0 : kStNoKeys);
+      h.k0 = k0;
+      const uint32_t qbytes = t == 0 ? uint32_t(n_rows * D * 2) : 0u;
+      if (!claim(st, par, h, uint32_t(n_live) * box_bytes * 2u + qbytes, t == 0)) {
+        ok = false;
+        break;
+      }
+      if (t == 0) {
+        // q rows of the item, one bulk copy per packed row
+        for (int r = lane; r < n_rows; r += 32) {
+          const int pr = it.row0 + r;
+          const T* src = static_cast<const T*>(p.q) + int64_t(tok_b + pr / G) * p.q_stride_tok +
+                         int64_t(it.kv_head * G + pr % G) * p.q_stride_head;
+          bulk_load(smem_u32(sQ + r * D), src, uint32_t(D * 2), FULL(st));
+        }
+        ++n_item;
+      }
+      const uint32_t dk = smem_u32(sK + st * STAGE), dv = smem_u32(sV + st * STAGE);
+#pragma unroll
+      for (int j = 0; j < BPL; ++j) {
+        const int i = lane + 32 * j;
+        if (i < n_live) {
+          if constexpr (W::kSwizzled) {
+            // one box per 64-column half; half x of the stage at x * KT * 128
+            const uint32_t off = uint32_t(i * box_rows) * 128u;
+#pragma unroll
+            for (int x = 0; x < D / 64; ++x) {
+              tma_load_4d(dk + x * KT * 128 + off, tkp, FULL(st), x * 64, it.kv_head, slot[j], page[j]);
+              tma_load_4d(dv + x * KT * 128 + off, tvp, FULL(st), x * 64, it.kv_head, slot[j], page[j]);
+            }
+          } else {
+            const uint32_t off = uint32_t(i) * box_bytes;
+            tma_load_4d(dk + off, tkp, FULL(st), 0, it.kv_head, slot[j], page[j]);
+            tma_load_4d(dv + off, tvp, FULL(st), 0, it.kv_head, slot[j], page[j]);
+          }
+        }
+      }
+    }
+  }
+  if (ok) {
+    // end of work: a header-only stage tells the consumers to stop
+    StageHdr h = {};
+    h.flags = kStEnd;
+    const int st = c % NS;
+    if (!claim(st, uint32_t(c / NS) & 1u, h, 0u, false)) ok = false;
+  }
+  // Drain: the last fill of every slot has landed before the CTA exits
+  // (the consumers waited for all of them unless a wait expired; this wait
+  // ignores the abort flag but keeps its time bound, and an expiry is
+  // reported too).
+  if (lane == 0) {
+    volatile int no_abort = 0;
+#pragma unroll
+    for (int s = 0; s < NS; ++s)
+      if (armed[s] && !mbar_wait(FULL(s), last_par[s], &no_abort)) *abort_flag = 1;
+  }
+}
 
-// MMA selects the tensor-core consumer (stages 128B-swizzled, 64-column
-// boxes; needs boxes of at least 8 slots, i.e. whole 1024-byte swizzle
-// atoms), else the shuffle-reduction consumer (plain rows).
-template <int D, int G, bool BF16, bool MMA>
-__global__ void __launch_bounds__(TmaCfg<D>::THREADS, TmaCfg<D>::MINB)
+// MMA: the tensor-core consumer (128B-swizzled stages, 64-column boxes of
+// at least 8 slots, i.e. whole 1024-byte swizzle atoms), with RH live row
+// halves; else the shuffle consumer (plain rows, decode only).
+template <int D, int G, bool BF16, bool MMA, int RH>
+__global__ void __launch_bounds__(TmaCfg<D, MMA>::THREADS, TmaCfg<D, MMA>::MINB)
     decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, int box_rows) {
-  using C = TmaCfg<D>;
+  using C = TmaCfg<D, MMA>;
   constexpr int NCW = C::NCW, KT = C::KT, NS = C::NS, STAGE = C::STAGE;
-  using W = typename std::conditional<MMA, DecodeMmaWarp<D, G, BF16, NCW, KT>,
+  using W = typename std::conditional<MMA, DecodeMmaWarp<D, G, BF16, NCW, KT, RH>,
                                       DecodeWarp<D, G, BF16, NCW, KT>>::type;
   using T = typename W::T;
 
   extern __shared__ __align__(1024) uint8_t dsmem[];
+  const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
   if (MMA && (smem_u32(dsmem) & 1023u) != 0) {
     // the swizzle pattern is anchored to 1024-byte boundaries: report and
     // skip the work rather than compute with a shifted pattern
-    if (threadIdx.x == 0) atomicExch(&const_cast<WsHeader*>(static_cast<const WsHeader*>(p.ws))->err_flag, 1);
+    if (threadIdx.x == 0) atomicExch(&const_cast<WsHeader*>(hdr)->err_flag, 1);
     return;
   }
   T* sK = reinterpret_cast<T*>(dsmem);
   T* sV = sK + NS * STAGE;
-  float* sm_o = reinterpret_cast<float*>(dsmem + C::template o_off<G>());
-  float (*sm_m)[G] = reinterpret_cast<float (*)[G]>(dsmem + C::template ml_off<G>());
-  float (*sm_l)[G] = sm_m + NCW;
-  T* sQ = reinterpret_cast<T*>(dsmem + C::template q_off<G>());  // [NS][G][D]
-  StageHdr* sH = reinterpret_cast<StageHdr*>(dsmem + C::template hdr_off<G>());
-  const uint32_t bar0 = smem_u32(dsmem + C::template bar_off<G>());
+  float* sm_o = reinterpret_cast<float*>(dsmem + C::O_OFF);
+  float (*sm_m)[kMaxRows] = reinterpret_cast<float (*)[kMaxRows]>(dsmem + C::ML_OFF);
+  float (*sm_l)[kMaxRows] = sm_m + NCW;
+  T* sQ = reinterpret_cast<T*>(dsmem + C::Q_OFF);
+  StageHdr* sH = reinterpret_cast<StageHdr*>(dsmem + C::HDR_OFF);
+  const uint32_t bar0 = smem_u32(dsmem + C::BAR_OFF);
   auto FULL = [&](int s) { return bar0 + 8u * uint32_t(s); };
   auto EMPTY = [&](int s) { return bar0 + 8u * uint32_t(NS + s); };
-  const uint32_t MERGE = bar0 + 8u * uint32_t(2 * NS);
-  volatile int* abort_flag =
-      reinterpret_cast<volatile int*>(dsmem + C::template bar_off<G>() + C::NBAR * 8);
+  const uint32_t QFREE = bar0 + 8u * uint32_t(2 * NS);
+  const uint32_t MERGE = bar0 + 8u * uint32_t(2 * NS + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(dsmem + C::BAR_OFF + C::NBAR * 8);
 
-  const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -600,154 +823,20 @@ __global__ void __launch_bounds__(TmaCfg<D>::THREADS, TmaCfg<D>::MINB)
       mbar_init(FULL(s), 1);
       mbar_init(EMPTY(s), NCW);
     }
+    mbar_init(QFREE, NCW);
     mbar_init(MERGE, NCW * 32);
     *abort_flag = 0;
     mbar_init_fence();
   }
+  const int causal = hdr->causal;
+  const int window_left = hdr->window_left;
   __syncthreads();
 
   if (warp == NCW) {
-    // ------------------------------------------------------------ producer
-    // Stage c of this CTA's sequence goes to slot c % NS; its (c / NS)-th
-    // fill waits for the consumers' release of the previous one. Everything
-    // a stage needs from global memory (the item's metadata, the page
-    // indices) is loaded before that wait, so a full ring hides it.
-    const int n_items = hdr->n_items;
-    const WorkItem* items = ws_ptr<const WorkItem>(p.ws, hdr->off_items);
-    const int32_t* qo_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_qo_indptr);
-    const int32_t* kv_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_kv_indptr);
-    const int32_t* kv_len = ws_ptr<const int32_t>(p.ws, hdr->off_kv_len);
-    const int window_left = hdr->window_left;
-    const int n_boxes = KT / box_rows;  // a stage is n_boxes boxes of box_rows slots of one page
-    const uint32_t box_bytes = uint32_t(box_rows) * D * 2;
-    constexpr int BPL = (KT + 31) / 32;  // boxes per lane, at most
-    int c = 0;
-    bool ok = true;
-    uint32_t last_par[NS];
-    bool armed[NS];
-#pragma unroll
-    for (int s = 0; s < NS; ++s) {
-      armed[s] = false;
-      last_par[s] = 0;
-    }
-    // claim slot st for stage c: wait for its release, then write the header
-    // and arm its barrier for `bytes` (lane 0); false once the CTA aborts.
-    // Every armed phase is recorded (the end-of-work stage too), so the drain
-    // below waits on each slot's latest phase.
-    auto claim = [&](int st, uint32_t par, const StageHdr& h, uint32_t bytes) {
-      bool okl = true;
-      if (lane == 0) {
-        if (c >= NS) okl = mbar_wait(EMPTY(st), par ^ 1u, abort_flag);
-        if (okl) {
-          sH[st] = h;
-          mbar_expect_tx(FULL(st), bytes);
-        }
-      }
-      okl = __shfl_sync(0xffffffffu, okl, 0) != 0;
-      if (okl) {
-#pragma unroll
-        for (int s = 0; s < NS; ++s)
-          if (s == st) {
-            armed[s] = true;
-            last_par[s] = par;
-          }
-      }
-      return okl;
-    };
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const WorkItem it = items[w];
-      if (it.b < 0) continue;  // schedule padding
-      const int token = qo_indptr[it.b];
-      const DecodeRange R = decode_range(it, kv_len[it.b], window_left, box_rows, KT);
-      const int32_t* pages = p.kv_indices + kv_indptr[it.b];
-      const T* qsrc = static_cast<const T*>(p.q) + int64_t(token) * p.q_stride_tok +
-                      int64_t(it.kv_head * G) * p.q_stride_head;
-      const int n_st = max(R.n_tiles, 1);  // an item without keys still writes its output
-      for (int t = 0; t < n_st; ++t, ++c) {
-        const int st = c % NS;
-        const uint32_t par = uint32_t(c / NS) & 1u;
-        const int k0 = R.start + t * KT;
-        const int n_live = R.n_tiles ? min(n_boxes, (R.hi - k0 + box_rows - 1) / box_rows) : 0;
-        int page[BPL], slot[BPL];
-#pragma unroll
-        for (int j = 0; j < BPL; ++j) {
-          const int i = lane + 32 * j;
-          page[j] = 0;
-          slot[j] = 0;
-          if (i < n_live) {
-            const int kb = k0 + i * box_rows;
-            int pi;
-            if (p.page_shift >= 0) {
-              pi = kb >> p.page_shift;
-              slot[j] = kb & ((1 << p.page_shift) - 1);
-            } else {
-              pi = kb / p.page_size;
-              slot[j] = kb - pi * p.page_size;
-            }
-            page[j] = __ldg(pages + pi);
-          }
-        }
-        StageHdr h;
-        h.flags = (t == 0 ? kStFirst : 0) | (t == n_st - 1 ? kStLast : 0) |
-                  (R.n_tiles ? 0 : kStNoKeys);
-        h.k0 = k0;
-        h.lo = R.lo;
-        h.hi = R.hi;
-        h.token = token;
-        h.kv_head = it.kv_head;
-        h.chunk = it.chunk;
-        h.partial_base = it.partial_base;
-        const uint32_t qbytes = t == 0 ? uint32_t(G * D * 2) : 0u;
-        if (!claim(st, par, h, uint32_t(n_live) * box_bytes * 2u + qbytes)) {
-          ok = false;
-          break;
-        }
-        if (t == 0 && lane < G)
-          bulk_load(smem_u32(sQ + (st * G + lane) * D), qsrc + int64_t(lane) * p.q_stride_head,
-                    uint32_t(D * 2), FULL(st));
-        const uint32_t dk = smem_u32(sK + st * STAGE), dv = smem_u32(sV + st * STAGE);
-#pragma unroll
-        for (int j = 0; j < BPL; ++j) {
-          const int i = lane + 32 * j;
-          if (i < n_live) {
-            if constexpr (W::kSwizzled) {
-              // one box per 64-column half; half h of the stage at h * KT * 128
-              const uint32_t off = uint32_t(i * box_rows) * 128u;
-#pragma unroll
-              for (int h = 0; h < D / 64; ++h) {
-                tma_load_4d(dk + h * KT * 128 + off, &tk, FULL(st), h * 64, it.kv_head, slot[j], page[j]);
-                tma_load_4d(dv + h * KT * 128 + off, &tv, FULL(st), h * 64, it.kv_head, slot[j], page[j]);
-              }
-            } else {
-              const uint32_t off = uint32_t(i) * box_bytes;
-              tma_load_4d(dk + off, &tk, FULL(st), 0, it.kv_head, slot[j], page[j]);
-              tma_load_4d(dv + off, &tv, FULL(st), 0, it.kv_head, slot[j], page[j]);
-            }
-          }
-        }
-      }
-    }
-    if (ok) {
-      // end of work: a header-only stage tells the consumers to stop
-      StageHdr h = {};
-      h.flags = kStEnd;
-      const int st = c % NS;
-      if (!claim(st, uint32_t(c / NS) & 1u, h, 0u)) ok = false;
-    }
-    // Drain: the last fill of every slot has landed before the CTA exits
-    // (the consumers waited for all of them unless a wait expired; this wait
-    // ignores the abort flag but keeps its time bound).
-    if (lane == 0) {
-      volatile int no_abort = 0;
-#pragma unroll
-      for (int s = 0; s < NS; ++s)
-        if (armed[s] && !mbar_wait(FULL(s), last_par[s], &no_abort)) *abort_flag = 1;
-    }
+    decode_producer<D, G, BF16, MMA, W>(p, &tk, &tv, box_rows, dsmem, lane, causal, window_left,
+                                   abort_flag);
   } else {
     // ------------------------------------------------------------ consumers
-    // Consumers read nothing from global memory: each stage's header says
-    // which keys it holds and where the item's output goes, and an item's
-    // first stage brings its q.
     float* tmp_lse = ws_ptr<float>(p.ws, hdr->off_tmp_lse);
     float* tmp_o = ws_ptr<float>(p.ws, hdr->off_tmp_o);
     W wk;
@@ -764,15 +853,44 @@ __global__ void __launch_bounds__(TmaCfg<D>::THREADS, TmaCfg<D>::MINB)
       // an expired wait ends the warp's work (the abort flag then makes
       // every other wait return at once); the error is reported below
       if (!mbar_wait(FULL(st), uint32_t(c / NS) & 1u, abort_flag)) break;
-      const StageHdr h = sH[st];
-      if (h.flags & kStEnd) break;
-      if (h.flags & kStFirst) wk.begin_smem(sQ + st * G * D, p.sm_scale_log2);
-      if (!(h.flags & kStNoKeys)) wk.stage(sK + st * STAGE, sV + st * STAGE, h.k0, h.lo, h.hi);
+      // the header is read in place (fields load where they are used); the
+      // output fields are copied out before the slot is released
+      const StageHdr& h = sH[st];
+      const int flags = h.flags;
+      if (flags & kStEnd) break;
+      if (flags & kStFirst) {
+        wk.begin(sQ, h.n_rows, p.sm_scale_log2);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(QFREE);
+      }
+      if (!(flags & kStNoKeys)) wk.stage(sK + st * STAGE, sV + st * STAGE, h, causal, window_left);
+      StageHdr out;
+      if (flags & kStLast) out = h;
       __syncwarp();
       if (lane == 0) mbar_arrive(EMPTY(st));
-      if (h.flags & kStLast)
-        wk.finish(p, h.token, h.kv_head, h.chunk, h.partial_base, tmp_o, tmp_lse, tid, sm_o,
-                  sm_m, sm_l, consumer_sync);
+      if (flags & kStLast) {
+        wk.publish_ml(sm_m, sm_l);
+        consumer_sync();
+#pragma unroll
+        for (int round = 0; round < W::ROUNDS; ++round) {
+          if (C::MB == 2) {
+            // warps 0 and 2 store into buffers 0 and 1, then 1 and 3 add
+            float* buf = sm_o + (warp >> 1) * 8 * D;
+            if ((warp & 1) == 0) wk.add_o(round, out.n_rows, true, buf, sm_m);
+            consumer_sync();
+            if (warp & 1) wk.add_o(round, out.n_rows, false, buf, sm_m);
+            consumer_sync();
+          } else {
+            for (int w = 0; w < NCW; ++w) {
+              if (warp == w) wk.add_o(round, out.n_rows, w == 0, sm_o, sm_m);
+              consumer_sync();
+            }
+          }
+          write_rows<D, G, BF16, NCW, C::MB>(p, out, 8 * round, tmp_o, tmp_lse, tid, sm_o, sm_m,
+                                             sm_l);
+          consumer_sync();
+        }
+      }
     }
   }
   __syncthreads();
@@ -784,35 +902,46 @@ __global__ void __launch_bounds__(TmaCfg<D>::THREADS, TmaCfg<D>::MINB)
 
 // -------------------------------------------------------------- launchers
 
-template <int D, int G, bool BF16, bool MMA>
-cudaError_t launch_dg(const AttnParams& p, int grid, const CUtensorMap& tk, const CUtensorMap& tv,
-                      int box_rows, cudaStream_t s) {
-  using C = TmaCfg<D>;
-  auto k = decode_tma_kernel<D, G, BF16, MMA>;
-  constexpr int smem = C::template smem_bytes<G>();
+template <int D, int G, bool BF16, bool MMA, int RH>
+cudaError_t launch_k(const AttnParams& p, int grid, const CUtensorMap& tk, const CUtensorMap& tv,
+                     int box_rows, cudaStream_t s) {
+  using C = TmaCfg<D, MMA>;
+  auto k = decode_tma_kernel<D, G, BF16, MMA, RH>;
   // once per process, before any capture (no attribute call inside a captured run)
-  static cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (attr != cudaSuccess) return attr;
-  k<<<grid, C::THREADS, smem, s>>>(p, tk, tv, box_rows);
+  k<<<grid, C::THREADS, C::SMEM, s>>>(p, tk, tv, box_rows);
   return cudaGetLastError();
 }
 
-template <int D, bool BF16, bool MMA>
-cudaError_t launch_d(const AttnParams& p, int group, int grid, const CUtensorMap& tk,
-                     const CUtensorMap& tv, int box_rows, cudaStream_t s) {
+// the tensor-core consumer for groups 1, 2, 4, 8, 16, one or two row halves
+template <int D, bool BF16>
+cudaError_t launch_mma(const AttnParams& p, int group, int rh, int grid, const CUtensorMap& tk,
+                       const CUtensorMap& tv, int box_rows, cudaStream_t s) {
+#define FI_MMA_CASE(G)                                                                     \
+  case G:                                                                                  \
+    return rh == 1 ? launch_k<D, G, BF16, true, 1>(p, grid, tk, tv, box_rows, s)           \
+                   : launch_k<D, G, BF16, true, 2>(p, grid, tk, tv, box_rows, s);
   switch (group) {
-    case 1: return launch_dg<D, 1, BF16, MMA>(p, grid, tk, tv, box_rows, s);
-    case 2: return launch_dg<D, 2, BF16, MMA>(p, grid, tk, tv, box_rows, s);
-    case 4: return launch_dg<D, 4, BF16, MMA>(p, grid, tk, tv, box_rows, s);
+    FI_MMA_CASE(1)
+    FI_MMA_CASE(2)
+    FI_MMA_CASE(4)
+    FI_MMA_CASE(8)
+    case 16: return launch_k<D, 16, BF16, true, 2>(p, grid, tk, tv, box_rows, s);
     default: return cudaErrorInvalidValue;
   }
+#undef FI_MMA_CASE
 }
 
 template <int D, bool BF16>
-cudaError_t launch_dm(const AttnParams& p, int group, int grid, const CUtensorMap& tk,
-                      const CUtensorMap& tv, int box_rows, bool mma, cudaStream_t s) {
-  return mma ? launch_d<D, BF16, true>(p, group, grid, tk, tv, box_rows, s)
-             : launch_d<D, BF16, false>(p, group, grid, tk, tv, box_rows, s);
+cudaError_t launch_shuffle(const AttnParams& p, int group, int grid, const CUtensorMap& tk,
+                           const CUtensorMap& tv, int box_rows, cudaStream_t s) {
+  switch (group) {
+    case 1: return launch_k<D, 1, BF16, false, 1>(p, grid, tk, tv, box_rows, s);
+    case 2: return launch_k<D, 2, BF16, false, 1>(p, grid, tk, tv, box_rows, s);
+    case 4: return launch_k<D, 4, BF16, false, 1>(p, grid, tk, tv, box_rows, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 int gcd_int(int a, int b) {
@@ -824,23 +953,38 @@ int gcd_int(int a, int b) {
   return a;
 }
 
+int stage_keys(int head_dim) { return head_dim == 128 ? TmaCfg<128, true>::KT : TmaCfg<64, true>::KT; }
+
 }  // namespace
 
-int decode_ctas_per_sm(int head_dim) {
-  return head_dim == 64 ? TmaCfg<64>::MINB : TmaCfg<128>::MINB;
+bool decode_mma_supports(int head_dim, int page_size, int group) {
+  if (head_dim != 64 && head_dim != 128) return false;
+  if (group != 1 && group != 2 && group != 4 && group != 8 && group != 16) return false;
+  return gcd_int(page_size, stage_keys(head_dim)) >= 8;
+}
+
+bool decode_shuffle_supports(int head_dim, int group) {
+  return (head_dim == 64 || head_dim == 128) && (group == 1 || group == 2 || group == 4);
+}
+
+int decode_ctas_per_sm(int head_dim, int page_size, int group) {
+  const bool mma = decode_mma_supports(head_dim, page_size, group);
+  if (head_dim == 64) return mma ? TmaCfg<64, true>::MINB : TmaCfg<64, false>::MINB;
+  return mma ? TmaCfg<128, true>::MINB : TmaCfg<128, false>::MINB;
 }
 
 cudaError_t launch_decode(const AttnParams& p, int head_dim, int group, bool bf16,
-                          int64_t num_pages, int grid, cudaStream_t stream) {
+                          int64_t num_pages, int tile_rows, int grid, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
   if (head_dim != 128 && head_dim != 64) return cudaErrorInvalidValue;
   // Boxes of gcd(page_size, KT) slots never cross a page: every box starts
   // at a multiple of that size (tiles start at lo rounded down to it).
-  const int kt = head_dim == 128 ? TmaCfg<128>::KT : TmaCfg<64>::KT;
-  const int box_rows = gcd_int(p.page_size, kt);
-  // Tensor-core consumer when a box spans whole swizzle atoms (8 slots of
-  // 128 bytes per 64-column half); shuffle consumer for smaller boxes.
-  const bool mma = box_rows >= 8;
+  const int box_rows = gcd_int(p.page_size, stage_keys(head_dim));
+  const bool mma = decode_mma_supports(head_dim, p.page_size, group);
+  if (!mma && !(decode_shuffle_supports(head_dim, group) && tile_rows == group))
+    return cudaErrorInvalidValue;
+  if (tile_rows < 1 || tile_rows > kMaxRows) return cudaErrorInvalidValue;
+  const int rh = tile_rows > 8 ? 2 : 1;
   const int box_cols = mma ? 64 : head_dim;
   const CUtensorMapSwizzle swz = mma ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUtensorMap tk, tv;
@@ -852,11 +996,18 @@ cudaError_t launch_decode(const AttnParams& p, int head_dim, int group, bool bf1
                            p.v_stride_head, p.v_stride_tok, p.v_stride_page, box_cols, box_rows,
                            swz))
     return cudaErrorInvalidValue;
+  if (mma) {
+    if (head_dim == 128)
+      return bf16 ? launch_mma<128, true>(p, group, rh, grid, tk, tv, box_rows, stream)
+                  : launch_mma<128, false>(p, group, rh, grid, tk, tv, box_rows, stream);
+    return bf16 ? launch_mma<64, true>(p, group, rh, grid, tk, tv, box_rows, stream)
+                : launch_mma<64, false>(p, group, rh, grid, tk, tv, box_rows, stream);
+  }
   if (head_dim == 128)
-    return bf16 ? launch_dm<128, true>(p, group, grid, tk, tv, box_rows, mma, stream)
-                : launch_dm<128, false>(p, group, grid, tk, tv, box_rows, mma, stream);
-  return bf16 ? launch_dm<64, true>(p, group, grid, tk, tv, box_rows, mma, stream)
-              : launch_dm<64, false>(p, group, grid, tk, tv, box_rows, mma, stream);
+    return bf16 ? launch_shuffle<128, true>(p, group, grid, tk, tv, box_rows, stream)
+                : launch_shuffle<128, false>(p, group, grid, tk, tv, box_rows, stream);
+  return bf16 ? launch_shuffle<64, true>(p, group, grid, tk, tv, box_rows, stream)
+              : launch_shuffle<64, false>(p, group, grid, tk, tv, box_rows, stream);
 }
 
 }  // namespace fi

@@ -82,11 +82,18 @@ enum KernelId : int32_t {
 };
 
 // Launchers (defined in the .cu files). Each returns cudaGetLastError().
-// num_pages: pages in the K/V cache tensors (the TMA maps' outer extent).
+// The short-query kernel (kDecode): items of at most 16 packed rows.
+// num_pages: pages in the K/V cache tensors (the TMA maps' outer extent);
+// tile_rows: the plan's packed rows per item (at most 16).
 cudaError_t launch_decode(const AttnParams& p, int head_dim, int group, bool bf16,
-                          int64_t num_pages, int grid, cudaStream_t stream);
-// CTAs per SM the decode kernel is built for.
-int decode_ctas_per_sm(int head_dim);
+                          int64_t num_pages, int tile_rows, int grid, cudaStream_t stream);
+// Its tensor-core consumer: any query length with q_len * group <= 16, for
+// groups 1, 2, 4, 8, 16 and page sizes whose boxes span whole swizzle atoms.
+bool decode_mma_supports(int head_dim, int page_size, int group);
+// Its CUDA-core consumer: decode (one query row per request), groups 1, 2, 4.
+bool decode_shuffle_supports(int head_dim, int group);
+// CTAs per SM the short-query kernel is built for (depends on its consumer).
+int decode_ctas_per_sm(int head_dim, int page_size, int group);
 cudaError_t launch_prefill_mma(const AttnParams& p, int head_dim, int kernel, bool bf16,
                                int grid, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const AttnParams& p, int head_dim, int group, int tile_rows,
@@ -115,6 +122,6 @@ struct MergeTwoParams {
 cudaError_t launch_merge_two(const MergeTwoParams& p, cudaStream_t stream);
 
 // Occupancy of each run kernel (CTAs per SM), for persistent grid sizing.
-int kernel_ctas_per_sm(int kernel, int head_dim, int group, bool bf16);
+int kernel_ctas_per_sm(int kernel, int head_dim, int group, bool bf16, int page_size);
 
 }  // namespace fi

@@ -216,7 +216,7 @@ extern "C" fi_status fi_batch_decode_paged_noalloc(
   for (int sh = 0; sh < 31; ++sh)
     if ((1 << sh) == page_size) ap.page_shift = sh;
   const int grid = batch * hk * kv_chunks;
-  e = launch_decode(ap, d, g, q->dtype == FI_BF16, k_cache->shape[0], grid, s);
+  e = launch_decode(ap, d, g, q->dtype == FI_BF16, k_cache->shape[0], g, grid, s);
   if (e != cudaSuccess) return fail(FI_ERR_CUDA, "decode_noalloc: decode launch failed");
   if (kv_chunks > 1) {
     e = launch_merge_workspace(ws, out->data, ap.lse, hq, d, q->dtype == FI_BF16,

@@ -369,10 +369,10 @@ cudaError_t launch_prefill_mma(const AttnParams& p, int head_dim, int kernel, bo
   return cudaErrorInvalidValue;
 }
 
-int kernel_ctas_per_sm(int kernel, int head_dim, int group, bool bf16) {
+int kernel_ctas_per_sm(int kernel, int head_dim, int group, bool bf16, int page_size) {
   (void)bf16;
   switch (kernel) {
-    case kDecode: return decode_ctas_per_sm(head_dim);
+    case kDecode: return decode_ctas_per_sm(head_dim, page_size, group);
     case kPrefillM16: return head_dim == 128 ? 3 : 6;
     case kPrefillM64: return head_dim == 128 ? 2 : 4;
     case kPrefillM128: return 1;

@@ -79,11 +79,15 @@ def test_decode_head_dim_64_window(layout):
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)
-def test_verify_layouts(layout):
-    pb = workloads.make_paged_batch([4] * 5, [4, 60, 333, 1024, 9], 32, 8, 128, 16, "bf16", 55)
+@pytest.mark.parametrize("page_size,kernel", [(16, "decode"), (2, "prefill_m16")])
+def test_verify_layouts(layout, page_size, kernel):
+    """Verify runs on the short-query TMA kernel where its boxes span whole
+    swizzle atoms, else on the cp.async mma kernel."""
+    pb = workloads.make_paged_batch([4] * 5, [4, 60, 333, 1024, 9], 32, 8, 128, page_size, "bf16",
+                                    55 + page_size)
     out, lse, kern = run(pb, layout, "verify", True, -1, q_len_per_req=4)
-    assert kern == "prefill_m16"
-    assert_close(pb, out, lse, True, -1, what="verify %s" % layout)
+    assert kern == kernel
+    assert_close(pb, out, lse, True, -1, what="verify %s P=%d" % (layout, page_size))
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)
