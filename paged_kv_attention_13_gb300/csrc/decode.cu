@@ -893,6 +893,8 @@ __global__ void __launch_bounds__(TmaCfg<D, MMA>::THREADS, TmaCfg<D, MMA>::MINB)
       }
     }
   }
+  // the split-KV merge launched after this kernel may start its launch now
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __syncthreads();
   if (tid == 0 && *abort_flag) {
     int* err = const_cast<int*>(&hdr->err_flag);

@@ -66,6 +66,9 @@ __device__ void merge_one(const float* __restrict__ v, const float* __restrict__
 template <int OUT>
 __global__ void __launch_bounds__(256) merge_workspace_kernel(const void* ws, void* out,
                                                               float* lse, int H, int D) {
+  // launched as a programmatic dependent of the attention kernel: its launch
+  // overlaps that kernel's tail, and this wait makes the partials visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const WsHeader* hdr = static_cast<const WsHeader*>(ws);
   const int n_rows = hdr->n_merge_rows;
   const int32_t* merge_indptr = ws_ptr<const int32_t>(ws, hdr->off_merge_indptr);
@@ -156,8 +159,21 @@ int merge_grid(int64_t warps_needed) {
 
 cudaError_t launch_merge_workspace(const void* ws, void* out, float* lse, int H, int D,
                                    bool bf16, int grid, cudaStream_t s) {
-  if (bf16) merge_workspace_kernel<1><<<grid, 256, 0, s>>>(ws, out, lse, H, D);
-  else merge_workspace_kernel<0><<<grid, 256, 0, s>>>(ws, out, lse, H, D);
+  // programmatic dependent launch on the attention kernel before it in the
+  // stream (also inside a captured graph)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = bf16 ? cudaLaunchKernelEx(&cfg, merge_workspace_kernel<1>, ws, out, lse, H, D)
+                       : cudaLaunchKernelEx(&cfg, merge_workspace_kernel<0>, ws, out, lse, H, D);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
