@@ -163,8 +163,13 @@ class Runner:
         self.pb, self.causal, self.wl, self.mode = pb, causal, wl, mode
         self.dev = dev
         self.q = pb.q.to(dev)
-        self.k = pb.k_cache.to(dev)
-        self.v = pb.v_cache.to(dev)
+        if mode == "ragged":  # contiguous K/V rows (a page-size-1, unpermuted cache)
+            rows = pb.k_cache.shape[0]
+            self.k = pb.k_cache.reshape(rows, pb.num_kv_heads, pb.head_dim).to(dev)
+            self.v = pb.v_cache.reshape(rows, pb.num_kv_heads, pb.head_dim).to(dev)
+        else:
+            self.k = pb.k_cache.to(dev)
+            self.v = pb.v_cache.to(dev)
         self.idx = pb.kv_indices.to(dev)
         self.out = torch.empty_like(self.q)
         self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=dev)
@@ -177,7 +182,11 @@ class Runner:
     def do_plan(self):
         pb = self.pb
         dt = workloads.TORCH_DTYPE[pb.dtype]
-        if self.mode == "prefill":
+        if self.mode == "ragged":
+            self.plan.plan_ragged(pb.qo_indptr, pb.kv_indptr, pb.num_qo_heads, pb.num_kv_heads,
+                                  pb.head_dim, causal=self.causal, window_left=self.wl, dtype=dt,
+                                  force_kv_chunks=self.force)
+        elif self.mode == "prefill":
             self.plan.plan(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, pb.page_size,
                            pb.num_qo_heads, pb.num_kv_heads, pb.head_dim, causal=self.causal,
                            window_left=self.wl, dtype=dt, force_kv_chunks=self.force)
@@ -189,6 +198,10 @@ class Runner:
         self.info = self.plan.info()
 
     def run(self):
+        if self.mode == "ragged":
+            self.fi.fi_batch_prefill_ragged(self.plan, self.q, self.k, self.v, self.pb.sm_scale,
+                                            out=self.out, lse=self.lse)
+            return
         f = self.fi.fi_batch_prefill_paged if self.mode == "prefill" else self.fi.fi_batch_decode_paged
         f(self.plan, self.q, self.k, self.v, self.idx, self.pb.sm_scale, out=self.out, lse=self.lse)
 
@@ -407,6 +420,8 @@ def other_workloads(args, dev, ws, hbm_peak, bf16_peak):
         if P == 16:
             one("prefill_p16_noncausal", pb, False, -1, "prefill", bound="tensor")
             one("prefill_p16_causal_wl127", pb, True, 127, "prefill")
+    pb = workloads.ragged_prefill()
+    one("ragged_prefill_causal", pb, True, -1, "ragged", bound="tensor")
     pb = workloads.long_context()
     one("longctx_causal_split", pb, True, -1, "prefill")
     one("longctx_causal_force32", pb, True, -1, "prefill", force=32)
@@ -459,6 +474,7 @@ PROFILE_CASES = {
     "prefill_p1024_causal": (lambda: workloads.batch_prefill(page_size=1024), True, -1, "prefill"),
     "prefill_p16_noncausal": (lambda: workloads.batch_prefill(page_size=16), False, -1, "prefill"),
     "longctx_causal": (lambda: workloads.long_context(), True, -1, "prefill"),
+    "ragged_prefill_causal": (lambda: workloads.ragged_prefill(), True, -1, "ragged"),
 }
 
 

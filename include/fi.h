@@ -184,6 +184,39 @@ fi_status fi_batch_decode_paged(fi_plan_t plan, const fi_tensor* q, const fi_ten
                                 float sm_scale, fi_tensor* out, fi_tensor* lse, void* stream);
 
 /*
+ * Ragged prefill over contiguous K/V: the third prefill entry point beside
+ * single and paged prefill ("Route non-causal windowed prefill to AITER's
+ * masked kernel" (#339), "Pull request overview", whose regression tests
+ * cover all three), which runs on K/V that is already contiguous, so there
+ * is no page gather ("Support speculative-decode verify on ROCm, and stop
+ * auto routing short-query prefill to AITER" (#362), "Architecture / design
+ * notes"). The keys of request b are rows kv_indptr[b] .. kv_indptr[b+1]-1 of
+ * one [rows, Hk, d] tensor, so no page table is read; masks, GQA grouping,
+ * lse and the split-KV merge are those of fi_batch_prefill_paged.
+ *
+ * fi_plan_ragged: as fi_plan for a prefill, with
+ *   kv_indptr  host int32 [batch+1]: each request's first K/V row (kv_len_b =
+ *              kv_indptr[b+1] - kv_indptr[b]); nondecreasing, kv_indptr[0] = 0.
+ * There is no page size or last_page_len. Refusals as for fi_plan
+ * (FI_ERR_KV_SHORTER_THAN_Q under the causal mask, ...).
+ *
+ * fi_batch_prefill_ragged: run a plan from fi_plan_ragged.
+ *   q     [T, Hq, d]  as for fi_batch_prefill_paged;
+ *   k, v  [rows, Hk, d], rows >= kv_indptr[batch], same dtype as q, last dim
+ *         contiguous, other strides multiples of 8 elements, 16-byte aligned;
+ *   out / lse as for fi_batch_prefill_paged.
+ * A paged plan given to this call, or a ragged plan to the paged calls, is
+ * refused with FI_ERR_PLAN_MISMATCH. Nothing is allocated or synchronised.
+ */
+fi_status fi_plan_ragged(fi_plan_t plan, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                         int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t causal, int32_t window_left, fi_dtype dtype,
+                         int32_t force_kv_chunks, void* stream);
+fi_status fi_batch_prefill_ragged(fi_plan_t plan, const fi_tensor* q, const fi_tensor* k,
+                                  const fi_tensor* v, float sm_scale, fi_tensor* out,
+                                  fi_tensor* lse, void* stream);
+
+/*
  * Merge two attention states by their log-sum-exp [P3 "Graph-mode
  * partial_state merge"]:
  *   m = max(s_a, s_b), s = m + ln(exp(s_a - m) + exp(s_b - m)),

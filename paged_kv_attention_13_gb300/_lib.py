@@ -24,7 +24,7 @@ EXPORTED = [
     "fi_batch_decode_paged", "fi_merge_state", "fi_merge_states", "fi_plan_get_info",
     "fi_plan_read_device", "fi_plan_destroy", "fi_last_error", "fi_status_str",
     "fi_batch_decode_paged_noalloc", "fi_noalloc_scratch_bytes", "fi_noalloc_last_error",
-    "fi_plan_device_error",
+    "fi_plan_device_error", "fi_plan_ragged", "fi_batch_prefill_ragged",
 ]
 
 
@@ -75,6 +75,10 @@ def load():
     lib.fi_plan_get_info.argtypes = [P, ctypes.POINTER(FiPlanInfo), pi32, i32, pi32, i32]
     lib.fi_plan_read_device.restype = ctypes.c_int
     lib.fi_plan_read_device.argtypes = [P, pi32, i32, pi32, i32, P]
+    lib.fi_plan_ragged.restype = ctypes.c_int
+    lib.fi_plan_ragged.argtypes = [P, pi32, pi32, i32, i32, i32, i32, i32, i32, ctypes.c_int, i32, P]
+    lib.fi_batch_prefill_ragged.restype = ctypes.c_int
+    lib.fi_batch_prefill_ragged.argtypes = [P, PT, PT, PT, ctypes.c_float, PT, PT, P]
     lib.fi_plan_device_error.restype = ctypes.c_int
     lib.fi_plan_device_error.argtypes = [P, pi32, ctypes.c_int, P]
     lib.fi_plan_destroy.restype = None

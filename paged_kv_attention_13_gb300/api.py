@@ -125,6 +125,21 @@ class Plan:
         self.q_len_per_req = q_len_per_req
         return self
 
+    def plan_ragged(self, qo_indptr, kv_indptr, num_qo_heads, num_kv_heads, head_dim,
+                    causal=False, window_left=-1, dtype=torch.bfloat16, force_kv_chunks=0,
+                    stream=None):
+        """fi_plan_ragged: kv_indptr holds each request's first row of a
+        contiguous [rows, Hk, d] K/V (host int32 tensors, arrays or lists)."""
+        qo, qo_p = _host_i32(qo_indptr)
+        kv, kv_p = _host_i32(kv_indptr)
+        batch = len(kv) - 1 if kv is not None else 0
+        _check(self._lib.fi_plan_ragged(self.handle, qo_p, kv_p, batch, int(num_qo_heads),
+                                        int(num_kv_heads), int(head_dim), int(bool(causal)),
+                                        int(window_left), _DTYPES[dtype], int(force_kv_chunks),
+                                        _stream_handle(stream)))
+        self.q_len_per_req = 0
+        return self
+
     def info(self, with_arrays=False):
         inf = FiPlanInfo()
         _check(self._lib.fi_plan_get_info(self.handle, ctypes.byref(inf), None, 0, None, 0))
@@ -190,6 +205,21 @@ def fi_batch_decode_paged(plan, q, k_cache, v_cache, kv_indices, sm_scale, out=N
     """Batched paged decode / speculative verify; returns (out, lse)."""
     return _run(_lib.load().fi_batch_decode_paged, plan, q, k_cache, v_cache, kv_indices,
                 sm_scale, out, lse, return_lse, stream)
+
+
+def fi_batch_prefill_ragged(plan, q, k, v, sm_scale, out=None, lse=None, return_lse=True,
+                            stream=None):
+    """Batched prefill over contiguous K/V [rows, Hk, d]; returns (out, lse)."""
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    qd, kd, vd, od = tensor_desc(q), tensor_desc(k), tensor_desc(v), tensor_desc(out)
+    ld = tensor_desc(lse) if lse is not None else None
+    _check(_lib.load().fi_batch_prefill_ragged(
+        plan.handle, ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd), ctypes.c_float(sm_scale),
+        ctypes.byref(od), ctypes.byref(ld) if ld is not None else None, _stream_handle(stream)))
+    return out, lse
 
 
 def fi_merge_state(v_a, s_a, v_b, s_b, v_out=None, s_out=None, num_rows_dev=None, stream=None):

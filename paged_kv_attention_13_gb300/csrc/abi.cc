@@ -47,7 +47,8 @@ struct PlanState {
   int32_t batch = 0, total_rows = 0, page_size = 0, hq = 0, hk = 0, d = 0;
   int32_t causal = 0, window_left = -1, dtype = 0, q_len_per_req = 0, group = 1;
   int32_t kernel = 0, tile_rows = 0, grid = 0, max_chunks = 1, n_partials = 0;
-  int32_t kv_indices_len = 0;
+  int32_t kv_indices_len = 0;  // page-table entries (ragged: K/V rows) the plan reads
+  int32_t ragged = 0;          // contiguous K/V rows instead of a page table
   std::vector<int32_t> qo_indptr, kv_indptr, kv_len, merge_indptr, merge_rows;
   std::vector<WorkItem> items;
   WsHeader hdr{};
@@ -80,6 +81,7 @@ struct fi_plan_s {
   // shape frozen by the first plan of a graph-mode plan object
   bool frozen = false;
   int32_t fz_kernel = 0, fz_qlpr = 0, fz_hq = 0, fz_hk = 0, fz_d = 0, fz_dtype = 0, fz_page = 0;
+  int32_t fz_ragged = 0;
 };
 
 extern "C" const char* fi_last_error(void) { return g_last_error.c_str(); }
@@ -218,14 +220,18 @@ struct Tile {
 };
 
 // Build a complete plan into `ns` without touching the plan object.
+// ragged: kv_indptr_h holds each request's first K/V row (contiguous K/V),
+// last_page_len_h is unused, and page_size is kRaggedPage (one logical page).
+constexpr int32_t kRaggedPage = 1 << 30;
+
 fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
                      const int32_t* last_page_len_h, int32_t batch, int32_t page_size,
                      int32_t hq, int32_t hk, int32_t d, int32_t causal, int32_t window_left,
                      fi_dtype dtype, int32_t q_len_per_req, int32_t force_kv_chunks,
-                     PlanState& ns) {
+                     bool ragged, PlanState& ns) {
   // ---- argument validation, before anything is written [P2 "Review notes"]
   if (batch < 0) return fail(FI_ERR_INVALID_ARG, "plan: batch=%d must be >= 0", batch);
-  if (batch > 0 && (!kv_indptr_h || !last_page_len_h))
+  if (batch > 0 && (!kv_indptr_h || (!ragged && !last_page_len_h)))
     return fail(FI_ERR_INVALID_ARG, "plan: kv_indptr and last_page_len must be non-NULL");
   if (page_size < 1) return fail(FI_ERR_INVALID_ARG, "plan: page_size=%d must be >= 1", page_size);
   // [P3 "GQA head divisibility"]: refuse zero kv heads and a group that does not divide
@@ -255,6 +261,7 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
   ns = PlanState();
   ns.batch = batch; ns.page_size = page_size; ns.hq = hq; ns.hk = hk; ns.d = d;
   ns.causal = eff_causal; ns.window_left = window_left; ns.dtype = dtype;
+  ns.ragged = ragged ? 1 : 0;
   ns.q_len_per_req = q_len_per_req; ns.group = g;
   ns.qo_indptr.resize(batch + 1);
   ns.kv_indptr.resize(batch + 1);
@@ -284,7 +291,9 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
     // [P2 "Review notes"]: kv_len from the page metadata (paged_kv_t::get_length)
     int64_t pages = int64_t(ns.kv_indptr[b + 1]) - ns.kv_indptr[b];
     int64_t lk = 0;
-    if (pages > 0) {
+    if (ragged) {
+      lk = pages;  // rows of the contiguous K/V
+    } else if (pages > 0) {
       int32_t last = last_page_len_h[b];
       if (last < 1 || last > page_size)
         return fail(FI_ERR_INVALID_ARG, "plan: last_page_len[%d]=%d outside [1, page_size=%d]",
@@ -327,6 +336,7 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
     else if (d != P.fz_d) { field = "head_dim"; want = P.fz_d; got = d; }
     else if (dtype != P.fz_dtype) { field = "dtype"; want = P.fz_dtype; got = dtype; }
     else if (page_size != P.fz_page) { field = "page_size"; want = P.fz_page; got = page_size; }
+    else if (int32_t(ragged) != P.fz_ragged) { field = "ragged"; want = P.fz_ragged; got = ragged; }
     else if (ns.kernel != P.fz_kernel) { field = "kernel"; want = P.fz_kernel; got = ns.kernel; }
     if (field)
       return fail(FI_ERR_CAPACITY, "plan: %s is frozen at %d by the first graph-mode plan, got %d",
@@ -585,16 +595,18 @@ void write_staging(const PlanState& s, uint8_t* dst) {
 
 }  // namespace
 
-extern "C" fi_status fi_plan(fi_plan_t p, const int32_t* qo_indptr, const int32_t* kv_indptr,
-                             const int32_t* last_page_len, int32_t batch, int32_t page_size,
-                             int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
-                             int32_t causal, int32_t window_left, fi_dtype dtype,
-                             int32_t q_len_per_req, int32_t force_kv_chunks, void* stream) {
+namespace {
+
+fi_status plan_common(fi_plan_t p, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                      const int32_t* last_page_len, int32_t batch, int32_t page_size,
+                      int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t causal, int32_t window_left, fi_dtype dtype,
+                      int32_t q_len_per_req, int32_t force_kv_chunks, bool ragged, void* stream) {
   if (!p) return fail(FI_ERR_INVALID_ARG, "plan: plan is NULL");
   PlanState ns;
   fi_status st = build_plan(*p, qo_indptr, kv_indptr, last_page_len, batch, page_size,
                             num_qo_heads, num_kv_heads, head_dim, causal, window_left, dtype,
-                            q_len_per_req, force_kv_chunks, ns);
+                            q_len_per_req, force_kv_chunks, ragged, ns);
   if (st != FI_OK) return st;  // the previous plan stays usable
   if (!p->host_only) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -633,10 +645,33 @@ extern "C" fi_status fi_plan(fi_plan_t p, const int32_t* qo_indptr, const int32_
     p->frozen = true;
     p->fz_kernel = ns.kernel; p->fz_qlpr = ns.q_len_per_req; p->fz_hq = ns.hq;
     p->fz_hk = ns.hk; p->fz_d = ns.d; p->fz_dtype = ns.dtype; p->fz_page = ns.page_size;
+    p->fz_ragged = ns.ragged;
   }
   p->st = std::move(ns);
   p->planned = true;
   return ok();
+}
+
+}  // namespace
+
+extern "C" fi_status fi_plan(fi_plan_t p, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                             const int32_t* last_page_len, int32_t batch, int32_t page_size,
+                             int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t causal, int32_t window_left, fi_dtype dtype,
+                             int32_t q_len_per_req, int32_t force_kv_chunks, void* stream) {
+  return plan_common(p, qo_indptr, kv_indptr, last_page_len, batch, page_size, num_qo_heads,
+                     num_kv_heads, head_dim, causal, window_left, dtype, q_len_per_req,
+                     force_kv_chunks, false, stream);
+}
+
+extern "C" fi_status fi_plan_ragged(fi_plan_t p, const int32_t* qo_indptr,
+                                    const int32_t* kv_indptr, int32_t batch, int32_t num_qo_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t causal,
+                                    int32_t window_left, fi_dtype dtype, int32_t force_kv_chunks,
+                                    void* stream) {
+  return plan_common(p, qo_indptr, kv_indptr, nullptr, batch, kRaggedPage, num_qo_heads,
+                     num_kv_heads, head_dim, causal, window_left, dtype, 0, force_kv_chunks, true,
+                     stream);
 }
 
 extern "C" fi_status fi_plan_get_info(fi_plan_t p, fi_plan_info* info, int32_t* items,
@@ -758,14 +793,20 @@ fi_status check_packed(const fi_tensor* t, const char* name) {
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
 
-fi_status run_common(fi_plan_t p, bool decode_api, const fi_tensor* q, const fi_tensor* k,
-                     const fi_tensor* v, const fi_tensor* kv_indices, float sm_scale,
-                     fi_tensor* out, fi_tensor* lse, void* stream) {
-  const char* api = decode_api ? "batch_decode_paged" : "batch_prefill_paged";
+// ragged: k / v are [rows, Hk, d] contiguous K/V (kv_indices unused) and the
+// plan came from fi_plan_ragged.
+fi_status run_common(fi_plan_t p, bool decode_api, bool ragged, const fi_tensor* q,
+                     const fi_tensor* k, const fi_tensor* v, const fi_tensor* kv_indices,
+                     float sm_scale, fi_tensor* out, fi_tensor* lse, void* stream) {
+  const char* api = ragged ? "batch_prefill_ragged"
+                           : decode_api ? "batch_decode_paged" : "batch_prefill_paged";
   if (!p) return fail(FI_ERR_INVALID_ARG, "%s: plan is NULL", api);
   // [P3 "Plan-vs-run shapes"]: a half-planned object refuses run()
   if (!p->planned) return fail(FI_ERR_NOT_PLANNED, "%s: call fi_plan() first", api);
   const PlanState& s = p->st;
+  if (ragged != (s.ragged != 0))
+    return fail(FI_ERR_PLAN_MISMATCH, "%s: the plan is for a %s K/V cache (fi_plan%s)", api,
+                s.ragged ? "ragged" : "paged", s.ragged ? "_ragged" : "");
   if (decode_api && s.q_len_per_req < 1)
     return fail(FI_ERR_PLAN_MISMATCH, "%s: q_len_per_req: planned %d (a prefill plan), "
                 "expected >= 1", api, s.q_len_per_req);
@@ -773,21 +814,26 @@ fi_status run_common(fi_plan_t p, bool decode_api, const fi_tensor* q, const fi_
     return fail(FI_ERR_PLAN_MISMATCH, "%s: q_len_per_req: planned %d (a decode plan), "
                 "expected 0", api, s.q_len_per_req);
   fi_status st;
+  const int kv_ndim = ragged ? 3 : 4;  // ragged: [rows, Hk, d]; paged: [pages, P, Hk, d]
   if ((st = check_tensor(q, "q", 3)) != FI_OK) return st;
-  if ((st = check_tensor(k, "k_cache", 4)) != FI_OK) return st;
-  if ((st = check_tensor(v, "v_cache", 4)) != FI_OK) return st;
-  if ((st = check_tensor(kv_indices, "kv_indices", 1)) != FI_OK) return st;
+  if ((st = check_tensor(k, "k_cache", kv_ndim)) != FI_OK) return st;
+  if ((st = check_tensor(v, "v_cache", kv_ndim)) != FI_OK) return st;
+  if (!ragged && (st = check_tensor(kv_indices, "kv_indices", 1)) != FI_OK) return st;
   if ((st = check_tensor(out, "out", 3)) != FI_OK) return st;
   if (lse && (st = check_tensor(lse, "lse", 2)) != FI_OK) return st;
   // [P3 "Plan-vs-run shapes"]: heads, head dims, page size, token minimums
   if (q->shape[0] < s.total_rows) return check_dim("q", "rows (minimum)", s.total_rows, q->shape[0]);
   if (q->shape[1] != s.hq) return check_dim("q", "num_qo_heads", s.hq, q->shape[1]);
   if (q->shape[2] != s.d) return check_dim("q", "head_dim", s.d, q->shape[2]);
+  const int kh = ragged ? 1 : 2;  // index of the kv-head dim
   for (const fi_tensor* c : {k, v}) {
     const char* n = (c == k) ? "k_cache" : "v_cache";
-    if (c->shape[1] != s.page_size) return check_dim(n, "page_size", s.page_size, c->shape[1]);
-    if (c->shape[2] != s.hk) return check_dim(n, "num_kv_heads", s.hk, c->shape[2]);
-    if (c->shape[3] != s.d) return check_dim(n, "head_dim", s.d, c->shape[3]);
+    if (!ragged && c->shape[1] != s.page_size)
+      return check_dim(n, "page_size", s.page_size, c->shape[1]);
+    if (ragged && c->shape[0] < s.kv_indices_len)
+      return check_dim(n, "rows (minimum, kv_indptr[batch])", s.kv_indices_len, c->shape[0]);
+    if (c->shape[kh] != s.hk) return check_dim(n, "num_kv_heads", s.hk, c->shape[kh]);
+    if (c->shape[kh + 1] != s.d) return check_dim(n, "head_dim", s.d, c->shape[kh + 1]);
     if (c->dtype != s.dtype)
       return fail(FI_ERR_PLAN_MISMATCH, "run: %s dtype: planned %s, got %s", n,
                   dtype_name(s.dtype), dtype_name(c->dtype));
@@ -801,10 +847,12 @@ fi_status run_common(fi_plan_t p, bool decode_api, const fi_tensor* q, const fi_
   if (out->dtype != s.dtype)
     return fail(FI_ERR_PLAN_MISMATCH, "run: out dtype: planned %s, got %s",
                 dtype_name(s.dtype), dtype_name(out->dtype));
-  if (kv_indices->dtype != FI_I32)
-    return fail(FI_ERR_INVALID_ARG, "run: kv_indices must be int32");
-  if (kv_indices->shape[0] < s.kv_indices_len)
-    return check_dim("kv_indices", "length (minimum)", s.kv_indices_len, kv_indices->shape[0]);
+  if (!ragged) {
+    if (kv_indices->dtype != FI_I32)
+      return fail(FI_ERR_INVALID_ARG, "run: kv_indices must be int32");
+    if (kv_indices->shape[0] < s.kv_indices_len)
+      return check_dim("kv_indices", "length (minimum)", s.kv_indices_len, kv_indices->shape[0]);
+  }
   if (out->shape[0] < s.total_rows)
     return check_dim("out", "rows (minimum)", s.total_rows, out->shape[0]);
   if (out->shape[1] != s.hq) return check_dim("out", "num_qo_heads", s.hq, out->shape[1]);
@@ -822,9 +870,11 @@ fi_status run_common(fi_plan_t p, bool decode_api, const fi_tensor* q, const fi_
     return fail(FI_ERR_INVALID_ARG, "%s: sm_scale=%g must be positive and finite", api,
                 double(sm_scale));
   // 16-byte vector loads of every row
+  bool kv_strides_ok = true;
+  for (int i = 0; i < kv_ndim - 1; ++i)
+    if (k->stride[i] % 8 || v->stride[i] % 8) kv_strides_ok = false;
   if (!aligned16(q->data) || !aligned16(k->data) || !aligned16(v->data) || !aligned16(out->data) ||
-      q->stride[0] % 8 || q->stride[1] % 8 || k->stride[0] % 8 || k->stride[1] % 8 ||
-      k->stride[2] % 8 || v->stride[0] % 8 || v->stride[1] % 8 || v->stride[2] % 8)
+      q->stride[0] % 8 || q->stride[1] % 8 || !kv_strides_ok)
     return fail(FI_ERR_UNSUPPORTED, "run: q/k/v/out rows must start on 16-byte boundaries "
                 "(strides multiples of 8 elements)");
 
@@ -833,11 +883,21 @@ fi_status run_common(fi_plan_t p, bool decode_api, const fi_tensor* q, const fi_
 
   fi::AttnParams ap;
   ap.q = q->data; ap.q_stride_tok = q->stride[0]; ap.q_stride_head = q->stride[1];
-  ap.k = k->data; ap.k_stride_page = k->stride[0]; ap.k_stride_tok = k->stride[1];
-  ap.k_stride_head = k->stride[2];
-  ap.v = v->data; ap.v_stride_page = v->stride[0]; ap.v_stride_tok = v->stride[1];
-  ap.v_stride_head = v->stride[2];
-  ap.kv_indices = static_cast<const int32_t*>(kv_indices->data);
+  if (ragged) {  // one logical page of all rows: page stride unused
+    ap.k = k->data; ap.k_stride_page = 0; ap.k_stride_tok = k->stride[0];
+    ap.k_stride_head = k->stride[1];
+    ap.v = v->data; ap.v_stride_page = 0; ap.v_stride_tok = v->stride[0];
+    ap.v_stride_head = v->stride[1];
+    ap.kv_indices = nullptr;
+  } else {
+    ap.k = k->data; ap.k_stride_page = k->stride[0]; ap.k_stride_tok = k->stride[1];
+    ap.k_stride_head = k->stride[2];
+    ap.v = v->data; ap.v_stride_page = v->stride[0]; ap.v_stride_tok = v->stride[1];
+    ap.v_stride_head = v->stride[2];
+    ap.kv_indices = static_cast<const int32_t*>(kv_indices->data);
+  }
+  ap.ragged = ragged ? 1 : 0;
+  ap.kv_rows = ragged ? std::min(k->shape[0], v->shape[0]) : 0;
   ap.out = out->data;
   ap.lse = lse ? static_cast<float*>(lse->data) : nullptr;
   ap.ws = p->ws;
@@ -854,10 +914,11 @@ fi_status run_common(fi_plan_t p, bool decode_api, const fi_tensor* q, const fi_
   if (any_work) {
     cudaError_t e;
     if (s.kernel == fi::kDecode)
-      e = fi::launch_decode(ap, s.d, s.group, bf16, k->shape[0], s.tile_rows, s.grid, cs);
+      e = fi::launch_decode(ap, s.d, s.group, bf16, ragged ? 1 : k->shape[0], s.tile_rows,
+                            s.grid, cs);
     else if (s.kernel == fi::kPrefillM128)
-      e = fi::launch_prefill_tc(ap, s.d, s.group, s.tile_rows, q->shape[0], k->shape[0], bf16,
-                                s.grid, cs);
+      e = fi::launch_prefill_tc(ap, s.d, s.group, s.tile_rows, q->shape[0],
+                                ragged ? 1 : k->shape[0], bf16, s.grid, cs);
     else e = fi::launch_prefill_mma(ap, s.d, s.kernel, bf16, s.grid, cs);
     if (e != cudaSuccess)
       return fail(FI_ERR_CUDA, "%s: attention launch failed: %s", api, cudaGetErrorString(e));
@@ -880,14 +941,20 @@ extern "C" fi_status fi_batch_prefill_paged(fi_plan_t p, const fi_tensor* q, con
                                             const fi_tensor* v, const fi_tensor* kv_indices,
                                             float sm_scale, fi_tensor* out, fi_tensor* lse,
                                             void* stream) {
-  return run_common(p, false, q, k, v, kv_indices, sm_scale, out, lse, stream);
+  return run_common(p, false, false, q, k, v, kv_indices, sm_scale, out, lse, stream);
 }
 
 extern "C" fi_status fi_batch_decode_paged(fi_plan_t p, const fi_tensor* q, const fi_tensor* k,
                                            const fi_tensor* v, const fi_tensor* kv_indices,
                                            float sm_scale, fi_tensor* out, fi_tensor* lse,
                                            void* stream) {
-  return run_common(p, true, q, k, v, kv_indices, sm_scale, out, lse, stream);
+  return run_common(p, true, false, q, k, v, kv_indices, sm_scale, out, lse, stream);
+}
+
+extern "C" fi_status fi_batch_prefill_ragged(fi_plan_t p, const fi_tensor* q, const fi_tensor* k,
+                                             const fi_tensor* v, float sm_scale, fi_tensor* out,
+                                             fi_tensor* lse, void* stream) {
+  return run_common(p, false, true, q, k, v, nullptr, sm_scale, out, lse, stream);
 }
 
 // ------------------------------------------------------------------ merges

@@ -113,10 +113,12 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
   }
 }
 
-// Key j of a request: its row in the cache (page from the page table).
+// Key j of a request: its row in the cache (page from the page table), or
+// with a ragged cache, row kv_start + j.
 __device__ __forceinline__ int64_t kv_row_offset(const int32_t* pages, int32_t j, int page_size,
                                                  int page_shift, int64_t stride_page,
-                                                 int64_t stride_tok) {
+                                                 int64_t stride_tok, bool ragged, int kv_start) {
+  if (ragged) return int64_t(kv_start + j) * stride_tok;
   int32_t pi, slot;
   if (page_shift >= 0) {
     pi = j >> page_shift;

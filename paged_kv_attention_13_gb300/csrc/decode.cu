@@ -696,7 +696,8 @@ __device__ __noinline__ void decode_producer(const AttnParams& p, const CUtensor
     h.pad = 0;
     const int start = lo & ~(box_rows - 1);
     const int n_tiles = hi > lo ? (hi - start + KT - 1) / KT : 0;
-    const int32_t* pages = p.kv_indices + kv_indptr[it.b];
+    const int kv_start = kv_indptr[it.b];  // ragged: first row; paged: first page-table entry
+    const int32_t* pages = p.ragged ? nullptr : p.kv_indices + kv_start;
     const int n_st = max(n_tiles, 1);  // an item without keys still writes its output
     for (int t = 0; t < n_st; ++t, ++c) {
       const int st = c % NS;
@@ -711,15 +712,19 @@ __device__ __noinline__ void decode_producer(const AttnParams& p, const CUtensor
         slot[j] = 0;
         if (i < n_live) {
           const int kb = k0 + i * box_rows;
-          int pi;
-          if (p.page_shift >= 0) {
-            pi = kb >> p.page_shift;
-            slot[j] = kb & ((1 << p.page_shift) - 1);
+          if (p.ragged) {  // one logical page: the slot is the row
+            slot[j] = kv_start + kb;
           } else {
-            pi = kb / p.page_size;
-            slot[j] = kb - pi * p.page_size;
+            int pi;
+            if (p.page_shift >= 0) {
+              pi = kb >> p.page_shift;
+              slot[j] = kb & ((1 << p.page_shift) - 1);
+            } else {
+              pi = kb / p.page_size;
+              slot[j] = kb - pi * p.page_size;
+            }
+            page[j] = __ldg(pages + pi);
           }
-          page[j] = __ldg(pages + pi);
         }
       }
       h.flags = (t == 0 ? kStFirst : 0) | (t == n_st - 1 ? kStLast : 0) |
@@ -990,13 +995,9 @@ cudaError_t launch_decode(const AttnParams& p, int head_dim, int group, bool bf1
   const int box_cols = mma ? 64 : head_dim;
   const CUtensorMapSwizzle swz = mma ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUtensorMap tk, tv;
-  if (num_pages <= 0 ||
-      !encode_paged_kv_map(&tk, bf16, p.k, head_dim, p.num_kv_heads, p.page_size, num_pages,
-                           p.k_stride_head, p.k_stride_tok, p.k_stride_page, box_cols, box_rows,
-                           swz) ||
-      !encode_paged_kv_map(&tv, bf16, p.v, head_dim, p.num_kv_heads, p.page_size, num_pages,
-                           p.v_stride_head, p.v_stride_tok, p.v_stride_page, box_cols, box_rows,
-                           swz))
+  if ((!p.ragged && num_pages <= 0) ||
+      !encode_kv_map(&tk, p, true, bf16, head_dim, num_pages, box_cols, box_rows, swz) ||
+      !encode_kv_map(&tv, p, false, bf16, head_dim, num_pages, box_cols, box_rows, swz))
     return cudaErrorInvalidValue;
   if (mma) {
     if (head_dim == 128)

@@ -72,6 +72,11 @@ struct AttnParams {
   int32_t num_kv_heads;
   int32_t page_size;
   int32_t page_shift;   // log2(page_size) when it is a power of two, else -1
+  // Ragged (contiguous) K/V: key j of request b is row kv_indptr[b] + j of
+  // k / v ([rows, Hk, d]); kv_indices is unused, and page_size / page_shift
+  // are 1 << 30 / 30 (one logical page per request).
+  int32_t ragged;
+  int64_t kv_rows;      // ragged: rows of k / v (the TMA maps' extent)
 };
 
 enum KernelId : int32_t {

@@ -88,7 +88,9 @@ __global__ void __launch_bounds__(kThreads) prefill_mma_kernel(const AttnParams 
     int lo_t = wl >= 0 ? max(0, lk - lq + i0 - wl) : 0;
     const int kv_lo = max(it.kv_begin, lo_t);
     const int kv_hi = min(it.kv_end, hi_t);
-    const int32_t* pages = p.kv_indices + kv_indptr[b];
+    const bool ragged = p.ragged != 0;
+    const int kv_start = kv_indptr[b];  // ragged: first row; paged: first page-table entry
+    const int32_t* pages = ragged ? nullptr : p.kv_indices + kv_start;
 
     // ---- stage Q (packed rows) and the first K/V tile
     for (int idx = tid; idx < C::M * C::CH; idx += kThreads) {
@@ -112,9 +114,11 @@ __global__ void __launch_bounds__(kThreads) prefill_mma_kernel(const AttnParams 
         const T* vs = static_cast<const T*>(p.v);
         int bytes = 0;
         if (j < kv_hi) {
-          ks += kv_row_offset(pages, j, p.page_size, p.page_shift, p.k_stride_page, p.k_stride_tok) +
+          ks += kv_row_offset(pages, j, p.page_size, p.page_shift, p.k_stride_page, p.k_stride_tok,
+                              ragged, kv_start) +
                 int64_t(hk) * p.k_stride_head + c * 8;
-          vs += kv_row_offset(pages, j, p.page_size, p.page_shift, p.v_stride_page, p.v_stride_tok) +
+          vs += kv_row_offset(pages, j, p.page_size, p.page_shift, p.v_stride_page, p.v_stride_tok,
+                              ragged, kv_start) +
                 int64_t(hk) * p.v_stride_head + c * 8;
           bytes = 16;
         }

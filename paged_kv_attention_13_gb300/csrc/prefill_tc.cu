@@ -165,6 +165,7 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool b_mn_major, int
 struct ItemGeom {
   int b, hk, token0, lq, lk, n_rows, i0, kv_lo, kv_hi, t_start, n_tiles;
   int chunk, num_chunks, partial_base, row0;
+  int kv_start;  // ragged cache: the request's first row (set by the producer)
 };
 
 __device__ __forceinline__ ItemGeom item_geom(const WorkItem& it, const int32_t* qo_indptr,
@@ -185,6 +186,7 @@ __device__ __forceinline__ ItemGeom item_geom(const WorkItem& it, const int32_t*
   G.t_start = (G.kv_lo / 128) * 128;
   G.n_tiles = G.kv_lo < G.kv_hi ? (G.kv_hi - G.t_start + 127) / 128 : 0;
   G.chunk = it.chunk; G.num_chunks = it.num_chunks; G.partial_base = it.partial_base;
+  G.kv_start = 0;
   return G;
 }
 
@@ -318,7 +320,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       okl = __shfl_sync(0xffffffffu, okl, 0);
       if (okl && has) {
-        const int slot0 = (kv_box_rows == 128) ? (t0 % p.page_size) : 0;
+        // ragged: one logical page per request, the slot is the row
+        const int slot0 = p.ragged ? G.kv_start + t0 : (kv_box_rows == 128) ? (t0 % p.page_size) : 0;
         const uint32_t roff = uint32_t(lane * kv_box_rows) * 128u;
         const uint32_t dst = sbase + (which ? kOffV : kOffK) + st * kTile + roff;
         for (int h = 0; h < 2; ++h)
@@ -328,16 +331,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       if (items[w].b < 0) continue;  // schedule padding
-      const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
+      ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
       if (G.n_tiles == 0) continue;
+      G.kv_start = kv_indptr[G.b];
       const bool hasB = G.n_rows > tr;
-      const int32_t* pages = p.kv_indices + kv_indptr[G.b];
-      const int n_pages = kv_indptr[G.b + 1] - kv_indptr[G.b];
+      const int32_t* pages = p.ragged ? nullptr : p.kv_indices + kv_indptr[G.b];
+      const int n_pages = kv_indptr[G.b + 1] - kv_indptr[G.b];  // ragged: rows, > 0 when n_tiles > 0
       // page index of lane L for batch bt: tile bt * tiles_per_batch + L / npg,
       // its page L % npg (0 when past the request)
       auto fetch = [&](int bt) {
         const int t = bt * tiles_per_batch + lane / npg;
         const int pg = (G.t_start + t * 128) / p.page_size + lane % npg;
+        if (p.ragged) return 0;
         return (t < G.n_tiles && pg < n_pages && lane < tiles_per_batch * npg) ? __ldg(pages + pg) : 0;
       };
       int idx_cur = fetch(0), idx_nxt = fetch(1);
@@ -704,12 +709,10 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int head_dim, int group, int 
     if (!encode_tensor_map(&tq, bf16, 3, p.q, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  if (!encode_paged_kv_map(&tk, bf16, p.k, head_dim, p.num_kv_heads, p.page_size, num_pages,
-                           p.k_stride_head, p.k_stride_tok, p.k_stride_page, 64, box_rows,
-                           CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_paged_kv_map(&tv, bf16, p.v, head_dim, p.num_kv_heads, p.page_size, num_pages,
-                           p.v_stride_head, p.v_stride_tok, p.v_stride_page, 64, box_rows,
-                           CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!encode_kv_map(&tk, p, true, bf16, head_dim, num_pages, 64, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_kv_map(&tv, p, false, bf16, head_dim, num_pages, 64, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (bf16) {
     static cudaError_t attr = cudaFuncSetAttribute(

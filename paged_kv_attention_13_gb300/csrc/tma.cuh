@@ -105,4 +105,10 @@ bool encode_paged_kv_map(CUtensorMap* m, bool bf16, const void* base, int head_d
                          int64_t stride_tok, int64_t stride_page, int box_cols, int box_rows,
                          CUtensorMapSwizzle swizzle);
 
+// Host: the 4-D map of K (is_k) or V for a run: over the paged cache as
+// above, or, with a ragged cache, over [rows, kv head, dim] as one logical
+// page of p.kv_rows slots (dims [head_dim, kv head, rows, 1]).
+bool encode_kv_map(CUtensorMap* m, const AttnParams& p, bool is_k, bool bf16, int head_dim,
+                   int64_t num_pages, int box_cols, int box_rows, CUtensorMapSwizzle swizzle);
+
 }  // namespace fi

@@ -50,4 +50,19 @@ bool encode_paged_kv_map(CUtensorMap* m, bool bf16, const void* base, int head_d
   return encode_tensor_map(m, bf16, 4, base, dims, str, box, swizzle);
 }
 
+bool encode_kv_map(CUtensorMap* m, const AttnParams& p, bool is_k, bool bf16, int head_dim,
+                   int64_t num_pages, int box_cols, int box_rows, CUtensorMapSwizzle swizzle) {
+  const void* base = is_k ? p.k : p.v;
+  const int64_t sh = is_k ? p.k_stride_head : p.v_stride_head;
+  const int64_t st = is_k ? p.k_stride_tok : p.v_stride_tok;
+  if (p.ragged) {
+    if (p.kv_rows <= 0 || p.kv_rows > (int64_t(1) << 31)) return false;
+    return encode_paged_kv_map(m, bf16, base, head_dim, p.num_kv_heads, int(p.kv_rows), 1, sh, st,
+                               st * p.kv_rows, box_cols, box_rows, swizzle);
+  }
+  const int64_t sp = is_k ? p.k_stride_page : p.v_stride_page;
+  return encode_paged_kv_map(m, bf16, base, head_dim, p.num_kv_heads, p.page_size, num_pages, sh,
+                             st, sp, box_cols, box_rows, swizzle);
+}
+
 }  // namespace fi

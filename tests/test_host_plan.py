@@ -265,3 +265,57 @@ def test_schedule_balances_the_persistent_grid():
         if it[0] >= 0:
             load[i % G] += max(0, min(int(it[4]), kv[it[0]]) - int(it[3])) + 64
     assert load.max() / load.mean() < 1.03
+
+
+# ----------------------------------------------------------- ragged prefill
+
+def _ragged(q_lens, kv_lens, hq=8, hk=2, d=128, seed=3):
+    """A batch whose page-size-1, unpermuted cache is the contiguous K/V."""
+    return workloads.make_paged_batch(q_lens, kv_lens, hq, hk, d, 1, "bf16", seed,
+                                      permute_pages=False)
+
+
+@pytest.mark.parametrize("causal,wl,forced", [(True, -1, 0), (False, 7, 0), (True, 3, 5)])
+def test_ragged_plan_is_an_exact_cover(causal, wl, forced):
+    pb = _ragged([5, 300, 0, 17, 2000], [5, 400, 9, 17, 2100])
+    p = _plan()
+    p.plan_ragged(pb.qo_indptr, pb.kv_indptr, 8, 2, 128, causal=causal, window_left=wl,
+                  force_kv_chunks=forced)
+    _check_cover(p, pb, causal, wl, forced)
+
+
+def test_ragged_plan_refusals():
+    p = _plan()
+    # decreasing row offsets
+    with pytest.raises(fi.FiError) as e:
+        p.plan_ragged([0, 4, 8], [0, 10, 5], 8, 2, 128)
+    assert _status(e) == "FI_ERR_INVALID_ARG"
+    # fewer keys than query rows under the causal mask (kv_len from the offsets)
+    with pytest.raises(fi.FiError) as e:
+        p.plan_ragged([0, 4, 8], [0, 10, 13], 8, 2, 128, causal=True)
+    assert _status(e) == "FI_ERR_KV_SHORTER_THAN_Q"
+    p.plan_ragged([0, 4, 8], [0, 10, 13], 8, 2, 128, causal=False)
+
+
+def test_ragged_and_paged_plans_do_not_cross():
+    """A ragged plan refuses the paged run calls and a paged plan the ragged
+    one (checked on the host, before any launch)."""
+    pb = _ragged([3, 4], [10, 12])
+    T = int(pb.qo_indptr[-1])
+    q = torch.zeros((T, 8, 128), dtype=torch.bfloat16)
+    kv = torch.zeros((22, 2, 128), dtype=torch.bfloat16)
+    out = torch.zeros_like(q)
+    p = _plan()
+    p.plan_ragged(pb.qo_indptr, pb.kv_indptr, 8, 2, 128)
+    with pytest.raises(fi.FiError) as e:
+        fi.fi_batch_prefill_paged(p, q, pb.k_cache, pb.v_cache, pb.kv_indices, 0.1, out=out)
+    assert _status(e) == "FI_ERR_PLAN_MISMATCH"
+    p2 = _plan()
+    p2.plan(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, 1, 8, 2, 128)
+    with pytest.raises(fi.FiError) as e:
+        fi.fi_batch_prefill_ragged(p2, q, kv, kv, 0.1, out=out)
+    assert _status(e) == "FI_ERR_PLAN_MISMATCH"
+    # K/V with fewer rows than the plan's last offset
+    with pytest.raises(fi.FiError) as e:
+        fi.fi_batch_prefill_ragged(p, q, kv[:21], kv[:21], 0.1, out=out)
+    assert _status(e) == "FI_ERR_PLAN_MISMATCH"

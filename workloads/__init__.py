@@ -159,6 +159,19 @@ def batch_prefill(page_size: int = 16, variant: int = 0, batch: int = 16,
                             dtype, seed_for(4, variant) + page_size)
 
 
+def ragged_prefill(variant: int = 0, batch: int = 16, q_lo: int = 512, q_hi: int = 2048,
+                   prefix_lo: int = 0, prefix_hi: int = 4096, num_qo_heads: int = 32,
+                   num_kv_heads: int = 8, head_dim: int = 128, dtype: str = "bf16") -> PagedBatch:
+    """The batch-prefill shapes over contiguous K/V: a page-size-1 cache with
+    an unpermuted page table, whose rows are the ragged K/V in request order
+    (k_cache.reshape(rows, Hk, d)); kv_indptr is then each request's first row."""
+    rng = np.random.default_rng(seed_for(4, variant) + 7)
+    ql = rng.integers(q_lo, q_hi + 1, size=batch)
+    pre = rng.integers(prefix_lo, prefix_hi + 1, size=batch)
+    return make_paged_batch(ql, ql + pre, num_qo_heads, num_kv_heads, head_dim, 1, dtype,
+                            seed_for(4, variant) + 1, permute_pages=False)
+
+
 PREFILL_CASES = ([dict(causal=True, window_left=w) for w in (-1, 0, 127, 4095)]
                  + [dict(causal=False, window_left=w) for w in (-1, 127)])
 
