@@ -22,6 +22,10 @@
  *   o     = sum_{valid j} exp(s_j - lse) v[j, h / g, :]   (0 if none)
  * Lk comes from the page metadata, not from the caller:
  *   Lk = (kv_indptr[b+1] - kv_indptr[b] - 1) * P + last_page_len[b].
+ * With a custom (tree) mask, valid is further ANDed with bit (i * Lk + j) of
+ * request b's bit-packed mask: tree drafts need a topology mask because the
+ * causal one lets a draft attend to a sibling on another branch ([P2
+ * "Architecture / design notes"]).
  */
 #include <math.h>
 #include <stdint.h>
@@ -81,12 +85,26 @@ int oracle_key_valid(int64_t i, int64_t j, int64_t lq, int64_t lk, int causal,
 }
 
 /*
+ * Bit (i * lk + j) of request b's custom mask. Request b's segment starts at
+ * byte mask_indptr[b]; bit n of the segment is bit (n % 8) of byte n / 8,
+ * least significant bit first.
+ */
+int oracle_custom_bit(const uint8_t* custom_mask, const int64_t* mask_indptr, int32_t b,
+                      int64_t i, int64_t j, int64_t lk) {
+  const int64_t n = i * lk + j;
+  const uint8_t byte = custom_mask[mask_indptr[b] + n / 8];
+  return (byte >> (n % 8)) & 1;
+}
+
+/*
  * Attention for selected (token, head) rows.
  *
  * q        [T, Hq, d] contiguous, dtype q_dtype
  * k_cache  [num_pages, P, Hk, d] contiguous, dtype kv_dtype (v_cache alike)
  * n_sel    number of rows; sel_token[r] in [0, T), sel_head[r] in [0, Hq)
  * o_out    [n_sel, d] fp64; lse_out [n_sel] fp64 (natural log)
+ * custom_mask, mask_indptr: a bit-packed mask per request (see
+ *          oracle_custom_bit) ANDed into the mask, or both NULL for none.
  * Returns 0, or -1 on an argument the definition does not cover.
  */
 int oracle_attention_rows(const void* q, int q_dtype, const void* k_cache,
@@ -98,7 +116,8 @@ int oracle_attention_rows(const void* q, int q_dtype, const void* k_cache,
                           int32_t num_kv_heads, int32_t head_dim, int causal,
                           int32_t window_left, double sm_scale, int64_t n_sel,
                           const int64_t* sel_token, const int32_t* sel_head,
-                          double* o_out, double* lse_out) {
+                          double* o_out, double* lse_out, const uint8_t* custom_mask,
+                          const int64_t* mask_indptr) {
   if (num_kv_heads <= 0 || num_qo_heads % num_kv_heads != 0 || page_size <= 0)
     return -1;
   const int32_t group = num_qo_heads / num_kv_heads;
@@ -132,6 +151,7 @@ int oracle_attention_rows(const void* q, int q_dtype, const void* k_cache,
     for (int64_t j = 0; j < lk; ++j) {
       s[j] = -INFINITY;
       if (!oracle_key_valid(i, j, lq, lk, causal, window_left)) continue;
+      if (custom_mask && !oracle_custom_bit(custom_mask, mask_indptr, b, i, j, lk)) continue;
       const int64_t page = kv_indices[kv_indptr[b] + j / page_size];
       const int64_t k_off = page * page_stride_kv + (j % page_size) * tok_stride_kv + hk * d;
       double dot = 0.0;

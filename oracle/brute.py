@@ -37,8 +37,10 @@ def mask_matrix(lq, lk, causal, window_left):
 
 
 def attention(q, k_cache, v_cache, kv_indices, qo_indptr, kv_indptr, last_page_len,
-              page_size, causal, window_left, sm_scale):
-    """o [T, Hq, d] and natural-log lse [T, Hq], both float64."""
+              page_size, causal, window_left, sm_scale, custom=None):
+    """o [T, Hq, d] and natural-log lse [T, Hq], both float64. custom: per
+    request a boolean [Lq, Lk] matrix ANDed into the mask (a tree topology),
+    or None."""
     q = np.asarray(q, np.float64)
     k_cache = np.asarray(k_cache, np.float64)
     v_cache = np.asarray(v_cache, np.float64)
@@ -56,6 +58,8 @@ def attention(q, k_cache, v_cache, kv_indices, qo_indptr, kv_indptr, last_page_l
         if lq == 0:
             continue
         mask = mask_matrix(lq, lk, causal, window_left)
+        if custom is not None:
+            mask = mask & np.asarray(custom[b], dtype=bool)
         for h in range(Hq):
             S = sm_scale * (q[q0:q1, h, :] @ K[:, h // g, :].T)  # [lq, lk]
             for i in range(lq):

@@ -22,7 +22,9 @@ def _load():
         lib.oracle_attention_rows.restype = ctypes.c_int
         lib.oracle_attention_rows.argtypes = [
             P, ctypes.c_int, P, P, ctypes.c_int, P, P, P, P, i32, i32, i32, i32, i32,
-            ctypes.c_int, i32, dbl, i64, P, P, P, P]
+            ctypes.c_int, i32, dbl, i64, P, P, P, P, P, P]
+        lib.oracle_custom_bit.restype = ctypes.c_int
+        lib.oracle_custom_bit.argtypes = [P, P, i32, i64, i64, i64]
         lib.oracle_merge_states.restype = None
         lib.oracle_merge_states.argtypes = [P, P, i64, i64, i64, P, P]
         lib.oracle_kv_len.restype = i64
@@ -62,13 +64,22 @@ def _as_raw(a, dtype):
     raise TypeError("unsupported oracle input dtype %s" % a.dtype)
 
 
+def custom_bit(custom_mask, mask_indptr, b, i, j, lk):
+    """Bit (i * lk + j) of request b's packed custom mask, as the oracle reads it."""
+    custom_mask = _c(custom_mask, np.uint8)
+    mask_indptr = _c(mask_indptr, np.int64)
+    return _load().oracle_custom_bit(_ptr(custom_mask), _ptr(mask_indptr), b, i, j, lk)
+
+
 def attention_rows(q, k_cache, v_cache, kv_indices, qo_indptr, kv_indptr, last_page_len,
                    page_size, causal, window_left, sm_scale, sel_token, sel_head,
-                   dtype="bf16"):
+                   dtype="bf16", custom_mask=None, mask_indptr=None):
     """fp64 (o [n, d], lse [n]) for rows (sel_token[r], sel_head[r]).
 
     q [T, Hq, d]; k_cache/v_cache [num_pages, P, Hk, d]. Arrays are float32,
     float16, or uint16/int16 raw bits of ``dtype`` ("bf16" or "f16").
+    custom_mask (uint8, bit-packed per request) / mask_indptr (byte offsets,
+    [batch + 1]): a mask ANDed into the causal / window mask, or None.
     """
     q, q_dt = _as_raw(q, dtype)
     k_cache, kv_dt = _as_raw(k_cache, dtype)
@@ -87,25 +98,31 @@ def attention_rows(q, k_cache, v_cache, kv_indices, qo_indptr, kv_indptr, last_p
     n = sel_token.shape[0]
     o = np.zeros((n, d), np.float64)
     lse = np.zeros((n,), np.float64)
+    cm = mi = None
+    if custom_mask is not None:
+        cm = _c(custom_mask, np.uint8)
+        mi = _c(mask_indptr, np.int64)
     rc = _load().oracle_attention_rows(
         _ptr(q), _DT[q_dt], _ptr(k_cache), _ptr(v_cache), _DT[kv_dt], _ptr(kv_indices),
         _ptr(qo_indptr), _ptr(kv_indptr), _ptr(last_page_len), len(qo_indptr) - 1,
         page_size, Hq, Hk, d, int(bool(causal)), int(window_left), float(sm_scale), n,
-        _ptr(sel_token), _ptr(sel_head), _ptr(o), _ptr(lse))
+        _ptr(sel_token), _ptr(sel_head), _ptr(o), _ptr(lse),
+        _ptr(cm) if cm is not None else None, _ptr(mi) if mi is not None else None)
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return o, lse
 
 
 def attention_all(q, k_cache, v_cache, kv_indices, qo_indptr, kv_indptr, last_page_len,
-                  page_size, causal, window_left, sm_scale, dtype="bf16"):
+                  page_size, causal, window_left, sm_scale, dtype="bf16", custom_mask=None,
+                  mask_indptr=None):
     """fp64 o [T, Hq, d] and lse [T, Hq] for every row."""
     T, Hq, d = q.shape
     tok = np.repeat(np.arange(T, dtype=np.int64), Hq)
     head = np.tile(np.arange(Hq, dtype=np.int32), T)
     o, lse = attention_rows(q, k_cache, v_cache, kv_indices, qo_indptr, kv_indptr,
                             last_page_len, page_size, causal, window_left, sm_scale,
-                            tok, head, dtype)
+                            tok, head, dtype, custom_mask, mask_indptr)
     return o.reshape(T, Hq, d), lse.reshape(T, Hq)
 
 

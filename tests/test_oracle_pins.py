@@ -339,3 +339,116 @@ def test_oracle_rejects_indivisible_heads():
                        np.array([0, 1], np.int32), np.array([0, 1], np.int32),
                        np.array([1], np.int32), 1, False, -1, 1.0, np.array([0]),
                        np.array([0]))
+
+
+# ------------------------------------------------------ custom (tree) masks
+# A tree draft needs a topology mask: the causal one lets a draft attend to a
+# sibling on another branch ("Support speculative-decode verify on ROCm, and
+# stop auto routing short-query prefill to AITER" (#362), "Architecture /
+# design notes"). The mask is ANDed into the causal / window mask.
+
+def _mask_batch(seed, causal, n_req=3):
+    """Tiny requests with random boolean masks (each row keeps >= 0 keys)."""
+    rng = np.random.default_rng(seed)
+    ql, kl, masks = [], [], []
+    for _ in range(n_req):
+        lk = int(rng.integers(1, 9))
+        lq = int(rng.integers(1, lk + 1))
+        ql.append(lq)
+        kl.append(lk)
+        masks.append(rng.random((lq, lk)) < 0.6)
+    d, Hk, g = 5, 2, 2
+    pb = workloads.make_paged_batch(ql, kl, g * Hk, Hk, d, 3, "bf16", seed + 7,
+                                    extra_pool_pages=1)
+    packed, indptr = workloads.pack_masks(masks)
+    return pb, masks, packed, indptr
+
+
+def test_custom_mask_bit_order():
+    """Bit n of a request's segment is bit n % 8 of byte n / 8 (LSB first),
+    segments start on their own byte."""
+    m0 = np.zeros((3, 5), bool)
+    m0[0, 0] = m0[1, 2] = m0[2, 4] = True  # bits 0, 7, 14
+    m1 = np.zeros((1, 2), bool)
+    m1[0, 1] = True                         # bit 1 of request 1's segment
+    packed, indptr = workloads.pack_masks([m0, m1])
+    assert list(indptr) == [0, 2, 3]
+    assert list(packed) == [0b10000001, 0b01000000, 0b00000010]
+    from oracle.reference import custom_bit
+    for b, m in enumerate((m0, m1)):
+        for i in range(m.shape[0]):
+            for j in range(m.shape[1]):
+                assert custom_bit(packed, indptr, b, i, j, m.shape[1]) == int(m[i, j])
+
+
+@pytest.mark.parametrize("seed", range(5))
+@pytest.mark.parametrize("causal,wl", [(False, -1), (True, -1), (True, 2), (False, 1)])
+def test_custom_mask_c_oracle_agrees_with_brute_force(seed, causal, wl):
+    """The C oracle (reads packed bits) and the brute force (dense booleans)
+    agree with random masks ANDed into every causal / window combination."""
+    pb, masks, packed, indptr = _mask_batch(200 + seed, causal)
+    o, lse = attention_all(*pb.oracle_args(), causal, wl, 0.6, custom_mask=packed,
+                           mask_indptr=indptr)
+    ob, lb = brute.attention(pb.q.double().numpy(), pb.k_cache.double().numpy(),
+                             pb.v_cache.double().numpy(), pb.kv_indices.numpy(),
+                             pb.qo_indptr.numpy(), pb.kv_indptr.numpy(),
+                             pb.last_page_len.numpy(), pb.page_size, causal, wl, 0.6,
+                             custom=masks)
+    np.testing.assert_allclose(o, ob, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(lb))
+    fin = ~np.isneginf(lb)
+    np.testing.assert_allclose(lse[fin], lb[fin], atol=1e-12)
+
+
+def test_all_ones_mask_is_no_mask_and_causal_pattern_is_causal():
+    pb, masks, _, _ = _mask_batch(300, True)
+    args = pb.oracle_args()
+    ones = [np.ones_like(m) for m in masks]
+    p1, i1 = workloads.pack_masks(ones)
+    for causal in (True, False):
+        o0, l0 = attention_all(*args, causal, -1, 0.6)
+        o1, l1 = attention_all(*args, causal, -1, 0.6, custom_mask=p1, mask_indptr=i1)
+        np.testing.assert_array_equal(o0, o1)
+        np.testing.assert_array_equal(l0, l1)
+    # the bottom-right causal pattern as a custom mask on a non-causal plan
+    cm = [np.array([[j <= i + m.shape[1] - m.shape[0] for j in range(m.shape[1])]
+                    for i in range(m.shape[0])]) for m in masks]
+    pc, ic = workloads.pack_masks(cm)
+    o0, l0 = attention_all(*args, True, -1, 0.6)
+    o1, l1 = attention_all(*args, False, -1, 0.6, custom_mask=pc, mask_indptr=ic)
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(l0, l1)
+
+
+def test_tree_mask_closed_form():
+    """Constant keys under a tree mask: lse - s = ln(#keys the row sees), the
+    prefix plus the node's depth + 1 (its ancestors and itself)."""
+    parents = [-1, 0, 0, 1, 1, 2, 4]
+    prefix = 5
+    m = workloads.tree_masks(parents, prefix)
+    depth = []
+    for i in range(len(parents)):
+        k, a = 0, i
+        while a >= 0:
+            k, a = k + 1, parents[a]
+        depth.append(k)
+    assert [int(r.sum()) for r in m] == [prefix + x for x in depth]
+    lq, lk, d = len(parents), prefix + len(parents), 6
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((lq, 1, d)).astype(np.float32)
+    kvec = rng.standard_normal(d).astype(np.float32)
+    K = np.tile(kvec, (lk, 1, 1)).astype(np.float32)
+    V = np.zeros((lk, 1, d), np.float32)
+    V[:, 0, 0] = np.arange(lk)
+    packed, indptr = workloads.pack_masks([m])
+    kc = K.reshape(lk, 1, 1, d)
+    vc = V.reshape(lk, 1, 1, d)
+    o, lse = attention_all(q, kc, vc, np.arange(lk, dtype=np.int32),
+                           np.array([0, lq], np.int32), np.array([0, lk], np.int32),
+                           np.array([1], np.int32), 1, True, -1, 0.5, custom_mask=packed,
+                           mask_indptr=indptr)
+    for i in range(lq):
+        s = 0.5 * float(np.dot(q[i, 0].astype(np.float64), kvec.astype(np.float64)))
+        assert lse[i, 0] - s == pytest.approx(math.log(prefix + depth[i]), abs=1e-10)
+        seen = np.nonzero(m[i])[0]
+        assert o[i, 0, 0] == pytest.approx(seen.mean(), abs=1e-9)

@@ -172,6 +172,57 @@ def ragged_prefill(variant: int = 0, batch: int = 16, q_lo: int = 512, q_hi: int
                             seed_for(4, variant) + 1, permute_pages=False)
 
 
+def pack_masks(masks):
+    """Bit-pack per-request boolean [Lq, Lk] masks: request b's bits (row-major,
+    i * Lk + j) start on byte mask_indptr[b], least significant bit first.
+    Returns (uint8 array, int32 byte offsets [batch + 1])."""
+    segs = [np.packbits(np.asarray(m, dtype=np.uint8).reshape(-1), bitorder="little")
+            for m in masks]
+    indptr = np.zeros(len(segs) + 1, np.int32)
+    indptr[1:] = np.cumsum([len(x) for x in segs])
+    data = np.concatenate(segs) if segs else np.zeros(0, np.uint8)
+    if data.size == 0:
+        data = np.zeros(1, np.uint8)  # never empty, so it always has an address
+    return data.astype(np.uint8), indptr
+
+
+def tree_masks(parents, prefix_len):
+    """Topology mask of one request's draft tree: row i (draft node i) sees
+    every prefix key and the keys of its ancestors and itself; parents[i] < i
+    (parents[0] = -1, the root under the prefix)."""
+    n = len(parents)
+    m = np.zeros((n, prefix_len + n), dtype=bool)
+    m[:, :prefix_len] = True
+    for i in range(n):
+        a = i
+        while a >= 0:
+            m[i, prefix_len + a] = True
+            a = parents[a]
+    return m
+
+
+def tree_verify(batch: int = 32, variant: int = 0, n_draft: int = 8, kv_lo: int = 1024,
+                kv_hi: int = 4096, num_qo_heads: int = 32, num_kv_heads: int = 8,
+                head_dim: int = 128, page_size: int = 16, dtype: str = "bf16") -> PagedBatch:
+    """Tree verify: n_draft draft nodes per request with random parents
+    (node i's parent uniform in [0, i)), kv_len = prefix + n_draft; the
+    topology masks are in extra["masks"] (dense) and packed in
+    extra["mask"] / extra["mask_indptr"]."""
+    rng = np.random.default_rng(seed_for(6, variant) + batch)
+    kv = rng.integers(kv_lo, kv_hi + 1, size=batch)
+    masks = []
+    for b in range(batch):
+        parents = [-1] + [int(rng.integers(0, i)) for i in range(1, n_draft)]
+        masks.append(tree_masks(parents, int(kv[b]) - n_draft))
+    pb = make_paged_batch([n_draft] * batch, kv, num_qo_heads, num_kv_heads, head_dim,
+                          page_size, dtype, seed_for(6, variant) + 3 * batch)
+    packed, indptr = pack_masks(masks)
+    pb.extra["masks"] = masks
+    pb.extra["mask"] = torch.from_numpy(packed)
+    pb.extra["mask_indptr"] = torch.from_numpy(indptr)
+    return pb
+
+
 PREFILL_CASES = ([dict(causal=True, window_left=w) for w in (-1, 0, 127, 4095)]
                  + [dict(causal=False, window_left=w) for w in (-1, 127)])
 
