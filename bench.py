@@ -56,10 +56,20 @@ def accounting(pb, causal, wl):
     flops = 0
     kv_rows = 0
     pages = 0
-    for lq, lk in zip(pb.q_lens, pb.kv_lens):
+    masks = pb.extra.get("masks")  # custom (tree) masks, ANDed in
+    for b, (lq, lk) in enumerate(zip(pb.q_lens, pb.kv_lens)):
         if lq == 0 or lk == 0:
             continue
         cnt = valid_counts(lq, lk, causal, wl)
+        if masks is not None:
+            i = np.arange(lq)[:, None]
+            j = np.arange(lk)[None, :]
+            std = np.ones((lq, lk), bool)
+            if causal:
+                std &= j <= i + lk - lq
+            if wl >= 0:
+                std &= j + lq + wl >= lk + i
+            cnt = (std & np.asarray(masks[b], bool)).sum(axis=1)
         flops += 4 * d * Hq * int(cnt.sum())
         # distinct live keys: union of the rows' ranges [lo_i, hi_i]
         i = np.arange(lq)
@@ -171,6 +181,7 @@ class Runner:
             self.k = pb.k_cache.to(dev)
             self.v = pb.v_cache.to(dev)
         self.idx = pb.kv_indices.to(dev)
+        self.mask = pb.extra["mask"].to(dev) if mode == "masked" else None
         self.out = torch.empty_like(self.q)
         self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=dev)
         self.ws = ws if ws is not None else torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -182,7 +193,12 @@ class Runner:
     def do_plan(self):
         pb = self.pb
         dt = workloads.TORCH_DTYPE[pb.dtype]
-        if self.mode == "ragged":
+        if self.mode == "masked":
+            self.plan.plan_masked(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, pb.page_size,
+                                  pb.num_qo_heads, pb.num_kv_heads, pb.head_dim,
+                                  pb.extra["mask_indptr"], causal=self.causal,
+                                  window_left=self.wl, dtype=dt, force_kv_chunks=self.force)
+        elif self.mode == "ragged":
             self.plan.plan_ragged(pb.qo_indptr, pb.kv_indptr, pb.num_qo_heads, pb.num_kv_heads,
                                   pb.head_dim, causal=self.causal, window_left=self.wl, dtype=dt,
                                   force_kv_chunks=self.force)
@@ -198,6 +214,11 @@ class Runner:
         self.info = self.plan.info()
 
     def run(self):
+        if self.mode == "masked":
+            self.fi.fi_batch_prefill_paged_masked(self.plan, self.q, self.k, self.v, self.idx,
+                                                  self.mask, self.pb.sm_scale, out=self.out,
+                                                  lse=self.lse)
+            return
         if self.mode == "ragged":
             self.fi.fi_batch_prefill_ragged(self.plan, self.q, self.k, self.v, self.pb.sm_scale,
                                             out=self.out, lse=self.lse)
@@ -422,6 +443,8 @@ def other_workloads(args, dev, ws, hbm_peak, bf16_peak):
             one("prefill_p16_causal_wl127", pb, True, 127, "prefill")
     pb = workloads.ragged_prefill()
     one("ragged_prefill_causal", pb, True, -1, "ragged", bound="tensor")
+    pb = workloads.tree_verify(batch=32)
+    one("tree_verify_b32", pb, True, -1, "masked")
     pb = workloads.long_context()
     one("longctx_causal_split", pb, True, -1, "prefill")
     one("longctx_causal_force32", pb, True, -1, "prefill", force=32)
@@ -475,6 +498,7 @@ PROFILE_CASES = {
     "prefill_p16_noncausal": (lambda: workloads.batch_prefill(page_size=16), False, -1, "prefill"),
     "longctx_causal": (lambda: workloads.long_context(), True, -1, "prefill"),
     "ragged_prefill_causal": (lambda: workloads.ragged_prefill(), True, -1, "ragged"),
+    "tree_verify_b32": (lambda: workloads.tree_verify(batch=32), True, -1, "masked"),
 }
 
 

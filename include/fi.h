@@ -66,7 +66,7 @@ typedef enum fi_status {
   FI_ERR_CUDA = 10                 /* a CUDA runtime call failed */
 } fi_status;
 
-typedef enum fi_dtype { FI_F16 = 0, FI_BF16 = 1, FI_F32 = 2, FI_I32 = 3 } fi_dtype;
+typedef enum fi_dtype { FI_F16 = 0, FI_BF16 = 1, FI_F32 = 2, FI_I32 = 3, FI_U8 = 4 } fi_dtype;
 
 /* A strided view of caller-owned device memory. Unused trailing entries of
  * shape/stride are ignored. */
@@ -208,6 +208,40 @@ fi_status fi_batch_decode_paged(fi_plan_t plan, const fi_tensor* q, const fi_ten
  * A paged plan given to this call, or a ragged plan to the paged calls, is
  * refused with FI_ERR_PLAN_MISMATCH. Nothing is allocated or synchronised.
  */
+/*
+ * Paged prefill with a custom (tree) mask. Tree drafts (EAGLE-2, Medusa,
+ * SpecInfer) need a topology mask: the causal verify mask lets a draft attend
+ * to a sibling on another branch ("Support speculative-decode verify on ROCm,
+ * and stop auto routing short-query prefill to AITER" (#362), "Architecture /
+ * design notes"). The mask is ANDed into the mask that causal / window_left
+ * define; plan with causal = 0 to apply it alone.
+ *
+ * fi_plan_masked: as fi_plan for a prefill, plus
+ *   mask_indptr  host int32 [batch+1]: request b's mask bits start at byte
+ *                mask_indptr[b] of the custom_mask tensor; its segment holds
+ *                Lq_b * Lk_b bits (query row i, key j at bit i * Lk_b + j,
+ *                least significant bit of each byte first), so
+ *                mask_indptr[b+1] - mask_indptr[b] >= ceil(Lq_b * Lk_b / 8).
+ * Masked plans run on the short-query kernel (at most 16 packed rows per
+ * request) or on the mma.sync kernels. FI_ERR_INVALID_ARG for a segment
+ * shorter than its request's bits or a decreasing mask_indptr.
+ *
+ * fi_batch_prefill_paged_masked: as fi_batch_prefill_paged, plus
+ *   custom_mask  device FI_U8 [>= mask_indptr[batch]] bytes, contiguous.
+ * A masked plan refuses the unmasked run calls and an unmasked plan this one
+ * (FI_ERR_PLAN_MISMATCH).
+ */
+fi_status fi_plan_masked(fi_plan_t plan, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                         const int32_t* last_page_len, int32_t batch, int32_t page_size,
+                         int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t causal, int32_t window_left, fi_dtype dtype,
+                         const int32_t* mask_indptr, int32_t force_kv_chunks, void* stream);
+fi_status fi_batch_prefill_paged_masked(fi_plan_t plan, const fi_tensor* q,
+                                        const fi_tensor* k_cache, const fi_tensor* v_cache,
+                                        const fi_tensor* kv_indices, const fi_tensor* custom_mask,
+                                        float sm_scale, fi_tensor* out, fi_tensor* lse,
+                                        void* stream);
+
 fi_status fi_plan_ragged(fi_plan_t plan, const int32_t* qo_indptr, const int32_t* kv_indptr,
                          int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
                          int32_t head_dim, int32_t causal, int32_t window_left, fi_dtype dtype,

@@ -6,6 +6,7 @@ LSE merging of split-KV partial states. This package holds its CUDA sources
 (``csrc/``), its build script and a thin ctypes binding with the C names.
 """
 from .api import (FiError, Plan, fi_batch_decode_paged, fi_batch_decode_paged_noalloc,  # noqa: F401
-                  fi_batch_prefill_paged, fi_batch_prefill_ragged, fi_merge_state, fi_merge_states,
+                  fi_batch_prefill_paged, fi_batch_prefill_paged_masked, fi_batch_prefill_ragged,
+                  fi_merge_state, fi_merge_states,
                   fi_plan, tensor_desc, workspace_bytes)
 from ._lib import EXPORTED, LIB_PATH, load  # noqa: F401

@@ -16,7 +16,7 @@ STATUS_NAMES = {
     6: "FI_ERR_NOT_PLANNED", 7: "FI_ERR_KV_SHORTER_THAN_Q", 8: "FI_ERR_CAPACITY",
     9: "FI_ERR_UNSUPPORTED", 10: "FI_ERR_CUDA",
 }
-FI_F16, FI_BF16, FI_F32, FI_I32 = 0, 1, 2, 3
+FI_F16, FI_BF16, FI_F32, FI_I32, FI_U8 = 0, 1, 2, 3, 4
 
 # Every symbol include/fi.h declares.
 EXPORTED = [
@@ -24,7 +24,8 @@ EXPORTED = [
     "fi_batch_decode_paged", "fi_merge_state", "fi_merge_states", "fi_plan_get_info",
     "fi_plan_read_device", "fi_plan_destroy", "fi_last_error", "fi_status_str",
     "fi_batch_decode_paged_noalloc", "fi_noalloc_scratch_bytes", "fi_noalloc_last_error",
-    "fi_plan_device_error", "fi_plan_ragged", "fi_batch_prefill_ragged",
+    "fi_plan_device_error", "fi_plan_ragged", "fi_batch_prefill_ragged", "fi_plan_masked",
+    "fi_batch_prefill_paged_masked",
 ]
 
 
@@ -75,6 +76,11 @@ def load():
     lib.fi_plan_get_info.argtypes = [P, ctypes.POINTER(FiPlanInfo), pi32, i32, pi32, i32]
     lib.fi_plan_read_device.restype = ctypes.c_int
     lib.fi_plan_read_device.argtypes = [P, pi32, i32, pi32, i32, P]
+    lib.fi_plan_masked.restype = ctypes.c_int
+    lib.fi_plan_masked.argtypes = [P, pi32, pi32, pi32, i32, i32, i32, i32, i32, i32, i32,
+                                   ctypes.c_int, pi32, i32, P]
+    lib.fi_batch_prefill_paged_masked.restype = ctypes.c_int
+    lib.fi_batch_prefill_paged_masked.argtypes = [P, PT, PT, PT, PT, PT, ctypes.c_float, PT, PT, P]
     lib.fi_plan_ragged.restype = ctypes.c_int
     lib.fi_plan_ragged.argtypes = [P, pi32, pi32, i32, i32, i32, i32, i32, i32, ctypes.c_int, i32, P]
     lib.fi_batch_prefill_ragged.restype = ctypes.c_int

@@ -13,7 +13,7 @@ from . import _lib
 from ._lib import FiPlanInfo, FiTensor
 
 _DTYPES = {torch.float16: _lib.FI_F16, torch.bfloat16: _lib.FI_BF16,
-           torch.float32: _lib.FI_F32, torch.int32: _lib.FI_I32}
+           torch.float32: _lib.FI_F32, torch.int32: _lib.FI_I32, torch.uint8: _lib.FI_U8}
 
 KERNEL_NAMES = {0: "decode", 1: "prefill_m16", 2: "prefill_m64", 3: "prefill_m128"}
 
@@ -125,6 +125,23 @@ class Plan:
         self.q_len_per_req = q_len_per_req
         return self
 
+    def plan_masked(self, qo_indptr, kv_indptr, last_page_len, page_size, num_qo_heads,
+                    num_kv_heads, head_dim, mask_indptr, causal=False, window_left=-1,
+                    dtype=torch.bfloat16, force_kv_chunks=0, stream=None):
+        """fi_plan_masked: a paged prefill with a custom (tree) mask whose
+        request b starts at byte mask_indptr[b] (host int32)."""
+        qo, qo_p = _host_i32(qo_indptr)
+        kv, kv_p = _host_i32(kv_indptr)
+        last, last_p = _host_i32(last_page_len)
+        mi, mi_p = _host_i32(mask_indptr)
+        batch = len(kv) - 1 if kv is not None else 0
+        _check(self._lib.fi_plan_masked(self.handle, qo_p, kv_p, last_p, batch, int(page_size),
+                                        int(num_qo_heads), int(num_kv_heads), int(head_dim),
+                                        int(bool(causal)), int(window_left), _DTYPES[dtype], mi_p,
+                                        int(force_kv_chunks), _stream_handle(stream)))
+        self.q_len_per_req = 0
+        return self
+
     def plan_ragged(self, qo_indptr, kv_indptr, num_qo_heads, num_kv_heads, head_dim,
                     causal=False, window_left=-1, dtype=torch.bfloat16, force_kv_chunks=0,
                     stream=None):
@@ -205,6 +222,23 @@ def fi_batch_decode_paged(plan, q, k_cache, v_cache, kv_indices, sm_scale, out=N
     """Batched paged decode / speculative verify; returns (out, lse)."""
     return _run(_lib.load().fi_batch_decode_paged, plan, q, k_cache, v_cache, kv_indices,
                 sm_scale, out, lse, return_lse, stream)
+
+
+def fi_batch_prefill_paged_masked(plan, q, k_cache, v_cache, kv_indices, custom_mask, sm_scale,
+                                  out=None, lse=None, return_lse=True, stream=None):
+    """Paged prefill with a custom (tree) mask: custom_mask is a device uint8
+    tensor of bit-packed per-request masks; returns (out, lse)."""
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    descs = [tensor_desc(t) for t in (q, k_cache, v_cache, kv_indices, custom_mask, out)]
+    ld = tensor_desc(lse) if lse is not None else None
+    _check(_lib.load().fi_batch_prefill_paged_masked(
+        plan.handle, *[ctypes.byref(d) for d in descs[:5]], ctypes.c_float(sm_scale),
+        ctypes.byref(descs[5]), ctypes.byref(ld) if ld is not None else None,
+        _stream_handle(stream)))
+    return out, lse
 
 
 def fi_batch_prefill_ragged(plan, q, k, v, sm_scale, out=None, lse=None, return_lse=True,

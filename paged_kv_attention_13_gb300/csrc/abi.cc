@@ -49,7 +49,9 @@ struct PlanState {
   int32_t kernel = 0, tile_rows = 0, grid = 0, max_chunks = 1, n_partials = 0;
   int32_t kv_indices_len = 0;  // page-table entries (ragged: K/V rows) the plan reads
   int32_t ragged = 0;          // contiguous K/V rows instead of a page table
-  std::vector<int32_t> qo_indptr, kv_indptr, kv_len, merge_indptr, merge_rows;
+  int32_t masked = 0;          // a custom mask is ANDed in
+  int32_t mask_bytes = 0;      // custom mask bytes the plan reads (mask_indptr[batch])
+  std::vector<int32_t> qo_indptr, kv_indptr, kv_len, merge_indptr, merge_rows, mask_indptr;
   std::vector<WorkItem> items;
   WsHeader hdr{};
   int64_t meta_bytes = 0;   // header + metadata arrays (uploaded)
@@ -81,7 +83,7 @@ struct fi_plan_s {
   // shape frozen by the first plan of a graph-mode plan object
   bool frozen = false;
   int32_t fz_kernel = 0, fz_qlpr = 0, fz_hq = 0, fz_hk = 0, fz_d = 0, fz_dtype = 0, fz_page = 0;
-  int32_t fz_ragged = 0;
+  int32_t fz_ragged = 0, fz_masked = 0;
 };
 
 extern "C" const char* fi_last_error(void) { return g_last_error.c_str(); }
@@ -114,6 +116,7 @@ int64_t meta_bytes_for(int64_t batch, int64_t rows, int64_t n_merge, int64_t n_i
   off = align_up(off + 4 * (rows + 1), 16);   // merge_indptr
   off = align_up(off + 4 * n_merge, 32);      // merge_rows
   off += 32 * n_items;                        // items
+  off = align_up(off + 4 * (batch + 1), 16);  // mask_indptr
   return align_up(off, kAlign);
 }
 
@@ -189,8 +192,12 @@ namespace {
 // rows on its tensor-core consumer when the group and page size allow, and
 // decode on its CUDA-core consumer otherwise (groups 1, 2, 4).
 int choose_kernel(int32_t q_len_per_req, int32_t g, int64_t max_rows_per_req, int32_t d,
-                  int32_t page_size) {
+                  int32_t page_size, bool masked) {
   if (max_rows_per_req <= 16 && fi::decode_mma_supports(d, page_size, g)) return fi::kDecode;
+  if (masked) {  // the custom mask is read by the short-query and mma.sync kernels
+    if (max_rows_per_req <= 16 && g <= 16) return fi::kPrefillM16;
+    return g <= 64 ? fi::kPrefillM64 : -1;
+  }
   if (q_len_per_req == 1 && fi::decode_shuffle_supports(d, g)) return fi::kDecode;
   if (max_rows_per_req <= 16 && g <= 16) return fi::kPrefillM16;
   if (max_rows_per_req > 64 && fi::prefill_tc_supports(d, page_size, g)) return fi::kPrefillM128;
@@ -228,7 +235,7 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
                      const int32_t* last_page_len_h, int32_t batch, int32_t page_size,
                      int32_t hq, int32_t hk, int32_t d, int32_t causal, int32_t window_left,
                      fi_dtype dtype, int32_t q_len_per_req, int32_t force_kv_chunks,
-                     bool ragged, PlanState& ns) {
+                     bool ragged, const int32_t* mask_indptr_h, PlanState& ns) {
   // ---- argument validation, before anything is written [P2 "Review notes"]
   if (batch < 0) return fail(FI_ERR_INVALID_ARG, "plan: batch=%d must be >= 0", batch);
   if (batch > 0 && (!kv_indptr_h || (!ragged && !last_page_len_h)))
@@ -311,6 +318,23 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
     ns.kv_len[b] = static_cast<int32_t>(lk);
     max_rows_per_req = std::max<int64_t>(max_rows_per_req, lq * g);
   }
+  // custom mask segments: byte offsets, each long enough for its Lq x Lk bits
+  ns.masked = mask_indptr_h ? 1 : 0;
+  ns.mask_indptr.assign(batch + 1, 0);
+  if (mask_indptr_h) {
+    if (mask_indptr_h[0] < 0) return fail(FI_ERR_INVALID_ARG, "plan: mask_indptr[0] < 0");
+    for (int32_t b = 0; b < batch; ++b) {
+      const int64_t lq = int64_t(ns.qo_indptr[b + 1]) - ns.qo_indptr[b];
+      const int64_t need = (lq * ns.kv_len[b] + 7) / 8;
+      const int64_t have = int64_t(mask_indptr_h[b + 1]) - mask_indptr_h[b];
+      if (have < need)
+        return fail(FI_ERR_INVALID_ARG, "plan: mask_indptr gives request %d %lld bytes, its %lld x "
+                    "%d mask needs %lld", b, (long long)have, (long long)lq, ns.kv_len[b],
+                    (long long)need);
+    }
+    for (int32_t b = 0; b <= batch; ++b) ns.mask_indptr[b] = mask_indptr_h[b];
+    ns.mask_bytes = mask_indptr_h[batch];
+  }
 
   // ---- graph-mode capacities and frozen shape [P2 "Architecture / design notes"]
   if (P.graph) {
@@ -324,7 +348,7 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
     max_rows_per_req = (q_len_per_req >= 1) ? int64_t(q_len_per_req) * g
                                              : int64_t(P.max_total_rows) * g;
   }
-  ns.kernel = choose_kernel(q_len_per_req, g, max_rows_per_req, d, page_size);
+  ns.kernel = choose_kernel(q_len_per_req, g, max_rows_per_req, d, page_size, mask_indptr_h != nullptr);
   if (ns.kernel < 0)
     return fail(FI_ERR_UNSUPPORTED, "plan: GQA group %d is larger than the widest tile", g);
   if (P.graph && P.frozen) {
@@ -337,6 +361,7 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
     else if (dtype != P.fz_dtype) { field = "dtype"; want = P.fz_dtype; got = dtype; }
     else if (page_size != P.fz_page) { field = "page_size"; want = P.fz_page; got = page_size; }
     else if (int32_t(ragged) != P.fz_ragged) { field = "ragged"; want = P.fz_ragged; got = ragged; }
+    else if (ns.masked != P.fz_masked) { field = "masked"; want = P.fz_masked; got = ns.masked; }
     else if (ns.kernel != P.fz_kernel) { field = "kernel"; want = P.fz_kernel; got = ns.kernel; }
     if (field)
       return fail(FI_ERR_CAPACITY, "plan: %s is frozen at %d by the first graph-mode plan, got %d",
@@ -568,6 +593,7 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
   h.off_merge_indptr = off; off = align_up(off + 4 * (ns.total_rows + 1), 16);
   h.off_merge_rows = off; off = align_up(off + 4 * int64_t(ns.merge_rows.size()), 32);
   h.off_items = off; off += 32 * n_items;
+  h.off_mask_indptr = off; off = align_up(off + 4 * (batch + 1), 16);
   ns.meta_bytes = align_up(off, kAlign);
   h.off_tmp_lse = ns.meta_bytes;
   h.off_tmp_o = ns.meta_bytes + align_up(4 * int64_t(ns.n_partials) * hq, kAlign);
@@ -591,6 +617,7 @@ void write_staging(const PlanState& s, uint8_t* dst) {
   put(s.hdr.off_merge_indptr, s.merge_indptr.data(), 4 * s.merge_indptr.size());
   put(s.hdr.off_merge_rows, s.merge_rows.data(), 4 * s.merge_rows.size());
   put(s.hdr.off_items, s.items.data(), sizeof(WorkItem) * s.items.size());
+  put(s.hdr.off_mask_indptr, s.mask_indptr.data(), 4 * s.mask_indptr.size());
 }
 
 }  // namespace
@@ -601,12 +628,13 @@ fi_status plan_common(fi_plan_t p, const int32_t* qo_indptr, const int32_t* kv_i
                       const int32_t* last_page_len, int32_t batch, int32_t page_size,
                       int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                       int32_t causal, int32_t window_left, fi_dtype dtype,
-                      int32_t q_len_per_req, int32_t force_kv_chunks, bool ragged, void* stream) {
+                      int32_t q_len_per_req, int32_t force_kv_chunks, bool ragged,
+                      const int32_t* mask_indptr, void* stream) {
   if (!p) return fail(FI_ERR_INVALID_ARG, "plan: plan is NULL");
   PlanState ns;
   fi_status st = build_plan(*p, qo_indptr, kv_indptr, last_page_len, batch, page_size,
                             num_qo_heads, num_kv_heads, head_dim, causal, window_left, dtype,
-                            q_len_per_req, force_kv_chunks, ragged, ns);
+                            q_len_per_req, force_kv_chunks, ragged, mask_indptr, ns);
   if (st != FI_OK) return st;  // the previous plan stays usable
   if (!p->host_only) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -646,6 +674,7 @@ fi_status plan_common(fi_plan_t p, const int32_t* qo_indptr, const int32_t* kv_i
     p->fz_kernel = ns.kernel; p->fz_qlpr = ns.q_len_per_req; p->fz_hq = ns.hq;
     p->fz_hk = ns.hk; p->fz_d = ns.d; p->fz_dtype = ns.dtype; p->fz_page = ns.page_size;
     p->fz_ragged = ns.ragged;
+    p->fz_masked = ns.masked;
   }
   p->st = std::move(ns);
   p->planned = true;
@@ -661,7 +690,22 @@ extern "C" fi_status fi_plan(fi_plan_t p, const int32_t* qo_indptr, const int32_
                              int32_t q_len_per_req, int32_t force_kv_chunks, void* stream) {
   return plan_common(p, qo_indptr, kv_indptr, last_page_len, batch, page_size, num_qo_heads,
                      num_kv_heads, head_dim, causal, window_left, dtype, q_len_per_req,
-                     force_kv_chunks, false, stream);
+                     force_kv_chunks, false, nullptr, stream);
+}
+
+extern "C" fi_status fi_plan_masked(fi_plan_t p, const int32_t* qo_indptr,
+                                    const int32_t* kv_indptr, const int32_t* last_page_len,
+                                    int32_t batch, int32_t page_size, int32_t num_qo_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t causal,
+                                    int32_t window_left, fi_dtype dtype,
+                                    const int32_t* mask_indptr, int32_t force_kv_chunks,
+                                    void* stream) {
+  if (batch > 0 && !mask_indptr)
+    return fail(FI_ERR_INVALID_ARG, "plan: mask_indptr is NULL for a masked plan");
+  static const int32_t zero[1] = {0};
+  return plan_common(p, qo_indptr, kv_indptr, last_page_len, batch, page_size, num_qo_heads,
+                     num_kv_heads, head_dim, causal, window_left, dtype, 0, force_kv_chunks,
+                     false, mask_indptr ? mask_indptr : zero, stream);
 }
 
 extern "C" fi_status fi_plan_ragged(fi_plan_t p, const int32_t* qo_indptr,
@@ -671,7 +715,7 @@ extern "C" fi_status fi_plan_ragged(fi_plan_t p, const int32_t* qo_indptr,
                                     void* stream) {
   return plan_common(p, qo_indptr, kv_indptr, nullptr, batch, kRaggedPage, num_qo_heads,
                      num_kv_heads, head_dim, causal, window_left, dtype, 0, force_kv_chunks, true,
-                     stream);
+                     nullptr, stream);
 }
 
 extern "C" fi_status fi_plan_get_info(fi_plan_t p, fi_plan_info* info, int32_t* items,
@@ -758,6 +802,7 @@ const char* dtype_name(int d) {
     case FI_BF16: return "bf16";
     case FI_F32: return "f32";
     case FI_I32: return "i32";
+    case FI_U8: return "u8";
   }
   return "?";
 }
@@ -797,13 +842,28 @@ bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15)
 // plan came from fi_plan_ragged.
 fi_status run_common(fi_plan_t p, bool decode_api, bool ragged, const fi_tensor* q,
                      const fi_tensor* k, const fi_tensor* v, const fi_tensor* kv_indices,
-                     float sm_scale, fi_tensor* out, fi_tensor* lse, void* stream) {
+                     const fi_tensor* custom_mask, float sm_scale, fi_tensor* out, fi_tensor* lse,
+                     void* stream) {
   const char* api = ragged ? "batch_prefill_ragged"
-                           : decode_api ? "batch_decode_paged" : "batch_prefill_paged";
+                    : decode_api ? "batch_decode_paged"
+                    : custom_mask ? "batch_prefill_paged_masked" : "batch_prefill_paged";
   if (!p) return fail(FI_ERR_INVALID_ARG, "%s: plan is NULL", api);
   // [P3 "Plan-vs-run shapes"]: a half-planned object refuses run()
   if (!p->planned) return fail(FI_ERR_NOT_PLANNED, "%s: call fi_plan() first", api);
   const PlanState& s = p->st;
+  if ((custom_mask != nullptr) != (s.masked != 0))
+    return fail(FI_ERR_PLAN_MISMATCH, "%s: the plan is %s (fi_plan%s)", api,
+                s.masked ? "for a custom mask" : "without a custom mask",
+                s.masked ? "_masked" : "");
+  if (custom_mask) {
+    fi_status cst = check_tensor(custom_mask, "custom_mask", 1);
+    if (cst != FI_OK) return cst;
+    if (custom_mask->dtype != FI_U8)
+      return fail(FI_ERR_INVALID_ARG, "%s: custom_mask must be FI_U8", api);
+    if (custom_mask->shape[0] < s.mask_bytes)
+      return check_dim("custom_mask", "bytes (minimum, mask_indptr[batch])", s.mask_bytes,
+                       custom_mask->shape[0]);
+  }
   if (ragged != (s.ragged != 0))
     return fail(FI_ERR_PLAN_MISMATCH, "%s: the plan is for a %s K/V cache (fi_plan%s)", api,
                 s.ragged ? "ragged" : "paged", s.ragged ? "_ragged" : "");
@@ -898,6 +958,7 @@ fi_status run_common(fi_plan_t p, bool decode_api, bool ragged, const fi_tensor*
   }
   ap.ragged = ragged ? 1 : 0;
   ap.kv_rows = ragged ? std::min(k->shape[0], v->shape[0]) : 0;
+  ap.custom_mask = custom_mask ? static_cast<const uint8_t*>(custom_mask->data) : nullptr;
   ap.out = out->data;
   ap.lse = lse ? static_cast<float*>(lse->data) : nullptr;
   ap.ws = p->ws;
@@ -941,20 +1002,31 @@ extern "C" fi_status fi_batch_prefill_paged(fi_plan_t p, const fi_tensor* q, con
                                             const fi_tensor* v, const fi_tensor* kv_indices,
                                             float sm_scale, fi_tensor* out, fi_tensor* lse,
                                             void* stream) {
-  return run_common(p, false, false, q, k, v, kv_indices, sm_scale, out, lse, stream);
+  return run_common(p, false, false, q, k, v, kv_indices, nullptr, sm_scale, out, lse, stream);
+}
+
+extern "C" fi_status fi_batch_prefill_paged_masked(fi_plan_t p, const fi_tensor* q,
+                                                   const fi_tensor* k, const fi_tensor* v,
+                                                   const fi_tensor* kv_indices,
+                                                   const fi_tensor* custom_mask, float sm_scale,
+                                                   fi_tensor* out, fi_tensor* lse, void* stream) {
+  if (!custom_mask)
+    return fail(FI_ERR_INVALID_ARG, "batch_prefill_paged_masked: custom_mask is NULL");
+  return run_common(p, false, false, q, k, v, kv_indices, custom_mask, sm_scale, out, lse,
+                    stream);
 }
 
 extern "C" fi_status fi_batch_decode_paged(fi_plan_t p, const fi_tensor* q, const fi_tensor* k,
                                            const fi_tensor* v, const fi_tensor* kv_indices,
                                            float sm_scale, fi_tensor* out, fi_tensor* lse,
                                            void* stream) {
-  return run_common(p, true, false, q, k, v, kv_indices, sm_scale, out, lse, stream);
+  return run_common(p, true, false, q, k, v, kv_indices, nullptr, sm_scale, out, lse, stream);
 }
 
 extern "C" fi_status fi_batch_prefill_ragged(fi_plan_t p, const fi_tensor* q, const fi_tensor* k,
                                              const fi_tensor* v, float sm_scale, fi_tensor* out,
                                              fi_tensor* lse, void* stream) {
-  return run_common(p, false, true, q, k, v, nullptr, sm_scale, out, lse, stream);
+  return run_common(p, false, true, q, k, v, nullptr, nullptr, sm_scale, out, lse, stream);
 }
 
 // ------------------------------------------------------------------ merges

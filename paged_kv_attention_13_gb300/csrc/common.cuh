@@ -113,6 +113,14 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
   }
 }
 
+// Bit (i * lk + j) of a request's custom mask, whose bits start at byte
+// `base` (least significant bit first).
+__device__ __forceinline__ bool custom_mask_bit(const uint8_t* mask, int base, int i, int j,
+                                                int lk) {
+  const int64_t n = int64_t(i) * lk + j;
+  return (__ldg(mask + base + (n >> 3)) >> (n & 7)) & 1;
+}
+
 // Key j of a request: its row in the cache (page from the page table), or
 // with a ragged cache, row kv_start + j.
 __device__ __forceinline__ int64_t kv_row_offset(const int32_t* pages, int32_t j, int page_size,

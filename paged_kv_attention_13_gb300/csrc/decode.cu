@@ -33,6 +33,7 @@
 //   [P1] "Route non-causal windowed prefill to AITER's masked kernel" (#339)
 //   [P2] "Support speculative-decode verify on ROCm, and stop auto routing
 //         short-query prefill to AITER" (#362)
+#include <climits>
 #include <type_traits>
 
 #include "tma.cuh"
@@ -50,7 +51,8 @@ struct alignas(16) StageHdr {
   int32_t flags, k0, lo, hi;
   int32_t lo_full, hi_full, token0, kv_head;  // token0: global token of query row i0
   int32_t row0, n_rows, diff, chunk;          // first packed row, rows, Lk - Lq, chunk (-1: direct)
-  int32_t num_chunks, partial_base, i0, pad;
+  int32_t num_chunks, partial_base, i0, lk;
+  int32_t mask_base, lq, pad0, pad1;          // custom mask: the request's first byte; Lq
 };
 
 // Write rows [r0, r0 + 8) of an item: sm_o holds those rows' o summed over
@@ -192,9 +194,11 @@ struct DecodeWarp {
       for (int e = 0; e < 4; ++e) o2[h][e] = make_float2(0.f, 0.f);
   }
 
-  __device__ __forceinline__ void stage(T* cK, T* cV, const StageHdr& h, int causal, int wl) {
+  __device__ __forceinline__ void stage(T* cK, T* cV, const StageHdr& h, int causal, int wl,
+                                        const uint8_t* p_mask) {
     (void)causal;
     (void)wl;
+    (void)p_mask;  // decode plans carry no custom mask
     stage_keys(cK, cV, h.k0, h.lo, h.hi);
   }
 
@@ -417,7 +421,8 @@ struct DecodeMmaWarp {
   // every row's range the per-element mask runs; where it is not inside the
   // item's live range the warp first zeroes its V rows outside it (they may
   // hold anything, a neighbour's slots, and 0 * NaN would reach o).
-  __device__ __forceinline__ void stage(T* cK, T* cV, const StageHdr& h, int causal, int wl) {
+  __device__ __forceinline__ void stage(T* cK, T* cV, const StageHdr& h, int causal, int wl,
+                                        const uint8_t* p_mask) {
     const uint32_t sk = smem_u32(cK), sv = smem_u32(cV);
     const int kb = warp * KPW;  // this warp's first key in the stage
     const int k0 = h.k0;
@@ -467,6 +472,8 @@ struct DecodeMmaWarp {
             bool ok = r < h.n_rows && kk >= h.lo && kk < h.hi;
             if (causal && kk > i + h.diff) ok = false;
             if (wl >= 0 && kk + wl < h.diff + i) ok = false;
+            // custom mask (ANDed): its bits are read only for real rows and keys
+            if (ok && p_mask && !custom_mask_bit(p_mask, h.mask_base, i, kk, h.lk)) ok = false;
             if (!ok) x = neg_inf();
           }
           s[nt][2 * hr + e] = x;
@@ -693,7 +700,16 @@ __device__ __noinline__ void decode_producer(const AttnParams& p, const CUtensor
     h.num_chunks = it.num_chunks;
     h.partial_base = it.partial_base;
     h.i0 = i0;
-    h.pad = 0;
+    h.lk = lk;
+    h.lq = lq;
+    h.mask_base = 0;
+    h.pad0 = h.pad1 = 0;
+    if (p.custom_mask) {
+      // an arbitrary mask: every stage runs the per-element test
+      h.mask_base = ws_ptr<const int32_t>(p.ws, hdr->off_mask_indptr)[it.b];
+      h.lo_full = INT_MAX;
+      h.hi_full = INT_MIN;
+    }
     const int start = lo & ~(box_rows - 1);
     const int n_tiles = hi > lo ? (hi - start + KT - 1) / KT : 0;
     const int kv_start = kv_indptr[it.b];  // ragged: first row; paged: first page-table entry
@@ -868,7 +884,8 @@ __global__ void __launch_bounds__(TmaCfg<D, MMA>::THREADS, TmaCfg<D, MMA>::MINB)
         __syncwarp();
         if (lane == 0) mbar_arrive(QFREE);
       }
-      if (!(flags & kStNoKeys)) wk.stage(sK + st * STAGE, sV + st * STAGE, h, causal, window_left);
+      if (!(flags & kStNoKeys))
+        wk.stage(sK + st * STAGE, sV + st * STAGE, h, causal, window_left, p.custom_mask);
       StageHdr out;
       if (flags & kStLast) out = h;
       __syncwarp();

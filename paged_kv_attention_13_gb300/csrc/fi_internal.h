@@ -47,6 +47,7 @@ struct alignas(128) WsHeader {
   int64_t off_items;         // WorkItem [n_items]
   int64_t off_tmp_lse;       // float [partials, Hq]
   int64_t off_tmp_o;         // float [partials, Hq, d]
+  int64_t off_mask_indptr;   // int32 [batch+1]: byte offset of each request's custom mask
 };
 static_assert(sizeof(WsHeader) == 128, "header is 128 bytes");
 
@@ -77,6 +78,10 @@ struct AttnParams {
   // are 1 << 30 / 30 (one logical page per request).
   int32_t ragged;
   int64_t kv_rows;      // ragged: rows of k / v (the TMA maps' extent)
+  // Custom (tree) mask or null: request b's bits (query row i, key j at bit
+  // i * Lk + j, least significant bit first) start at byte
+  // mask_indptr[b] (workspace array); ANDed into the causal / window mask.
+  const uint8_t* custom_mask;
 };
 
 enum KernelId : int32_t {

@@ -217,6 +217,7 @@ extern "C" fi_status fi_batch_decode_paged_noalloc(
     if ((1 << sh) == page_size) ap.page_shift = sh;
   ap.ragged = 0;
   ap.kv_rows = 0;
+  ap.custom_mask = nullptr;
   const int grid = batch * hk * kv_chunks;
   e = launch_decode(ap, d, g, q->dtype == FI_BF16, k_cache->shape[0], g, grid, s);
   if (e != cudaSuccess) return fail(FI_ERR_CUDA, "decode_noalloc: decode launch failed");

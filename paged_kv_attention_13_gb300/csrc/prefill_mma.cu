@@ -89,6 +89,8 @@ __global__ void __launch_bounds__(kThreads) prefill_mma_kernel(const AttnParams 
     const int kv_lo = max(it.kv_begin, lo_t);
     const int kv_hi = min(it.kv_end, hi_t);
     const bool ragged = p.ragged != 0;
+    const bool custom = p.custom_mask != nullptr;
+    const int mask_base = custom ? ws_ptr<const int32_t>(p.ws, hdr->off_mask_indptr)[b] : 0;
     const int kv_start = kv_indptr[b];  // ragged: first row; paged: first page-table entry
     const int32_t* pages = ragged ? nullptr : p.kv_indices + kv_start;
 
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(kThreads) prefill_mma_kernel(const AttnParams 
         }
       }
       // scale into the log2 domain, mask boundary tiles
-      const bool need_mask = (kt + kN > kv_hi) ||
+      const bool need_mask = (kt + kN > kv_hi) || custom ||
                              (causal && kt + kN - 1 > i0 + lk - lq) ||
                              (wl >= 0 && kt < lk - lq + i1 - wl);
 #pragma unroll
@@ -197,6 +199,10 @@ __global__ void __launch_bounds__(kThreads) prefill_mma_kernel(const AttnParams 
             bool ok = j < kv_hi;
             if (causal && j > i + lk - lq) ok = false;
             if (wl >= 0 && j + lq + wl < lk + i) ok = false;
+            // custom mask: read only for the tile's real rows (i < lq), whose
+            // bits lie inside the request's segment
+            if (custom && ok && (i >= lq || !custom_mask_bit(p.custom_mask, mask_base, i, j, lk)))
+              ok = false;
             if (!ok) x = neg_inf();
           }
           s[nt][e] = x;

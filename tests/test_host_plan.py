@@ -319,3 +319,48 @@ def test_ragged_and_paged_plans_do_not_cross():
     with pytest.raises(fi.FiError) as e:
         fi.fi_batch_prefill_ragged(p, q, kv[:21], kv[:21], 0.1, out=out)
     assert _status(e) == "FI_ERR_PLAN_MISMATCH"
+
+
+# ------------------------------------------------------------ custom masks
+
+def test_masked_plan_refusals_and_kernel_choice():
+    pb = workloads.tree_verify(batch=3, n_draft=4, kv_lo=20, kv_hi=40)
+    mi = pb.extra["mask_indptr"].numpy()
+    p = _plan()
+    p.plan_masked(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, 16, 32, 8, 128, mi, causal=True)
+    assert p.info()["kernel_name"] == "decode"  # 16 packed rows, page 16
+    # a segment one byte short of its request's bits
+    short = mi.copy()
+    short[1:] -= 1
+    short[1] = max(short[1], 0)
+    with pytest.raises(fi.FiError) as e:
+        p.plan_masked(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, 16, 32, 8, 128, short)
+    assert _status(e) == "FI_ERR_INVALID_ARG"
+    # more than 64 packed rows: the mma.sync M = 64 kernel, never the tcgen05 one
+    pb2 = workloads.tree_verify(batch=2, n_draft=40, kv_lo=100, kv_hi=200)
+    p.plan_masked(pb2.qo_indptr, pb2.kv_indptr, pb2.last_page_len, 16, 32, 8, 128,
+                  pb2.extra["mask_indptr"].numpy())
+    assert p.info()["kernel_name"] == "prefill_m64"
+
+
+def test_masked_and_unmasked_plans_do_not_cross():
+    pb = workloads.tree_verify(batch=2, n_draft=4, kv_lo=20, kv_hi=30)
+    T = int(pb.qo_indptr[-1])
+    q = torch.zeros((T, 32, 128), dtype=torch.bfloat16)
+    out = torch.zeros_like(q)
+    args = (q, pb.k_cache, pb.v_cache, pb.kv_indices)
+    p = _plan()
+    p.plan_masked(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, 16, 32, 8, 128,
+                  pb.extra["mask_indptr"].numpy())
+    with pytest.raises(fi.FiError) as e:
+        fi.fi_batch_prefill_paged(p, *args, 0.1, out=out)
+    assert _status(e) == "FI_ERR_PLAN_MISMATCH"
+    # a mask tensor shorter than the plan's segments
+    with pytest.raises(fi.FiError) as e:
+        fi.fi_batch_prefill_paged_masked(p, *args, pb.extra["mask"][:-1], 0.1, out=out)
+    assert _status(e) == "FI_ERR_PLAN_MISMATCH"
+    p2 = _plan()
+    p2.plan(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, 16, 32, 8, 128)
+    with pytest.raises(fi.FiError) as e:
+        fi.fi_batch_prefill_paged_masked(p2, *args, pb.extra["mask"], 0.1, out=out)
+    assert _status(e) == "FI_ERR_PLAN_MISMATCH"
