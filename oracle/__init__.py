@@ -9,6 +9,7 @@ imports, links or runs anything here, and nothing here imports the product.
 - ``reference.py``: ctypes wrapper around it.
 - ``brute.py``: a numpy brute force for tiny inputs that materialises the
   boolean mask matrix element by element.
+- ``speculative.py``: the chain speculative-sampling acceptance step.
 """
 from .build import build_oracle  # noqa: F401
 from .reference import attention_rows, attention_all, merge_states, kv_len  # noqa: F401

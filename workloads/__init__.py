@@ -223,6 +223,37 @@ def tree_verify(batch: int = 32, variant: int = 0, n_draft: int = 8, kv_lo: int 
     return pb
 
 
+def spec_sampling_batch(batch: int = 64, n_draft: int = 4, vocab: int = 128256,
+                        variant: int = 0, temperature: float = 0.7, draft_noise: float = 0.5):
+    """Inputs of the chain speculative-sampling step: target probabilities
+    [B, n+1, V] (softmax of N(0,1) logits / temperature, fp32), draft
+    probabilities [B, n, V] (the same logits plus N(0, draft_noise) noise), draft
+    tokens drawn from the draft rows, and the uniforms of the acceptance tests
+    [B, n] and of the final draw [B]. Returns a dict of CPU torch tensors."""
+    rng = np.random.default_rng(seed_for(7, variant) + batch + n_draft)
+    logits = rng.standard_normal((batch, n_draft + 1, vocab), dtype=np.float32)
+    noise = rng.standard_normal((batch, n_draft, vocab), dtype=np.float32) * draft_noise
+
+    def softmax(x):
+        x = x / temperature
+        x = x - x.max(axis=-1, keepdims=True)
+        e = np.exp(x)
+        return (e / e.sum(axis=-1, keepdims=True)).astype(np.float32)
+
+    target = softmax(logits)
+    draft = softmax(logits[:, :n_draft] + noise)
+    ids = np.zeros((batch, n_draft), np.int32)
+    for b in range(batch):
+        for i in range(n_draft):
+            c = np.cumsum(draft[b, i].astype(np.float64))
+            ids[b, i] = min(int(np.searchsorted(c, rng.random() * c[-1], side="right")), vocab - 1)
+    u_accept = rng.random((batch, n_draft), dtype=np.float32)
+    u_sample = rng.random(batch, dtype=np.float32)
+    return {"draft_probs": torch.from_numpy(draft), "draft_ids": torch.from_numpy(ids),
+            "target_probs": torch.from_numpy(target), "u_accept": torch.from_numpy(u_accept),
+            "u_sample": torch.from_numpy(u_sample)}
+
+
 PREFILL_CASES = ([dict(causal=True, window_left=w) for w in (-1, 0, 127, 4095)]
                  + [dict(causal=False, window_left=w) for w in (-1, 127)])
 
