@@ -412,6 +412,45 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def spec_sampling_entry(dev, steps, hbm_peak, batch=64, n_draft=4, vocab=128256):
+    """The chain speculative-sampling step (acceptance + one draw per request).
+    Algorithmic bytes: the n acceptance lookups and the drawn row (p, and q
+    when a draft was rejected) of every request, plus the outputs; counted
+    from the step's own acceptance result."""
+    import paged_kv_attention_13_gb300 as fi
+    d = workloads.spec_sampling_batch(batch=batch, n_draft=n_draft, vocab=vocab)
+    t = {k: v.to(dev) for k, v in d.items()}
+    outs = (torch.empty((batch, n_draft + 1), dtype=torch.int32, device=dev),
+            torch.empty(batch, dtype=torch.int32, device=dev),
+            torch.empty(batch, dtype=torch.int32, device=dev))
+
+    def step():
+        fi.fi_chain_speculative_sampling(t["draft_probs"], t["draft_ids"], t["target_probs"],
+                                         t["u_accept"], t["u_sample"], *outs)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    acc = outs[1].cpu().numpy()
+    byts = int(sum(vocab * 4 * (2 if a < n_draft else 1) for a in acc)) + \
+        batch * n_draft * (4 + 4 + 4 + 4) + batch * 4 + batch * (n_draft + 1) * 4 + 8 * batch
+    buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+    ms = []
+    for i in range(steps):
+        buf.fill_(i & 0xFF)  # the rows start out of L2
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        step()
+        b.record(s)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    m = float(np.median(ms))
+    gbs = byts / (m * 1e-3) / 1e9
+    return {"ms": round(m, 4), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4),
+            "kernel": "chain_spec_kernel", "accepted_mean": round(float(acc.mean()), 3)}
+
+
 def other_workloads(args, dev, ws, hbm_peak, bf16_peak):
     res = {}
     steps = max(3, min(args.steps, 10))
@@ -445,6 +484,7 @@ def other_workloads(args, dev, ws, hbm_peak, bf16_peak):
     one("ragged_prefill_causal", pb, True, -1, "ragged", bound="tensor")
     pb = workloads.tree_verify(batch=32)
     one("tree_verify_b32", pb, True, -1, "masked")
+    res["spec_sampling_b64_n4_v128256"] = spec_sampling_entry(dev, steps, hbm_peak)
     pb = workloads.long_context()
     one("longctx_causal_split", pb, True, -1, "prefill")
     one("longctx_causal_force32", pb, True, -1, "prefill", force=32)

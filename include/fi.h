@@ -277,6 +277,42 @@ fi_status fi_merge_states(const fi_tensor* v, const fi_tensor* s, const int32_t*
                           int32_t rows, fi_tensor* v_out, fi_tensor* s_out,
                           const int32_t* num_rows_dev, void* stream);
 
+/*
+ * Chain speculative-sampling acceptance step: the sampler the multi-token
+ * verify feeds ("Support speculative-decode verify on ROCm, and stop auto
+ * routing short-query prefill to AITER" (#362), "Summary"; it takes a chain
+ * of num_speculate_tokens drafts per request, not a tree, "Architecture /
+ * design notes"). The steps are the published speculative sampling
+ * (Leviathan, Kalman and Matias 2023; Chen et al. 2023):
+ *   draft i (token x_i) is accepted while u_i * q_i(x_i) <= p_i(x_i), the
+ *   product and compare in fp32; at the first rejection i one token is drawn
+ *   from max(0, p_i - q_i) (p_i when that is all zero), or from p_n if all n
+ *   drafts are accepted. A draw with uniform u picks the smallest token t
+ *   whose cumulative weight (fp64) exceeds u * total weight.
+ *
+ *   draft_probs       F32 [B, n, V]   q; vocabulary dim contiguous
+ *   draft_token_ids   I32 [B, n]      x
+ *   target_probs      F32 [B, n+1, V] p (row n: the bonus distribution)
+ *   uniform_accept    F32 [B, n]      the acceptance tests' uniforms
+ *   uniform_sample    F32 [B]         the final draw's uniform, in [0, 1)
+ *   output_token_ids  I32 [B, n+1]    out: accepted drafts, the drawn token,
+ *                                     then -1 (packed)
+ *   accepted_num      I32 [B]         out: drafts accepted before the first
+ *                                     rejection
+ *   emitted_num       I32 [B] or NULL out: accepted_num + 1
+ * All device memory, caller-owned; one CTA per request on `stream`; nothing
+ * is allocated. The draft arguments may be NULL when n = 0. Errors:
+ * FI_ERR_INVALID_ARG (shapes, dtypes), FI_ERR_STRIDED_LAST_DIM,
+ * FI_ERR_NONCONTIGUOUS_OUTPUT, FI_ERR_CUDA.
+ */
+fi_status fi_chain_speculative_sampling(const fi_tensor* draft_probs,
+                                        const fi_tensor* draft_token_ids,
+                                        const fi_tensor* target_probs,
+                                        const fi_tensor* uniform_accept,
+                                        const fi_tensor* uniform_sample,
+                                        fi_tensor* output_token_ids, fi_tensor* accepted_num,
+                                        fi_tensor* emitted_num, void* stream);
+
 /* Copy a plan's host metadata out (any pointer may be NULL):
  *   items [num_items * 8] int32: per work item {request, kv_head, first packed
  *         row, packed rows, kv_begin, kv_end, chunk (-1 = written directly),

@@ -25,7 +25,7 @@ EXPORTED = [
     "fi_plan_read_device", "fi_plan_destroy", "fi_last_error", "fi_status_str",
     "fi_batch_decode_paged_noalloc", "fi_noalloc_scratch_bytes", "fi_noalloc_last_error",
     "fi_plan_device_error", "fi_plan_ragged", "fi_batch_prefill_ragged", "fi_plan_masked",
-    "fi_batch_prefill_paged_masked",
+    "fi_batch_prefill_paged_masked", "fi_chain_speculative_sampling",
 ]
 
 
@@ -76,6 +76,8 @@ def load():
     lib.fi_plan_get_info.argtypes = [P, ctypes.POINTER(FiPlanInfo), pi32, i32, pi32, i32]
     lib.fi_plan_read_device.restype = ctypes.c_int
     lib.fi_plan_read_device.argtypes = [P, pi32, i32, pi32, i32, P]
+    lib.fi_chain_speculative_sampling.restype = ctypes.c_int
+    lib.fi_chain_speculative_sampling.argtypes = [PT, PT, PT, PT, PT, PT, PT, PT, P]
     lib.fi_plan_masked.restype = ctypes.c_int
     lib.fi_plan_masked.argtypes = [P, pi32, pi32, pi32, i32, i32, i32, i32, i32, i32, i32,
                                    ctypes.c_int, pi32, i32, P]

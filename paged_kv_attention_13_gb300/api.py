@@ -241,6 +241,32 @@ def fi_batch_prefill_paged_masked(plan, q, k_cache, v_cache, kv_indices, custom_
     return out, lse
 
 
+def fi_chain_speculative_sampling(draft_probs, draft_token_ids, target_probs, uniform_accept,
+                                  uniform_sample, output_token_ids=None, accepted_num=None,
+                                  emitted_num=None, stream=None):
+    """Chain speculative-sampling acceptance step on the device; returns
+    (output_token_ids [B, n+1], accepted_num [B], emitted_num [B])."""
+    B, n1 = target_probs.shape[0], target_probs.shape[1]
+    dev = target_probs.device
+    if output_token_ids is None:
+        output_token_ids = torch.empty((B, n1), dtype=torch.int32, device=dev)
+    if accepted_num is None:
+        accepted_num = torch.empty((B,), dtype=torch.int32, device=dev)
+    if emitted_num is None:
+        emitted_num = torch.empty((B,), dtype=torch.int32, device=dev)
+    n = n1 - 1
+    ins = [tensor_desc(t) if n > 0 else None
+           for t in (draft_probs, draft_token_ids)] + [tensor_desc(target_probs)]
+    ua = tensor_desc(uniform_accept) if n > 0 else None
+    us = tensor_desc(uniform_sample)
+    outs = [tensor_desc(t) for t in (output_token_ids, accepted_num, emitted_num)]
+    ref = lambda d: ctypes.byref(d) if d is not None else None  # noqa: E731
+    _check(_lib.load().fi_chain_speculative_sampling(
+        ref(ins[0]), ref(ins[1]), ref(ins[2]), ref(ua), ref(us), *[ref(d) for d in outs],
+        _stream_handle(stream)))
+    return output_token_ids, accepted_num, emitted_num
+
+
 def fi_batch_prefill_ragged(plan, q, k, v, sm_scale, out=None, lse=None, return_lse=True,
                             stream=None):
     """Batched prefill over contiguous K/V [rows, Hk, d]; returns (out, lse)."""

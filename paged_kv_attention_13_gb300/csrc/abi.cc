@@ -1029,6 +1029,80 @@ extern "C" fi_status fi_batch_prefill_ragged(fi_plan_t p, const fi_tensor* q, co
   return run_common(p, false, true, q, k, v, nullptr, nullptr, sm_scale, out, lse, stream);
 }
 
+// ------------------------------------------------ speculative sampling
+extern "C" fi_status fi_chain_speculative_sampling(
+    const fi_tensor* draft_probs, const fi_tensor* draft_token_ids,
+    const fi_tensor* target_probs, const fi_tensor* uniform_accept,
+    const fi_tensor* uniform_sample, fi_tensor* output_token_ids, fi_tensor* accepted_num,
+    fi_tensor* emitted_num, void* stream) {
+  const char* api = "chain_speculative_sampling";
+  fi_status st;
+  if ((st = check_tensor(target_probs, "target_probs", 3)) != FI_OK) return st;
+  const int64_t B = target_probs->shape[0];
+  const int64_t n = target_probs->shape[1] - 1;
+  const int64_t V = target_probs->shape[2];
+  if (n < 0 || V < 1 || n > 4096)
+    return fail(FI_ERR_INVALID_ARG, "%s: target_probs [B, n+1, V] needs n+1 >= 1, V >= 1", api);
+  if (V > fi::chain_spec_max_vocab())
+    return fail(FI_ERR_UNSUPPORTED, "%s: vocabulary %lld > %d", api, (long long)V,
+                fi::chain_spec_max_vocab());
+  if ((st = check_tensor(uniform_sample, "uniform_sample", 1)) != FI_OK) return st;
+  if ((st = check_tensor(output_token_ids, "output_token_ids", 2)) != FI_OK) return st;
+  if ((st = check_tensor(accepted_num, "accepted_num", 1)) != FI_OK) return st;
+  if (emitted_num && (st = check_tensor(emitted_num, "emitted_num", 1)) != FI_OK) return st;
+  if (n > 0) {
+    if ((st = check_tensor(draft_probs, "draft_probs", 3)) != FI_OK) return st;
+    if ((st = check_tensor(draft_token_ids, "draft_token_ids", 2)) != FI_OK) return st;
+    if ((st = check_tensor(uniform_accept, "uniform_accept", 2)) != FI_OK) return st;
+    if (draft_probs->shape[0] != B || draft_probs->shape[1] != n || draft_probs->shape[2] != V)
+      return fail(FI_ERR_INVALID_ARG, "%s: draft_probs must be [B, n, V] = [%lld, %lld, %lld]",
+                  api, (long long)B, (long long)n, (long long)V);
+    if (draft_token_ids->shape[0] != B || draft_token_ids->shape[1] != n ||
+        uniform_accept->shape[0] != B || uniform_accept->shape[1] != n)
+      return fail(FI_ERR_INVALID_ARG, "%s: draft_token_ids and uniform_accept must be [B, n]", api);
+    if (draft_probs->dtype != FI_F32 || draft_token_ids->dtype != FI_I32 ||
+        uniform_accept->dtype != FI_F32)
+      return fail(FI_ERR_INVALID_ARG, "%s: draft_probs / uniform_accept F32, draft_token_ids I32",
+                  api);
+  }
+  if (target_probs->dtype != FI_F32 || uniform_sample->dtype != FI_F32 ||
+      output_token_ids->dtype != FI_I32 || accepted_num->dtype != FI_I32 ||
+      (emitted_num && emitted_num->dtype != FI_I32))
+    return fail(FI_ERR_INVALID_ARG, "%s: probabilities and uniforms F32, outputs I32", api);
+  if (uniform_sample->shape[0] != B || accepted_num->shape[0] != B ||
+      (emitted_num && emitted_num->shape[0] != B) || output_token_ids->shape[0] != B ||
+      output_token_ids->shape[1] != n + 1)
+    return fail(FI_ERR_INVALID_ARG, "%s: uniform_sample / accepted_num / emitted_num [B], "
+                "output_token_ids [B, n+1]", api);
+  if ((st = check_packed(output_token_ids, "output_token_ids")) != FI_OK) return st;
+  if ((st = check_packed(accepted_num, "accepted_num")) != FI_OK) return st;
+  if (emitted_num && (st = check_packed(emitted_num, "emitted_num")) != FI_OK) return st;
+  fi::SpecParams sp;
+  sp.target_probs = static_cast<const float*>(target_probs->data);
+  sp.tp_sb = target_probs->stride[0];
+  sp.tp_si = target_probs->stride[1];
+  sp.u_sample = static_cast<const float*>(uniform_sample->data);
+  sp.draft_probs = n > 0 ? static_cast<const float*>(draft_probs->data) : nullptr;
+  sp.dp_sb = n > 0 ? draft_probs->stride[0] : 0;
+  sp.dp_si = n > 0 ? draft_probs->stride[1] : 0;
+  sp.draft_ids = n > 0 ? static_cast<const int32_t*>(draft_token_ids->data) : nullptr;
+  sp.ids_sb = n > 0 ? draft_token_ids->stride[0] : 0;
+  sp.u_accept = n > 0 ? static_cast<const float*>(uniform_accept->data) : nullptr;
+  sp.ua_sb = n > 0 ? uniform_accept->stride[0] : 0;
+  sp.n = int32_t(n);
+  sp.vocab = int32_t(V);
+  sp.out_tokens = static_cast<int32_t*>(output_token_ids->data);
+  sp.out_accepted = static_cast<int32_t*>(accepted_num->data);
+  sp.out_emitted = emitted_num ? static_cast<int32_t*>(emitted_num->data) : nullptr;
+  if (n > 0 && (draft_token_ids->stride[1] != 1 || uniform_accept->stride[1] != 1))
+    return fail(FI_ERR_STRIDED_LAST_DIM, "%s: draft_token_ids / uniform_accept rows", api);
+  if (uniform_sample->shape[0] > 1 && uniform_sample->stride[0] != 1)
+    return fail(FI_ERR_STRIDED_LAST_DIM, "%s: uniform_sample must be contiguous", api);
+  cudaError_t e = fi::launch_chain_spec_sampling(sp, int(B), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FI_ERR_CUDA, "%s: launch failed: %s", api, cudaGetErrorString(e));
+  return ok();
+}
+
 // ------------------------------------------------------------------ merges
 extern "C" fi_status fi_merge_state(const fi_tensor* va, const fi_tensor* sa, const fi_tensor* vb,
                                     const fi_tensor* sb, fi_tensor* vo, fi_tensor* so,

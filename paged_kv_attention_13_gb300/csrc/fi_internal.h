@@ -131,6 +131,29 @@ struct MergeTwoParams {
 };
 cudaError_t launch_merge_two(const MergeTwoParams& p, cudaStream_t stream);
 
+// Chain speculative-sampling acceptance step (element strides; the vocabulary
+// dim is contiguous): draft_probs [B, n, V], draft_ids [B, n], target_probs
+// [B, n+1, V], u_accept [B, n], u_sample [B] -> out_tokens [B, n+1] (packed),
+// out_accepted [B], out_emitted [B] (or null).
+struct SpecParams {
+  const float* draft_probs;
+  int64_t dp_sb, dp_si;
+  const int32_t* draft_ids;
+  int64_t ids_sb;
+  const float* target_probs;
+  int64_t tp_sb, tp_si;
+  const float* u_accept;
+  int64_t ua_sb;
+  const float* u_sample;
+  int32_t n, vocab;
+  int32_t* out_tokens;
+  int32_t* out_accepted;
+  int32_t* out_emitted;
+};
+cudaError_t launch_chain_spec_sampling(const SpecParams& sp, int batch, cudaStream_t stream);
+// Largest vocabulary it takes (its block sums live in 48 KB of shared memory).
+int chain_spec_max_vocab();
+
 // Occupancy of each run kernel (CTAs per SM), for persistent grid sizing.
 int kernel_ctas_per_sm(int kernel, int head_dim, int group, bool bf16, int page_size);
 
