@@ -191,9 +191,16 @@ namespace {
 // The short-query kernel (kDecode) takes every request of at most 16 packed
 // rows on its tensor-core consumer when the group and page size allow, and
 // decode on its CUDA-core consumer otherwise (groups 1, 2, 4).
+// Requests of up to kShortRowsMax packed rows go to the short-query kernel
+// too, in 16-row tiles: each tile reads the request's K/V once, and at two
+// tiles that beats the mma.sync M = 64 kernel's single pass (measured on 8-node
+// tree verify at GQA 4: 32 rows per request).
+constexpr int64_t kShortRowsMax = 32;
+
 int choose_kernel(int32_t q_len_per_req, int32_t g, int64_t max_rows_per_req, int32_t d,
                   int32_t page_size, bool masked) {
-  if (max_rows_per_req <= 16 && fi::decode_mma_supports(d, page_size, g)) return fi::kDecode;
+  if (max_rows_per_req <= kShortRowsMax && fi::decode_mma_supports(d, page_size, g))
+    return fi::kDecode;
   if (masked) {  // the custom mask is read by the short-query and mma.sync kernels
     if (max_rows_per_req <= 16 && g <= 16) return fi::kPrefillM16;
     return g <= 64 ? fi::kPrefillM64 : -1;

@@ -93,3 +93,13 @@ def test_all_ones_mask_equals_no_mask():
     out, lse, _, _, _ = run_masked(pb, True, -1, masks=ones)
     out0, lse0, _ = run_gpu(pb, True, -1, mode="prefill")
     assert torch.equal(out, out0) and torch.equal(lse, lse0)
+
+
+@pytest.mark.parametrize("force", [0, 3])
+def test_tree_verify_two_row_tiles(force):
+    """8 draft nodes at GQA 4 (32 packed rows): two 16-row tiles of the
+    short-query kernel per request."""
+    pb = workloads.tree_verify(batch=6, n_draft=8, kv_lo=40, kv_hi=900)
+    out, lse, kern, mask, mi = run_masked(pb, True, -1, force)
+    assert kern == "decode"
+    check(pb, out, lse, True, -1, mask, mi, what="tree 2 tiles force=%d" % force)

@@ -63,3 +63,17 @@ def test_runs_are_bitwise_reproducible():
     a = run_gpu(pb, False, -1, mode="decode")
     b = run_gpu(pb, False, -1, mode="decode")
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("force", [0, 4])
+@pytest.mark.parametrize("window_left", [-1, 6])
+def test_verify_32_rows_in_two_tiles(force, window_left):
+    """8 draft rows at GQA 4: 32 packed rows, two 16-row tiles per request."""
+    kv = [8, 11, 300, 1200, 77]
+    pb = workloads.make_paged_batch([8] * len(kv), kv, 32, 8, 128, 16, "bf16", 61)
+    out, lse, plan = run_gpu(pb, True, window_left, mode="verify", force_kv_chunks=force,
+                             q_len_per_req=8)
+    info = plan.info()
+    assert info["kernel_name"] == "decode" and info["tile_rows"] == 16
+    assert_close(pb, out, lse, True, window_left, what="verify 32 rows f=%d wl=%d" % (
+        force, window_left))
