@@ -539,6 +539,7 @@ PROFILE_CASES = {
     "longctx_causal": (lambda: workloads.long_context(), True, -1, "prefill"),
     "ragged_prefill_causal": (lambda: workloads.ragged_prefill(), True, -1, "ragged"),
     "tree_verify_b32": (lambda: workloads.tree_verify(batch=32), True, -1, "masked"),
+    "spec_sampling_b64": None,  # the sampling step (spec_sampling_entry)
 }
 
 
@@ -548,6 +549,10 @@ def run_case(args):
     __graft_entry__.build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    if args.case == "spec_sampling_b64":
+        print(json.dumps({"case": args.case,
+                          **spec_sampling_entry(dev, args.steps, peaks()[0])}))
+        return
     make, causal, wl, mode = PROFILE_CASES[args.case]
     pb = make()
     r = Runner(pb, causal, wl, mode, dev)
