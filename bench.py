@@ -167,7 +167,7 @@ class ClockSampler:
 class Runner:
     """One planned workload resident on the device."""
 
-    def __init__(self, pb, causal, wl, mode, dev, force_kv_chunks=0, ws=None):
+    def __init__(self, pb, causal, wl, mode, dev, force_kv_chunks=0, ws=None, graph=False):
         import paged_kv_attention_13_gb300 as fi
         self.fi = fi
         self.pb, self.causal, self.wl, self.mode = pb, causal, wl, mode
@@ -185,10 +185,26 @@ class Runner:
         self.out = torch.empty_like(self.q)
         self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=dev)
         self.ws = ws if ws is not None else torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-        self.plan = fi.Plan(self.ws)
+        T = int(self.q.shape[0])
+        self.plan = fi.Plan(self.ws, enable_graph_capture=graph, max_batch=len(pb.kv_lens),
+                            max_total_rows=T) if graph else fi.Plan(self.ws)
         self.force = force_kv_chunks
         self.do_plan()
         self.flops, self.bytes = accounting(pb, causal or mode == "verify", wl)
+        self.graph = None
+        if graph:  # planned once, captured once, replayed every step
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                for _ in range(2):
+                    self._launch()
+            torch.cuda.current_stream().wait_stream(s)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._launch()
+            torch.cuda.synchronize()
+            self.graph = g
 
     def do_plan(self):
         pb = self.pb
@@ -214,6 +230,12 @@ class Runner:
         self.info = self.plan.info()
 
     def run(self):
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self._launch()
+
+    def _launch(self):
         if self.mode == "masked":
             self.fi.fi_batch_prefill_paged_masked(self.plan, self.q, self.k, self.v, self.idx,
                                                   self.mask, self.pb.sm_scale, out=self.out,
@@ -455,14 +477,16 @@ def other_workloads(args, dev, ws, hbm_peak, bf16_peak):
     res = {}
     steps = max(3, min(args.steps, 10))
 
-    def one(name, pb, causal, wl, mode, force=0, bound="hbm"):
-        r = Runner(pb, causal, wl, mode, dev, force_kv_chunks=force, ws=ws)
+    def one(name, pb, causal, wl, mode, force=0, bound="hbm", graph=False):
+        r = Runner(pb, causal, wl, mode, dev, force_kv_chunks=force, ws=ws, graph=graph)
         ms, med = r.time(steps, 3, flush=r.bytes < (512 << 20))
         tf = r.flops / (ms * 1e-3) / 1e12
         gbs = r.bytes / (ms * 1e-3) / 1e9
         ent = {"ms": round(ms, 4), "TFLOPS": round(tf, 2), "GB/s": round(gbs, 1),
                "kernel": r.info["kernel_name"], "items": r.info["num_items"],
                "chunks": r.info["max_chunks"]}
+        if graph:
+            ent["replay"] = "CUDA graph (planned once, captured, replayed)"
         if bound == "tensor":
             ent["frac_of_bf16_peak"] = round(tf / bf16_peak, 4)
         else:
@@ -471,9 +495,11 @@ def other_workloads(args, dev, ws, hbm_peak, bf16_peak):
         del r
 
     pb = workloads.speculative_verify(batch=32)
-    one("verify_b32", pb, True, -1, "verify")
+    one("verify_b32", pb, True, -1, "verify", graph=True)
+    one("verify_b32_eager", pb, True, -1, "verify")
     pb = workloads.speculative_verify(batch=4)
-    one("verify_b4", pb, True, -1, "verify")
+    one("verify_b4", pb, True, -1, "verify", graph=True)
+    one("verify_b4_eager", pb, True, -1, "verify")
     for P in (16, 1024):
         pb = workloads.batch_prefill(page_size=P)
         one("prefill_p%d_causal" % P, pb, True, -1, "prefill", bound="tensor")

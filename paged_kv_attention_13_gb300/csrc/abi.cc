@@ -7,6 +7,7 @@
 #include "../../include/fi.h"
 
 #include <algorithm>
+#include <functional>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -428,7 +429,52 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
     // balances them), no chunk shorter than min_chunk keys
     int64_t want = (total_len * hk + 2 * grid_cap - 1) / (2 * grid_cap);
     want = std::max<int64_t>(min_chunk, (want + 63) / 64 * 64);
-    if (max_len > want && units < 4 * grid_cap * 4) chunk_len = want;
+    if (max_len > want && units < 4 * grid_cap * 4) {
+      chunk_len = want;
+      // A few long units over many CTAs balance badly when their chunk count
+      // does not fit the grid (8 units of 5 chunks on 19 bundles: 16 bundles
+      // carry 3). Try the chunk lengths that cut the longest unit into
+      // k0 - 3 .. k0 + 4 pieces and keep the one whose static schedule ends
+      // first, counting each split item's partial state (written, then read
+      // by the merge: about 2 x rows keys' worth of traffic).
+      auto makespan = [&](int64_t cl) {
+        std::vector<int64_t> costs;
+        for (const Tile& t : tiles) {
+          const int64_t len = t.hi - t.lo;
+          const int64_t n = (cl > 0 && len > cl) ? (len + cl - 1) / cl : 1;
+          for (int64_t c = 0; c < n; ++c) {
+            const int64_t live = n > 1 ? std::min<int64_t>(cl, len - c * cl) : len;
+            costs.push_back(live * t.rows + 64 + (n > 1 ? 2 * int64_t(t.rows) * t.rows : 0));
+          }
+        }
+        std::sort(costs.begin(), costs.end(), std::greater<int64_t>());
+        const int64_t n_all = int64_t(costs.size()) * hk;
+        const int64_t Gs = std::max<int64_t>(1, P.graph ? grid_cap : std::min<int64_t>(n_all, grid_cap));
+        const int64_t per = (Gs % hk == 0) ? hk : 1;  // CTAs that take one group together
+        const int64_t reps = hk / per;                 // takes per group
+        std::vector<int64_t> heap(size_t(Gs / per), 0);  // min-heap of bin loads
+        int64_t worst = 0;
+        for (int64_t c : costs)
+          for (int64_t r = 0; r < reps; ++r) {
+            std::pop_heap(heap.begin(), heap.end(), std::greater<int64_t>());
+            heap.back() += c;
+            worst = std::max(worst, heap.back());
+            std::push_heap(heap.begin(), heap.end(), std::greater<int64_t>());
+          }
+        return worst;
+      };
+      int64_t best = makespan(want);
+      const int64_t k0 = (max_len + want - 1) / want;
+      for (int64_t k = std::max<int64_t>(2, k0 - 3); k <= k0 + 4; ++k) {
+        const int64_t cl = ((max_len + k - 1) / k + 63) / 64 * 64;
+        if (cl < min_chunk || cl >= max_len || cl == chunk_len) continue;
+        const int64_t m = makespan(cl);
+        if (m < best) {
+          best = m;
+          chunk_len = cl;
+        }
+      }
+    }
     // grow the chunks until the partial states fit the workspace
     while (chunk_len > 0) {
       int64_t ni, np;

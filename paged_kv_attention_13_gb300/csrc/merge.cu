@@ -38,24 +38,89 @@ __device__ __forceinline__ float4 load4(const void* base, int64_t idx) {
   }
 }
 
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
 // Merge states [beg, end) of v [n, H, D] / s [n, H] for one (row, head) into
 // (v_out + out_off, s_out). D is a multiple of 4; lane handles 4-wide columns.
+// The scores and value columns of the first kMB states are loaded together
+// before any arithmetic, and later states kMB at a time, so a row costs about
+// one memory round trip per kMB states rather than one per state and pass.
+constexpr int kMB = 6;
+
 template <int OUT>
 __device__ void merge_one(const float* __restrict__ v, const float* __restrict__ s, int beg,
                           int end, int H, int D, int h, void* v_out, int64_t out_off,
                           float* s_out, int64_t s_off, int lane) {
-  float m = neg_inf();
-  for (int i = beg; i < end; ++i) m = fmaxf(m, __ldg(s + int64_t(i) * H + h));
+  const int n = end - beg;
+  const int c0 = lane * 4;
+  float s0[kMB];
+  float4 x0[kMB];
+#pragma unroll
+  for (int k = 0; k < kMB; ++k) {
+    const bool live = k < n;
+    s0[k] = live ? __ldg(s + int64_t(beg + k) * H + h) : neg_inf();
+    x0[k] = (live && c0 < D)
+                ? *reinterpret_cast<const float4*>(v + (int64_t(beg + k) * H + h) * D + c0)
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float m = s0[0];
+#pragma unroll
+  for (int k = 1; k < kMB; ++k) m = fmaxf(m, s0[k]);
+  if (n > kMB) {  // warp-uniform: the remaining scores, spread over the lanes
+    float mr = neg_inf();
+    for (int i = beg + kMB + lane; i < end; i += 32) mr = fmaxf(mr, __ldg(s + int64_t(i) * H + h));
+    m = fmaxf(m, warp_max(mr));
+  }
   const float mu = (m == neg_inf()) ? 0.f : m;
+  float w0[kMB];
   float den = 0.f;
-  for (int i = beg; i < end; ++i) den += ex2((__ldg(s + int64_t(i) * H + h) - mu) * kLog2e);
+#pragma unroll
+  for (int k = 0; k < kMB; ++k) {
+    w0[k] = ex2((s0[k] - mu) * kLog2e);
+    den += w0[k];
+  }
+  if (n > kMB) {
+    float dr = 0.f;
+    for (int i = beg + kMB + lane; i < end; i += 32)
+      dr += ex2((__ldg(s + int64_t(i) * H + h) - mu) * kLog2e);
+    den += warp_sum(dr);
+  }
   const float inv = den > 0.f ? 1.f / den : 0.f;
-  for (int c = lane * 4; c < D; c += 128) {
+  for (int c = c0; c < D; c += 128) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = beg; i < end; ++i) {
-      const float w = ex2((__ldg(s + int64_t(i) * H + h) - mu) * kLog2e) * inv;
-      const float4 x = *reinterpret_cast<const float4*>(v + (int64_t(i) * H + h) * D + c);
-      acc.x += w * x.x; acc.y += w * x.y; acc.z += w * x.z; acc.w += w * x.w;
+    int i = beg;
+    if (c == c0) {  // the first states' columns are already in registers
+#pragma unroll
+      for (int k = 0; k < kMB; ++k) {
+        const float w = w0[k] * inv;
+        acc.x += w * x0[k].x; acc.y += w * x0[k].y; acc.z += w * x0[k].z; acc.w += w * x0[k].w;
+      }
+      i = beg + kMB;
+    }
+    for (; i < end; i += kMB) {
+      float sk[kMB];
+      float4 xk[kMB];
+#pragma unroll
+      for (int k = 0; k < kMB; ++k) {
+        const bool live = i + k < end;
+        sk[k] = live ? __ldg(s + int64_t(i + k) * H + h) : neg_inf();
+        xk[k] = live ? *reinterpret_cast<const float4*>(v + (int64_t(i + k) * H + h) * D + c)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < kMB; ++k) {
+        const float w = ex2((sk[k] - mu) * kLog2e) * inv;
+        acc.x += w * xk[k].x; acc.y += w * xk[k].y; acc.z += w * xk[k].z; acc.w += w * xk[k].w;
+      }
     }
     store4<OUT>(v_out, out_off + c, acc.x, acc.y, acc.z, acc.w);
   }
@@ -64,11 +129,11 @@ __device__ void merge_one(const float* __restrict__ v, const float* __restrict__
 
 // Workspace partials of a plan -> out / lse (rows listed in merge_rows).
 template <int OUT>
-__global__ void __launch_bounds__(256) merge_workspace_kernel(const void* ws, void* out,
-                                                              float* lse, int H, int D) {
-  // launched as a programmatic dependent of the attention kernel: its launch
-  // overlaps that kernel's tail, and this wait makes the partials visible
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+__global__ void __launch_bounds__(256, 4) merge_workspace_kernel(const void* ws, void* out,
+                                                                 float* lse, int H, int D) {
+  // The plan's metadata (header, merge rows, merge_indptr) was copied in
+  // before the attention kernel started, so the first task's bounds are read
+  // while that kernel is still running.
   const WsHeader* hdr = static_cast<const WsHeader*>(ws);
   const int n_rows = hdr->n_merge_rows;
   const int32_t* merge_indptr = ws_ptr<const int32_t>(ws, hdr->off_merge_indptr);
@@ -78,12 +143,26 @@ __global__ void __launch_bounds__(256) merge_workspace_kernel(const void* ws, vo
   const int lane = threadIdx.x & 31;
   const int64_t total = int64_t(n_rows) * H;
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t wi = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); wi < total;
-       wi += warps) {
-    const int r = int(wi / H), h = int(wi % H);
-    const int t = merge_rows[r];
-    merge_one<OUT>(tmp_o, tmp_lse, merge_indptr[t], merge_indptr[t + 1], H, D, h, out,
-                   (int64_t(t) * H + h) * D, lse, int64_t(t) * H + h, lane);
+  int64_t wi = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  int t = 0, beg = 0, end = 0;
+  if (wi < total) {
+    t = merge_rows[wi / H];
+    beg = merge_indptr[t];
+    end = merge_indptr[t + 1];
+  }
+  // launched as a programmatic dependent of the attention kernel: its launch
+  // overlaps that kernel's tail, and this wait makes the partials visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (; wi < total; wi += warps) {
+    const int h = int(wi % H);
+    merge_one<OUT>(tmp_o, tmp_lse, beg, end, H, D, h, out, (int64_t(t) * H + h) * D, lse,
+                   int64_t(t) * H + h, lane);
+    const int64_t nx = wi + warps;
+    if (nx < total) {
+      t = merge_rows[nx / H];
+      beg = merge_indptr[t];
+      end = merge_indptr[t + 1];
+    }
   }
 }
 

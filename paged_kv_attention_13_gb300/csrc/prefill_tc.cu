@@ -44,11 +44,13 @@ constexpr int kOffQ = 0;              // Q tiles A and B
 constexpr int kOffK = kOffQ + 2 * kTile;  // 2 stages
 constexpr int kOffV = kOffK + 2 * kTile;
 constexpr int kOffBar = kOffV + 2 * kTile;
-constexpr int kSmemTc = kOffBar + 256 + 1024;  // barriers, alignment slack
+constexpr int kOffMl = kOffBar + 256;          // row max and sum handed between warpgroups
+constexpr int kSmemTc = kOffMl + 1024 + 1024;  // barriers, exchange rows, alignment slack
 
 // barrier slots
 constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 4, B_VFULL = 6, B_VEMPTY = 8,
-              B_SFULL = 10, B_PFULL = 12, B_ODONE = 14, B_OFREE = 16, B_FINAL = 18, N_BARS = 19;
+              B_SFULL = 10, B_PFULL = 12, B_ODONE = 14, B_OFREE = 16, B_FINAL = 18,
+              B_MLFULL = 19, B_MLFREE = 20, N_BARS = 21;
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -98,33 +100,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-// 16 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld_tied16(uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.wait::ld.sync.aligned;"
-      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
-        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
-        "+r"(r[14]), "+r"(r[15])
-      :
-      : "memory");
-}
-// 8 packed columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-      : "memory");
 }
 // Wait for outstanding TMEM loads; the registers of `r` are tied to the wait,
 // so no use of them can be scheduled above it.
@@ -217,6 +192,10 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
 // alternates between them - S_A(j+1) and PV_B(j) run while softmax A works,
 // PV_A(j+1) and S_B(j+1) while softmax B works - and P is written back into
 // tensor memory over the S columns it came from.
+// An item of one Q tile and at least two key tiles is split instead: both
+// warpgroups run the same rows, A on the even key tiles and B on the odd
+// ones, each with its own S/P and O in tensor memory, and at the end A
+// combines the two states (m, l, O) by their maxima and writes the output.
 template <bool BF16>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tq,
@@ -265,6 +244,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(BAR(B_OFREE + s), 128);
     }
     mbar_init(BAR(B_FINAL), 1);
+    mbar_init(BAR(B_MLFULL), 128);
+    mbar_init(BAR(B_MLFREE), 128);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -405,12 +386,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(BF16, false, 128, 128);
       constexpr uint32_t kIdO = idesc_f16(BF16, true, 128, 128);
-      auto issue_s = [&](int x, int st) {  // S_x = Q_x K^T
+      // S_x = Q_xq K^T into the S columns of warpgroup x (xq = x, or Q tile
+      // A for both warpgroups of a split item)
+      auto issue_s = [&](int x, int st, int xq) {
         const uint32_t d = tmem + uint32_t(x) * 128u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t koff = uint32_t(kk >> 2) * kBlk + uint32_t(kk & 3) * 32u;
-          const uint64_t ad = sdesc_sw128(sbase + kOffQ + x * kTile + koff, 16, 1024);
+          const uint64_t ad = sdesc_sw128(sbase + kOffQ + xq * kTile + koff, 16, 1024);
           const uint64_t bd = sdesc_sw128(sbase + kOffK + st * kTile + koff, 16, 1024);
           tc_mma(d, ad, bd, kIdS, kk > 0 ? 1u : 0u);
         }
@@ -434,10 +417,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool hasB = G.n_rows > tr;
         const int n = G.n_tiles;
         if (!mbar_wait(BAR(B_QFULL), qc & 1, abort_flag)) { ok = false; break; }
+        if (!hasB && n >= 2) {
+          // split item: key tile j goes to warpgroup j & 1, both on Q tile A
+          for (int j0 = 0; j0 < 2 && ok; ++j0) {
+            const int g0 = gt + j0;
+            if (!mbar_wait(BAR(B_KFULL + (g0 & 1)), (g0 >> 1) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(j0, g0 & 1, 0);
+            tc_commit(BAR(B_KEMPTY + (g0 & 1)));
+          }
+          if (!ok) break;
+          if (n == 2) tc_commit(BAR(B_QEMPTY));
+          for (int j = 0; j < n && ok; ++j) {
+            const int xw = j & 1, jx = j >> 1, g1 = gt + j, st = g1 & 1;
+            if (jx == 0 && itc[xw] > 0 &&
+                !mbar_wait(BAR(B_OFREE + xw), (itc[xw] - 1) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_PFULL + xw), (cnt[xw] + jx) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_VFULL + st), (g1 >> 1) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(xw, st, jx > 0);
+            if (j >= n - 2) tc_commit(BAR(B_ODONE + xw));  // the warpgroup's last tile
+            tc_commit(BAR(B_VEMPTY + st));
+            if (j + 2 < n) {  // tile j + 2 reuses tile j's K stage
+              if (!mbar_wait(BAR(B_KFULL + st), ((g1 + 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+              tc_fence_after();
+              issue_s(xw, st, 0);
+              tc_commit(BAR(B_KEMPTY + st));
+              if (j + 2 == n - 1) tc_commit(BAR(B_QEMPTY));
+            }
+          }
+          gt += n;
+          ++qc;
+          cnt[0] += (n + 1) / 2;
+          cnt[1] += n / 2;
+          ++itc[0];
+          ++itc[1];
+          continue;
+        }
         if (!mbar_wait(BAR(B_KFULL + (gt & 1)), (gt >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        issue_s(0, gt & 1);
-        if (hasB) issue_s(1, gt & 1);
+        issue_s(0, gt & 1, 0);
+        if (hasB) issue_s(1, gt & 1, 1);
         tc_commit(BAR(B_KEMPTY + (gt & 1)));
         if (n == 1) tc_commit(BAR(B_QEMPTY));
         for (int j = 0; j < n && ok; ++j) {
@@ -453,7 +473,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (j + 1 < n) {
             if (!mbar_wait(BAR(B_KFULL + st1), ((g1 + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            issue_s(0, st1);
+            issue_s(0, st1, 0);
             if (!hasB) {
               tc_commit(BAR(B_KEMPTY + st1));
               if (j + 1 == n - 1) tc_commit(BAR(B_QEMPTY));
@@ -468,7 +488,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_commit(BAR(B_VEMPTY + st));
             if (j == n - 1) tc_commit(BAR(B_ODONE + 1));
             if (j + 1 < n) {
-              issue_s(1, st1);
+              issue_s(1, st1, 1);
               tc_commit(BAR(B_KEMPTY + st1));
               if (j + 1 == n - 1) tc_commit(BAR(B_QEMPTY));
             }
@@ -506,17 +526,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool okl = mbar_wait(bar, parity, abort_flag);
       return __all_sync(0xffffffffu, okl);
     };
-    int gt = 0, cnt = 0, itc = 0;
+    float* sml = reinterpret_cast<float*>(smem + kOffMl);  // [2][128]: B's row max, row sum
+    // gt: key tiles of the CTA so far (stage and phase); cnt, itc: S tiles and
+    // items of this warpgroup; itc_b: items of warpgroup B (its O phases);
+    // nsplit: split items (the exchange phases)
+    int gt = 0, cnt = 0, itc = 0, itc_b = 0, nsplit = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       if (items[w].b < 0) continue;  // schedule padding
       const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
       const bool hasB = G.n_rows > tr;
       const int n = G.n_tiles;
-      const int nx = x == 0 ? min(tr, G.n_rows) : max(0, G.n_rows - tr);  // rows of my tile
-      const bool active = n > 0 && (x == 0 || hasB);
+      const bool split = !hasB && n >= 2;
+      const int xr = split ? 0 : x;  // the Q tile whose rows this warpgroup runs
+      const int nx = xr == 0 ? min(tr, G.n_rows) : max(0, G.n_rows - tr);  // rows of that tile
+      const bool active = n > 0 && (x == 0 || hasB || split);
       const bool row_ok = r < nx;
-      const int pr = G.row0 + x * tr + r;
+      const int pr = G.row0 + xr * tr + r;
       const int qi = pr / g;
       const int tok = G.token0 + qi;
       const int head = G.hk * g + pr % g;
@@ -541,13 +567,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int jmin = G.kv_lo, jmax = G.kv_hi - 1;
       if (wl >= 0) jmin = max(jmin, G.lk - G.lq + qi - wl);
       if (causal) jmax = min(jmax, qi + G.lk - G.lq);
-      const int ix0 = (G.row0 + x * tr) / g;              // first / last query row of my tile
-      const int ix1 = (G.row0 + x * tr + nx) / g - 1;
+      const int ix0 = (G.row0 + xr * tr) / g;              // first / last query row of my tile
+      const int ix1 = (G.row0 + xr * tr + nx) / g - 1;
+      // key tiles of this warpgroup: all of them, or every other one (split)
+      const int nt = split ? (n - x + 1) / 2 : n;
       float m_run = neg_inf(), l_run = 0.f;
-      for (int j = 0; j < n; ++j) {
+      for (int jj = 0; jj < nt; ++jj) {
+        const int j = split ? 2 * jj + x : jj;
         const int g1 = gt + j, st = g1 & 1;
         const int t0 = G.t_start + j * 128;
-        if (!wwait(BAR(B_SFULL + x), (cnt + j) & 1)) { ok = false; break; }
+        if (!wwait(BAR(B_SFULL + x), (cnt + jj) & 1)) { ok = false; break; }
         tc_fence_after();
         const bool need_mask = (t0 < G.kv_lo) || (t0 + 128 > G.kv_hi) ||
                                (causal && t0 + 127 > ix0 + G.lk - G.lq) ||
@@ -587,7 +616,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float corr = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
         const float mu = (m_new == neg_inf()) ? 0.f : m_new;
         // O rescale: S_x(j) is complete, so the P V product before it is too
-        if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+        if (jj > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t ov[32];
@@ -599,7 +628,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         bool zeroed = false;
-        if (x == 0 && t0 + 128 > G.lk) {
+        if ((x == 0 || split) && t0 + 128 > G.lk) {  // the tile's first (or only) reader
           // rows of V past the request's last key may hold anything: zero them
           if (!wwait(BAR(B_VFULL + st), (g1 >> 1) & 1)) { ok = false; break; }
           if (t0 + r >= G.lk) {
@@ -640,16 +669,56 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_arrive(BAR(B_PFULL + x));
       }
       if (!ok) break;
-      // epilogue
+      if (split && x == 1) {
+        // hand this warpgroup's row state to A, which reads O_B from tensor
+        // memory and releases it
+        if (nsplit > 0 && !wwait(BAR(B_MLFREE), (nsplit - 1) & 1)) { ok = false; break; }
+        sml[r] = m_run;
+        sml[128 + r] = l_run;
+        mbar_arrive(BAR(B_MLFULL));
+        gt += n;
+        cnt += nt;
+        ++itc;
+        ++nsplit;
+        continue;
+      }
+      // epilogue; for a split item, combine with B's state first:
+      //   m = max(m_A, m_B), O = O_A 2^(m_A - m) + O_B 2^(m_B - m), same for l
+      float fa = 1.f, fb = 0.f;
+      if (split) {
+        if (!wwait(BAR(B_MLFULL), nsplit & 1)) { ok = false; break; }
+        const float mb = sml[r], lb = sml[128 + r];
+        mbar_arrive(BAR(B_MLFREE));
+        const float m = fmaxf(m_run, mb);
+        fa = m_run == neg_inf() ? 0.f : ex2(m_run - m);
+        fb = mb == neg_inf() ? 0.f : ex2(mb - m);
+        l_run = l_run * fa + lb * fb;
+        m_run = m;
+      }
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const float lse = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : neg_inf();
+      fa *= inv;
+      fb *= inv;
       if (!wwait(BAR(B_ODONE + x), itc & 1)) { ok = false; break; }
+      if (split && !wwait(BAR(B_ODONE + 1), itc_b & 1)) { ok = false; break; }
       tc_fence_after();
+      const uint32_t tOb = tmem + lane_addr + 384u;  // O of warpgroup B
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t ov[32];
         tmem_ld32(tO + uint32_t(c) * 32u, ov);
         tmem_wait_ld();
+        if (split) {
+          uint32_t ob[32];
+          tmem_ld32(tOb + uint32_t(c) * 32u, ob);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * fa + __uint_as_float(ob[e]) * fb);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * fa);
+        }
         if (row_ok) {
           if (direct) {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) +
@@ -657,21 +726,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               dst[q] = make_uint4(
-                  DT::pack(__uint_as_float(ov[8 * q + 0]) * inv, __uint_as_float(ov[8 * q + 1]) * inv),
-                  DT::pack(__uint_as_float(ov[8 * q + 2]) * inv, __uint_as_float(ov[8 * q + 3]) * inv),
-                  DT::pack(__uint_as_float(ov[8 * q + 4]) * inv, __uint_as_float(ov[8 * q + 5]) * inv),
-                  DT::pack(__uint_as_float(ov[8 * q + 6]) * inv, __uint_as_float(ov[8 * q + 7]) * inv));
+                  DT::pack(__uint_as_float(ov[8 * q + 0]), __uint_as_float(ov[8 * q + 1])),
+                  DT::pack(__uint_as_float(ov[8 * q + 2]), __uint_as_float(ov[8 * q + 3])),
+                  DT::pack(__uint_as_float(ov[8 * q + 4]), __uint_as_float(ov[8 * q + 5])),
+                  DT::pack(__uint_as_float(ov[8 * q + 6]), __uint_as_float(ov[8 * q + 7])));
           } else {
             float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * 128 + c * 32);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(__uint_as_float(ov[4 * q]) * inv, __uint_as_float(ov[4 * q + 1]) * inv,
-                                   __uint_as_float(ov[4 * q + 2]) * inv, __uint_as_float(ov[4 * q + 3]) * inv);
+              dst[q] = make_float4(__uint_as_float(ov[4 * q]), __uint_as_float(ov[4 * q + 1]),
+                                   __uint_as_float(ov[4 * q + 2]), __uint_as_float(ov[4 * q + 3]));
           }
         }
       }
       tc_fence_before();
       mbar_arrive(BAR(B_OFREE + x));
+      if (split) mbar_arrive(BAR(B_OFREE + 1));  // O_B is read too
       if (row_ok) {
         if (direct) {
           if (p.lse) p.lse[int64_t(tok) * Hq + head] = lse;
@@ -680,8 +750,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       gt += n;
-      cnt += n;
+      cnt += nt;
       ++itc;
+      if (hasB || split) ++itc_b;
+      if (split) ++nsplit;
     }
   }
 
