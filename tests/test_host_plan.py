@@ -267,6 +267,32 @@ def test_schedule_balances_the_persistent_grid():
     assert load.max() / load.mean() < 1.03
 
 
+def _cta_loads(info, kv_lens):
+    items, G = info["items"], info["grid"]
+    load = np.zeros(G)
+    for i, it in enumerate(items):
+        if it[0] >= 0:
+            load[i % G] += max(0, min(int(it[4]), kv_lens[it[0]]) - int(it[3]))
+    return load
+
+
+def test_long_context_split_is_balanced():
+    """A few long units over many CTAs: 8 requests x 8 kv heads of 32768 keys
+    on the 152-CTA tcgen05 grid. The chunk length is chosen by the simulated
+    makespan, so no CTA carries much more than the mean (an even 5-way cut
+    leaves 16 CTAs with a third chunk, 24% above it)."""
+    pb = workloads.long_context()
+    p = _plan()
+    for causal in (True, False):
+        p.plan(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, 16, 64, 8, 128, causal=causal)
+        info = p.info(with_arrays=True)
+        assert info["kernel_name"] == "prefill_m128"
+        load = _cta_loads(info, np.array(pb.kv_lens))
+        assert load.sum() == 8 * 8 * 32768  # every key of every unit, once
+        assert load.max() / load.mean() < 1.05
+        _check_cover(p, pb, causal, -1, 0)
+
+
 # ----------------------------------------------------------- ragged prefill
 
 def _ragged(q_lens, kv_lens, hq=8, hk=2, d=128, seed=3):
