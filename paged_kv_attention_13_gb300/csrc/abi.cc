@@ -432,11 +432,14 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
     if (max_len > want && units < 4 * grid_cap * 4) {
       chunk_len = want;
       // A few long units over many CTAs balance badly when their chunk count
-      // does not fit the grid (8 units of 5 chunks on 19 bundles: 16 bundles
-      // carry 3). Try the chunk lengths that cut the longest unit into
-      // k0 - 3 .. k0 + 4 pieces and keep the one whose static schedule ends
-      // first, counting each split item's partial state (written, then read
-      // by the merge: about 2 x rows keys' worth of traffic).
+      // does not fit the grid (8 units of 5 chunks on 19 bundles: 2 bundles
+      // in 19 carry a third). When the units number at most half the bins,
+      // try the chunk lengths that cut the longest unit into k0 - 3 .. k0 + 4
+      // pieces and keep the one whose static schedule ends first, counting
+      // each split item's partial state (written, then read by the merge:
+      // about 2 x rows keys' worth of traffic). With more units the longest-
+      // first schedule balances them already, and the search (about 3 us per
+      // candidate on 200 groups) is skipped.
       auto makespan = [&](int64_t cl) {
         std::vector<int64_t> costs;
         for (const Tile& t : tiles) {
@@ -463,9 +466,13 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
           }
         return worst;
       };
-      int64_t best = makespan(want);
+      const bool bundled = grid_cap % hk == 0;
+      const int64_t bins = bundled ? grid_cap / hk : grid_cap;
+      const int64_t units_b = int64_t(tiles.size()) * (bundled ? 1 : hk);
+      const bool few = 2 * units_b <= bins;
+      int64_t best = few ? makespan(want) : 0;
       const int64_t k0 = (max_len + want - 1) / want;
-      for (int64_t k = std::max<int64_t>(2, k0 - 3); k <= k0 + 4; ++k) {
+      for (int64_t k = std::max<int64_t>(2, k0 - 3); few && k <= k0 + 4; ++k) {
         const int64_t cl = ((max_len + k - 1) / k + 63) / 64 * 64;
         if (cl < min_chunk || cl >= max_len || cl == chunk_len) continue;
         const int64_t m = makespan(cl);
