@@ -33,26 +33,31 @@ def _check(status: int):
         raise FiError(status, msg)
 
 
+_I64x4 = ctypes.c_int64 * 4
+
+
 def tensor_desc(t: torch.Tensor) -> FiTensor:
     """fi_tensor view of a torch tensor (no copy; strides in elements)."""
-    if t.dim() < 1 or t.dim() > 4:
-        raise ValueError("fi_tensor supports ranks 1..4, got %d" % t.dim())
-    if t.dtype not in _DTYPES:
+    nd = t.dim()
+    if nd < 1 or nd > 4:
+        raise ValueError("fi_tensor supports ranks 1..4, got %d" % nd)
+    code = _DTYPES.get(t.dtype)
+    if code is None:
         raise ValueError("unsupported dtype %s" % t.dtype)
-    d = FiTensor()
-    d.data = t.data_ptr()
-    d.dtype = _DTYPES[t.dtype]
-    d.ndim = t.dim()
-    for i in range(t.dim()):
-        d.shape[i] = t.shape[i]
-        d.stride[i] = t.stride(i)
-    return d
+    # one constructor call: per-field assignment costs several microseconds
+    return FiTensor(t.data_ptr(), code, nd, _I64x4(*t.shape), _I64x4(*t.stride()))
+
+
+_PI32 = ctypes.POINTER(ctypes.c_int32)
 
 
 def _host_i32(x):
     if x is None:
         return None, None
     if isinstance(x, torch.Tensor):
+        if x.dtype == torch.int32 and x.device.type == "cpu" and x.is_contiguous():
+            # already host int32: pass its storage (the caller keeps x alive)
+            return x, ctypes.cast(x.data_ptr(), _PI32)
         x = x.detach().cpu().numpy()
     a = np.ascontiguousarray(np.asarray(x), dtype=np.int32)
     return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
