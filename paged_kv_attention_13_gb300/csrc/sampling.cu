@@ -17,11 +17,13 @@
 // of the drawn row in blocks of 128 tokens, dealt round-robin to its warps
 // (one coalesced 16-byte load per lane per block, eight blocks in flight per
 // warp), summing each block's weight in fp32 into shared memory, and its
-// quarter's total in fp64. After a cluster barrier every CTA reads the four
-// totals through distributed shared memory and finds the quarter that holds
-// u * total; the CTA that owns it scans its block sums (fp64), re-reads the
-// one block that holds the target and writes the outputs. The kernel is bound
-// by the one or two rows of V floats it reads per request. (Weights are
+// quarter's total in fp64 (after a rejection, p's own block sums come from the
+// same pass, for the all-zero-residual fallback). After a cluster barrier
+// every CTA reads the four totals through distributed shared memory and finds
+// the quarter that holds u * total; the CTA that owns it scans its block sums
+// (fp64), re-reads the one block that holds the target and writes the
+// outputs. The kernel is bound by the one or two rows of V floats it reads
+// per request. (Weights are
 // summed in fp32 inside a 128-token block and in fp64 across blocks, so a
 // draw within about 1e-6 of a cumulative boundary may land on the
 // neighbouring token of an all-fp64 sum.)
@@ -103,6 +105,39 @@ __device__ void block_sums(const float* p, const float* q, int V, bool vec, int 
   }
 }
 
+// The residual's block sums into bsum and p's into bsum_p, in one pass over
+// p and q (same arithmetic, in the same order, as block_sums of each); half
+// the unroll, since each block brings two rows' loads.
+constexpr int kUnroll2 = kUnroll / 2;
+__device__ void block_sums_both(const float* p, const float* q, int V, bool vec, int b0, int b1,
+                                float* bsum, float* bsum_p, int warp, int lane) {
+  for (int blk0 = b0 + warp; blk0 < b1; blk0 += kSampWarps * kUnroll2) {
+    float4 a[kUnroll2], c[kUnroll2];
+#pragma unroll
+    for (int u = 0; u < kUnroll2; ++u) {
+      const int blk = blk0 + u * kSampWarps;
+      a[u] = blk < b1 ? lane_weights(p, nullptr, blk, lane, V, vec) : make_float4(0.f, 0.f, 0.f, 0.f);
+      c[u] = blk < b1 ? lane_weights(q, nullptr, blk, lane, V, vec) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll2; ++u) {
+      const float4 r = make_float4(fmaxf(0.f, __fsub_rn(a[u].x, c[u].x)), fmaxf(0.f, __fsub_rn(a[u].y, c[u].y)),
+                                   fmaxf(0.f, __fsub_rn(a[u].z, c[u].z)), fmaxf(0.f, __fsub_rn(a[u].w, c[u].w)));
+      float s = lane_sum(r), sp = lane_sum(a[u]);
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, off));
+        sp = __fadd_rn(sp, __shfl_xor_sync(0xffffffffu, sp, off));
+      }
+      const int blk = blk0 + u * kSampWarps;
+      if (lane == 0 && blk < b1) {
+        bsum[blk - b0] = s;
+        bsum_p[blk - b0] = sp;
+      }
+    }
+  }
+}
+
 // fp64 total of n fp32 values (one warp).
 __device__ double warp_total(const float* v, int n, int lane) {
   double t = 0.0;
@@ -112,7 +147,7 @@ __device__ double warp_total(const float* v, int n, int lane) {
   return t;
 }
 
-__global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kSampThreads)
+__global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kSampThreads, 2)
     chain_spec_kernel(const SpecParams sp) {
   extern __shared__ float bsum[];  // this CTA's block sums (drawn row, then p alone)
   cg::cluster_group cluster = cg::this_cluster();
@@ -159,8 +194,8 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kSampThreads)
                            : nullptr;
   const bool vec = (reinterpret_cast<uintptr_t>(p) % 16 == 0) &&
                    (!q || reinterpret_cast<uintptr_t>(q) % 16 == 0);
-  block_sums(p, q, V, vec, b0, b1, bsum, warp, lane);
-  if (q) block_sums(p, nullptr, V, vec, b0, b1, bsum_p, warp, lane);
+  if (q) block_sums_both(p, q, V, vec, b0, b1, bsum, bsum_p, warp, lane);
+  else block_sums(p, nullptr, V, vec, b0, b1, bsum, warp, lane);
   __syncthreads();
   if (warp == 0) {
     const double t0 = warp_total(bsum, mb, lane);
