@@ -222,8 +222,8 @@ fi_status fi_batch_decode_paged(fi_plan_t plan, const fi_tensor* q, const fi_ten
  *                Lq_b * Lk_b bits (query row i, key j at bit i * Lk_b + j,
  *                least significant bit of each byte first), so
  *                mask_indptr[b+1] - mask_indptr[b] >= ceil(Lq_b * Lk_b / 8).
- * Masked plans run on the short-query kernel (at most 16 packed rows per
- * request) or on the mma.sync kernels. FI_ERR_INVALID_ARG for a segment
+ * Masked plans run on the short-query kernel (at most 32 packed rows per
+ * request, in 16-row tiles) or on the mma.sync kernels. FI_ERR_INVALID_ARG for a segment
  * shorter than its request's bits or a decreasing mask_indptr.
  *
  * fi_batch_prefill_paged_masked: as fi_batch_prefill_paged, plus

@@ -190,7 +190,7 @@ extern "C" void fi_plan_destroy(fi_plan_t p) {
 namespace {
 
 // The short-query kernel (kDecode) takes every request of at most 16 packed
-// rows on its tensor-core consumer when the group and page size allow, and
+// rows (one tile) on its tensor-core consumer when the group and page size allow, and
 // decode on its CUDA-core consumer otherwise (groups 1, 2, 4).
 // Requests of up to kShortRowsMax packed rows go to the short-query kernel
 // too, in 16-row tiles: each tile reads the request's K/V once, and at two

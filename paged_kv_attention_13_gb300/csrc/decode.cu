@@ -1,14 +1,14 @@
 // Short-query attention kernels (decode, speculative verify, and any request
-// of at most 16 packed rows: query row x head of the GQA group), against
-// the paged KV. Bandwidth-bound: every K/V byte is read exactly once, the
-// online softmax is kept in fp32.
+// of at most 32 packed rows, in 16-row tiles: query row x head of the GQA
+// group), against the paged KV. Bandwidth-bound: every K/V byte is read
+// exactly once, the online softmax is kept in fp32.
 //
 // Work item = (request tile, kv head, key chunk). One producer warp streams
 // the item's live keys through a ring of stages in shared memory: per page
 // of a stage it issues one cp.async.bulk.tensor box of K and one of V (4-D
 // maps over [pages, slot, kv head, dim]), and for an item's first stage its
 // q rows by plain bulk copy into a q buffer. mbarriers hand the stages to the
-// consumer warps and back; each stage carries a 64-byte header with the
+// consumer warps and back; each stage carries an 80-byte header with the
 // item's geometry, so consumer warps read no global memory before they write
 // the output. The producer runs ahead across work items, so the ring stays
 // full through item boundaries.
