@@ -242,6 +242,54 @@ def test_decode_split_cover_and_long_context_split():
             assert p.info()["max_chunks"] == forced
 
 
+def _meta_batch(ql, kl, hq, hk, P):
+    """Plan metadata only (no tensors): qo/kv indptr, last_page_len, kv_lens."""
+    from types import SimpleNamespace
+    pages = [(k + P - 1) // P for k in kl]
+    return SimpleNamespace(
+        qo_indptr=torch.tensor(np.concatenate([[0], np.cumsum(ql)]), dtype=torch.int32),
+        kv_indptr=torch.tensor(np.concatenate([[0], np.cumsum(pages)]), dtype=torch.int32),
+        last_page_len=torch.tensor([k - (n - 1) * P if n else 0 for k, n in zip(kl, pages)],
+                                   dtype=torch.int32),
+        kv_lens=list(kl), num_qo_heads=hq, num_kv_heads=hk)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_plans_are_exact_covers(seed):
+    """Seeded random batches through every planning path (prefill on each
+    kernel, decode, verify, forced and planner-chosen splits, few long units
+    that take the chunk-length search): the work list covers every
+    (request, row tile, kv head) once and each tile's chunks partition its
+    live key range."""
+    rng = np.random.default_rng(7000 + seed)
+    hk = int(rng.choice([1, 2, 8]))
+    g = int(rng.choice([1, 4, 8]))
+    d = int(rng.choice([64, 128]))
+    B = int(rng.integers(1, 12))
+    mode = ["prefill", "decode", "verify", "long"][seed % 4]
+    causal = bool(rng.integers(0, 2)) or mode == "verify"
+    wl = int(rng.choice([-1, -1, 0, 37, 500]))
+    forced = int(rng.choice([0, 0, 3]))
+    if mode == "long":  # few long units: the makespan-chosen chunk length
+        kl = [int(rng.integers(20000, 40000))] * B
+        ql = [int(rng.integers(1, 17))] * B
+    else:
+        kl = [int(x) for x in rng.integers(1, 3000, size=B)]
+        ql = [1] * B if mode == "decode" else (
+            [4] * B if mode == "verify" else [int(x) for x in rng.integers(1, 400, size=B)])
+    if causal:
+        kl = [max(k, q) for k, q in zip(kl, ql)]
+    pb = _meta_batch(ql, kl, g * hk, hk, 16)
+    p = _plan()
+    if mode in ("decode", "verify"):
+        p.plan(None, pb.kv_indptr, pb.last_page_len, 16, g * hk, hk, d, causal=causal,
+               window_left=wl, q_len_per_req=ql[0], force_kv_chunks=forced)
+    else:
+        p.plan(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, 16, g * hk, hk, d, causal=causal,
+               window_left=wl, force_kv_chunks=forced)
+    _check_cover(p, pb, causal or mode == "verify", wl, forced)
+
+
 def test_workspace_bytes_grows_with_chunks():
     a = fi.workspace_bytes(64, 64, 32, 128, 1)
     b = fi.workspace_bytes(64, 64, 32, 128, 32)
