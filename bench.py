@@ -76,9 +76,9 @@ def accounting(pb, causal, wl):
         hi = np.minimum(lk - 1, i + lk - lq) if causal else np.full(lq, lk - 1)
         lo = np.maximum(0, lk - lq + i - wl) if wl >= 0 else np.zeros(lq, np.int64)
         live = np.zeros(lk, bool)
-        for a, b in zip(lo, hi):
-            if b >= a:
-                live[a:b + 1] = True
+        for r0, r1 in zip(lo, hi):
+            if r1 >= r0:
+                live[r0:r1 + 1] = True
         n_live = int(live.sum())
         kv_rows += n_live
         pages += len({j // pb.page_size for j in np.nonzero(live)[0]}) if n_live < lk else \
