@@ -438,3 +438,40 @@ def test_masked_and_unmasked_plans_do_not_cross():
     with pytest.raises(fi.FiError) as e:
         fi.fi_batch_prefill_paged_masked(p2, *args, pb.extra["mask"], 0.1, out=out)
     assert _status(e) == "FI_ERR_PLAN_MISMATCH"
+
+
+def test_plan_metadata_inputs_are_equivalent():
+    """The binding takes host metadata as int32/int64 tensors (contiguous or
+    not), numpy arrays or lists; every form gives the same plan."""
+    pb = workloads.speculative_verify(batch=8, kv_lo=64, kv_hi=900)
+    base = pb.kv_indptr.to(torch.int32)
+    last = pb.last_page_len.to(torch.int32)
+    forms = [
+        (base, last),
+        (base.to(torch.int64), last.to(torch.int64)),
+        (base.numpy(), last.numpy()),
+        (base.tolist(), last.tolist()),
+        (torch.stack([base, base], 1)[:, 0], torch.stack([last, last], 1)[:, 1]),  # strided
+    ]
+    ref = None
+    for kv, lp in forms:
+        p = _plan()
+        p.plan(None, kv, lp, 16, 32, 8, 128, causal=True, q_len_per_req=4)
+        info = p.info(with_arrays=True)
+        got = (info["items"].tobytes(), info["merge_indptr"].tobytes(), info["grid"])
+        if ref is None:
+            ref = got
+        assert got == ref
+
+
+def test_tensor_desc_shapes_and_strides():
+    t = torch.zeros((5, 3, 4, 8), dtype=torch.bfloat16)
+    d = fi.tensor_desc(t.permute(0, 2, 1, 3))
+    assert d.ndim == 4 and list(d.shape) == [5, 4, 3, 8] and list(d.stride) == [96, 8, 32, 1]
+    assert d.data == t.data_ptr()
+    d = fi.tensor_desc(torch.zeros(7, dtype=torch.int32))
+    assert d.ndim == 1 and list(d.shape) == [7, 0, 0, 0] and list(d.stride) == [1, 0, 0, 0]
+    with pytest.raises(ValueError):
+        fi.tensor_desc(torch.zeros((1, 1, 1, 1, 1)))
+    with pytest.raises(ValueError):
+        fi.tensor_desc(torch.zeros(3, dtype=torch.float64))
