@@ -634,9 +634,13 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
       }
     }
   }
-  for (int32_t t = 0; t < ns.total_rows; ++t) {
-    ns.merge_indptr[t + 1] = ns.merge_indptr[t] + merge_count[t];
-    if (merge_count[t] > 1) ns.merge_rows.push_back(t);
+  if (partial_cursor > 0) {  // else merge_indptr stays all zero (no row is split)
+    int32_t acc = 0;  // running sum in a register: no store-to-load chain
+    for (int32_t t = 0; t < ns.total_rows; ++t) {
+      acc += merge_count[t];
+      ns.merge_indptr[t + 1] = acc;
+      if (merge_count[t] > 1) ns.merge_rows.push_back(t);
+    }
   }
   ns.n_partials = partial_cursor;
   ns.max_chunks = max_chunks;
