@@ -46,3 +46,21 @@ def test_status_strings():
     lib = fi.load()
     assert lib.fi_status_str(0) == b"FI_OK"
     assert lib.fi_status_str(4) == b"FI_ERR_GQA_INDIVISIBLE"
+
+
+def test_plain_c_caller(tmp_path):
+    """The header compiles as C99 (no CUDA headers) and a C program can plan
+    and read refusals through libfi.so without a GPU (tests/c_abi_host.c)."""
+    import shutil
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(fi._lib.LIB_PATH)
+    exe = str(tmp_path / "c_abi_host")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), os.path.join(ROOT, "tests", "c_abi_host.c"),
+                        "-o", exe, "-L", libdir, "-lfi", "-Wl,-rpath," + libdir],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and "c abi ok" in r.stdout, r.stdout + r.stderr
