@@ -41,6 +41,27 @@
  *   - Errors are return codes; nothing aborts or traps. fi_last_error() gives
  *     a thread-local message naming the field, the expected value and the
  *     value given [P3 "Plan-vs-run shapes"].
+ *   - Stream order between a plan and its runs (outside stream capture) is
+ *     kept by the library: a run() on another stream than the one fi_plan()
+ *     uploaded on waits for that upload, a run() on another stream than the
+ *     plan's previous run() waits for that run (the runs of one plan share its
+ *     split-KV scratch), and fi_plan() waits for the plan's latest run() before
+ *     it overwrites the workspace. A run() captured in a CUDA graph reads the
+ *     plan that the workspace holds when the graph is launched: launch the
+ *     graph on the stream that re-plans, or order the two yourself, and do not
+ *     re-plan on another stream while a launch of the graph is in flight
+ *     [P2 "Architecture / design notes"]. fi_plan() itself refuses a stream
+ *     that is capturing.
+ *   - Kernel configuration (the dynamic shared-memory limit) is applied once
+ *     per device at the first run() there; make that first run() before any
+ *     capture on that device.
+ *   - Environment, read once per process: FI_LOG=1 prints every refusal and
+ *     CUDA failure on stderr, 2 also each committed plan (kernel, tile rows,
+ *     items, chunks, grid), 3 also each run() launch; unset or 0 prints
+ *     nothing. FI_CHECK_INDICES=1 makes every paged run() check the plan's
+ *     page-table entries on the device first (see fi_check_kv_indices); a run
+ *     whose table fails does no attention work and fi_plan_device_error
+ *     reports it.
  */
 #ifndef FI_H_
 #define FI_H_
@@ -327,15 +348,41 @@ fi_status fi_plan_get_info(fi_plan_t plan, fi_plan_info* info, int32_t* items,
 fi_status fi_plan_read_device(fi_plan_t plan, int32_t* items, int32_t items_capacity,
                               int32_t* merge_indptr, int32_t merge_capacity, void* stream);
 
-/* Read the device error flag of the plan's workspace (synchronises the
- * stream). A kernel sets it when one of its bounded waits on an mbarrier
- * expired (2 s): it then gives up the rest of its work, waits (bounded) for
- * its own copies in flight and exits, so the context stays usable but that
- * launch's output is not valid. *err_flag receives 0 (no expiry since the
- * last fi_plan or clear) or 1. clear != 0 resets the flag afterwards. Errors:
- * FI_ERR_INVALID_ARG (NULL plan or pointer, host-only plan),
- * FI_ERR_NOT_PLANNED, FI_ERR_CUDA. */
+/* Read the device error flags of the plan's workspace (ordered after the
+ * plan's latest upload and run(); synchronises the stream). *err_flag is a bit
+ * set, 0 when nothing went wrong since the last fi_plan or clear:
+ *   1  a kernel's bounded wait on an mbarrier expired (2 s, or the limit of
+ *      fi_plan_set_wait_limit): the kernel gave up the rest of its work,
+ *      waited (bounded) for its own copies and tensor-core work in flight and
+ *      exited, so the context stays usable but that launch's output is not
+ *      valid;
+ *   2  the page-table check (fi_check_kv_indices, or FI_CHECK_INDICES) found
+ *      entries outside the cache; the attention work of the run it guarded
+ *      was not done.
+ * clear != 0 resets both afterwards. Errors: FI_ERR_INVALID_ARG (NULL plan or
+ * pointer, host-only plan), FI_ERR_NOT_PLANNED, FI_ERR_CUDA. */
 fi_status fi_plan_device_error(fi_plan_t plan, int32_t* err_flag, int clear, void* stream);
+
+/* Limit, in nanoseconds, of every bounded wait on an mbarrier in the plan's
+ * kernels, from the next fi_plan on; 0 restores the default of 2 s. A small
+ * limit makes waits expire on purpose, which is how the failure path (abort,
+ * drain, error flag, usable context) is tested; the waits that drain a CTA's
+ * own copies and tensor-core work before it exits always keep the 2 s limit.
+ * Errors: FI_ERR_INVALID_ARG (NULL plan). */
+fi_status fi_plan_set_wait_limit(fi_plan_t plan, uint64_t limit_ns);
+
+/* Range check of the plan's page table on the device ([P2 "Review notes"]: a
+ * wrong page table or indptr becomes a memory fault; [P3 "What changed"]).
+ * Counts the entries kv_indices[0 .. kv_indptr[batch]) outside
+ * [0, num_pages) into the plan's workspace, where fi_plan_device_error reads
+ * them as bit 2 and where the attention kernels of a run read them and then
+ * do no work. Launches one small kernel on `stream`, never traps; the count
+ * stays until the next check, fi_plan or clear. kv_indices: device int32,
+ * contiguous, at least kv_indptr[batch] entries; num_pages: pages in the K/V
+ * cache. Errors: FI_ERR_INVALID_ARG, FI_ERR_NOT_PLANNED, FI_ERR_PLAN_MISMATCH
+ * (a ragged plan, or a table shorter than planned), FI_ERR_CUDA. */
+fi_status fi_check_kv_indices(fi_plan_t plan, const fi_tensor* kv_indices, int64_t num_pages,
+                              void* stream);
 
 /*
  * Batch decode that allocates nothing (the pages have no counterpart; this is
@@ -375,6 +422,12 @@ fi_status fi_batch_decode_paged_noalloc(const fi_tensor* q, const fi_tensor* k_c
                                         fi_tensor* out, fi_tensor* lse, void* stream);
 /* Size of the fixed scratch array behind fi_batch_decode_paged_noalloc. */
 size_t fi_noalloc_scratch_bytes(void);
+/* Error flag of the latest fi_batch_decode_paged_noalloc on the current device
+ * (the flag belongs to that call; the next call clears it): 1 when one of its
+ * bounded waits expired and its out / lse are not valid, else 0 (also before
+ * the first call). clear != 0 resets it. Synchronises `stream`; allocates
+ * nothing. Errors: FI_ERR_INVALID_ARG (NULL err_flag), FI_ERR_CUDA. */
+fi_status fi_noalloc_device_error(int32_t* err_flag, int clear, void* stream);
 /* Thread-local message of the last refusal of fi_batch_decode_paged_noalloc. */
 const char* fi_noalloc_last_error(void);
 

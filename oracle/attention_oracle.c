@@ -31,6 +31,47 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/*
+ * Accumulation type. The parity oracle is the default build: fp64, single
+ * thread. The same source is compiled a second time as the timed CPU
+ * baseline with -DORC_ACC_FLOAT (fp32 accumulation, expf / logf) and OpenMP
+ * over the selected rows; every row is still computed by one thread, in the
+ * same order of operations, so the fp64 build's results are those of the
+ * plain loops below.
+ */
+#ifdef ORC_ACC_FLOAT
+typedef float orc_acc;
+#define ORC_EXP expf
+#define ORC_LOG logf
+#else
+typedef double orc_acc;
+#define ORC_EXP exp
+#define ORC_LOG log
+#endif
+
+/* Threads the row loop may use (the OpenMP build; 1 otherwise). */
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+int oracle_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* 1 in the fp32-accumulate build, 0 in the fp64 parity build. */
+int oracle_acc_is_float(void) { return (int)(sizeof(orc_acc) == sizeof(float)); }
 
 enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2 };
 
@@ -129,10 +170,21 @@ int oracle_attention_rows(const void* q, int q_dtype, const void* k_cache,
     int64_t lk = oracle_kv_len(kv_indptr, last_page_len, b, page_size);
     if (lk > max_lk) max_lk = lk;
   }
-  double* s = (double*)malloc(sizeof(double) * (size_t)(max_lk > 0 ? max_lk : 1));
-  if (!s) return -1;
+  int bad = 0;
 
+#pragma omp parallel
+  {
+  /* per-thread scratch: the scores of one row and its output accumulator */
+  orc_acc* s = (orc_acc*)malloc(sizeof(orc_acc) * (size_t)(max_lk > 0 ? max_lk : 1));
+  orc_acc* o = (orc_acc*)malloc(sizeof(orc_acc) * (size_t)(d > 0 ? d : 1));
+  if (!s || !o) {
+#pragma omp atomic write
+    bad = 1;
+  }
+
+#pragma omp for schedule(dynamic, 4)
   for (int64_t r = 0; r < n_sel; ++r) {
+    if (!s || !o) continue;
     const int64_t t = sel_token[r];
     const int32_t h = sel_head[r];
     /* the request that owns token t */
@@ -140,44 +192,56 @@ int oracle_attention_rows(const void* q, int q_dtype, const void* k_cache,
     for (int32_t bb = 0; bb < batch; ++bb) {
       if (t >= qo_indptr[bb] && t < qo_indptr[bb + 1]) { b = bb; break; }
     }
-    if (b < 0 || h < 0 || h >= num_qo_heads) { free(s); return -1; }
+    if (b < 0 || h < 0 || h >= num_qo_heads) {
+#pragma omp atomic write
+      bad = 1;
+      continue;
+    }
     const int64_t lq = (int64_t)qo_indptr[b + 1] - qo_indptr[b];
     const int64_t lk = oracle_kv_len(kv_indptr, last_page_len, b, page_size);
     const int64_t i = t - qo_indptr[b];
     const int32_t hk = h / group;
     const int64_t q_off = (t * num_qo_heads + h) * d;
 
-    double m = -INFINITY;
+    orc_acc m = -INFINITY;
     for (int64_t j = 0; j < lk; ++j) {
       s[j] = -INFINITY;
       if (!oracle_key_valid(i, j, lq, lk, causal, window_left)) continue;
       if (custom_mask && !oracle_custom_bit(custom_mask, mask_indptr, b, i, j, lk)) continue;
       const int64_t page = kv_indices[kv_indptr[b] + j / page_size];
       const int64_t k_off = page * page_stride_kv + (j % page_size) * tok_stride_kv + hk * d;
-      double dot = 0.0;
+      orc_acc dot = 0;
       for (int64_t c = 0; c < d; ++c)
-        dot += orc_load(q, q_dtype, q_off + c) * orc_load(k_cache, kv_dtype, k_off + c);
-      s[j] = sm_scale * dot;
+        dot += (orc_acc)orc_load(q, q_dtype, q_off + c) *
+               (orc_acc)orc_load(k_cache, kv_dtype, k_off + c);
+      s[j] = (orc_acc)sm_scale * dot;
       if (s[j] > m) m = s[j];
     }
-    double* o = o_out + r * d;
-    for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
-    if (m == -INFINITY) { lse_out[r] = -INFINITY; continue; }
-    double sum = 0.0;
+    for (int64_t c = 0; c < d; ++c) o[c] = 0;
+    double* o_row = o_out + r * d;
+    if (m == -INFINITY) {
+      for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
+      lse_out[r] = -INFINITY;
+      continue;
+    }
+    orc_acc sum = 0;
     for (int64_t j = 0; j < lk; ++j)
-      if (s[j] != -INFINITY) sum += exp(s[j] - m);
-    const double lse = m + log(sum);
-    lse_out[r] = lse;
+      if (s[j] != -INFINITY) sum += ORC_EXP(s[j] - m);
+    const orc_acc lse = m + ORC_LOG(sum);
+    lse_out[r] = (double)lse;
     for (int64_t j = 0; j < lk; ++j) {
       if (s[j] == -INFINITY) continue;
-      const double w = exp(s[j] - lse);
+      const orc_acc w = ORC_EXP(s[j] - lse);
       const int64_t page = kv_indices[kv_indptr[b] + j / page_size];
       const int64_t v_off = page * page_stride_kv + (j % page_size) * tok_stride_kv + hk * d;
-      for (int64_t c = 0; c < d; ++c) o[c] += w * orc_load(v_cache, kv_dtype, v_off + c);
+      for (int64_t c = 0; c < d; ++c) o[c] += w * (orc_acc)orc_load(v_cache, kv_dtype, v_off + c);
     }
+    for (int64_t c = 0; c < d; ++c) o_row[c] = (double)o[c];
   }
   free(s);
-  return 0;
+  free(o);
+  }
+  return bad ? -1 : 0;
 }
 
 /*

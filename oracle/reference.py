@@ -7,32 +7,59 @@ oracle reads exactly the quantised values the GPU reads.
 import ctypes
 import numpy as np
 
-from .build import build_oracle
+from .build import build_oracle, build_oracle_fp32omp
 
 _DT = {"f16": 0, "bf16": 1, "f32": 2}
 _lib = None
+_lib_fast = None
+
+
+def _bind(lib):
+    P = ctypes.c_void_p
+    i32, i64, dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+    lib.oracle_attention_rows.restype = ctypes.c_int
+    lib.oracle_attention_rows.argtypes = [
+        P, ctypes.c_int, P, P, ctypes.c_int, P, P, P, P, i32, i32, i32, i32, i32,
+        ctypes.c_int, i32, dbl, i64, P, P, P, P, P, P]
+    lib.oracle_custom_bit.restype = ctypes.c_int
+    lib.oracle_custom_bit.argtypes = [P, P, i32, i64, i64, i64]
+    lib.oracle_merge_states.restype = None
+    lib.oracle_merge_states.argtypes = [P, P, i64, i64, i64, P, P]
+    lib.oracle_kv_len.restype = i64
+    lib.oracle_kv_len.argtypes = [P, P, i32, i32]
+    lib.oracle_key_valid.restype = ctypes.c_int
+    lib.oracle_key_valid.argtypes = [i64, i64, i64, i64, ctypes.c_int, i64]
+    lib.oracle_set_threads.restype = None
+    lib.oracle_set_threads.argtypes = [ctypes.c_int]
+    lib.oracle_threads.restype = ctypes.c_int
+    lib.oracle_threads.argtypes = []
+    lib.oracle_acc_is_float.restype = ctypes.c_int
+    lib.oracle_acc_is_float.argtypes = []
+    return lib
 
 
 def _load():
+    """The fp64 parity build."""
     global _lib
     if _lib is None:
-        lib = ctypes.CDLL(build_oracle())
-        P = ctypes.c_void_p
-        i32, i64, dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
-        lib.oracle_attention_rows.restype = ctypes.c_int
-        lib.oracle_attention_rows.argtypes = [
-            P, ctypes.c_int, P, P, ctypes.c_int, P, P, P, P, i32, i32, i32, i32, i32,
-            ctypes.c_int, i32, dbl, i64, P, P, P, P, P, P]
-        lib.oracle_custom_bit.restype = ctypes.c_int
-        lib.oracle_custom_bit.argtypes = [P, P, i32, i64, i64, i64]
-        lib.oracle_merge_states.restype = None
-        lib.oracle_merge_states.argtypes = [P, P, i64, i64, i64, P, P]
-        lib.oracle_kv_len.restype = i64
-        lib.oracle_kv_len.argtypes = [P, P, i32, i32]
-        lib.oracle_key_valid.restype = ctypes.c_int
-        lib.oracle_key_valid.argtypes = [i64, i64, i64, i64, ctypes.c_int, i64]
-        _lib = lib
+        _lib = _bind(ctypes.CDLL(build_oracle()))
     return _lib
+
+
+def _load_fast():
+    """The fp32-accumulate OpenMP build of the same source (timed baseline)."""
+    global _lib_fast
+    if _lib_fast is None:
+        _lib_fast = _bind(ctypes.CDLL(build_oracle_fp32omp()))
+    return _lib_fast
+
+
+def fp32omp_threads(n=None):
+    """Set (when n is given) and return the thread count of the timed build."""
+    lib = _load_fast()
+    if n is not None:
+        lib.oracle_set_threads(int(n))
+    return int(lib.oracle_threads())
 
 
 def _ptr(a):
@@ -73,8 +100,10 @@ def custom_bit(custom_mask, mask_indptr, b, i, j, lk):
 
 def attention_rows(q, k_cache, v_cache, kv_indices, qo_indptr, kv_indptr, last_page_len,
                    page_size, causal, window_left, sm_scale, sel_token, sel_head,
-                   dtype="bf16", custom_mask=None, mask_indptr=None):
+                   dtype="bf16", custom_mask=None, mask_indptr=None, fp32omp=False):
     """fp64 (o [n, d], lse [n]) for rows (sel_token[r], sel_head[r]).
+    fp32omp=True runs the timed baseline build instead (fp32 accumulation,
+    OpenMP over the rows); its results are not the parity oracle's.
 
     q [T, Hq, d]; k_cache/v_cache [num_pages, P, Hk, d]. Arrays are float32,
     float16, or uint16/int16 raw bits of ``dtype`` ("bf16" or "f16").
@@ -102,7 +131,8 @@ def attention_rows(q, k_cache, v_cache, kv_indices, qo_indptr, kv_indptr, last_p
     if custom_mask is not None:
         cm = _c(custom_mask, np.uint8)
         mi = _c(mask_indptr, np.int64)
-    rc = _load().oracle_attention_rows(
+    lib = _load_fast() if fp32omp else _load()
+    rc = lib.oracle_attention_rows(
         _ptr(q), _DT[q_dt], _ptr(k_cache), _ptr(v_cache), _DT[kv_dt], _ptr(kv_indices),
         _ptr(qo_indptr), _ptr(kv_indptr), _ptr(last_page_len), len(qo_indptr) - 1,
         page_size, Hq, Hk, d, int(bool(causal)), int(window_left), float(sm_scale), n,

@@ -26,6 +26,7 @@ EXPORTED = [
     "fi_batch_decode_paged_noalloc", "fi_noalloc_scratch_bytes", "fi_noalloc_last_error",
     "fi_plan_device_error", "fi_plan_ragged", "fi_batch_prefill_ragged", "fi_plan_masked",
     "fi_batch_prefill_paged_masked", "fi_chain_speculative_sampling",
+    "fi_plan_set_wait_limit", "fi_check_kv_indices", "fi_noalloc_device_error",
 ]
 
 
@@ -89,6 +90,12 @@ def load():
     lib.fi_batch_prefill_ragged.argtypes = [P, PT, PT, PT, ctypes.c_float, PT, PT, P]
     lib.fi_plan_device_error.restype = ctypes.c_int
     lib.fi_plan_device_error.argtypes = [P, pi32, ctypes.c_int, P]
+    lib.fi_plan_set_wait_limit.restype = ctypes.c_int
+    lib.fi_plan_set_wait_limit.argtypes = [P, ctypes.c_uint64]
+    lib.fi_check_kv_indices.restype = ctypes.c_int
+    lib.fi_check_kv_indices.argtypes = [P, PT, ctypes.c_int64, P]
+    lib.fi_noalloc_device_error.restype = ctypes.c_int
+    lib.fi_noalloc_device_error.argtypes = [pi32, ctypes.c_int, P]
     lib.fi_plan_destroy.restype = None
     lib.fi_plan_destroy.argtypes = [P]
     lib.fi_last_error.restype = ctypes.c_char_p

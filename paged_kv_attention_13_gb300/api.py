@@ -189,12 +189,25 @@ class Plan:
 
 
     def device_error(self, clear=False, stream=None) -> int:
-        """fi_plan_device_error: 1 when a kernel run on this plan's workspace
-        gave up an expired bounded wait since the last plan / clear, else 0."""
+        """fi_plan_device_error: a bit set, 0 when nothing went wrong since the
+        last plan / clear; 1 = a kernel gave up an expired bounded wait, 2 =
+        the page-table check found entries outside the cache."""
         v = ctypes.c_int32(0)
         _check(self._lib.fi_plan_device_error(self.handle, ctypes.byref(v), int(bool(clear)),
                                               _stream_handle(stream)))
         return int(v.value)
+
+    def set_wait_limit(self, limit_ns: int):
+        """fi_plan_set_wait_limit: the bounded-wait limit of this plan's kernels
+        from the next plan on (0 = the default 2 s)."""
+        _check(self._lib.fi_plan_set_wait_limit(self.handle, int(limit_ns)))
+
+    def check_kv_indices(self, kv_indices, num_pages: int, stream=None):
+        """fi_check_kv_indices: count page-table entries outside [0, num_pages)
+        on the device (read back with device_error(), bit 2)."""
+        d = tensor_desc(kv_indices)
+        _check(self._lib.fi_check_kv_indices(self.handle, ctypes.byref(d), int(num_pages),
+                                             _stream_handle(stream)))
 
 
 def fi_plan(plan: Plan, *args, **kwargs) -> Plan:
@@ -318,23 +331,36 @@ def fi_merge_states(v, s, merge_indptr, rows, v_out=None, s_out=None, out_dtype=
 
 def fi_batch_decode_paged_noalloc(q, k_cache, v_cache, kv_indices, kv_indptr, last_page_len,
                                   sm_scale, window_left=-1, kv_chunks=4, out=None, lse=None,
-                                  stream=None):
+                                  return_lse=True, stream=None):
     """Batch decode whose split-KV scratch is a fixed device array inside the
     library: the call itself allocates no device memory (``out``/``lse`` are
-    allocated here only when not passed). kv_indptr / last_page_len are device
-    int32 tensors; the batch is ``len(kv_indptr) - 1``."""
+    allocated here only when not passed; with ``return_lse=False`` no lse is
+    written and NULL is passed). kv_indptr / last_page_len are device int32
+    tensors; the batch is ``len(kv_indptr) - 1``."""
     lib = _lib.load()
     batch = kv_indptr.shape[0] - 1
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
-    if lse is None:
+    if lse is None and return_lse:
         lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
     descs = [tensor_desc(t) for t in (q, k_cache, v_cache, kv_indices)]
-    od, ld = tensor_desc(out), tensor_desc(lse)
+    od = tensor_desc(out)
+    ld = tensor_desc(lse) if lse is not None else None
     st = lib.fi_batch_decode_paged_noalloc(
         *[ctypes.byref(d) for d in descs], kv_indptr.data_ptr(), last_page_len.data_ptr(),
         int(batch), int(window_left), int(kv_chunks), ctypes.c_float(sm_scale), ctypes.byref(od),
-        ctypes.byref(ld), _stream_handle(stream))
+        ctypes.byref(ld) if ld is not None else None, _stream_handle(stream))
     if st != _lib.FI_OK:
         raise FiError(st, lib.fi_noalloc_last_error().decode(errors="replace"))
     return out, lse
+
+
+def fi_noalloc_device_error(clear=False, stream=None) -> int:
+    """fi_noalloc_device_error: 1 when the latest no-allocation decode on the
+    current device gave up an expired bounded wait, else 0."""
+    lib = _lib.load()
+    v = ctypes.c_int32(0)
+    st = lib.fi_noalloc_device_error(ctypes.byref(v), int(bool(clear)), _stream_handle(stream))
+    if st != _lib.FI_OK:
+        raise FiError(st, lib.fi_noalloc_last_error().decode(errors="replace"))
+    return int(v.value)

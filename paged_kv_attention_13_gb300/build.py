@@ -16,7 +16,7 @@ LIB = os.path.join(HERE, "libfi.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["abi.cc", "decode.cu", "prefill_mma.cu", "prefill_tc.cu", "merge.cu", "noalloc.cu",
-           "tma_map.cu", "sampling.cu"]
+           "tma_map.cu", "sampling.cu", "check.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -25,6 +25,29 @@ namespace {
 
 thread_local std::string g_last_error;
 
+// FI_LOG (read once per process): 0 or unset = silent; 1 = every refusal or
+// CUDA failure on stderr; 2 = also each committed plan (kernel, tile, items,
+// chunks, grid); 3 = also each run() launch. Costs one branch at level 0.
+int log_level() {
+  static const int lvl = [] {
+    const char* e = std::getenv("FI_LOG");
+    return e ? std::atoi(e) : 0;
+  }();
+  return lvl;
+}
+
+// FI_CHECK_INDICES=1 (read once per process): every paged run() first checks
+// the plan's page-table entries against the cache's page count on the device;
+// a bad entry is counted in the workspace header and the attention kernels of
+// that run do no work (fi_plan_device_error then reports it).
+bool check_indices_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("FI_CHECK_INDICES");
+    return e && std::atoi(e) != 0;
+  }();
+  return on;
+}
+
 fi_status fail(fi_status st, const char* fmt, ...) {
   char buf[512];
   va_list ap;
@@ -32,6 +55,7 @@ fi_status fail(fi_status st, const char* fmt, ...) {
   vsnprintf(buf, sizeof buf, fmt, ap);
   va_end(ap);
   g_last_error = buf;
+  if (log_level() >= 1) std::fprintf(stderr, "[fi] %s: %s\n", st == FI_ERR_CUDA ? "error" : "refused", buf);
   return st;
 }
 
@@ -79,6 +103,16 @@ struct fi_plan_s {
   size_t staging_bytes = 0;
   cudaEvent_t upload_done = nullptr;
   bool upload_pending = false;
+  cudaStream_t upload_stream = nullptr;  // the stream of the last metadata upload
+  // Stream order between plan() and run(): every run() outside a capture
+  // records run_done on its stream; a run on another stream than the upload's
+  // waits for upload_done, a run on another stream than the previous run's
+  // waits for run_done, and plan() waits for run_done before it overwrites
+  // the workspace.
+  cudaEvent_t run_done = nullptr;
+  bool run_recorded = false;
+  cudaStream_t last_run_stream = nullptr;
+  uint64_t wait_limit_ns = 0;  // written into each plan's header (0: the kernels' 2 s)
   bool planned = false;
   PlanState st;
   // shape frozen by the first plan of a graph-mode plan object
@@ -170,7 +204,9 @@ extern "C" fi_status fi_plan_create(fi_plan_t* out, void* workspace, size_t work
                   cudaGetErrorString(cudaGetLastError()));
     }
     p->num_sms = n;
-    if (cudaEventCreateWithFlags(&p->upload_done, cudaEventDisableTiming) != cudaSuccess) {
+    if (cudaEventCreateWithFlags(&p->upload_done, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->run_done, cudaEventDisableTiming) != cudaSuccess) {
+      if (p->upload_done) cudaEventDestroy(p->upload_done);
       delete p;
       return fail(FI_ERR_CUDA, "plan_create: cudaEventCreate failed");
     }
@@ -183,6 +219,7 @@ extern "C" void fi_plan_destroy(fi_plan_t p) {
   if (!p) return;
   if (p->upload_pending && p->upload_done) cudaEventSynchronize(p->upload_done);
   if (p->upload_done) cudaEventDestroy(p->upload_done);
+  if (p->run_done) cudaEventDestroy(p->run_done);
   if (p->staging) cudaFreeHost(p->staging);
   delete p;
 }
@@ -710,8 +747,15 @@ fi_status plan_common(fi_plan_t p, const int32_t* qo_indptr, const int32_t* kv_i
                             num_qo_heads, num_kv_heads, head_dim, causal, window_left, dtype,
                             q_len_per_req, force_kv_chunks, ragged, mask_indptr, ns);
   if (st != FI_OK) return st;  // the previous plan stays usable
+  ns.hdr.wait_limit_ns = p->wait_limit_ns;
   if (!p->host_only) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The upload copies from a host buffer that the next plan() rewrites, so
+    // it cannot become a node of a captured graph.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+      return fail(FI_ERR_INVALID_ARG, "plan: the stream is capturing a graph (plan outside the "
+                  "capture; a captured run() reads the latest plan when the graph is launched)");
     // the previous upload must have left the pinned buffer before it is reused
     if (p->upload_pending) {
       if (cudaEventSynchronize(p->upload_done) != cudaSuccess) {
@@ -733,15 +777,28 @@ fi_status plan_common(fi_plan_t p, const int32_t* qo_indptr, const int32_t* kv_i
       p->staging_bytes = want;
     }
     write_staging(ns, static_cast<uint8_t*>(p->staging));
+    // the workspace is rewritten only after the previous run() has read it
+    cudaError_t e = cudaSuccess;
+    if (p->run_recorded && p->last_run_stream != s) e = cudaStreamWaitEvent(s, p->run_done, 0);
     // from here the device copy changes: a failure leaves run() refusing
-    cudaError_t e = cudaMemcpyAsync(p->ws, p->staging, size_t(ns.meta_bytes),
-                                    cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(p->ws, p->staging, size_t(ns.meta_bytes), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaEventRecord(p->upload_done, s);
     if (e != cudaSuccess) {
       p->planned = false;
       return fail(FI_ERR_CUDA, "plan: metadata upload failed: %s", cudaGetErrorString(e));
     }
     p->upload_pending = true;
+    p->upload_stream = s;
+  }
+  if (log_level() >= 2) {
+    static const char* kname[] = {"decode", "prefill_m16", "prefill_m64", "prefill_m128"};
+    std::fprintf(stderr, "[fi] plan: kernel=%s tile_rows=%d batch=%d rows=%d items=%zu "
+                 "max_chunks=%d partials=%d merge_rows=%zu grid=%d graph=%d causal=%d "
+                 "window_left=%d q_len_per_req=%d%s%s\n", kname[ns.kernel & 3], ns.tile_rows,
+                 ns.batch, ns.total_rows, ns.items.size(), ns.max_chunks, ns.n_partials,
+                 ns.merge_rows.size(), ns.grid, p->graph ? 1 : 0, ns.causal, ns.window_left,
+                 ns.q_len_per_req, ns.ragged ? " ragged" : "", ns.masked ? " masked" : "");
   }
   if (p->graph && !p->frozen) {
     p->frozen = true;
@@ -825,6 +882,18 @@ extern "C" fi_status fi_plan_get_info(fi_plan_t p, fi_plan_info* info, int32_t* 
   return ok();
 }
 
+namespace {
+// A stream that reads or writes the workspace outside run(): after the latest
+// metadata upload and the latest run().
+cudaError_t order_after_plan_and_run(fi_plan_t p, cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
+  if (p->upload_pending && p->upload_stream != st) e = cudaStreamWaitEvent(st, p->upload_done, 0);
+  if (e == cudaSuccess && p->run_recorded && p->last_run_stream != st)
+    e = cudaStreamWaitEvent(st, p->run_done, 0);
+  return e;
+}
+}  // namespace
+
 extern "C" fi_status fi_plan_read_device(fi_plan_t p, int32_t* items, int32_t items_capacity,
                                          int32_t* merge_indptr, int32_t merge_capacity,
                                          void* stream) {
@@ -834,7 +903,9 @@ extern "C" fi_status fi_plan_read_device(fi_plan_t p, int32_t* items, int32_t it
   const PlanState& s = p->st;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   std::vector<uint8_t> buf(size_t(s.meta_bytes));
-  cudaError_t e = cudaMemcpyAsync(buf.data(), p->ws, buf.size(), cudaMemcpyDeviceToHost, st);
+  cudaError_t e = order_after_plan_and_run(p, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(buf.data(), p->ws, buf.size(), cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess)
     return fail(FI_ERR_CUDA, "plan_read_device: %s", cudaGetErrorString(e));
@@ -857,13 +928,23 @@ extern "C" fi_status fi_plan_device_error(fi_plan_t p, int32_t* err_flag, int cl
   if (!p->planned) return fail(FI_ERR_NOT_PLANNED, "plan_device_error: call fi_plan() first");
   if (p->host_only) return fail(FI_ERR_INVALID_ARG, "plan_device_error: host-only plan");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // err_flag and index_error are adjacent int32 fields of the header
+  static_assert(offsetof(WsHeader, index_error) == offsetof(WsHeader, err_flag) + 4,
+                "adjacent flags");
   uint8_t* flag = static_cast<uint8_t*>(p->ws) + offsetof(WsHeader, err_flag);
-  int32_t v = 0;
-  cudaError_t e = cudaMemcpyAsync(&v, flag, sizeof v, cudaMemcpyDeviceToHost, st);
+  int32_t v[2] = {0, 0};
+  cudaError_t e = order_after_plan_and_run(p, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(v, flag, sizeof v, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess && clear) e = cudaMemsetAsync(flag, 0, sizeof v, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return fail(FI_ERR_CUDA, "plan_device_error: %s", cudaGetErrorString(e));
-  *err_flag = v;
+  *err_flag = (v[0] ? 1 : 0) | (v[1] ? 2 : 0);
+  return ok();
+}
+
+extern "C" fi_status fi_plan_set_wait_limit(fi_plan_t p, uint64_t limit_ns) {
+  if (!p) return fail(FI_ERR_INVALID_ARG, "plan_set_wait_limit: plan is NULL");
+  p->wait_limit_ns = limit_ns;
   return ok();
 }
 
@@ -1046,6 +1127,35 @@ fi_status run_common(fi_plan_t p, bool decode_api, bool ragged, const fi_tensor*
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const bool bf16 = s.dtype == FI_BF16;
   const bool any_work = p->graph || !s.items.empty();
+  // Stream order against plan() and earlier runs (outside a capture; a
+  // captured run reads whatever plan the workspace holds at graph launch).
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(cs, &cap) != cudaSuccess)
+    return fail(FI_ERR_CUDA, "%s: cudaStreamIsCapturing failed", api);
+  const bool capturing = cap != cudaStreamCaptureStatusNone;
+  if (!capturing) {
+    cudaError_t e = cudaSuccess;
+    if (p->upload_pending && p->upload_stream != cs) e = cudaStreamWaitEvent(cs, p->upload_done, 0);
+    if (e == cudaSuccess && p->run_recorded && p->last_run_stream != cs)
+      e = cudaStreamWaitEvent(cs, p->run_done, 0);
+    if (e != cudaSuccess)
+      return fail(FI_ERR_CUDA, "%s: ordering after plan(): %s", api, cudaGetErrorString(e));
+  }
+  if (log_level() >= 3)
+    std::fprintf(stderr, "[fi] %s: kernel=%d grid=%d items=%zu merge_rows=%zu stream=%p%s%s\n",
+                 api, s.kernel, s.grid, s.items.size(), s.merge_rows.size(),
+                 static_cast<void*>(cs), capturing ? " (capturing)" : "",
+                 (!ragged && check_indices_enabled()) ? " index-check" : "");
+  if (!ragged && check_indices_enabled() && any_work) {
+    // count page-table entries outside [0, num_pages); the attention kernels
+    // and the merge read the count and do nothing when it is non-zero
+    cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(p->ws) + offsetof(WsHeader, index_error),
+                                    0, sizeof(int32_t), cs);
+    if (e == cudaSuccess)
+      e = fi::launch_check_indices(p->ws, ap.kv_indices, k->shape[0], p->num_sms, cs);
+    if (e != cudaSuccess)
+      return fail(FI_ERR_CUDA, "%s: index check launch failed: %s", api, cudaGetErrorString(e));
+  }
   if (any_work) {
     cudaError_t e;
     if (s.kernel == fi::kDecode)
@@ -1067,10 +1177,44 @@ fi_status run_common(fi_plan_t p, bool decode_api, bool ragged, const fi_tensor*
     if (e != cudaSuccess)
       return fail(FI_ERR_CUDA, "%s: merge launch failed: %s", api, cudaGetErrorString(e));
   }
+  if (!capturing) {
+    cudaError_t e = cudaEventRecord(p->run_done, cs);
+    if (e != cudaSuccess)
+      return fail(FI_ERR_CUDA, "%s: cudaEventRecord: %s", api, cudaGetErrorString(e));
+    p->run_recorded = true;
+    p->last_run_stream = cs;
+  }
   return ok();
 }
 
 }  // namespace
+
+extern "C" fi_status fi_check_kv_indices(fi_plan_t p, const fi_tensor* kv_indices,
+                                         int64_t num_pages, void* stream) {
+  if (!p) return fail(FI_ERR_INVALID_ARG, "check_kv_indices: plan is NULL");
+  if (!p->planned) return fail(FI_ERR_NOT_PLANNED, "check_kv_indices: call fi_plan() first");
+  if (p->host_only) return fail(FI_ERR_INVALID_ARG, "check_kv_indices: host-only plan");
+  if (p->st.ragged)
+    return fail(FI_ERR_PLAN_MISMATCH, "check_kv_indices: a ragged plan has no page table");
+  fi_status fs = check_tensor(kv_indices, "kv_indices", 1);
+  if (fs != FI_OK) return fs;
+  if (kv_indices->dtype != FI_I32)
+    return fail(FI_ERR_INVALID_ARG, "check_kv_indices: kv_indices must be int32");
+  if (kv_indices->shape[0] < p->st.kv_indices_len)
+    return check_dim("kv_indices", "length (minimum)", p->st.kv_indices_len, kv_indices->shape[0]);
+  if (num_pages < 0) return fail(FI_ERR_INVALID_ARG, "check_kv_indices: num_pages < 0");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = order_after_plan_and_run(p, st);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(static_cast<uint8_t*>(p->ws) + offsetof(WsHeader, index_error), 0,
+                        sizeof(int32_t), st);
+  if (e == cudaSuccess)
+    e = fi::launch_check_indices(p->ws, static_cast<const int32_t*>(kv_indices->data), num_pages,
+                                 p->num_sms, st);
+  if (e != cudaSuccess)
+    return fail(FI_ERR_CUDA, "check_kv_indices: %s", cudaGetErrorString(e));
+  return ok();
+}
 
 extern "C" fi_status fi_batch_prefill_paged(fi_plan_t p, const fi_tensor* q, const fi_tensor* k,
                                             const fi_tensor* v, const fi_tensor* kv_indices,

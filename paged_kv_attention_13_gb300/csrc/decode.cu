@@ -607,7 +607,7 @@ template <int D, int G, bool BF16, bool MMA, class W>
 __device__ __noinline__ void decode_producer(const AttnParams& p, const CUtensorMap* tkp,
                                              const CUtensorMap* tvp, int box_rows, uint8_t* dsmem,
                                              int lane, int causal, int window_left,
-                                             volatile int* abort_flag) {
+                                             volatile WaitCtl* ctl) {
   using C = TmaCfg<D, MMA>;
   constexpr int NCW = C::NCW, KT = C::KT, NS = C::NS, STAGE = C::STAGE;
   using T = typename W::T;
@@ -653,9 +653,9 @@ __device__ __noinline__ void decode_producer(const AttnParams& p, const CUtensor
   auto claim = [&](int st, uint32_t par, const StageHdr& h, uint32_t bytes, bool first) {
     bool okl = true;
     if (lane == 0) {
-      if (c >= NS) okl = mbar_wait(EMPTY(st), par ^ 1u, abort_flag);
+      if (c >= NS) okl = mbar_wait(EMPTY(st), par ^ 1u, ctl);
       if (okl && first && n_item > 0)
-        okl = mbar_wait(QFREE, uint32_t(n_item - 1) & 1u, abort_flag);
+        okl = mbar_wait(QFREE, uint32_t(n_item - 1) & 1u, ctl);
       if (okl) {
         sH[st] = h;
         mbar_expect_tx(FULL(st), bytes);
@@ -795,10 +795,10 @@ __device__ __noinline__ void decode_producer(const AttnParams& p, const CUtensor
   // ignores the abort flag but keeps its time bound, and an expiry is
   // reported too).
   if (lane == 0) {
-    volatile int no_abort = 0;
+    volatile WaitCtl drain = {0, 0, kWaitLimitNs};
 #pragma unroll
     for (int s = 0; s < NS; ++s)
-      if (armed[s] && !mbar_wait(FULL(s), last_par[s], &no_abort)) *abort_flag = 1;
+      if (armed[s] && !mbar_wait(FULL(s), last_par[s], &drain)) ctl->abort = 1;
   }
 }
 
@@ -817,6 +817,9 @@ __global__ void __launch_bounds__(TmaCfg<D, MMA>::THREADS, TmaCfg<D, MMA>::MINB)
 
   extern __shared__ __align__(1024) uint8_t dsmem[];
   const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
+  // the page table failed the index check: the whole CTA leaves before any
+  // barrier or copy
+  if (hdr->index_error) return;
   if (MMA && (smem_u32(dsmem) & 1023u) != 0) {
     // the swizzle pattern is anchored to 1024-byte boundaries: report and
     // skip the work rather than compute with a shifted pattern
@@ -835,7 +838,7 @@ __global__ void __launch_bounds__(TmaCfg<D, MMA>::THREADS, TmaCfg<D, MMA>::MINB)
   auto EMPTY = [&](int s) { return bar0 + 8u * uint32_t(NS + s); };
   const uint32_t QFREE = bar0 + 8u * uint32_t(2 * NS);
   const uint32_t MERGE = bar0 + 8u * uint32_t(2 * NS + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(dsmem + C::BAR_OFF + C::NBAR * 8);
+  volatile WaitCtl* ctl = reinterpret_cast<volatile WaitCtl*>(dsmem + C::BAR_OFF + C::NBAR * 8);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -846,7 +849,8 @@ __global__ void __launch_bounds__(TmaCfg<D, MMA>::THREADS, TmaCfg<D, MMA>::MINB)
     }
     mbar_init(QFREE, NCW);
     mbar_init(MERGE, NCW * 32);
-    *abort_flag = 0;
+    ctl->abort = 0;
+    ctl->limit_ns = wait_limit_of(hdr);
     mbar_init_fence();
   }
   const int causal = hdr->causal;
@@ -855,7 +859,7 @@ __global__ void __launch_bounds__(TmaCfg<D, MMA>::THREADS, TmaCfg<D, MMA>::MINB)
 
   if (warp == NCW) {
     decode_producer<D, G, BF16, MMA, W>(p, &tk, &tv, box_rows, dsmem, lane, causal, window_left,
-                                   abort_flag);
+                                   ctl);
   } else {
     // ------------------------------------------------------------ consumers
     float* tmp_lse = ws_ptr<float>(p.ws, hdr->off_tmp_lse);
@@ -866,14 +870,14 @@ __global__ void __launch_bounds__(TmaCfg<D, MMA>::THREADS, TmaCfg<D, MMA>::MINB)
     // barrier over the consumer threads, bounded like every other wait
     auto consumer_sync = [&] {
       mbar_arrive(MERGE);
-      mbar_wait(MERGE, n_sync & 1u, abort_flag);
+      mbar_wait(MERGE, n_sync & 1u, ctl);
       ++n_sync;
     };
     for (int c = 0;; ++c) {
       const int st = c % NS;
       // an expired wait ends the warp's work (the abort flag then makes
       // every other wait return at once); the error is reported below
-      if (!mbar_wait(FULL(st), uint32_t(c / NS) & 1u, abort_flag)) break;
+      if (!mbar_wait(FULL(st), uint32_t(c / NS) & 1u, ctl)) break;
       // the header is read in place (fields load where they are used); the
       // output fields are copied out before the slot is released
       const StageHdr& h = sH[st];
@@ -918,7 +922,7 @@ __global__ void __launch_bounds__(TmaCfg<D, MMA>::THREADS, TmaCfg<D, MMA>::MINB)
   // the split-KV merge launched after this kernel may start its launch now
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __syncthreads();
-  if (tid == 0 && *abort_flag) {
+  if (tid == 0 && ctl->abort) {
     int* err = const_cast<int*>(&hdr->err_flag);
     atomicExch(err, 1);
   }
@@ -931,8 +935,9 @@ cudaError_t launch_k(const AttnParams& p, int grid, const CUtensorMap& tk, const
                      int box_rows, cudaStream_t s) {
   using C = TmaCfg<D, MMA>;
   auto k = decode_tma_kernel<D, G, BF16, MMA, RH>;
-  // once per process, before any capture (no attribute call inside a captured run)
-  static cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  // once per device, before any capture (no attribute call inside a captured run)
+  static std::atomic<uint64_t> done{0};
+  const cudaError_t attr = smem_attr_once(k, C::SMEM, done);
   if (attr != cudaSuccess) return attr;
   k<<<grid, C::THREADS, C::SMEM, s>>>(p, tk, tv, box_rows);
   return cudaGetLastError();

@@ -2,6 +2,7 @@
 // the planner and read by the kernels, and the kernel launch parameters.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -38,7 +39,8 @@ struct alignas(128) WsHeader {
   int32_t num_qo_heads;
   int32_t head_dim;
   int32_t err_flag;      // set by a kernel whose bounded wait expired
-  int32_t pad1;
+  int32_t index_error;   // kv_indices entries out of range, counted by the index check;
+                         // the attention kernels do no work while it is non-zero
   int64_t off_qo_indptr;     // int32 [batch+1]
   int64_t off_kv_indptr;     // int32 [batch+1]
   int64_t off_kv_len;        // int32 [batch]
@@ -48,6 +50,7 @@ struct alignas(128) WsHeader {
   int64_t off_tmp_lse;       // float [partials, Hq]
   int64_t off_tmp_o;         // float [partials, Hq, d]
   int64_t off_mask_indptr;   // int32 [batch+1]: byte offset of each request's custom mask
+  uint64_t wait_limit_ns;    // limit of every bounded wait on an mbarrier (0: 2 s)
 };
 static_assert(sizeof(WsHeader) == 128, "header is 128 bytes");
 
@@ -153,6 +156,27 @@ struct SpecParams {
 cudaError_t launch_chain_spec_sampling(const SpecParams& sp, int batch, cudaStream_t stream);
 // Largest vocabulary it takes (its block sums live in 48 KB of shared memory).
 int chain_spec_max_vocab();
+
+// Count page-table entries of the plan in `ws` outside [0, num_pages) into
+// the header's index_error (which the caller zeroes first).
+cudaError_t launch_check_indices(void* ws, const int32_t* kv_indices, int64_t num_pages,
+                                 int num_sms, cudaStream_t stream);
+
+// Raise a kernel's dynamic shared-memory limit on the current device, once
+// per device: the attribute belongs to each device's context, so the first
+// launch on every device sets it (before any capture on that device). `done`
+// is the kernel's own bit set of devices already configured.
+template <class K>
+cudaError_t smem_attr_once(K kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Occupancy of each run kernel (CTAs per SM), for persistent grid sizing.
 int kernel_ctas_per_sm(int kernel, int head_dim, int group, bool bf16, int page_size);

@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(256, 4) merge_workspace_kernel(const void* ws,
   // before the attention kernel started, so the first task's bounds are read
   // while that kernel is still running.
   const WsHeader* hdr = static_cast<const WsHeader*>(ws);
+  if (hdr->index_error) return;  // the page table failed the index check: no work
   const int n_rows = hdr->n_merge_rows;
   const int32_t* merge_indptr = ws_ptr<const int32_t>(ws, hdr->off_merge_indptr);
   const int32_t* merge_rows = ws_ptr<const int32_t>(ws, hdr->off_merge_rows);

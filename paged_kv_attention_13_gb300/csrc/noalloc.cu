@@ -4,8 +4,10 @@
 // memory at all - code that runs inside another framework's memory pool or a
 // serving loop that reserved all memory up front, and host code that must
 // not call cudaMalloc/cudaFree on the hot path.
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/fi.h"
 #include "common.cuh"
@@ -20,6 +22,29 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 void* g_scratch_addr[kMaxDevices] = {};  // device address of the array, per device
+std::mutex g_scratch_mu;                 // guards the first lookup on each device
+
+// The array's device address on the current device: looked up once per
+// device (with that device current) and kept; nullptr and an error message on
+// failure.
+void* scratch_address(const char** err) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = "no usable current device";
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr) {
+      *err = cudaGetErrorString(e);
+      return nullptr;
+    }
+    g_scratch_addr[dev] = ptr;
+  }
+  return g_scratch_addr[dev];
+}
 
 struct NoAllocLayout {
   int64_t off_qo, off_kv, off_len, off_merge, off_rows, off_items, off_lse, off_o, total;
@@ -138,8 +163,8 @@ extern "C" fi_status fi_batch_decode_paged_noalloc(
                 "kv_indices [n], lse [B, Hq]");
   const int hq = int(q->shape[1]), d = int(q->shape[2]);
   const int page_size = int(k_cache->shape[1]), hk = int(k_cache->shape[2]);
-  if (batch < 0 || q->shape[0] < batch || out->shape[0] < batch)
-    return fail(FI_ERR_INVALID_ARG, "decode_noalloc: q and out need >= batch rows");
+  if (batch < 0 || q->shape[0] < batch || out->shape[0] < batch || (lse && lse->shape[0] < batch))
+    return fail(FI_ERR_INVALID_ARG, "decode_noalloc: q, out and lse need >= batch rows");
   if (hk <= 0 || hq % hk != 0)
     return fail(FI_ERR_GQA_INDIVISIBLE, "decode_noalloc: num_qo_heads is not a multiple of num_kv_heads");
   const int g = hq / hk;
@@ -155,6 +180,8 @@ extern "C" fi_status fi_batch_decode_paged_noalloc(
   if (out->stride[2] != 1 || out->stride[1] != d || out->stride[0] != int64_t(hq) * d ||
       (lse && (lse->stride[1] != 1 || lse->stride[0] != hq)))
     return fail(FI_ERR_NONCONTIGUOUS_OUTPUT, "decode_noalloc: out and lse must be packed");
+  if (k_cache->shape[0] != v_cache->shape[0])
+    return fail(FI_ERR_INVALID_ARG, "decode_noalloc: k_cache and v_cache have different page counts");
   if (v_cache->shape[1] != page_size || v_cache->shape[2] != hk || v_cache->shape[3] != d ||
       k_cache->shape[3] != d || out->shape[1] != hq || out->shape[2] != d ||
       (lse && lse->shape[1] != hq))
@@ -179,20 +206,13 @@ extern "C" fi_status fi_batch_decode_paged_noalloc(
   }
   if (batch == 0) return FI_OK;
   // once per device, with that device current: the array's device address
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-    return fail(FI_ERR_CUDA, "decode_noalloc: no usable current device");
-  if (!g_scratch_addr[dev]) {
-    void* ptr = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess || !ptr) {
-      snprintf(g_noalloc_err, sizeof g_noalloc_err, "decode_noalloc: cudaGetSymbolAddress: %s",
-               cudaGetErrorString(e));
-      return FI_ERR_CUDA;
-    }
-    g_scratch_addr[dev] = ptr;
+  // (the name g_noalloc_scratch in host code is only a stand-in for it)
+  const char* why = nullptr;
+  uint8_t* ws = static_cast<uint8_t*>(scratch_address(&why));
+  if (!ws) {
+    snprintf(g_noalloc_err, sizeof g_noalloc_err, "decode_noalloc: cudaGetSymbolAddress: %s", why);
+    return FI_ERR_CUDA;
   }
-  uint8_t* ws = static_cast<uint8_t*>(g_scratch_addr[dev]);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   noalloc_setup_kernel<<<64, 256, 0, s>>>(ws, L, kv_indptr_dev, last_page_len_dev, batch,
                                            page_size, hq, hk, d, window_left, kv_chunks);
@@ -226,5 +246,40 @@ extern "C" fi_status fi_batch_decode_paged_noalloc(
                                (batch * hq + 7) / 8, s);
     if (e != cudaSuccess) return fail(FI_ERR_CUDA, "decode_noalloc: merge launch failed");
   }
+  return FI_OK;
+}
+
+// The error flag of the last no-allocation decode on the current device: 1 when
+// one of its bounded waits expired (that call's out / lse are not valid), else
+// 0; 0 as well before the first call. Synchronises `stream`.
+extern "C" fi_status fi_noalloc_device_error(int32_t* err_flag, int clear, void* stream) {
+  using namespace fi;
+  if (!err_flag) {
+    snprintf(g_noalloc_err, sizeof g_noalloc_err, "noalloc_device_error: err_flag is NULL");
+    return FI_ERR_INVALID_ARG;
+  }
+  *err_flag = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    snprintf(g_noalloc_err, sizeof g_noalloc_err, "noalloc_device_error: no usable current device");
+    return FI_ERR_CUDA;
+  }
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    base = g_scratch_addr[dev];
+  }
+  if (!base) return FI_OK;  // no call on this device yet
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* flag = static_cast<uint8_t*>(base) + offsetof(WsHeader, err_flag);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, flag, sizeof v, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(flag, 0, sizeof v, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    snprintf(g_noalloc_err, sizeof g_noalloc_err, "noalloc_device_error: %s", cudaGetErrorString(e));
+    return FI_ERR_CUDA;
+  }
+  *err_flag = v ? 1 : 0;
   return FI_OK;
 }

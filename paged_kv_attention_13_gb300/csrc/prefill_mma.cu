@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kThreads) prefill_mma_kernel(const AttnParams 
   T* sV = sK + C::STAGES * C::KV_ELEMS;    // [STAGES][kN][D]
 
   const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
+  if (hdr->index_error) return;  // the page table failed the index check: no work
   const int n_items = hdr->n_items;
   const WorkItem* items = ws_ptr<const WorkItem>(p.ws, hdr->off_items);
   const int32_t* qo_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_qo_indptr);
@@ -353,10 +354,10 @@ template <int D, int WM, bool BF16>
 cudaError_t launch_t(const AttnParams& p, int grid, cudaStream_t s) {
   using C = MmaCfg<D, WM>;
   auto k = prefill_mma_kernel<D, WM, BF16>;
-  // once per process (not per launch, so a run() inside stream capture makes
-  // no attribute call); the first run() must precede any capture
-  static cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 C::SMEM_BYTES);
+  // once per device (not per launch, so a run() inside stream capture makes
+  // no attribute call); the first run() on a device must precede any capture
+  static std::atomic<uint64_t> done{0};
+  const cudaError_t attr = smem_attr_once(k, C::SMEM_BYTES, done);
   if (attr != cudaSuccess) return attr;
   k<<<grid, kThreads, C::SMEM_BYTES, s>>>(p);
   return cudaGetLastError();

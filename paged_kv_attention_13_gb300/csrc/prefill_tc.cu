@@ -203,6 +203,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       int kv_box_rows) {
   using DT = Dt<BF16>;
   using T = typename DT::T;
+  // the page table failed the index check: the whole CTA leaves before any
+  // barrier, tensor-memory allocation or copy
+  if (static_cast<const WsHeader*>(p.ws)->index_error) return;
   extern __shared__ uint8_t smem_raw[];
   uint32_t sbase = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (sbase & 1023u)) & 1023u;
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t bar0 = sbase + kOffBar;
   auto BAR = [&](int i) { return bar0 + 8u * uint32_t(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * N_BARS);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * N_BARS + 8);
+  volatile WaitCtl* ctl = reinterpret_cast<volatile WaitCtl*>(smem + kOffBar + 8 * N_BARS + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -246,7 +249,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(BAR(B_FINAL), 1);
     mbar_init(BAR(B_MLFULL), 128);
     mbar_init(BAR(B_MLFREE), 128);
-    *abort_flag = 0;
+    ctl->abort = 0;
+    ctl->limit_ns = wait_limit_of(hdr);
     mbar_init_fence();
   }
   // K/V stages start zeroed so rows no copy has written yet hold finite values
@@ -292,7 +296,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int full = which ? B_VFULL : B_KFULL, empty = which ? B_VEMPTY : B_KEMPTY;
       bool okl = true;
       if (lane == 0) {
-        if (cntr >= 2 && !mbar_wait(BAR(empty + st), ((cntr >> 1) - 1) & 1, abort_flag)) okl = false;
+        if (cntr >= 2 && !mbar_wait(BAR(empty + st), ((cntr >> 1) - 1) & 1, ctl)) okl = false;
         if (okl) {
           mbar_expect_tx(BAR(full + st), uint32_t(nvalid) * uint32_t(kv_box_rows) * 128u * 2u);
           armed[which][st] = true;
@@ -328,7 +332,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       };
       int idx_cur = fetch(0), idx_nxt = fetch(1);
       if (lane == 0) {
-        if (qc > 0 && !mbar_wait(BAR(B_QEMPTY), (qc - 1) & 1, abort_flag)) ok = false;
+        if (qc > 0 && !mbar_wait(BAR(B_QEMPTY), (qc - 1) & 1, ctl)) ok = false;
         if (ok) {
           mbar_expect_tx(BAR(B_QFULL), (hasB ? 2u : 1u) * 2u * uint32_t(tr) * 128u);
           q_armed = true;
@@ -372,13 +376,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // before exit: every copy this warp started has landed (these waits
     // ignore the abort flag but keep the time bound)
     if (lane == 0) {
-      volatile int no_abort = 0;
-      if (q_armed) mbar_wait(BAR(B_QFULL), q_par, &no_abort);
+      volatile WaitCtl drain = {0, 0, kWaitLimitNs};
+      if (q_armed) mbar_wait(BAR(B_QFULL), q_par, &drain);
       for (int which = 0; which < 2; ++which)
         for (int s = 0; s < 2; ++s)
           if (armed[which][s])
-            mbar_wait(BAR((which ? B_VFULL : B_KFULL) + s), apar[which][s], &no_abort);
-      if (no_abort) *abort_flag = 1;  // an expired drain wait is reported too
+            mbar_wait(BAR((which ? B_VFULL : B_KFULL) + s), apar[which][s], &drain);
+      if (drain.abort) ctl->abort = 1;  // an expired drain wait is reported too
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -416,12 +420,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (G.n_tiles == 0) continue;
         const bool hasB = G.n_rows > tr;
         const int n = G.n_tiles;
-        if (!mbar_wait(BAR(B_QFULL), qc & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(BAR(B_QFULL), qc & 1, ctl)) { ok = false; break; }
         if (!hasB && n >= 2) {
           // split item: key tile j goes to warpgroup j & 1, both on Q tile A
           for (int j0 = 0; j0 < 2 && ok; ++j0) {
             const int g0 = gt + j0;
-            if (!mbar_wait(BAR(B_KFULL + (g0 & 1)), (g0 >> 1) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_KFULL + (g0 & 1)), (g0 >> 1) & 1, ctl)) { ok = false; break; }
             tc_fence_after();
             issue_s(j0, g0 & 1, 0);
             tc_commit(BAR(B_KEMPTY + (g0 & 1)));
@@ -431,15 +435,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int j = 0; j < n && ok; ++j) {
             const int xw = j & 1, jx = j >> 1, g1 = gt + j, st = g1 & 1;
             if (jx == 0 && itc[xw] > 0 &&
-                !mbar_wait(BAR(B_OFREE + xw), (itc[xw] - 1) & 1, abort_flag)) { ok = false; break; }
-            if (!mbar_wait(BAR(B_PFULL + xw), (cnt[xw] + jx) & 1, abort_flag)) { ok = false; break; }
-            if (!mbar_wait(BAR(B_VFULL + st), (g1 >> 1) & 1, abort_flag)) { ok = false; break; }
+                !mbar_wait(BAR(B_OFREE + xw), (itc[xw] - 1) & 1, ctl)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_PFULL + xw), (cnt[xw] + jx) & 1, ctl)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_VFULL + st), (g1 >> 1) & 1, ctl)) { ok = false; break; }
             tc_fence_after();
             issue_pv(xw, st, jx > 0);
             if (j >= n - 2) tc_commit(BAR(B_ODONE + xw));  // the warpgroup's last tile
             tc_commit(BAR(B_VEMPTY + st));
             if (j + 2 < n) {  // tile j + 2 reuses tile j's K stage
-              if (!mbar_wait(BAR(B_KFULL + st), ((g1 + 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+              if (!mbar_wait(BAR(B_KFULL + st), ((g1 + 2) >> 1) & 1, ctl)) { ok = false; break; }
               tc_fence_after();
               issue_s(xw, st, 0);
               tc_commit(BAR(B_KEMPTY + st));
@@ -454,7 +458,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ++itc[1];
           continue;
         }
-        if (!mbar_wait(BAR(B_KFULL + (gt & 1)), (gt >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(BAR(B_KFULL + (gt & 1)), (gt >> 1) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
         issue_s(0, gt & 1, 0);
         if (hasB) issue_s(1, gt & 1, 1);
@@ -463,15 +467,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int j = 0; j < n && ok; ++j) {
           const int g1 = gt + j, st = g1 & 1, st1 = (g1 + 1) & 1;
           // ---- tile A
-          if (j == 0 && itc[0] > 0 && !mbar_wait(BAR(B_OFREE), (itc[0] - 1) & 1, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(BAR(B_PFULL), (cnt[0] + j) & 1, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(BAR(B_VFULL + st), (g1 >> 1) & 1, abort_flag)) { ok = false; break; }
+          if (j == 0 && itc[0] > 0 && !mbar_wait(BAR(B_OFREE), (itc[0] - 1) & 1, ctl)) { ok = false; break; }
+          if (!mbar_wait(BAR(B_PFULL), (cnt[0] + j) & 1, ctl)) { ok = false; break; }
+          if (!mbar_wait(BAR(B_VFULL + st), (g1 >> 1) & 1, ctl)) { ok = false; break; }
           tc_fence_after();
           issue_pv(0, st, j > 0);
           if (j == n - 1) tc_commit(BAR(B_ODONE));
           if (!hasB) tc_commit(BAR(B_VEMPTY + st));
           if (j + 1 < n) {
-            if (!mbar_wait(BAR(B_KFULL + st1), ((g1 + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_KFULL + st1), ((g1 + 1) >> 1) & 1, ctl)) { ok = false; break; }
             tc_fence_after();
             issue_s(0, st1, 0);
             if (!hasB) {
@@ -481,8 +485,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           // ---- tile B
           if (hasB) {
-            if (j == 0 && itc[1] > 0 && !mbar_wait(BAR(B_OFREE + 1), (itc[1] - 1) & 1, abort_flag)) { ok = false; break; }
-            if (!mbar_wait(BAR(B_PFULL + 1), (cnt[1] + j) & 1, abort_flag)) { ok = false; break; }
+            if (j == 0 && itc[1] > 0 && !mbar_wait(BAR(B_OFREE + 1), (itc[1] - 1) & 1, ctl)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_PFULL + 1), (cnt[1] + j) & 1, ctl)) { ok = false; break; }
             tc_fence_after();
             issue_pv(1, st, j > 0);
             tc_commit(BAR(B_VEMPTY + st));
@@ -505,8 +509,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // every MMA this thread issued has completed before tensor memory is freed
       tc_commit(BAR(B_FINAL));
-      volatile int no_abort = 0;
-      if (!mbar_wait(BAR(B_FINAL), 0, &no_abort)) *abort_flag = 1;
+      volatile WaitCtl drain = {0, 0, kWaitLimitNs};
+      if (!mbar_wait(BAR(B_FINAL), 0, &drain)) ctl->abort = 1;
     }
     __syncwarp();
   }
@@ -523,7 +527,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // every wait here is warp-uniform, so a timeout never splits a warp in
     // front of a .sync.aligned instruction
     auto wwait = [&](uint32_t bar, uint32_t parity) {
-      const bool okl = mbar_wait(bar, parity, abort_flag);
+      const bool okl = mbar_wait(bar, parity, ctl);
       return __all_sync(0xffffffffu, okl);
     };
     float* sml = reinterpret_cast<float*>(smem + kOffMl);  // [2][128]: B's row max, row sum
@@ -760,7 +764,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (threadIdx.x == 0 && *abort_flag) {
+  if (threadIdx.x == 0 && ctl->abort) {
     int* err = const_cast<int*>(&hdr->err_flag);
     atomicExch(err, 1);
   }
@@ -796,14 +800,15 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int head_dim, int group, int 
       !encode_kv_map(&tv, p, false, bf16, head_dim, num_pages, 64, box_rows,
                      CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  // the shared-memory limit: once per device, before any capture
   if (bf16) {
-    static cudaError_t attr = cudaFuncSetAttribute(
-        prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
+    static std::atomic<uint64_t> done{0};
+    const cudaError_t attr = smem_attr_once(prefill_tc_kernel<true>, kSmemTc, done);
     if (attr != cudaSuccess) return attr;
     prefill_tc_kernel<true><<<grid, kTcThreads, kSmemTc, s>>>(p, tq, tk, tv, box_rows);
   } else {
-    static cudaError_t attr = cudaFuncSetAttribute(
-        prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
+    static std::atomic<uint64_t> done{0};
+    const cudaError_t attr = smem_attr_once(prefill_tc_kernel<false>, kSmemTc, done);
     if (attr != cudaSuccess) return attr;
     prefill_tc_kernel<false><<<grid, kTcThreads, kSmemTc, s>>>(p, tq, tk, tv, box_rows);
   }

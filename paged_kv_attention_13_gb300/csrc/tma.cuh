@@ -16,6 +16,17 @@ namespace fi {
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
+// Shared by the threads of one CTA: the abort flag that an expired wait
+// raises (every later wait then returns false at once) and the limit of each
+// wait. The limit comes from the workspace header (0 there means kWaitLimitNs);
+// waits that drain a CTA's own copies before it exits use a private block with
+// the default limit, so they still wait for those copies.
+struct WaitCtl {
+  int abort;
+  int pad;
+  unsigned long long limit_ns;
+};
+
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -48,19 +59,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of `parity` to complete; false on timeout or abort.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// The abort flag and the clock are looked at every 32 failed polls.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile WaitCtl* ctl) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
+    if ((i & 31) == 0) {
+      if (ctl->abort) return false;
+      if (globaltimer() - t0 > ctl->limit_ns) {
+        ctl->abort = 1;
         return false;
       }
     }
   }
+}
+
+// The wait limit of a launch: the header's, or kWaitLimitNs when it is 0.
+__device__ __forceinline__ unsigned long long wait_limit_of(const WsHeader* hdr) {
+  const unsigned long long l = hdr->wait_limit_ns;
+  return l ? l : kWaitLimitNs;
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,

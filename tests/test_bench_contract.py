@@ -58,8 +58,8 @@ def test_accounting_by_hand():
 
 
 def test_reference_arm_line():
-    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
-                        "--warmup", "1", "--cpu-budget", "2"], cwd=ROOT, capture_output=True,
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2",
+                        "--warmup", "1"], cwd=ROOT, capture_output=True,
                        text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     line = json.loads(r.stdout.strip().splitlines()[-1])
@@ -72,3 +72,8 @@ def test_reference_arm_line():
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
     assert line["config"]["workload"].startswith("batch decode")
+    # every core of the affinity, and a measured step: steps x ms_per_step is
+    # the time the timed steps took (nothing scaled up from a sample)
+    assert cb["cores"] == len(os.sched_getaffinity(0))
+    assert abs(line["ms_per_step"] * line["steps"] / 1e3 - line["timed_wall_s"]) <= \
+        0.1 * line["timed_wall_s"] + 0.05

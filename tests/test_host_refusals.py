@@ -58,3 +58,66 @@ def test_chain_speculative_sampling_refusals():
                    output_token_ids=torch.zeros((B, n), dtype=torch.int32)) == "FI_ERR_INVALID_ARG"
     # uniforms for the wrong batch
     assert _status(f, dp, ids, tp, ua, torch.zeros((B + 1,))) == "FI_ERR_INVALID_ARG"
+
+
+def test_noalloc_decode_refusals():
+    """The no-allocation decode checks its shapes on the host before it looks
+    up its scratch or launches anything, so host tensors suffice."""
+    B, Hq, Hk, d, P, pages = 3, 8, 2, 128, 16, 10
+    q = torch.zeros((B, Hq, d), dtype=torch.bfloat16)
+    k = torch.zeros((pages, P, Hk, d), dtype=torch.bfloat16)
+    v = torch.zeros_like(k)
+    idx = torch.zeros((pages,), dtype=torch.int32)
+    indptr = torch.zeros((B + 1,), dtype=torch.int32)
+    last = torch.ones((B,), dtype=torch.int32)
+    f = fi.fi_batch_decode_paged_noalloc
+    # a V cache with fewer pages than K: the K map's extent would let V's
+    # copies read past V's allocation
+    assert _status(f, q, k, v[: pages - 1], idx, indptr, last, 0.1) == "FI_ERR_INVALID_ARG"
+    # an lse with fewer rows than the batch
+    assert _status(f, q, k, v, idx, indptr, last, 0.1,
+                   lse=torch.zeros((B - 1, Hq))) == "FI_ERR_INVALID_ARG"
+    # an out with fewer rows than the batch
+    assert _status(f, q, k, v, idx, indptr, last, 0.1,
+                   out=torch.zeros((B - 1, Hq, d), dtype=torch.bfloat16)) == "FI_ERR_INVALID_ARG"
+    # kv_chunks outside [1, 64]
+    assert _status(f, q, k, v, idx, indptr, last, 0.1, kv_chunks=0) == "FI_ERR_INVALID_ARG"
+    # a group the kernel is not built for
+    assert _status(f, torch.zeros((B, 3 * Hk, d), dtype=torch.bfloat16), k, v, idx, indptr,
+                   last, 0.1) == "FI_ERR_UNSUPPORTED"
+
+
+def test_log_levels_print_refusals_and_plans():
+    """FI_LOG=1 prints each refusal on stderr, 2 also each committed plan;
+    unset prints nothing (host-only plans, no GPU)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = (
+        "import paged_kv_attention_13_gb300 as fi\n"
+        "p = fi.Plan(None)\n"
+        "p.plan([0, 4], [0, 2], [5], 16, 8, 2, 128, causal=True)\n"
+        "try:\n"
+        "    p.plan([0, 4], [0, 2], [5], 16, 8, 3, 128)\n"
+        "except fi.FiError:\n"
+        "    pass\n")
+
+    def run(level):
+        env = dict(os.environ)
+        env.pop("FI_LOG", None)
+        if level is not None:
+            env["FI_LOG"] = str(level)
+        r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                           text=True, timeout=300)
+        assert r.returncode == 0, r.stderr
+        return [ln for ln in r.stderr.splitlines() if ln.startswith("[fi]")]
+
+    assert run(None) == []
+    one = run(1)
+    assert len(one) == 1 and "refused" in one[0] and "num_kv_heads=3" in one[0], one
+    two = run(2)
+    plans = [ln for ln in two if ln.startswith("[fi] plan:")]
+    assert len(plans) == 1 and "kernel=" in plans[0] and "items=" in plans[0] \
+        and "grid=" in plans[0], two
+    assert any("refused" in ln for ln in two)
