@@ -277,53 +277,61 @@ class Runner:
         return float(np.mean(ms)), float(np.median(ms))
 
     def time_e2e(self, steps, warmup):
-        """End to end through the public API, host buffers pinned, every step:
-        fi_plan (its metadata upload included), one host-to-device copy of the
-        step's inputs (q and the page table, packed in one pinned buffer),
-        run(), one device-to-host copy of the result (o and lse, packed in one
-        device buffer) and the wait for it. The KV cache stays resident.
+        """End to end through the public API, every step: fi_plan (its metadata
+        upload included), one host-to-device copy of the step's inputs (q and
+        the page table, packed in one pinned host buffer), run(), one
+        device-to-host copy of the result (o and lse, packed in one device
+        buffer) into pinned host memory, and the wait for that result. The KV
+        cache stays resident, as in a serving engine.
 
-        Two schedules are timed on the wall clock:
+        Two schedules, both timed on the wall clock:
           serial     each step's plan, copies, run and wait in turn;
-          pipelined  a serving loop: while the GPU runs step n the host makes
-                     the plan of step n+1 (its upload is stream-ordered after
-                     run n), then waits for step n's result.
+          pipelined  a serving loop that keeps one step in flight: it plans
+                     and enqueues step n+1 (inputs and outputs double-
+                     buffered), then waits for step n's result. The plan's
+                     upload is stream-ordered after run n.
         Returns (pipelined ms, serial ms, h2d bytes, d2h bytes, breakdown)."""
         pb = self.pb
         dev = self.dev
         q_bytes = self.q.numel() * self.q.element_size()
         idx_off = (q_bytes + 255) // 256 * 256
         in_bytes = idx_off + self.idx.numel() * 4
-        in_h = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
-        in_h[:q_bytes].copy_(pb.q.contiguous().view(-1).view(torch.uint8))
-        in_h[idx_off:].copy_(pb.kv_indices.contiguous().view(torch.uint8))
-        in_d = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
-        q = in_d[:q_bytes].view(self.q.dtype).view(self.q.shape)
-        idx = in_d[idx_off:].view(torch.int32)
         o_bytes = self.out.numel() * self.out.element_size()
         lse_off = (o_bytes + 255) // 256 * 256
         res_bytes = lse_off + self.lse.numel() * 4
-        res_d = torch.empty(res_bytes, dtype=torch.uint8, device=dev)
-        out = res_d[:o_bytes].view(self.out.dtype).view(self.out.shape)
-        lse = res_d[lse_off:].view(torch.float32).view(self.lse.shape)
-        res_h = torch.empty(res_bytes, dtype=torch.uint8).pin_memory()
+
+        def buffers():
+            in_h = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+            in_h[:q_bytes].copy_(pb.q.contiguous().view(-1).view(torch.uint8))
+            in_h[idx_off:].copy_(pb.kv_indices.contiguous().view(torch.uint8))
+            in_d = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+            res_d = torch.empty(res_bytes, dtype=torch.uint8, device=dev)
+            return dict(
+                in_h=in_h, in_d=in_d, res_d=res_d,
+                res_h=torch.empty(res_bytes, dtype=torch.uint8).pin_memory(),
+                q=in_d[:q_bytes].view(self.q.dtype).view(self.q.shape),
+                idx=in_d[idx_off:].view(torch.int32),
+                out=res_d[:o_bytes].view(self.out.dtype).view(self.out.shape),
+                lse=res_d[lse_off:].view(torch.float32).view(self.lse.shape))
+
+        bufs = [buffers(), buffers()]
         meta = 4 * (len(pb.kv_indptr) + len(pb.last_page_len) + len(pb.qo_indptr))
         fn = self.fi.fi_batch_decode_paged if self.mode in ("decode", "verify") else \
             self.fi.fi_batch_prefill_paged
         sm = self.pb.sm_scale
         s = torch.cuda.current_stream()
 
-        def enqueue():
-            in_d.copy_(in_h, non_blocking=True)
-            fn(self.plan, q, self.k, self.v, idx, sm, out=out, lse=lse)
-            res_h.copy_(res_d, non_blocking=True)
+        def enqueue(b):
+            b["in_d"].copy_(b["in_h"], non_blocking=True)
+            fn(self.plan, b["q"], self.k, self.v, b["idx"], sm, out=b["out"], lse=b["lse"])
+            b["res_h"].copy_(b["res_d"], non_blocking=True)
             ev = torch.cuda.Event()
             ev.record(s)
             return ev
 
         def serial_step():
             self.do_plan()
-            enqueue().synchronize()
+            enqueue(bufs[0]).synchronize()
 
         for _ in range(warmup):
             serial_step()
@@ -332,39 +340,42 @@ class Runner:
             serial_step()
         serial_ms = (time.perf_counter() - t0) / steps * 1e3
 
-        # pipelined: plan(n+1) overlaps run(n)
-        self.do_plan()
-        for _ in range(warmup):
-            ev = enqueue()
+        def pipelined(n):
             self.do_plan()
-            ev.synchronize()
+            prev = enqueue(bufs[0])
+            for i in range(1, n):
+                self.do_plan()
+                ev = enqueue(bufs[i & 1])
+                prev.synchronize()  # step i-1's result is on the host
+                prev = ev
+            prev.synchronize()
+
+        pipelined(warmup + 1)
         t0 = time.perf_counter()
-        for _ in range(steps):
-            ev = enqueue()
-            self.do_plan()
-            ev.synchronize()
+        pipelined(steps)
         pipe_ms = (time.perf_counter() - t0) / steps * 1e3
 
         # where the serial step's time goes (host wall clock per phase)
         n = max(steps, 5)
+        b = bufs[0]
         acc = {"plan_us": 0.0, "h2d_enqueue_us": 0.0, "run_call_us": 0.0, "d2h_enqueue_us": 0.0,
                "wait_us": 0.0}
         for _ in range(n):
             t = time.perf_counter()
             self.do_plan()
             t1 = time.perf_counter()
-            in_d.copy_(in_h, non_blocking=True)
+            b["in_d"].copy_(b["in_h"], non_blocking=True)
             t2 = time.perf_counter()
-            fn(self.plan, q, self.k, self.v, idx, sm, out=out, lse=lse)
+            fn(self.plan, b["q"], self.k, self.v, b["idx"], sm, out=b["out"], lse=b["lse"])
             t3 = time.perf_counter()
-            res_h.copy_(res_d, non_blocking=True)
+            b["res_h"].copy_(b["res_d"], non_blocking=True)
             t4 = time.perf_counter()
             s.synchronize()
             t5 = time.perf_counter()
-            for k_, a, b in (("plan_us", t, t1), ("h2d_enqueue_us", t1, t2),
-                             ("run_call_us", t2, t3), ("d2h_enqueue_us", t3, t4),
-                             ("wait_us", t4, t5)):
-                acc[k_] += (b - a) * 1e6 / n
+            for k_, a_, b_ in (("plan_us", t, t1), ("h2d_enqueue_us", t1, t2),
+                               ("run_call_us", t2, t3), ("d2h_enqueue_us", t3, t4),
+                               ("wait_us", t4, t5)):
+                acc[k_] += (b_ - a_) * 1e6 / n
         brk = {k_: round(v, 1) for k_, v in acc.items()}
         return pipe_ms, serial_ms, in_bytes + meta, res_bytes, brk
 
@@ -516,8 +527,9 @@ def run_ours(args):
                         "note": "every step: fi_plan (metadata upload) + one H2D copy of q and "
                                 "the page table from pinned memory + run + one D2H copy of o "
                                 "and lse + the wait for it; the KV cache stays resident. value: "
-                                "serving-loop order, the host plans step n+1 while the GPU runs "
-                                "step n; serial: each step's phases in turn"},
+                                "a serving loop with one step in flight (plan and enqueue step "
+                                "n+1, then wait for step n's result; double-buffered inputs "
+                                "and outputs); serial: each step's phases in turn"},
                 "gpu_launches": launches, "clocks": clocks, "roofline": roof,
                 "cpu_baseline": cpu, "workloads": extra}
         print(json.dumps(line))

@@ -68,7 +68,8 @@ def load():
     for name in ("fi_batch_prefill_paged", "fi_batch_decode_paged"):
         f = getattr(lib, name)
         f.restype = ctypes.c_int
-        f.argtypes = [P, PT, PT, PT, PT, ctypes.c_float, PT, PT, P]
+        # tensor descriptors as void*: a ctypes byref or the packed bytes
+        f.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, P]
     lib.fi_merge_state.restype = ctypes.c_int
     lib.fi_merge_state.argtypes = [PT, PT, PT, PT, PT, PT, P, P]
     lib.fi_merge_states.restype = ctypes.c_int

@@ -5,6 +5,7 @@ tensors into ``fi_tensor`` descriptors, passes the current CUDA stream, and
 raises ``FiError`` with the library's message on any non-OK status.
 """
 import ctypes
+import struct
 
 import numpy as np
 import torch
@@ -48,6 +49,23 @@ def tensor_desc(t: torch.Tensor) -> FiTensor:
     return FiTensor(t.data_ptr(), code, nd, _I64x4(*t.shape), _I64x4(*t.stride()))
 
 
+# fi_tensor as packed bytes (void*, dtype, ndim, shape[4], stride[4]): about
+# half the cost of building the ctypes structure, which matters on the run()
+# path where six descriptors are made per call.
+_FMT = struct.Struct("<Qii4q4q")
+_Z4 = (0, 0, 0, 0)
+
+
+def _desc(t: torch.Tensor) -> bytes:
+    """fi_tensor bytes of a torch tensor (no copy of its data)."""
+    code = _DTYPES.get(t.dtype)
+    nd = t.dim()
+    if code is None or nd < 1 or nd > 4:
+        return bytes(tensor_desc(t))  # raises the descriptive error
+    return _FMT.pack(t.data_ptr(), code, nd, *(tuple(t.shape) + _Z4)[:4],
+                     *(t.stride() + _Z4)[:4])
+
+
 _PI32 = ctypes.POINTER(ctypes.c_int32)
 
 
@@ -63,8 +81,15 @@ def _host_i32(x):
     return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
 
 
-def _stream_handle(stream):
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_handle(stream, t=None):
+    """The cudaStream_t to pass: `stream`, else torch's current stream (on
+    tensor t's device when t is given)."""
     if stream is None:
+        if t is not None and t.is_cuda and _raw_stream is not None:
+            return _raw_stream(t.get_device())
         if torch.cuda.is_available() and torch.cuda.is_initialized():
             return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
         return ctypes.c_void_p(0)
@@ -219,12 +244,11 @@ def _run(fn, plan, q, k_cache, v_cache, kv_indices, sm_scale, out, lse, return_l
         out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
     if lse is None and return_lse:
         lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
-    qd, kd, vd, idd, od = (tensor_desc(q), tensor_desc(k_cache), tensor_desc(v_cache),
-                           tensor_desc(kv_indices), tensor_desc(out))
-    ld = tensor_desc(lse) if lse is not None else None
-    _check(fn(plan.handle, ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd), ctypes.byref(idd),
-              ctypes.c_float(sm_scale), ctypes.byref(od), ctypes.byref(ld) if ld is not None else None,
-              _stream_handle(stream)))
+    st = fn(plan.handle, _desc(q), _desc(k_cache), _desc(v_cache), _desc(kv_indices),
+            sm_scale, _desc(out), _desc(lse) if lse is not None else None,
+            _stream_handle(stream, q))
+    if st:
+        _check(st)
     return out, lse
 
 

@@ -99,9 +99,15 @@ struct fi_plan_s {
   bool graph = false;
   int32_t max_batch = 0, max_total_rows = 0;
   int num_sms = 152;
-  void* staging = nullptr;  // pinned host buffer for the metadata upload
-  size_t staging_bytes = 0;
-  cudaEvent_t upload_done = nullptr;
+  // Two pinned host buffers for the metadata upload, used in turn: a plan
+  // waits (on the host) only for the upload made two plans earlier, so a
+  // serving loop can plan step n+1 while step n's upload is still queued.
+  void* staging[2] = {nullptr, nullptr};
+  size_t staging_bytes[2] = {0, 0};
+  cudaEvent_t staged[2] = {nullptr, nullptr};  // each buffer's upload has completed
+  bool staged_pending[2] = {false, false};
+  int stage_next = 0;
+  cudaEvent_t upload_done = nullptr;  // the latest upload (the one run() must follow)
   bool upload_pending = false;
   cudaStream_t upload_stream = nullptr;  // the stream of the last metadata upload
   // Stream order between plan() and run(): every run() outside a capture
@@ -204,11 +210,14 @@ extern "C" fi_status fi_plan_create(fi_plan_t* out, void* workspace, size_t work
                   cudaGetErrorString(cudaGetLastError()));
     }
     p->num_sms = n;
-    if (cudaEventCreateWithFlags(&p->upload_done, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&p->run_done, cudaEventDisableTiming) != cudaSuccess) {
-      if (p->upload_done) cudaEventDestroy(p->upload_done);
-      delete p;
-      return fail(FI_ERR_CUDA, "plan_create: cudaEventCreate failed");
+    cudaEvent_t* evs[4] = {&p->upload_done, &p->run_done, &p->staged[0], &p->staged[1]};
+    for (cudaEvent_t* e : evs) {
+      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) {
+        for (cudaEvent_t* f : evs)
+          if (*f) cudaEventDestroy(*f);
+        delete p;
+        return fail(FI_ERR_CUDA, "plan_create: cudaEventCreate failed");
+      }
     }
   }
   *out = p;
@@ -217,10 +226,13 @@ extern "C" fi_status fi_plan_create(fi_plan_t* out, void* workspace, size_t work
 
 extern "C" void fi_plan_destroy(fi_plan_t p) {
   if (!p) return;
-  if (p->upload_pending && p->upload_done) cudaEventSynchronize(p->upload_done);
+  for (int i = 0; i < 2; ++i) {
+    if (p->staged_pending[i]) cudaEventSynchronize(p->staged[i]);
+    if (p->staged[i]) cudaEventDestroy(p->staged[i]);
+    if (p->staging[i]) cudaFreeHost(p->staging[i]);
+  }
   if (p->upload_done) cudaEventDestroy(p->upload_done);
   if (p->run_done) cudaEventDestroy(p->run_done);
-  if (p->staging) cudaFreeHost(p->staging);
   delete p;
 }
 
@@ -756,38 +768,43 @@ fi_status plan_common(fi_plan_t p, const int32_t* qo_indptr, const int32_t* kv_i
     if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
       return fail(FI_ERR_INVALID_ARG, "plan: the stream is capturing a graph (plan outside the "
                   "capture; a captured run() reads the latest plan when the graph is launched)");
-    // the previous upload must have left the pinned buffer before it is reused
-    if (p->upload_pending) {
-      if (cudaEventSynchronize(p->upload_done) != cudaSuccess) {
+    // this buffer's previous upload (two plans ago) must have left it
+    const int slot = p->stage_next;
+    if (p->staged_pending[slot]) {
+      if (cudaEventSynchronize(p->staged[slot]) != cudaSuccess) {
         p->planned = false;
-        return fail(FI_ERR_CUDA, "plan: waiting for the previous upload failed");
+        return fail(FI_ERR_CUDA, "plan: waiting for an earlier upload failed");
       }
-      p->upload_pending = false;
+      p->staged_pending[slot] = false;
     }
-    if (p->staging_bytes < size_t(ns.meta_bytes)) {
-      if (p->staging) cudaFreeHost(p->staging);
-      p->staging = nullptr;
-      p->staging_bytes = 0;
+    if (p->staging_bytes[slot] < size_t(ns.meta_bytes)) {
+      if (p->staging[slot]) cudaFreeHost(p->staging[slot]);
+      p->staging[slot] = nullptr;
+      p->staging_bytes[slot] = 0;
       size_t want = size_t(align_up(ns.meta_bytes * 5 / 4 + 4096, 4096));
-      if (cudaHostAlloc(&p->staging, want, cudaHostAllocDefault) != cudaSuccess) {
-        p->staging = nullptr;
+      if (cudaHostAlloc(&p->staging[slot], want, cudaHostAllocDefault) != cudaSuccess) {
+        p->staging[slot] = nullptr;
         p->planned = false;
         return fail(FI_ERR_CUDA, "plan: cudaHostAlloc(%zu) failed", want);
       }
-      p->staging_bytes = want;
+      p->staging_bytes[slot] = want;
     }
-    write_staging(ns, static_cast<uint8_t*>(p->staging));
+    write_staging(ns, static_cast<uint8_t*>(p->staging[slot]));
     // the workspace is rewritten only after the previous run() has read it
     cudaError_t e = cudaSuccess;
     if (p->run_recorded && p->last_run_stream != s) e = cudaStreamWaitEvent(s, p->run_done, 0);
     // from here the device copy changes: a failure leaves run() refusing
     if (e == cudaSuccess)
-      e = cudaMemcpyAsync(p->ws, p->staging, size_t(ns.meta_bytes), cudaMemcpyHostToDevice, s);
+      e = cudaMemcpyAsync(p->ws, p->staging[slot], size_t(ns.meta_bytes), cudaMemcpyHostToDevice,
+                          s);
+    if (e == cudaSuccess) e = cudaEventRecord(p->staged[slot], s);
     if (e == cudaSuccess) e = cudaEventRecord(p->upload_done, s);
     if (e != cudaSuccess) {
       p->planned = false;
       return fail(FI_ERR_CUDA, "plan: metadata upload failed: %s", cudaGetErrorString(e));
     }
+    p->staged_pending[slot] = true;
+    p->stage_next = slot ^ 1;
     p->upload_pending = true;
     p->upload_stream = s;
   }

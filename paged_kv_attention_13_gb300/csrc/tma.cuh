@@ -59,18 +59,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of `parity` to complete; false on timeout or abort.
-// The abort flag and the clock are looked at every 32 failed polls.
+// try_wait itself suspends the thread for a while before it reports that
+// the phase is still open, so the abort flag and the clock are looked at
+// after every failed poll.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile WaitCtl* ctl) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31) == 0) {
-      if (ctl->abort) return false;
-      if (globaltimer() - t0 > ctl->limit_ns) {
-        ctl->abort = 1;
-        return false;
-      }
+    if (ctl->abort) return false;
+    if (globaltimer() - t0 > ctl->limit_ns) {
+      ctl->abort = 1;
+      return false;
     }
   }
 }
