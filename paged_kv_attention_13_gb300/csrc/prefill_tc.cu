@@ -32,6 +32,8 @@
 // (!causal || j <= i + Lk - Lq) && (wl < 0 || j + Lq + wl >= Lk + i). Key
 // tiles outside the item's live range are never loaded; the per-element
 // test runs on tiles that straddle a bound only.
+#include <type_traits>
+
 #include "tma.cuh"
 
 namespace fi {
@@ -68,8 +70,7 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.
@@ -183,8 +184,7 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // Two Q tiles per CTA (A: packed rows [row0, row0+tr), B: the next tr rows)
@@ -280,8 +280,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // V stages are released separately (K after the S products, V after the
     // P V products), and K is issued one tile ahead of V.
     int gk = 0, gv = 0, qc = 0;
-    bool armed[2][2] = {{false, false}, {false, false}};
-    uint32_t apar[2][2] = {{0, 0}, {0, 0}};
+    // stage (which, st) at bit 2 * which + st: armed at least once, and the
+    // parity of its latest arming (bit masks, so they stay in registers)
+    uint32_t armed = 0, apar = 0;
     bool q_armed = false;
     uint32_t q_par = 0;
     bool ok = true;
@@ -299,8 +300,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (cntr >= 2 && !mbar_wait(BAR(empty + st), ((cntr >> 1) - 1) & 1, ctl)) okl = false;
         if (okl) {
           mbar_expect_tx(BAR(full + st), uint32_t(nvalid) * uint32_t(kv_box_rows) * 128u * 2u);
-          armed[which][st] = true;
-          apar[which][st] = (cntr >> 1) & 1;
+          const uint32_t bit = 1u << (2 * which + st);
+          armed |= bit;
+          apar = ((cntr >> 1) & 1) ? (apar | bit) : (apar & ~bit);
         }
       }
       okl = __shfl_sync(0xffffffffu, okl, 0);
@@ -380,39 +382,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (q_armed) mbar_wait(BAR(B_QFULL), q_par, &drain);
       for (int which = 0; which < 2; ++which)
         for (int s = 0; s < 2; ++s)
-          if (armed[which][s])
-            mbar_wait(BAR((which ? B_VFULL : B_KFULL) + s), apar[which][s], &drain);
+          if ((armed >> (2 * which + s)) & 1)
+            mbar_wait(BAR((which ? B_VFULL : B_KFULL) + s), (apar >> (2 * which + s)) & 1, &drain);
       if (drain.abort) ctl->abort = 1;  // an expired drain wait is reported too
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Lane 0 runs the schedule, its waits and every tcgen05 operation. The
+    // shared-memory descriptors are made once: a descriptor's start address
+    // is its low 14 bits (address / 16), so the descriptor of an address plus
+    // an offset is the base descriptor plus offset / 16 (shared addresses stay
+    // below 256 KB). Building both descriptors per instruction cost about 130
+    // cycles per 128 x 128 x 16 MMA, twice the tensor core's 64.
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(BF16, false, 128, 128);
       constexpr uint32_t kIdO = idesc_f16(BF16, true, 128, 128);
+      const uint64_t dQ = sdesc_sw128(sbase + kOffQ, 16, 1024);
+      const uint64_t dK = sdesc_sw128(sbase + kOffK, 16, 1024);
+      const uint64_t dV = sdesc_sw128(sbase + kOffV, kBlk, 1024);
+      constexpr uint64_t kTile16 = kTile >> 4;
       // S_x = Q_xq K^T into the S columns of warpgroup x (xq = x, or Q tile
       // A for both warpgroups of a split item)
       auto issue_s = [&](int x, int st, int xq) {
         const uint32_t d = tmem + uint32_t(x) * 128u;
+        const uint64_t a0 = dQ + uint64_t(xq) * kTile16, b0 = dK + uint64_t(st) * kTile16;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t koff = uint32_t(kk >> 2) * kBlk + uint32_t(kk & 3) * 32u;
-          const uint64_t ad = sdesc_sw128(sbase + kOffQ + xq * kTile + koff, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sbase + kOffK + st * kTile + koff, 16, 1024);
-          tc_mma(d, ad, bd, kIdS, kk > 0 ? 1u : 0u);
+          const uint64_t off = uint64_t((kk >> 2) * kBlk + (kk & 3) * 32) >> 4;
+          tc_mma(d, a0 + off, b0 + off, kIdS, kk > 0 ? 1u : 0u);
         }
         tc_commit(BAR(B_SFULL + x));
       };
       auto issue_pv = [&](int x, int st, bool acc) {  // O_x += P_x V
         const uint32_t d = tmem + 256u + uint32_t(x) * 128u;
         const uint32_t a = tmem + uint32_t(x) * 128u;
+        const uint64_t b0 = dV + uint64_t(st) * kTile16;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = sdesc_sw128(sbase + kOffV + st * kTile + uint32_t(kk) * 2048u, kBlk, 1024);
-          tc_mma_ts(d, a + uint32_t(kk) * 8u, bd, kIdO, (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_ts(d, a + uint32_t(kk) * 8u, b0 + uint64_t(kk) * (2048 >> 4), kIdO,
+                    (acc || kk > 0) ? 1u : 0u);
       };
-      int gt = 0, qc = 0, cnt[2] = {0, 0}, itc[2] = {0, 0};
+      int gt = 0, qc = 0, cnt0 = 0, cnt1 = 0, itc0 = 0, itc1 = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
         if (items[w].b < 0) continue;  // schedule padding
@@ -434,9 +445,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (n == 2) tc_commit(BAR(B_QEMPTY));
           for (int j = 0; j < n && ok; ++j) {
             const int xw = j & 1, jx = j >> 1, g1 = gt + j, st = g1 & 1;
-            if (jx == 0 && itc[xw] > 0 &&
-                !mbar_wait(BAR(B_OFREE + xw), (itc[xw] - 1) & 1, ctl)) { ok = false; break; }
-            if (!mbar_wait(BAR(B_PFULL + xw), (cnt[xw] + jx) & 1, ctl)) { ok = false; break; }
+            const int itc_x = xw ? itc1 : itc0, cnt_x = xw ? cnt1 : cnt0;
+            if (jx == 0 && itc_x > 0 &&
+                !mbar_wait(BAR(B_OFREE + xw), (itc_x - 1) & 1, ctl)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_PFULL + xw), (cnt_x + jx) & 1, ctl)) { ok = false; break; }
             if (!mbar_wait(BAR(B_VFULL + st), (g1 >> 1) & 1, ctl)) { ok = false; break; }
             tc_fence_after();
             issue_pv(xw, st, jx > 0);
@@ -452,10 +464,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           gt += n;
           ++qc;
-          cnt[0] += (n + 1) / 2;
-          cnt[1] += n / 2;
-          ++itc[0];
-          ++itc[1];
+          cnt0 += (n + 1) / 2;
+          cnt1 += n / 2;
+          ++itc0;
+          ++itc1;
           continue;
         }
         if (!mbar_wait(BAR(B_KFULL + (gt & 1)), (gt >> 1) & 1, ctl)) { ok = false; break; }
@@ -467,8 +479,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int j = 0; j < n && ok; ++j) {
           const int g1 = gt + j, st = g1 & 1, st1 = (g1 + 1) & 1;
           // ---- tile A
-          if (j == 0 && itc[0] > 0 && !mbar_wait(BAR(B_OFREE), (itc[0] - 1) & 1, ctl)) { ok = false; break; }
-          if (!mbar_wait(BAR(B_PFULL), (cnt[0] + j) & 1, ctl)) { ok = false; break; }
+          if (j == 0 && itc0 > 0 && !mbar_wait(BAR(B_OFREE), (itc0 - 1) & 1, ctl)) { ok = false; break; }
+          if (!mbar_wait(BAR(B_PFULL), (cnt0 + j) & 1, ctl)) { ok = false; break; }
           if (!mbar_wait(BAR(B_VFULL + st), (g1 >> 1) & 1, ctl)) { ok = false; break; }
           tc_fence_after();
           issue_pv(0, st, j > 0);
@@ -485,8 +497,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           // ---- tile B
           if (hasB) {
-            if (j == 0 && itc[1] > 0 && !mbar_wait(BAR(B_OFREE + 1), (itc[1] - 1) & 1, ctl)) { ok = false; break; }
-            if (!mbar_wait(BAR(B_PFULL + 1), (cnt[1] + j) & 1, ctl)) { ok = false; break; }
+            if (j == 0 && itc1 > 0 && !mbar_wait(BAR(B_OFREE + 1), (itc1 - 1) & 1, ctl)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_PFULL + 1), (cnt1 + j) & 1, ctl)) { ok = false; break; }
             tc_fence_after();
             issue_pv(1, st, j > 0);
             tc_commit(BAR(B_VEMPTY + st));
@@ -500,11 +512,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         gt += n;
         ++qc;
-        cnt[0] += n;
-        ++itc[0];
+        cnt0 += n;
+        ++itc0;
         if (hasB) {
-          cnt[1] += n;
-          ++itc[1];
+          cnt1 += n;
+          ++itc1;
         }
       }
       // every MMA this thread issued has completed before tensor memory is freed
@@ -585,50 +597,126 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool need_mask = (t0 < G.kv_lo) || (t0 + 128 > G.kv_hi) ||
                                (causal && t0 + 127 > ix0 + G.lk - G.lq) ||
                                (wl >= 0 && t0 < G.lk - G.lq + ix1 - wl);
-        // the whole 128-column row in registers, one wait for the four loads
+        // The row's 128 scores end up in registers (sv). P = exp2(s * scale -
+        // m) is packed in pairs over the first 64 S columns; the scaling and
+        // the row sum run as packed fp32 pairs. (Computing a share of the
+        // exponentials on the FMA pipe instead of the SFU measured slower.)
         uint32_t sv[4][32];
+        const float2 sc2 = make_float2(scale, scale);
+        float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        auto mask_chunk = [&](auto cc) {
+          constexpr int c = decltype(cc)::value;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + uint32_t(c) * 32u, sv[c]);
+          for (int e = 0; e < 32; ++e) {
+            const int key = t0 + c * 32 + e;
+            if (key < jmin || key > jmax) sv[c][e] = __float_as_uint(neg_inf());
+          }
+        };
+        auto exp_chunk = [&](auto cc, float2 nmu2) {
+          constexpr int c = decltype(cc)::value;
+          uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_wait_ld_tied(sv[c]);
-        if (need_mask) {
+          for (int e = 0; e < 16; ++e) {
+            const float2 xx = __ffma2_rn(
+                make_float2(__uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1])), sc2,
+                nmu2);
+            const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
+            ps2[e & 1] = __fadd2_rn(ps2[e & 1], pp);
+            pk[e] = DT::pack(pp.x, pp.y);
+          }
+          tmem_st16(tS + uint32_t(c) * 16u, pk);
+        };
+        using C0 = std::integral_constant<int, 0>;
+        using C1 = std::integral_constant<int, 1>;
+        using C2 = std::integral_constant<int, 2>;
+        using C3 = std::integral_constant<int, 3>;
+        // Warm rows (a finite running max) take their exponentials against
+        // the running max straight away, with no max pass over the tile, and
+        // the second half of the row is still loading while the first half is
+        // exponentiated. If the tile's sum stays at most 2^8, no p exceeds
+        // 2^8, the bound the lazy rescale keeps, and the tile is done. Else
+        // (and for a warp with a cold row: the first tile, or a row whose keys
+        // have all been masked so far) the row max is taken and the tile
+        // follows the lazy rule: a new reference when the max exceeds the old
+        // by more than 2^8, O rescaled, P recomputed. Every choice is
+        // warp-uniform (the tensor-memory accesses are .sync.aligned).
+        const bool cold = __any_sync(0xffffffffu, m_run == neg_inf());
+        bool redo = cold;
+        if (!cold) {
+          tmem_ld32(tS, sv[0]);
+          tmem_ld32(tS + 32u, sv[1]);
+          tmem_wait_ld_tied(sv[0]);
+          tmem_wait_ld_tied(sv[1]);
+          tmem_ld32(tS + 64u, sv[2]);
+          tmem_ld32(tS + 96u, sv[3]);
+          const float2 nm2 = make_float2(-m_run, -m_run);
+          if (need_mask) {
+            mask_chunk(C0());
+            mask_chunk(C1());
+          }
+          exp_chunk(C0(), nm2);
+          exp_chunk(C1(), nm2);
+          tmem_wait_ld_tied(sv[2]);
+          tmem_wait_ld_tied(sv[3]);
+          if (need_mask) {
+            mask_chunk(C2());
+            mask_chunk(C3());
+          }
+          exp_chunk(C2(), nm2);
+          exp_chunk(C3(), nm2);
+          const float tsum = (ps2[0].x + ps2[1].x) + (ps2[0].y + ps2[1].y);
+          redo = __any_sync(0xffffffffu, tsum > 256.f);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + uint32_t(c) * 32u, sv[c]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_wait_ld_tied(sv[c]);
+          if (need_mask) {
+            mask_chunk(C0());
+            mask_chunk(C1());
+            mask_chunk(C2());
+            mask_chunk(C3());
+          }
+        }
+        float m_new = m_run, corr = 1.f;
+        if (redo) {
+          // row max of the raw scores: eight independent chains of
+          // three-input maxima
+          float mp[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) mp[q] = neg_inf();
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int jj = t0 + c * 32 + e;
-              if (jj < jmin || jj > jmax) sv[c][e] = __float_as_uint(neg_inf());
-            }
-        }
-        // row max of the raw scores: eight independent chains of three-input
-        // maxima (the softmax is bound by instruction issue, so every
-        // instruction per score counts)
-        float mp[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) mp[q] = neg_inf();
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            mp[e & 7] = fmax3(mp[e & 7], __uint_as_float(sv[c][2 * e]),
-                              __uint_as_float(sv[c][2 * e + 1]));
-        const float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                                 fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-        const float mx = mraw * scale;  // scale > 0
-        float m_new = m_run;
-        if (mx > m_run + 8.f || (m_run == neg_inf() && mraw != neg_inf())) m_new = mx;
-        const float corr = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
-        const float mu = (m_new == neg_inf()) ? 0.f : m_new;
-        // O rescale: S_x(j) is complete, so the P V product before it is too
-        if (jj > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+            for (int e = 0; e < 16; ++e)
+              mp[e & 7] = fmax3(mp[e & 7], __uint_as_float(sv[c][2 * e]),
+                                __uint_as_float(sv[c][2 * e + 1]));
+          const float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                   fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+          const float mx = mraw * scale;  // scale > 0
+          if (mx > m_run + 8.f || (m_run == neg_inf() && mraw != neg_inf())) m_new = mx;
+          corr = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
+          // a warm warp whose rows all keep their reference keeps its P
+          if (cold || __any_sync(0xffffffffu, m_new != m_run)) {
+            // O rescale: S_x(j) is complete, so the P V product before it is too
+            if (jj > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tO + uint32_t(c) * 32u, ov);
-            tmem_wait_ld();
+              for (int c = 0; c < 4; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(tO + uint32_t(c) * 32u, ov);
+                tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
-            tmem_st32(tO + uint32_t(c) * 32u, ov);
+                for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
+                tmem_st32(tO + uint32_t(c) * 32u, ov);
+              }
+            }
+            const float mu = (m_new == neg_inf()) ? 0.f : m_new;
+            const float2 nmu2 = make_float2(-mu, -mu);
+            ps2[0] = ps2[1] = make_float2(0.f, 0.f);
+            exp_chunk(C0(), nmu2);
+            exp_chunk(C1(), nmu2);
+            exp_chunk(C2(), nmu2);
+            exp_chunk(C3(), nmu2);
           }
         }
         bool zeroed = false;
@@ -644,26 +732,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
           zeroed = true;
-        }
-        // P = exp2(s * scale - m), packed in pairs, over the S columns; the
-        // scaling and the row sum run as packed fp32 pairs (one instruction per
-        // two scores). Computing a share of the exponentials on the FMA pipe
-        // instead of the SFU measured slower: this loop is issue-bound.
-        const float2 sc2 = make_float2(scale, scale), nmu2 = make_float2(-mu, -mu);
-        float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float2 xx = __ffma2_rn(
-                make_float2(__uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1])), sc2,
-                nmu2);
-            const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
-            ps2[e & 1] = __fadd2_rn(ps2[e & 1], pp);
-            pk[e] = DT::pack(pp.x, pp.y);
-          }
-          tmem_st16(tS + uint32_t(c) * 16u, pk);
         }
         tmem_wait_st();
         l_run = l_run * corr + ((ps2[0].x + ps2[1].x) + (ps2[0].y + ps2[1].y));
