@@ -610,6 +610,10 @@ def other_workloads(args, dev, ws, hbm_peak, bf16_peak):
         if P == 16:
             one("prefill_p16_noncausal", pb, False, -1, "prefill", bound="tensor")
             one("prefill_p16_causal_wl127", pb, True, 127, "prefill")
+    pb = workloads.batch_prefill_hd64()
+    one("prefill_hd64_f16_p16_causal", pb, True, -1, "prefill", bound="tensor")
+    pb = workloads.batch_prefill(page_size=48)
+    one("prefill_p48_causal", pb, True, -1, "prefill", bound="tensor")
     pb = workloads.ragged_prefill()
     one("ragged_prefill_causal", pb, True, -1, "ragged", bound="tensor")
     pb = workloads.tree_verify(batch=32)
@@ -685,6 +689,8 @@ PROFILE_CASES = {
     "prefill_b4_causal": (lambda: workloads.batch_prefill(page_size=16, batch=4), True, -1, "prefill"),
     "prefill_p1024_causal": (lambda: workloads.batch_prefill(page_size=1024), True, -1, "prefill"),
     "prefill_p16_noncausal": (lambda: workloads.batch_prefill(page_size=16), False, -1, "prefill"),
+    "prefill_hd64_f16_causal": (lambda: workloads.batch_prefill_hd64(), True, -1, "prefill"),
+    "prefill_p48_causal": (lambda: workloads.batch_prefill(page_size=48), True, -1, "prefill"),
     "longctx_causal": (lambda: workloads.long_context(), True, -1, "prefill"),
     "ragged_prefill_causal": (lambda: workloads.ragged_prefill(), True, -1, "ragged"),
     "tree_verify_b32": (lambda: workloads.tree_verify(batch=32), True, -1, "masked"),

@@ -256,8 +256,12 @@ int choose_kernel(int32_t q_len_per_req, int32_t g, int64_t max_rows_per_req, in
     return g <= 64 ? fi::kPrefillM64 : -1;
   }
   if (q_len_per_req == 1 && fi::decode_shuffle_supports(d, g)) return fi::kDecode;
+  // above the short-query kernel's rows: the tcgen05 kernel wherever its TMA
+  // boxes fit (head_dim 64 or 128, page sizes that are multiples of 8); the
+  // mma.sync kernels keep page sizes 1..7 and other odd sizes
+  if (max_rows_per_req > kShortRowsMax && fi::prefill_tc_supports(d, page_size, g))
+    return fi::kPrefillM128;
   if (max_rows_per_req <= 16 && g <= 16) return fi::kPrefillM16;
-  if (max_rows_per_req > 64 && fi::prefill_tc_supports(d, page_size, g)) return fi::kPrefillM128;
   if (g <= 64) return fi::kPrefillM64;
   if (fi::prefill_tc_supports(d, page_size, g)) return fi::kPrefillM128;
   return -1;

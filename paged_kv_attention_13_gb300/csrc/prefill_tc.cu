@@ -40,14 +40,22 @@ namespace fi {
 namespace {
 
 constexpr int kTcThreads = 384;  // 4 control warps + 2 softmax warpgroups
-constexpr int kBlk = 128 * 128;       // 128 rows x 128 bytes: one 64-column swizzled block
-constexpr int kTile = 2 * kBlk;       // 128 x 128 16-bit elements
-constexpr int kOffQ = 0;              // Q tiles A and B
-constexpr int kOffK = kOffQ + 2 * kTile;  // 2 stages
-constexpr int kOffV = kOffK + 2 * kTile;
-constexpr int kOffBar = kOffV + 2 * kTile;
-constexpr int kOffMl = kOffBar + 256;          // row max and sum handed between warpgroups
-constexpr int kSmemTc = kOffMl + 1024 + 1024;  // barriers, exchange rows, alignment slack
+constexpr int kBlk = 128 * 128;  // 128 rows x 128 bytes: one 64-column swizzled block
+
+// Shared-memory layout for head_dim D (64 or 128): a tile is 128 rows of D
+// 16-bit columns, D / 64 swizzled blocks; Q tiles A and B, two K and two V
+// stages, the barriers, and the rows handed between the warpgroups.
+template <int D>
+struct TcLayout {
+  static constexpr int kH = D / 64;
+  static constexpr int kTile = kH * kBlk;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kTile;
+  static constexpr int kOffV = kOffK + 2 * kTile;
+  static constexpr int kOffBar = kOffV + 2 * kTile;
+  static constexpr int kOffMl = kOffBar + 256;
+  static constexpr int kSmem = kOffMl + 1024 + 1024;  // + alignment slack
+};
 
 // barrier slots
 constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 4, B_VFULL = 6, B_VEMPTY = 8,
@@ -196,13 +204,16 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
 // warpgroups run the same rows, A on the even key tiles and B on the odd
 // ones, each with its own S/P and O in tensor memory, and at the end A
 // combines the two states (m, l, O) by their maxima and writes the output.
-template <bool BF16>
+template <bool BF16, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tq,
                       const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                       int kv_box_rows) {
   using DT = Dt<BF16>;
   using T = typename DT::T;
+  using L = TcLayout<D>;
+  constexpr int kH = L::kH, kTile = L::kTile, kOffQ = L::kOffQ, kOffK = L::kOffK,
+                kOffV = L::kOffV, kOffBar = L::kOffBar, kOffMl = L::kOffMl;
   // the page table failed the index check: the whole CTA leaves before any
   // barrier, tensor-memory allocation or copy
   if (static_cast<const WsHeader*>(p.ws)->index_error) return;
@@ -287,6 +298,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t q_par = 0;
     bool ok = true;
     const int npg = 128 / kv_box_rows;
+    // page and slot of key k (page_shift >= 0: a power-of-two page size)
+    const int pshift = p.page_shift, pmask = pshift >= 0 ? (1 << pshift) - 1 : 0;
+    auto page_of = [&](int k) { return pshift >= 0 ? (k >> pshift) : k / p.page_size; };
+    auto slot_of = [&](int k) { return pshift >= 0 ? (k & pmask) : k % p.page_size; };
     const int tiles_per_batch = 32 / npg;  // page indices the warp holds per batch of tiles
     // issue K (which = 0) or V (which = 1) of tile t, whose page index this
     // lane holds in `page` (valid when `has`)
@@ -299,7 +314,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) {
         if (cntr >= 2 && !mbar_wait(BAR(empty + st), ((cntr >> 1) - 1) & 1, ctl)) okl = false;
         if (okl) {
-          mbar_expect_tx(BAR(full + st), uint32_t(nvalid) * uint32_t(kv_box_rows) * 128u * 2u);
+          mbar_expect_tx(BAR(full + st), uint32_t(nvalid) * uint32_t(kv_box_rows) * uint32_t(D) * 2u);
           const uint32_t bit = 1u << (2 * which + st);
           armed |= bit;
           apar = ((cntr >> 1) & 1) ? (apar | bit) : (apar & ~bit);
@@ -307,11 +322,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       okl = __shfl_sync(0xffffffffu, okl, 0);
       if (okl && has) {
-        // ragged: one logical page per request, the slot is the row
-        const int slot0 = p.ragged ? G.kv_start + t0 : (kv_box_rows == 128) ? (t0 % p.page_size) : 0;
+        // box `lane` covers keys t0 + lane * kv_box_rows onwards, inside one
+        // page (kv_box_rows divides the page size); ragged: one logical page
+        // per request, the slot is the row
+        const int slot0 = p.ragged ? G.kv_start + t0 : slot_of(t0 + lane * kv_box_rows);
         const uint32_t roff = uint32_t(lane * kv_box_rows) * 128u;
         const uint32_t dst = sbase + (which ? kOffV : kOffK) + st * kTile + roff;
-        for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < kH; ++h)
           tma_load_4d(dst + h * kBlk, which ? &tv : &tk, BAR(full + st), h * 64, G.hk, slot0, page);
       }
       return okl;
@@ -328,7 +345,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // its page L % npg (0 when past the request)
       auto fetch = [&](int bt) {
         const int t = bt * tiles_per_batch + lane / npg;
-        const int pg = (G.t_start + t * 128) / p.page_size + lane % npg;
+        const int pg = page_of(G.t_start + t * 128 + (lane % npg) * kv_box_rows);
         if (p.ragged) return 0;
         return (t < G.n_tiles && pg < n_pages && lane < tiles_per_batch * npg) ? __ldg(pages + pg) : 0;
       };
@@ -336,11 +353,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) {
         if (qc > 0 && !mbar_wait(BAR(B_QEMPTY), (qc - 1) & 1, ctl)) ok = false;
         if (ok) {
-          mbar_expect_tx(BAR(B_QFULL), (hasB ? 2u : 1u) * 2u * uint32_t(tr) * 128u);
+          mbar_expect_tx(BAR(B_QFULL), (hasB ? 2u : 1u) * uint32_t(tr) * uint32_t(D) * 2u);
           q_armed = true;
           q_par = qc & 1;
           for (int x = 0; x < (hasB ? 2 : 1); ++x)
-            for (int h = 0; h < 2; ++h)
+            for (int h = 0; h < kH; ++h)
               tma_load_3d(sbase + kOffQ + x * kTile + h * kBlk, &tq, BAR(B_QFULL), h * 64,
                           G.hk * g, G.token0 + G.i0 + x * (tr / g));
         }
@@ -359,8 +376,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             idx_cur = idx_nxt;
             idx_nxt = fetch(bt + 1);
           }
-          const int pf = (G.t_start + step * 128) / p.page_size;
-          has = lane < npg && pf + lane < n_pages;
+          has = lane < npg && page_of(G.t_start + step * 128 + lane * kv_box_rows) < n_pages;
           page = __shfl_sync(0xffffffffu, idx_cur, (k * npg + lane) & 31);
           nvalid = __popc(__ballot_sync(0xffffffffu, has));
           ok = load(0, G, step, gk, has, page, nvalid);
@@ -397,7 +413,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // cycles per 128 x 128 x 16 MMA, twice the tensor core's 64.
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(BF16, false, 128, 128);
-      constexpr uint32_t kIdO = idesc_f16(BF16, true, 128, 128);
+      constexpr uint32_t kIdO = idesc_f16(BF16, true, 128, D);
       const uint64_t dQ = sdesc_sw128(sbase + kOffQ, 16, 1024);
       const uint64_t dK = sdesc_sw128(sbase + kOffK, 16, 1024);
       const uint64_t dV = sdesc_sw128(sbase + kOffV, kBlk, 1024);
@@ -408,7 +424,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t d = tmem + uint32_t(x) * 128u;
         const uint64_t a0 = dQ + uint64_t(xq) * kTile16, b0 = dK + uint64_t(st) * kTile16;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {  // the head dim in steps of 16
           const uint64_t off = uint64_t((kk >> 2) * kBlk + (kk & 3) * 32) >> 4;
           tc_mma(d, a0 + off, b0 + off, kIdS, kk > 0 ? 1u : 0u);
         }
@@ -567,12 +583,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!active) {
         if (n == 0 && row_ok) {  // no live key: o = 0, lse = -inf
           if (direct) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (int64_t(tok) * Hq + head) * 128);
-            for (int q = 0; q < 16; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (int64_t(tok) * Hq + head) * D);
+            for (int q = 0; q < D / 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);
             if (p.lse) p.lse[int64_t(tok) * Hq + head] = neg_inf();
           } else {
-            float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * 128);
-            for (int q = 0; q < 32; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * D);
+            for (int q = 0; q < D / 4; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
             tmp_lse[int64_t(slot) * Hq + head] = neg_inf();
           }
         }
@@ -701,7 +717,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // O rescale: S_x(j) is complete, so the P V product before it is too
             if (jj > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll 1
-              for (int c = 0; c < 4; ++c) {
+              for (int c = 0; c < D / 32; ++c) {
                 uint32_t ov[32];
                 tmem_ld32(tO + uint32_t(c) * 32u, ov);
                 tmem_wait_ld();
@@ -725,7 +741,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!wwait(BAR(B_VFULL + st), (g1 >> 1) & 1)) { ok = false; break; }
           if (t0 + r >= G.lk) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < kH; ++h) {
               uint4* row = reinterpret_cast<uint4*>(smem + kOffV + st * kTile + h * kBlk + r * 128);
 #pragma unroll
               for (int q = 0; q < 8; ++q) row[q] = make_uint4(0, 0, 0, 0);
@@ -776,7 +792,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       const uint32_t tOb = tmem + lane_addr + 384u;  // O of warpgroup B
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
         tmem_ld32(tO + uint32_t(c) * 32u, ov);
         tmem_wait_ld();
@@ -794,7 +810,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (row_ok) {
           if (direct) {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) +
-                                                  (int64_t(tok) * Hq + head) * 128 + c * 32);
+                                                  (int64_t(tok) * Hq + head) * D + c * 32);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               dst[q] = make_uint4(
@@ -803,7 +819,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   DT::pack(__uint_as_float(ov[8 * q + 4]), __uint_as_float(ov[8 * q + 5])),
                   DT::pack(__uint_as_float(ov[8 * q + 6]), __uint_as_float(ov[8 * q + 7])));
           } else {
-            float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * 128 + c * 32);
+            float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * D + c * 32);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               dst[q] = make_float4(__uint_as_float(ov[4 * q]), __uint_as_float(ov[4 * q + 1]),
@@ -843,10 +859,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 }  // namespace
 
+namespace {
+int gcd_i(int a, int b) {
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+template <bool BF16, int D>
+cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                      const CUtensorMap& tv, int box_rows, int grid, cudaStream_t s) {
+  // the shared-memory limit: once per device, before any capture
+  static std::atomic<uint64_t> done{0};
+  constexpr int kSmem = TcLayout<D>::kSmem;
+  const cudaError_t attr = smem_attr_once(prefill_tc_kernel<BF16, D>, kSmem, done);
+  if (attr != cudaSuccess) return attr;
+  prefill_tc_kernel<BF16, D><<<grid, kTcThreads, kSmem, s>>>(p, tq, tk, tv, box_rows);
+  return cudaGetLastError();
+}
+}  // namespace
+
+// head_dim 64 or 128; K/V boxes of gcd(page_size, 128) slots must be whole
+// 8-row swizzle atoms, so the page size is a multiple of 8 (any multiple:
+// a box never crosses a page because its size divides the page size).
 bool prefill_tc_supports(int head_dim, int page_size, int group) {
-  if (head_dim != 128 || group < 1 || group > 128) return false;
-  if (page_size >= 128) return page_size % 128 == 0;
-  return page_size >= 16 && 128 % page_size == 0;
+  if ((head_dim != 128 && head_dim != 64) || group < 1 || group > 128) return false;
+  return page_size >= 8 && page_size % 8 == 0;
 }
 
 cudaError_t launch_prefill_tc(const AttnParams& p, int head_dim, int group, int tile_rows,
@@ -855,7 +896,7 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int head_dim, int group, int 
   if (grid <= 0) return cudaSuccess;
   if (!prefill_tc_supports(head_dim, p.page_size, group)) return cudaErrorInvalidValue;
   CUtensorMap tq, tk, tv;
-  const int box_rows = p.page_size >= 128 ? 128 : p.page_size;
+  const int box_rows = gcd_i(p.page_size, 128);
   {
     cuuint64_t dims[3] = {cuuint64_t(head_dim), cuuint64_t(p.num_qo_heads), cuuint64_t(q_rows)};
     cuuint64_t str[2] = {cuuint64_t(p.q_stride_head) * 2, cuuint64_t(p.q_stride_tok) * 2};
@@ -868,19 +909,11 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int head_dim, int group, int 
       !encode_kv_map(&tv, p, false, bf16, head_dim, num_pages, 64, box_rows,
                      CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  // the shared-memory limit: once per device, before any capture
-  if (bf16) {
-    static std::atomic<uint64_t> done{0};
-    const cudaError_t attr = smem_attr_once(prefill_tc_kernel<true>, kSmemTc, done);
-    if (attr != cudaSuccess) return attr;
-    prefill_tc_kernel<true><<<grid, kTcThreads, kSmemTc, s>>>(p, tq, tk, tv, box_rows);
-  } else {
-    static std::atomic<uint64_t> done{0};
-    const cudaError_t attr = smem_attr_once(prefill_tc_kernel<false>, kSmemTc, done);
-    if (attr != cudaSuccess) return attr;
-    prefill_tc_kernel<false><<<grid, kTcThreads, kSmemTc, s>>>(p, tq, tk, tv, box_rows);
-  }
-  return cudaGetLastError();
+  if (head_dim == 128)
+    return bf16 ? launch_tc<true, 128>(p, tq, tk, tv, box_rows, grid, s)
+                : launch_tc<false, 128>(p, tq, tk, tv, box_rows, grid, s);
+  return bf16 ? launch_tc<true, 64>(p, tq, tk, tv, box_rows, grid, s)
+              : launch_tc<false, 64>(p, tq, tk, tv, box_rows, grid, s);
 }
 
 }  // namespace fi

@@ -91,11 +91,15 @@ def test_verify_layouts(layout, page_size, kernel):
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)
-def test_short_prefill_layouts(layout):
-    pb = workloads.make_paged_batch([20, 7, 31], [20, 300, 64], 8, 4, 64, 16, "bf16", 56)
+@pytest.mark.parametrize("page_size,kernel", [(16, "prefill_m128"), (2, "prefill_m64")])
+def test_short_prefill_layouts(layout, page_size, kernel):
+    """14..62 packed rows: the tcgen05 kernel (one half-used Q tile) where its
+    boxes fit, the cp.async mma kernel for page sizes under 8."""
+    pb = workloads.make_paged_batch([20, 7, 31], [20, 300, 64], 8, 4, 64, page_size, "bf16",
+                                    56 + page_size)
     out, lse, kern = run(pb, layout, "prefill", True, 31)
-    assert kern == "prefill_m64"
-    assert_close(pb, out, lse, True, 31, what="short prefill %s" % layout)
+    assert kern == kernel
+    assert_close(pb, out, lse, True, 31, what="short prefill %s P=%d" % (layout, page_size))
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)

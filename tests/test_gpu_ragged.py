@@ -4,8 +4,8 @@ The batch is generated as a page-size-1 cache with an unpermuted page table,
 so the cache rows are the contiguous K/V in request order: the ragged tensors
 are that cache with the page dim dropped, and the oracle reads the paged
 view of the same values. Every kernel path is covered: the short-query
-kernel (requests of at most 16 packed rows), the mma.sync M = 64 kernel and
-the tcgen05 kernel.
+kernel (requests of at most 16 packed rows) and the tcgen05 kernel (above 32
+packed rows, head_dim 64 and 128).
 """
 import pytest
 import torch
@@ -49,11 +49,13 @@ def test_ragged_tensor_core_prefill(causal, wl, force):
 
 @pytest.mark.parametrize("causal,wl", [(True, -1), (False, 31)])
 def test_ragged_mid_prefill(causal, wl):
-    """Requests of 17..64 packed rows (mma.sync M = 64), head_dim 64, fp16."""
+    """Requests of 17..64 packed rows, head_dim 64, fp16: above the
+    short-query kernel's 32 rows they take the tcgen05 kernel (one half-used
+    Q tile per item)."""
     pb = ragged_batch([20, 9, 32], [20, 333, 64], 8, 4, 64, "f16", 12)
     out, lse, kern = run_ragged(pb, causal, wl)
-    assert kern == "prefill_m64"
-    assert_close(pb, out, lse, causal, wl, what="ragged m64")
+    assert kern == "prefill_m128"
+    assert_close(pb, out, lse, causal, wl, what="ragged mid")
 
 
 @pytest.mark.parametrize("causal,wl", [(True, -1), (False, -1), (True, 9)])

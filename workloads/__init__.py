@@ -159,6 +159,12 @@ def batch_prefill(page_size: int = 16, variant: int = 0, batch: int = 16,
                             dtype, seed_for(4, variant) + page_size)
 
 
+def batch_prefill_hd64(page_size: int = 16, variant: int = 0) -> PagedBatch:
+    """The batch-prefill lengths at head_dim 64, 4 q / 2 kv heads, fp16."""
+    return batch_prefill(page_size=page_size, variant=variant, num_qo_heads=4, num_kv_heads=2,
+                         head_dim=64, dtype="f16")
+
+
 def ragged_prefill(variant: int = 0, batch: int = 16, q_lo: int = 512, q_hi: int = 2048,
                    prefix_lo: int = 0, prefix_hi: int = 4096, num_qo_heads: int = 32,
                    num_kv_heads: int = 8, head_dim: int = 128, dtype: str = "bf16") -> PagedBatch:
