@@ -20,6 +20,8 @@
 
 using fi::WorkItem;
 using fi::WsHeader;
+using fi::kItemPublicInts;
+using fi::kItemsOffset;
 
 namespace {
 
@@ -150,13 +152,13 @@ namespace {
 
 // Metadata bytes for a batch (header + int arrays + items), 256-aligned.
 int64_t meta_bytes_for(int64_t batch, int64_t rows, int64_t n_merge, int64_t n_items) {
-  int64_t off = sizeof(WsHeader);
+  int64_t off = kItemsOffset;
+  off += int64_t(sizeof(WorkItem)) * n_items;  // items
   off = align_up(off + 4 * (batch + 1), 16);  // qo_indptr
   off = align_up(off + 4 * (batch + 1), 16);  // kv_indptr
   off = align_up(off + 4 * batch, 16);        // kv_len
   off = align_up(off + 4 * (rows + 1), 16);   // merge_indptr
   off = align_up(off + 4 * n_merge, 32);      // merge_rows
-  off += 32 * n_items;                        // items
   off = align_up(off + 4 * (batch + 1), 16);  // mask_indptr
   return align_up(off, kAlign);
 }
@@ -251,7 +253,9 @@ int choose_kernel(int32_t q_len_per_req, int32_t g, int64_t max_rows_per_req, in
                   int32_t page_size, bool masked) {
   if (max_rows_per_req <= kShortRowsMax && fi::decode_mma_supports(d, page_size, g))
     return fi::kDecode;
-  if (masked) {  // the custom mask is read by the short-query and mma.sync kernels
+  if (masked) {  // the custom mask is read by every kernel
+    if (max_rows_per_req > kShortRowsMax && fi::prefill_tc_supports(d, page_size, g))
+      return fi::kPrefillM128;
     if (max_rows_per_req <= 16 && g <= 16) return fi::kPrefillM16;
     return g <= 64 ? fi::kPrefillM64 : -1;
   }
@@ -570,122 +574,269 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
   // ---- work items, partial slots and the merge index
   ns.merge_indptr.assign(ns.total_rows + 1, 0);
   std::vector<int32_t> merge_count(ns.total_rows, 0);
-  // Items are made per (tile, chunk) group - one per kv head, all of the same
-  // cost - and the groups are sorted by cost, longest first.
-  struct Group { int64_t cost; WorkItem it; };
-  std::vector<Group> groups;
-  {
-    size_t n_est = 0;
+  int32_t partial_cursor = 0;
+  int32_t max_chunks = 1;
+  int64_t G = 0;  // the grid
+
+  // Balanced spans (short-query kernel, when the plan splits keys): the live
+  // keys of all tiles, laid end to end, are cut into one contiguous span per
+  // bundle of Hk CTAs (one CTA per kv head), every span of about the same
+  // cost, (keys + kSpanItemKeys) x rows per piece. A bundle takes the rest of the
+  // tile it starts in and as much of the next ones as its share allows, so
+  // the CTAs end at about the same time: a longest-first schedule of
+  // fixed-length chunks left 5% of the CTA time idle on the batch-32 verify
+  // (and fewer, longer items cost fewer item ends). Cuts fall on multiples of
+  // 64 keys (whole stages) and no piece is shorter than kMinPiece keys.
+  auto schedule_spans = [&]() -> bool {
+    constexpr int64_t kMinPiece = 64;
+    // An item's fixed cost in keys: a per-item timeline of the batch-32
+    // verify and batch-64 decode runs (item end times against their keys)
+    // put it near zero once the producer runs ahead across items; 32 keys
+    // (half a stage) keeps pieces from being cut for nothing.
+    constexpr int64_t kSpanItemKeys = 32;
+    if (grid_cap % hk != 0) return false;
+    const int64_t B = grid_cap / hk;
+    if (B < 2) return false;
+    double total = 0;
+    for (const Tile& t : tiles) total += double(t.hi - t.lo + kSpanItemKeys) * double(t.rows);
+    struct Piece { int32_t bundle, tile, kb, ke; };
+    std::vector<Piece> pieces, trial;
+    pieces.reserve(tiles.size() + size_t(B));
+    trial.reserve(tiles.size() + size_t(B));
+    // One walk: every bundle takes up to `share` of cost from its own start
+    // (a piece that starts costs kSpanItemKeys x rows on top of its keys); cuts
+    // round to multiples of 64 keys, a remainder shorter than kMinPiece keys
+    // stays with its piece, and a bundle with room for less than kMinPiece
+    // keys ends there. Returns the bundles used, or B + 1 once it needs more.
+    // share >= (kSpanItemKeys + 2 kMinPiece) x the largest rows, so a fresh
+    // bundle always takes a piece and every step advances.
+    auto walk = [&](double share, std::vector<Piece>& out) {
+      out.clear();
+      int64_t bundle = 0;
+      double room = share;
+      for (size_t ti = 0; ti < tiles.size() && bundle < B; ++ti) {
+        const Tile& t = tiles[ti];
+        const double rows = double(t.rows);
+        int64_t pos = t.lo;
+        for (;;) {
+          const double fit = room / rows - double(kSpanItemKeys);  // keys a piece here may take
+          const int64_t rest = t.hi - pos;
+          if (fit >= double(rest - kMinPiece)) {
+            out.push_back({int32_t(bundle), int32_t(ti), int32_t(pos), int32_t(t.hi)});
+            room -= double(rest + kSpanItemKeys) * rows;
+            break;
+          }
+          if (fit < double(kMinPiece)) {  // too little room: the next bundle starts here
+            if (++bundle >= B) break;
+            room = share;
+            continue;
+          }
+          int64_t cut = (pos + int64_t(fit) + 32) / 64 * 64;
+          cut = std::max<int64_t>(cut, pos + kMinPiece);
+          out.push_back({int32_t(bundle), int32_t(ti), int32_t(pos), int32_t(cut)});
+          pos = cut;
+          if (++bundle >= B) break;
+          room = share;
+        }
+      }
+      if (bundle >= B) return B + 1;
+      return out.empty() ? int64_t(1) : int64_t(out.back().bundle) + 1;
+    };
+    // the smallest share whose walk fits the B bundles (bisection; each walk
+    // is tiles + bundles steps)
+    int64_t max_rows = 1;
+    for (const Tile& t : tiles) max_rows = std::max<int64_t>(max_rows, t.rows);
+    double lo_s = std::max(total / double(B), double(kSpanItemKeys + 2 * kMinPiece) * double(max_rows));
+    double hi_s = 2.0 * lo_s;
+    for (int iter = 0; iter < 24; ++iter) {
+      const double mid = 0.5 * (lo_s + hi_s);
+      if (walk(mid, trial) <= B) hi_s = mid;
+      else lo_s = mid;
+    }
+    if (walk(hi_s, pieces) > B) return false;
+    // pieces per tile -> chunk counts, partial slots; refuse (fall back to the
+    // chunked schedule) when the partial states do not fit the workspace
+    std::vector<int32_t> n_of(tiles.size(), 0), base_of(tiles.size(), -1), next(tiles.size(), 0);
+    for (const Piece& pc : pieces) n_of[size_t(pc.tile)]++;
+    int64_t np = 0;
+    for (size_t ti = 0; ti < tiles.size(); ++ti)
+      if (n_of[ti] > 1) np += int64_t(n_of[ti]) * tiles[ti].n_tokens;
+    const int64_t used = pieces.empty() ? 1 : int64_t(pieces.back().bundle) + 1;
+    const int64_t g_spans = P.graph ? grid_cap : used * hk;
+    std::vector<int32_t> per_bundle(size_t(used), 0);
+    for (const Piece& pc : pieces) per_bundle[size_t(pc.bundle)]++;
+    int32_t rounds = 0;
+    for (int32_t c : per_bundle) rounds = std::max(rounds, c);
+    const int64_t ni = int64_t(rounds) * g_spans;
+    if (np > INT32_MAX / 2 || ni > INT32_MAX / 2 || !fits(ni, np, ns.total_rows)) return false;
+    for (size_t ti = 0; ti < tiles.size(); ++ti) {
+      const Tile& t = tiles[ti];
+      max_chunks = std::max(max_chunks, n_of[ti]);
+      if (n_of[ti] > 1) {
+        base_of[ti] = partial_cursor;
+        partial_cursor += n_of[ti] * t.n_tokens;
+        for (int32_t k = 0; k < t.n_tokens; ++k) merge_count[size_t(t.first_token + k)] = n_of[ti];
+      }
+    }
+    WorkItem pad{};
+    pad.b = -1;
+    ns.items.assign(size_t(ni), pad);
+    std::fill(per_bundle.begin(), per_bundle.end(), 0);
+    for (const Piece& pc : pieces) {
+      const Tile& t = tiles[size_t(pc.tile)];
+      const int32_t n = n_of[size_t(pc.tile)];
+      WorkItem it{};
+      it.b = t.b;
+      it.row0 = t.row0;
+      it.kv_begin = pc.kb;
+      it.kv_end = pc.ke;
+      it.chunk = n > 1 ? next[size_t(pc.tile)]++ : -1;
+      it.num_chunks = n;
+      it.partial_base = base_of[size_t(pc.tile)];
+      const int64_t slot = per_bundle[size_t(pc.bundle)]++;
+      for (int32_t h = 0; h < hk; ++h) {
+        it.kv_head = h;
+        ns.items[size_t(slot * g_spans + int64_t(pc.bundle) * hk + h)] = it;
+      }
+    }
+    G = g_spans;
+    return true;
+  };
+  const bool spans = ns.kernel == fi::kDecode && force_kv_chunks == 0 && chunk_len > 0 &&
+                     schedule_spans();
+  if (!spans) {
+    // Items are made per (tile, chunk) group - one per kv head, all of the same
+    // cost - and the groups are sorted by cost, longest first.
+    struct Group { int64_t cost; WorkItem it; };
+    std::vector<Group> groups;
+    {
+      size_t n_est = 0;
+      for (const Tile& t : tiles) {
+        int64_t n = 1;
+        if (force_kv_chunks > 0) n = force_kv_chunks;
+        else if (chunk_len > 0 && t.hi - t.lo > chunk_len) n = (t.hi - t.lo + chunk_len - 1) / chunk_len;
+        n_est += size_t(n);
+      }
+      groups.reserve(n_est);
+    }
     for (const Tile& t : tiles) {
       int64_t n = 1;
       if (force_kv_chunks > 0) n = force_kv_chunks;
       else if (chunk_len > 0 && t.hi - t.lo > chunk_len) n = (t.hi - t.lo + chunk_len - 1) / chunk_len;
-      n_est += size_t(n);
-    }
-    groups.reserve(n_est);
-  }
-  int32_t partial_cursor = 0;
-  int32_t max_chunks = 1;
-  for (const Tile& t : tiles) {
-    int64_t n = 1;
-    if (force_kv_chunks > 0) n = force_kv_chunks;
-    else if (chunk_len > 0 && t.hi - t.lo > chunk_len) n = (t.hi - t.lo + chunk_len - 1) / chunk_len;
-    max_chunks = std::max<int32_t>(max_chunks, int32_t(n));
-    const int32_t base = (n > 1) ? partial_cursor : -1;
-    if (n > 1) {
-      partial_cursor += int32_t(n) * t.n_tokens;
-      for (int32_t k = 0; k < t.n_tokens; ++k) merge_count[t.first_token + k] = int32_t(n);
-    }
-    for (int64_t c = 0; c < n; ++c) {
-      int64_t kb, ke;
-      if (force_kv_chunks > 0) {  // even cut of the full key range [0, Lk)
-        kb = int64_t(t.lk) * c / n;
-        ke = int64_t(t.lk) * (c + 1) / n;
-      } else if (n > 1) {         // chunk_len cut of the live range
-        kb = t.lo + c * chunk_len;
-        ke = std::min<int64_t>(t.hi, kb + chunk_len);
-      } else {
-        kb = t.lo;
-        ke = t.hi;
+      max_chunks = std::max<int32_t>(max_chunks, int32_t(n));
+      const int32_t base = (n > 1) ? partial_cursor : -1;
+      if (n > 1) {
+        partial_cursor += int32_t(n) * t.n_tokens;
+        for (int32_t k = 0; k < t.n_tokens; ++k) merge_count[t.first_token + k] = int32_t(n);
       }
-      const int64_t live = std::max<int64_t>(0, std::min<int64_t>(ke, t.hi) - std::max<int64_t>(kb, t.lo));
-      Group gr;
-      gr.cost = item_cost(live, t.rows);
-      gr.it.b = t.b; gr.it.kv_head = 0; gr.it.row0 = t.row0;
-      gr.it.kv_begin = int32_t(kb); gr.it.kv_end = int32_t(ke);
-      gr.it.chunk = (n > 1) ? int32_t(c) : -1;
-      gr.it.num_chunks = int32_t(n);
-      gr.it.partial_base = base;
-      groups.push_back(gr);
-    }
-  }
-  std::stable_sort(groups.begin(), groups.end(),
-                   [](const Group& a, const Group& b) { return a.cost > b.cost; });
-  // Static longest-processing-time schedule for the persistent grid: groups,
-  // longest first, go to the least-loaded bundle of Hk CTAs (one item per CTA
-  // of the bundle; a bundle is one CTA when Hk does not divide the grid),
-  // found with a binary min-heap of bundle loads; CTA c then finds its list at
-  // positions c, c + grid, ... (padded with items whose request is -1, which
-  // every kernel skips).
-  const int64_t n_all = int64_t(groups.size()) * hk;
-  const int64_t G = std::max<int64_t>(1, P.graph ? grid_cap : std::min<int64_t>(n_all, grid_cap));
-  const int32_t bundle = (G % hk == 0) ? hk : 1;
-  const int32_t n_bundles = int32_t(G / bundle);
-  {
-    std::vector<int64_t> load(static_cast<size_t>(n_bundles), 0);
-    std::vector<int32_t> heap(static_cast<size_t>(n_bundles));  // heap-ordered by (load, id)
-    for (int32_t c = 0; c < n_bundles; ++c) heap[size_t(c)] = c;
-    auto less = [&](int32_t a, int32_t b) {
-      return load[size_t(a)] != load[size_t(b)] ? load[size_t(a)] < load[size_t(b)] : a < b;
-    };
-    auto take = [&](int64_t cost) {  // least-loaded bundle gets `cost`
-      const int32_t c = heap[0];
-      load[size_t(c)] += cost;
-      size_t k = 0;
-      const size_t n = size_t(n_bundles);
-      for (;;) {
-        size_t l = 2 * k + 1, r = l + 1, m = k;
-        if (l < n && less(heap[l], heap[m])) m = l;
-        if (r < n && less(heap[r], heap[m])) m = r;
-        if (m == k) break;
-        std::swap(heap[k], heap[m]);
-        k = m;
-      }
-      return c;
-    };
-    std::vector<int32_t> cta_of(static_cast<size_t>(n_all));
-    std::vector<int32_t> count(static_cast<size_t>(G), 0);
-    int64_t i = 0;
-    for (const Group& gr : groups) {
-      if (bundle == hk) {
-        const int32_t c0 = take(gr.cost) * hk;
-        for (int32_t h = 0; h < hk; ++h, ++i) {
-          cta_of[size_t(i)] = c0 + h;
-          count[size_t(c0 + h)]++;
+      for (int64_t c = 0; c < n; ++c) {
+        int64_t kb, ke;
+        if (force_kv_chunks > 0) {  // even cut of the full key range [0, Lk)
+          kb = int64_t(t.lk) * c / n;
+          ke = int64_t(t.lk) * (c + 1) / n;
+        } else if (n > 1) {         // chunk_len cut of the live range
+          kb = t.lo + c * chunk_len;
+          ke = std::min<int64_t>(t.hi, kb + chunk_len);
+        } else {
+          kb = t.lo;
+          ke = t.hi;
         }
-      } else {
-        for (int32_t h = 0; h < hk; ++h, ++i) {
-          const int32_t c = take(gr.cost);
-          cta_of[size_t(i)] = c;
-          count[size_t(c)]++;
+        const int64_t live = std::max<int64_t>(0, std::min<int64_t>(ke, t.hi) - std::max<int64_t>(kb, t.lo));
+        Group gr;
+        gr.cost = item_cost(live, t.rows);
+        gr.it.b = t.b; gr.it.kv_head = 0; gr.it.row0 = t.row0;
+        gr.it.kv_begin = int32_t(kb); gr.it.kv_end = int32_t(ke);
+        gr.it.chunk = (n > 1) ? int32_t(c) : -1;
+        gr.it.num_chunks = int32_t(n);
+        gr.it.partial_base = base;
+        groups.push_back(gr);
+      }
+    }
+    std::stable_sort(groups.begin(), groups.end(),
+                     [](const Group& a, const Group& b) { return a.cost > b.cost; });
+    // Static longest-processing-time schedule for the persistent grid: groups,
+    // longest first, go to the least-loaded bundle of Hk CTAs (one item per CTA
+    // of the bundle; a bundle is one CTA when Hk does not divide the grid),
+    // found with a binary min-heap of bundle loads; CTA c then finds its list at
+    // positions c, c + grid, ... (padded with items whose request is -1, which
+    // every kernel skips).
+    const int64_t n_all = int64_t(groups.size()) * hk;
+    G = std::max<int64_t>(1, P.graph ? grid_cap : std::min<int64_t>(n_all, grid_cap));
+    const int32_t bundle = (G % hk == 0) ? hk : 1;
+    const int32_t n_bundles = int32_t(G / bundle);
+    {
+      std::vector<int64_t> load(static_cast<size_t>(n_bundles), 0);
+      std::vector<int32_t> heap(static_cast<size_t>(n_bundles));  // heap-ordered by (load, id)
+      for (int32_t c = 0; c < n_bundles; ++c) heap[size_t(c)] = c;
+      auto less = [&](int32_t a, int32_t b) {
+        return load[size_t(a)] != load[size_t(b)] ? load[size_t(a)] < load[size_t(b)] : a < b;
+      };
+      auto take = [&](int64_t cost) {  // least-loaded bundle gets `cost`
+        const int32_t c = heap[0];
+        load[size_t(c)] += cost;
+        size_t k = 0;
+        const size_t n = size_t(n_bundles);
+        for (;;) {
+          size_t l = 2 * k + 1, r = l + 1, m = k;
+          if (l < n && less(heap[l], heap[m])) m = l;
+          if (r < n && less(heap[r], heap[m])) m = r;
+          if (m == k) break;
+          std::swap(heap[k], heap[m]);
+          k = m;
+        }
+        return c;
+      };
+      std::vector<int32_t> cta_of(static_cast<size_t>(n_all));
+      std::vector<int32_t> count(static_cast<size_t>(G), 0);
+      int64_t i = 0;
+      for (const Group& gr : groups) {
+        if (bundle == hk) {
+          const int32_t c0 = take(gr.cost) * hk;
+          for (int32_t h = 0; h < hk; ++h, ++i) {
+            cta_of[size_t(i)] = c0 + h;
+            count[size_t(c0 + h)]++;
+          }
+        } else {
+          for (int32_t h = 0; h < hk; ++h, ++i) {
+            const int32_t c = take(gr.cost);
+            cta_of[size_t(i)] = c;
+            count[size_t(c)]++;
+          }
         }
       }
+      int32_t rounds = 0;
+      for (int32_t c : count) rounds = std::max(rounds, c);
+      WorkItem pad{};
+      pad.b = -1;
+      ns.items.assign(size_t(rounds) * size_t(G), pad);
+      std::vector<int32_t> next(static_cast<size_t>(G), 0);
+      i = 0;
+      for (const Group& gr : groups) {
+        for (int32_t h = 0; h < hk; ++h, ++i) {
+          const int32_t c = cta_of[size_t(i)];
+          WorkItem it = gr.it;
+          it.kv_head = h;
+          ns.items[size_t(next[size_t(c)]++) * size_t(G) + size_t(c)] = it;
+        }
+      }
     }
-    int32_t rounds = 0;
-    for (int32_t c : count) rounds = std::max(rounds, c);
+  }
+  // A captured kernel keeps its grid: an empty graph-mode plan still holds a
+  // grid's worth of (padding) items, which the short-query kernel's CTAs load
+  // before they read the item count.
+  if (P.graph && ns.items.empty()) {
     WorkItem pad{};
     pad.b = -1;
-    ns.items.assign(size_t(rounds) * size_t(G), pad);
-    std::vector<int32_t> next(static_cast<size_t>(G), 0);
-    i = 0;
-    for (const Group& gr : groups) {
-      for (int32_t h = 0; h < hk; ++h, ++i) {
-        const int32_t c = cta_of[size_t(i)];
-        WorkItem it = gr.it;
-        it.kv_head = h;
-        ns.items[size_t(next[size_t(c)]++) * size_t(G) + size_t(c)] = it;
-      }
-    }
+    ns.items.assign(size_t(std::max<int64_t>(G, 1)), pad);
+  }
+  // every item repeats its request's metadata
+  for (WorkItem& it : ns.items) {
+    if (it.b < 0) continue;
+    it.tok0 = ns.qo_indptr[size_t(it.b)];
+    it.lq = ns.qo_indptr[size_t(it.b) + 1] - it.tok0;
+    it.lk = ns.kv_len[size_t(it.b)];
+    it.kv_start = ns.kv_indptr[size_t(it.b)];
+    it.mask_base = ns.mask_indptr[size_t(it.b)];
   }
   if (partial_cursor > 0) {  // else merge_indptr stays all zero (no row is split)
     int32_t acc = 0;  // running sum in a register: no store-to-load chain
@@ -713,13 +864,13 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
   h.tile_rows = ns.tile_rows;
   h.num_qo_heads = hq;
   h.head_dim = d;
-  int64_t off = sizeof(WsHeader);
+  int64_t off = kItemsOffset;
+  h.off_items = off; off += int64_t(sizeof(WorkItem)) * n_items;
   h.off_qo_indptr = off; off = align_up(off + 4 * (batch + 1), 16);
   h.off_kv_indptr = off; off = align_up(off + 4 * (batch + 1), 16);
   h.off_kv_len = off; off = align_up(off + 4 * batch, 16);
   h.off_merge_indptr = off; off = align_up(off + 4 * (ns.total_rows + 1), 16);
   h.off_merge_rows = off; off = align_up(off + 4 * int64_t(ns.merge_rows.size()), 32);
-  h.off_items = off; off += 32 * n_items;
   h.off_mask_indptr = off; off = align_up(off + 4 * (batch + 1), 16);
   ns.meta_bytes = align_up(off, kAlign);
   h.off_tmp_lse = ns.meta_bytes;
@@ -889,10 +1040,11 @@ extern "C" fi_status fi_plan_get_info(fi_plan_t p, fi_plan_info* info, int32_t* 
     info->graph_mode = p->graph ? 1 : 0;
   }
   if (items) {
-    if (items_capacity < int32_t(s.items.size() * 8))
+    if (items_capacity < int32_t(s.items.size() * kItemPublicInts))
       return fail(FI_ERR_CAPACITY, "plan_get_info: items_capacity=%d < %d", items_capacity,
-                  int32_t(s.items.size() * 8));
-    std::memcpy(items, s.items.data(), s.items.size() * sizeof(WorkItem));
+                  int32_t(s.items.size() * kItemPublicInts));
+    for (size_t i = 0; i < s.items.size(); ++i)  // the public fields of each item
+      std::memcpy(items + i * kItemPublicInts, &s.items[i], kItemPublicInts * sizeof(int32_t));
   }
   if (merge_indptr) {
     if (merge_capacity < int32_t(s.merge_indptr.size()))
@@ -933,8 +1085,11 @@ extern "C" fi_status fi_plan_read_device(fi_plan_t p, int32_t* items, int32_t it
   WsHeader h;
   std::memcpy(&h, buf.data(), sizeof h);
   if (items) {
-    if (items_capacity < h.n_items * 8) return fail(FI_ERR_CAPACITY, "plan_read_device: items");
-    std::memcpy(items, buf.data() + h.off_items, size_t(h.n_items) * sizeof(WorkItem));
+    if (items_capacity < h.n_items * kItemPublicInts) return fail(FI_ERR_CAPACITY, "plan_read_device: items");
+    for (int32_t i = 0; i < h.n_items; ++i)  // the public fields of each item
+      std::memcpy(items + size_t(i) * kItemPublicInts,
+                  buf.data() + h.off_items + int64_t(i) * int64_t(sizeof(WorkItem)),
+                  kItemPublicInts * sizeof(int32_t));
   }
   if (merge_indptr) {
     if (merge_capacity < h.total_rows + 1) return fail(FI_ERR_CAPACITY, "plan_read_device: merge");

@@ -128,6 +128,23 @@ __device__ __forceinline__ bool custom_mask_bit(const uint8_t* mask, int base, i
   return (__ldg(mask + base + (n >> 3)) >> (n & 7)) & 1;
 }
 
+// 32 consecutive bits n0 .. n0+31 of a request's custom mask (least
+// significant bit first within each byte), as bits 0..31 of the result; bits
+// at or past nbits (the segment's Lq * Lk bits) and before 0 read as 0.
+__device__ __forceinline__ uint32_t custom_mask_word(const uint8_t* seg, int64_t nbits,
+                                                     int64_t n0) {
+  const int64_t b0 = n0 >> 3;
+  const int64_t nbytes = (nbits + 7) >> 3;
+  uint64_t w = 0;
+#pragma unroll
+  for (int q = 0; q < 5; ++q) {
+    const int64_t bi = b0 + q;
+    const uint64_t v = (bi >= 0 && bi < nbytes) ? __ldg(seg + bi) : 0u;
+    w |= v << (8 * q);
+  }
+  return uint32_t(w >> (n0 & 7));
+}
+
 // Key j of a request: its row in the cache (page from the page table), or
 // with a ragged cache, row kv_start + j.
 __device__ __forceinline__ int64_t kv_row_offset(const int32_t* pages, int32_t j, int page_size,

@@ -46,13 +46,14 @@ constexpr int kMaxRows = 16;  // packed rows per item
 // Header of one stage, written by the producer before it arms the stage's
 // barrier. Keys [lo, hi) are live for some row of the item, keys
 // [lo_full, hi_full) for every row; diff = Lk - Lq of the request.
-enum : int32_t { kStFirst = 1, kStLast = 2, kStEnd = 4, kStNoKeys = 8 };
+// kStMaskOnes: the custom mask keeps every key of the stage for every row
+enum : int32_t { kStFirst = 1, kStLast = 2, kStEnd = 4, kStNoKeys = 8, kStMaskOnes = 16 };
 struct alignas(16) StageHdr {
   int32_t flags, k0, lo, hi;
   int32_t lo_full, hi_full, token0, kv_head;  // token0: global token of query row i0
   int32_t row0, n_rows, diff, chunk;          // first packed row, rows, Lk - Lq, chunk (-1: direct)
   int32_t num_chunks, partial_base, i0, lk;
-  int32_t mask_base, lq, pad0, pad1;          // custom mask: the request's first byte; Lq
+  int32_t pad2, lq, pad0, pad1;               // Lq
 };
 
 // Write rows [r0, r0 + 8) of an item: sm_o holds those rows' o summed over
@@ -195,10 +196,10 @@ struct DecodeWarp {
   }
 
   __device__ __forceinline__ void stage(T* cK, T* cV, const StageHdr& h, int causal, int wl,
-                                        const uint8_t* p_mask) {
+                                        const uint32_t* smask) {
     (void)causal;
     (void)wl;
-    (void)p_mask;  // decode plans carry no custom mask
+    (void)smask;  // decode plans carry no custom mask
     stage_keys(cK, cV, h.k0, h.lo, h.hi);
   }
 
@@ -418,11 +419,13 @@ struct DecodeMmaWarp {
   }
 
   // Consume one stage (keys h.k0 .. + KT). Where the stage is not inside
-  // every row's range the per-element mask runs; where it is not inside the
-  // item's live range the warp first zeroes its V rows outside it (they may
-  // hold anything, a neighbour's slots, and 0 * NaN would reach o).
+  // every row's range (or a custom mask drops a key of it) the per-element
+  // mask runs; where it is not inside the item's live range the warp first
+  // zeroes its V rows outside it (they may hold anything, a neighbour's
+  // slots, and 0 * NaN would reach o). smask: the stage's custom-mask bits,
+  // KT / 32 words per query row of the item (null: no custom mask).
   __device__ __forceinline__ void stage(T* cK, T* cV, const StageHdr& h, int causal, int wl,
-                                        const uint8_t* p_mask) {
+                                        const uint32_t* smask) {
     const uint32_t sk = smem_u32(cK), sv = smem_u32(cV);
     const int kb = warp * KPW;  // this warp's first key in the stage
     const int k0 = h.k0;
@@ -439,7 +442,8 @@ struct DecodeMmaWarp {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
     }
-    const bool full_tile = k0 >= h.lo_full && k0 + KT <= h.hi_full;
+    const bool full_tile = k0 >= h.lo_full && k0 + KT <= h.hi_full &&
+                           (!smask || (h.flags & kStMaskOnes));
     float s[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
@@ -472,8 +476,11 @@ struct DecodeMmaWarp {
             bool ok = r < h.n_rows && kk >= h.lo && kk < h.hi;
             if (causal && kk > i + h.diff) ok = false;
             if (wl >= 0 && kk + wl < h.diff + i) ok = false;
-            // custom mask (ANDed): its bits are read only for real rows and keys
-            if (ok && p_mask && !custom_mask_bit(p_mask, h.mask_base, i, kk, h.lk)) ok = false;
+            // custom mask (ANDed), as staged by the producer
+            if (ok && smask) {
+              const int kl = kb + nt * 8 + qc * 2 + e;
+              if (!((smask[(i - h.i0) * (KT / 32) + (kl >> 5)] >> (kl & 31)) & 1u)) ok = false;
+            }
             if (!ok) x = neg_inf();
           }
           s[nt][2 * hr + e] = x;
@@ -586,7 +593,7 @@ struct TmaCfg {
   static constexpr int RING_BYTES = NS * STAGE * 2 * 2;
   static constexpr int NBAR = 2 * NS + 2;          // full, empty per slot; q free; merge
   // dynamic shared memory: K/V ring | merge rows | per-warp row max, sum |
-  // q rows | stage headers | barriers, abort flag
+  // q rows | stage headers | barriers, abort flag | custom-mask bits
   // merge buffers of 8 rows: two (a pairwise merge, 3 barriers per round)
   // where shared memory allows, else one (warps take turns, 5 barriers)
   static constexpr int MB = MMA ? 2 : 1;
@@ -596,7 +603,11 @@ struct TmaCfg {
   static constexpr int Q_OFF = ML_OFF + 2 * NCW * kMaxRows * 4;
   static constexpr int HDR_OFF = Q_OFF + kMaxRows * D * 2;
   static constexpr int BAR_OFF = HDR_OFF + NS * int(sizeof(StageHdr));
-  static constexpr int SMEM = BAR_OFF + NBAR * 8 + 16;
+  // custom-mask bits of each stage (tensor-core consumer): KT / 32 words per
+  // query row of the item, written by the producer with the stage header
+  static constexpr int MASKW = KT / 32;
+  static constexpr int MASK_OFF = BAR_OFF + NBAR * 8 + 16;
+  static constexpr int SMEM = MASK_OFF + (MMA ? NS * kMaxRows * MASKW * 4 : 0);
   static_assert((KT & (KT - 1)) == 0, "keys per stage is a power of two");
   static_assert(MINB * (SMEM + 1024) <= 233472, "MINB CTAs fit one SM's shared memory");
 };
@@ -627,11 +638,16 @@ __device__ __noinline__ void decode_producer(const AttnParams& p, const CUtensor
   // buffer of item n waits for the consumers' release of item n - 1's q.
   // Everything a stage needs from global memory (the item's metadata, the
   // page indices) is loaded before those waits, so a full ring hides it.
+  // The start of the chain before the first K/V bytes move: the tensor maps'
+  // descriptors are prefetched, and the CTA's first item (at a fixed offset,
+  // and the plan always holds at least a grid's worth of items) loads in the
+  // same round trip as the header; an item carries its request's metadata,
+  // so the page-table read comes next.
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tkp)) : "memory");
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tvp)) : "memory");
+  const WorkItem* items = ws_ptr<const WorkItem>(p.ws, kItemsOffset);
+  WorkItem next_it = items[blockIdx.x];
   const int n_items = hdr->n_items;
-  const WorkItem* items = ws_ptr<const WorkItem>(p.ws, hdr->off_items);
-  const int32_t* qo_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_qo_indptr);
-  const int32_t* kv_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_kv_indptr);
-  const int32_t* kv_len = ws_ptr<const int32_t>(p.ws, hdr->off_kv_len);
   const int tile_rows = hdr->tile_rows;
   const int n_boxes = KT / box_rows;  // a stage is n_boxes boxes of box_rows slots of one page
   const uint32_t box_bytes = uint32_t(box_rows) * D * 2;
@@ -645,23 +661,34 @@ __device__ __noinline__ void decode_producer(const AttnParams& p, const CUtensor
     armed[s] = false;
     last_par[s] = 0;
   }
+  constexpr int MW = C::MASKW;
+  uint32_t* sMask = reinterpret_cast<uint32_t*>(dsmem + C::MASK_OFF);
   // claim slot st for stage c (and, for an item's first stage, the q
-  // buffer): wait for their release, then write the header and arm the
-  // slot's barrier for `bytes` (lane 0); false once the CTA aborts. Every
-  // armed phase is recorded (the end-of-work stage too), so the drain below
-  // waits on each slot's latest phase.
-  auto claim = [&](int st, uint32_t par, const StageHdr& h, uint32_t bytes, bool first) {
+  // buffer): wait for their release, then write the stage's custom-mask
+  // words (lanes below n_mask: lane = query row of the item), the header,
+  // and arm the slot's barrier for `bytes` (lane 0); false once the CTA
+  // aborts. Every armed phase is recorded (the end-of-work stage too), so the
+  // drain below waits on each slot's latest phase.
+  auto claim = [&](int st, uint32_t par, const StageHdr& h, uint32_t bytes, bool first,
+                   int n_mask, const uint32_t* mw) {
     bool okl = true;
     if (lane == 0) {
       if (c >= NS) okl = mbar_wait(EMPTY(st), par ^ 1u, ctl);
       if (okl && first && n_item > 0)
         okl = mbar_wait(QFREE, uint32_t(n_item - 1) & 1u, ctl);
-      if (okl) {
-        sH[st] = h;
-        mbar_expect_tx(FULL(st), bytes);
-      }
     }
     okl = __shfl_sync(0xffffffffu, okl, 0) != 0;
+    if (okl && n_mask > 0) {
+      if (lane < n_mask) {
+#pragma unroll
+        for (int w = 0; w < MW; ++w) sMask[(st * kMaxRows + lane) * MW + w] = mw[w];
+      }
+      __syncwarp();  // ordered before lane 0's arrive (release) below
+    }
+    if (okl && lane == 0) {
+      sH[st] = h;
+      mbar_expect_tx(FULL(st), bytes);
+    }
     if (okl) {
 #pragma unroll
       for (int s = 0; s < NS; ++s)
@@ -673,13 +700,15 @@ __device__ __noinline__ void decode_producer(const AttnParams& p, const CUtensor
     return okl;
   };
   for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-    const WorkItem it = items[w];
+    const WorkItem it = next_it;
+    // the CTA's next item loads while this one streams
+    if (w + int(gridDim.x) < n_items) next_it = items[w + gridDim.x];
     if (it.b < 0) continue;  // schedule padding
     // item geometry: packed rows [row0, row0 + n_rows) = query rows
     // i0..i1 of request b, and the key ranges their masks leave
-    const int tok_b = qo_indptr[it.b];
-    const int lq = qo_indptr[it.b + 1] - tok_b;
-    const int lk = kv_len[it.b];
+    const int tok_b = it.tok0;
+    const int lq = it.lq;
+    const int lk = it.lk;
     const int n_rows = min(tile_rows, lq * G - it.row0);
     const int i0 = it.row0 / G, i1 = (it.row0 + n_rows) / G - 1;
     const int diff = lk - lq;
@@ -702,17 +731,16 @@ __device__ __noinline__ void decode_producer(const AttnParams& p, const CUtensor
     h.i0 = i0;
     h.lk = lk;
     h.lq = lq;
-    h.mask_base = 0;
-    h.pad0 = h.pad1 = 0;
-    if (p.custom_mask) {
-      // an arbitrary mask: every stage runs the per-element test
-      h.mask_base = ws_ptr<const int32_t>(p.ws, hdr->off_mask_indptr)[it.b];
-      h.lo_full = INT_MAX;
-      h.hi_full = INT_MIN;
-    }
+    h.pad2 = h.pad0 = h.pad1 = 0;
+    // custom mask: request b's bits (row-major, bit i * Lk + j) start on
+    // byte mask_base; the producer stages each stage's KT bits per query row
+    const bool masked = MMA && p.custom_mask != nullptr;
+    const uint8_t* mseg =
+        masked ? p.custom_mask + it.mask_base : nullptr;
+    const int n_mask = masked ? i1 - i0 + 1 : 0;
     const int start = lo & ~(box_rows - 1);
     const int n_tiles = hi > lo ? (hi - start + KT - 1) / KT : 0;
-    const int kv_start = kv_indptr[it.b];  // ragged: first row; paged: first page-table entry
+    const int kv_start = it.kv_start;  // ragged: first row; paged: first page-table entry
     const int32_t* pages = p.ragged ? nullptr : p.kv_indices + kv_start;
     const int n_st = max(n_tiles, 1);  // an item without keys still writes its output
     for (int t = 0; t < n_st; ++t, ++c) {
@@ -745,9 +773,26 @@ __device__ __noinline__ void decode_producer(const AttnParams& p, const CUtensor
       }
       h.flags = (t == 0 ? kStFirst : 0) | (t == n_st - 1 ? kStLast : 0) |
                 (n_tiles ? 0 : kStNoKeys);
+      // this lane's query row's bits of keys k0 .. k0 + KT (bits past the
+      // segment read as 0; the consumers mask keys outside [lo, hi) anyway)
+      uint32_t mw[MW];
+#pragma unroll
+      for (int w = 0; w < MW; ++w) mw[w] = ~0u;
+      if (masked) {
+        if (lane < n_mask) {
+          const int64_t n0 = int64_t(i0 + lane) * lk + k0;
+#pragma unroll
+          for (int w = 0; w < MW; ++w)
+            mw[w] = custom_mask_word(mseg, int64_t(lq) * lk, n0 + 32 * w);
+        }
+        bool ones = true;
+#pragma unroll
+        for (int w = 0; w < MW; ++w) ones = ones && mw[w] == ~0u;
+        if (__all_sync(0xffffffffu, ones)) h.flags |= kStMaskOnes;
+      }
       h.k0 = k0;
       const uint32_t qbytes = t == 0 ? uint32_t(n_rows * D * 2) : 0u;
-      if (!claim(st, par, h, uint32_t(n_live) * box_bytes * 2u + qbytes, t == 0)) {
+      if (!claim(st, par, h, uint32_t(n_live) * box_bytes * 2u + qbytes, t == 0, n_mask, mw)) {
         ok = false;
         break;
       }
@@ -788,7 +833,7 @@ __device__ __noinline__ void decode_producer(const AttnParams& p, const CUtensor
     StageHdr h = {};
     h.flags = kStEnd;
     const int st = c % NS;
-    if (!claim(st, uint32_t(c / NS) & 1u, h, 0u, false)) ok = false;
+    if (!claim(st, uint32_t(c / NS) & 1u, h, 0u, false, 0, nullptr)) ok = false;
   }
   // Drain: the last fill of every slot has landed before the CTA exits
   // (the consumers waited for all of them unless a wait expired; this wait
@@ -833,6 +878,7 @@ __global__ void __launch_bounds__(TmaCfg<D, MMA>::THREADS, TmaCfg<D, MMA>::MINB)
   float (*sm_l)[kMaxRows] = sm_m + NCW;
   T* sQ = reinterpret_cast<T*>(dsmem + C::Q_OFF);
   StageHdr* sH = reinterpret_cast<StageHdr*>(dsmem + C::HDR_OFF);
+  const uint32_t* sMask = reinterpret_cast<const uint32_t*>(dsmem + C::MASK_OFF);
   const uint32_t bar0 = smem_u32(dsmem + C::BAR_OFF);
   auto FULL = [&](int s) { return bar0 + 8u * uint32_t(s); };
   auto EMPTY = [&](int s) { return bar0 + 8u * uint32_t(NS + s); };
@@ -889,7 +935,8 @@ __global__ void __launch_bounds__(TmaCfg<D, MMA>::THREADS, TmaCfg<D, MMA>::MINB)
         if (lane == 0) mbar_arrive(QFREE);
       }
       if (!(flags & kStNoKeys))
-        wk.stage(sK + st * STAGE, sV + st * STAGE, h, causal, window_left, p.custom_mask);
+        wk.stage(sK + st * STAGE, sV + st * STAGE, h, causal, window_left,
+                 MMA && p.custom_mask ? sMask + st * kMaxRows * C::MASKW : nullptr);
       StageHdr out;
       if (flags & kStLast) out = h;
       __syncwarp();

@@ -11,8 +11,10 @@
 namespace fi {
 
 // One unit of work: a tile of packed query rows (query row x head in the GQA
-// group) of one request and one kv head, against one chunk of its keys.
-struct alignas(32) WorkItem {
+// group) of one request and one kv head, against one chunk of its keys. The
+// second half repeats the request's metadata, so a kernel that starts an item
+// needs no further load before it reads the page table.
+struct alignas(64) WorkItem {
   int32_t b;             // request
   int32_t kv_head;
   int32_t row0;          // first packed row (query row * group + head in group)
@@ -21,8 +23,16 @@ struct alignas(32) WorkItem {
   int32_t chunk;         // -1: the tile has one chunk and writes out/lse directly
   int32_t num_chunks;    // chunks of this tile
   int32_t partial_base;  // partial slot of the tile's first token, chunk 0
+  int32_t tok0;          // qo_indptr[b]: global index of the request's first query row
+  int32_t lq;            // query rows of the request
+  int32_t lk;            // keys of the request
+  int32_t kv_start;      // kv_indptr[b]: first page-table entry (ragged: first K/V row)
+  int32_t mask_base;     // mask_indptr[b]: first byte of the request's custom mask
+  int32_t pad[3];
 };
-static_assert(sizeof(WorkItem) == 32, "work item is eight int32");
+static_assert(sizeof(WorkItem) == 64, "work item is sixteen int32");
+// the first eight fields of every item are reported by fi_plan_get_info
+constexpr int kItemPublicInts = 8;
 
 // Device workspace header (the first bytes of the caller's workspace). The
 // kernels read every offset from here, so a re-plan that moves arrays is seen
@@ -46,13 +56,16 @@ struct alignas(128) WsHeader {
   int64_t off_kv_len;        // int32 [batch]
   int64_t off_merge_indptr;  // int32 [T+1]
   int64_t off_merge_rows;    // int32 [n_merge_rows]
-  int64_t off_items;         // WorkItem [n_items]
+  int64_t off_items;         // WorkItem [n_items], always kItemsOffset
   int64_t off_tmp_lse;       // float [partials, Hq]
   int64_t off_tmp_o;         // float [partials, Hq, d]
   int64_t off_mask_indptr;   // int32 [batch+1]: byte offset of each request's custom mask
   uint64_t wait_limit_ns;    // limit of every bounded wait on an mbarrier (0: 2 s)
 };
 static_assert(sizeof(WsHeader) == 128, "header is 128 bytes");
+// The work items follow the header directly: a CTA loads its first item in
+// the same round trip as the header.
+constexpr int64_t kItemsOffset = sizeof(WsHeader);
 
 template <typename T>
 __host__ __device__ inline T* ws_ptr(const void* ws, int64_t off) {

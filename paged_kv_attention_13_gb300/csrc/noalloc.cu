@@ -54,13 +54,14 @@ int64_t up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 NoAllocLayout layout_for(int64_t batch, int64_t hk, int64_t hq, int64_t d, int64_t chunks) {
   NoAllocLayout L;
-  int64_t off = sizeof(WsHeader);
+  int64_t off = kItemsOffset;
+  L.off_items = off; off = up(off + int64_t(sizeof(WorkItem)) * batch * hk * chunks, 16);
   L.off_qo = off; off = up(off + 4 * (batch + 1), 16);
   L.off_kv = off; off = up(off + 4 * (batch + 1), 16);
   L.off_len = off; off = up(off + 4 * batch, 16);
   L.off_merge = off; off = up(off + 4 * (batch + 1), 16);
   L.off_rows = off; off = up(off + 4 * batch, 32);
-  L.off_items = off; off = up(off + 32 * batch * hk * chunks, 256);
+  off = up(off, 256);
   L.off_lse = off; off = up(off + 4 * batch * chunks * hq, 256);
   L.off_o = off; off = up(off + 4 * batch * chunks * hq * d, 256);
   L.total = off;
@@ -121,7 +122,7 @@ __global__ void noalloc_setup_kernel(uint8_t* ws, NoAllocLayout L, const int32_t
     const int c = i % chunks;
     const int pages = kv_indptr[b + 1] - kv_indptr[b];
     const int64_t lk = pages > 0 ? int64_t(pages - 1) * page_size + last_page_len[b] : 0;
-    WorkItem it;
+    WorkItem it = {};
     it.b = b;
     it.kv_head = h;
     it.row0 = 0;
@@ -130,6 +131,10 @@ __global__ void noalloc_setup_kernel(uint8_t* ws, NoAllocLayout L, const int32_t
     it.chunk = chunks > 1 ? c : -1;
     it.num_chunks = chunks;
     it.partial_base = chunks > 1 ? b * chunks : -1;
+    it.tok0 = b;
+    it.lq = 1;
+    it.lk = int32_t(lk);
+    it.kv_start = kv_indptr[b];
     items[i] = it;
   }
 }

@@ -204,7 +204,9 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
 // warpgroups run the same rows, A on the even key tiles and B on the odd
 // ones, each with its own S/P and O in tensor memory, and at the end A
 // combines the two states (m, l, O) by their maxima and writes the output.
-template <bool BF16, int D>
+// MASKED: the plan carries a custom mask (a separate build of the kernel, so
+// the unmasked softmax keeps its registers).
+template <bool BF16, int D, bool MASKED>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tq,
                       const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -237,6 +239,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int32_t* kv_len = ws_ptr<const int32_t>(p.ws, hdr->off_kv_len);
   float* tmp_lse = ws_ptr<float>(p.ws, hdr->off_tmp_lse);
   float* tmp_o = ws_ptr<float>(p.ws, hdr->off_tmp_o);
+  const int32_t* mask_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_mask_indptr);
   const int g = hdr->group;
   const int causal = hdr->causal;
   const int wl = hdr->window_left;
@@ -580,6 +583,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int head = G.hk * g + pr % g;
       const bool direct = G.chunk < 0;
       const int slot = direct ? 0 : G.partial_base + (qi - G.i0) * G.num_chunks + G.chunk;
+      // custom (tree) mask: request b's bits start on byte mbase (-1: none)
+      const int mbase = MASKED ? mask_indptr[G.b] : -1;
       if (!active) {
         if (n == 0 && row_ok) {  // no live key: o = 0, lse = -inf
           if (direct) {
@@ -610,7 +615,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int t0 = G.t_start + j * 128;
         if (!wwait(BAR(B_SFULL + x), (cnt + jj) & 1)) { ok = false; break; }
         tc_fence_after();
-        const bool need_mask = (t0 < G.kv_lo) || (t0 + 128 > G.kv_hi) ||
+        const bool need_mask = MASKED || (t0 < G.kv_lo) || (t0 + 128 > G.kv_hi) ||
                                (causal && t0 + 127 > ix0 + G.lk - G.lq) ||
                                (wl >= 0 && t0 < G.lk - G.lq + ix1 - wl);
         // The row's 128 scores end up in registers (sv). P = exp2(s * scale -
@@ -622,10 +627,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         auto mask_chunk = [&](auto cc) {
           constexpr int c = decltype(cc)::value;
+          // the custom mask's bits of these 32 keys: bit qi * Lk + key of
+          // the request's segment (bits past it read as 0; keys past Lk are
+          // masked by jmax anyway)
+          uint32_t bits = ~0u;
+          if constexpr (MASKED)
+            bits = custom_mask_word(p.custom_mask + mbase, int64_t(G.lq) * G.lk,
+                                    int64_t(qi) * G.lk + t0 + c * 32);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int key = t0 + c * 32 + e;
-            if (key < jmin || key > jmax) sv[c][e] = __float_as_uint(neg_inf());
+            if (key < jmin || key > jmax || !((bits >> e) & 1u))
+              sv[c][e] = __float_as_uint(neg_inf());
           }
         };
         auto exp_chunk = [&](auto cc, float2 nmu2) {
@@ -869,16 +882,24 @@ int gcd_i(int a, int b) {
   return a;
 }
 
-template <bool BF16, int D>
-cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                      const CUtensorMap& tv, int box_rows, int grid, cudaStream_t s) {
+template <bool BF16, int D, bool MASKED>
+cudaError_t launch_tc_m(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv, int box_rows, int grid, cudaStream_t s) {
   // the shared-memory limit: once per device, before any capture
   static std::atomic<uint64_t> done{0};
   constexpr int kSmem = TcLayout<D>::kSmem;
-  const cudaError_t attr = smem_attr_once(prefill_tc_kernel<BF16, D>, kSmem, done);
+  auto k = prefill_tc_kernel<BF16, D, MASKED>;
+  const cudaError_t attr = smem_attr_once(k, kSmem, done);
   if (attr != cudaSuccess) return attr;
-  prefill_tc_kernel<BF16, D><<<grid, kTcThreads, kSmem, s>>>(p, tq, tk, tv, box_rows);
+  k<<<grid, kTcThreads, kSmem, s>>>(p, tq, tk, tv, box_rows);
   return cudaGetLastError();
+}
+
+template <bool BF16, int D>
+cudaError_t launch_tc(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                      const CUtensorMap& tv, int box_rows, int grid, cudaStream_t s) {
+  return p.custom_mask ? launch_tc_m<BF16, D, true>(p, tq, tk, tv, box_rows, grid, s)
+                       : launch_tc_m<BF16, D, false>(p, tq, tk, tv, box_rows, grid, s);
 }
 }  // namespace
 

@@ -2,7 +2,8 @@
 
 Tree drafts: every request's draft nodes see the prefix and their own
 ancestors. Covered: the short-query kernel (at most 16 packed rows), the
-mma.sync M = 16 kernel (page size 2) and the M = 64 kernel (more rows),
+mma.sync M = 16 kernel (page size 2), the tcgen05 kernel (more than 32
+packed rows) and the mma.sync M = 64 kernel (the same at page size 2),
 masks ANDed with causal / window, split-KV, and an all-ones mask equal to
 no mask.
 """
@@ -67,12 +68,33 @@ def test_tree_verify_m16_kernel():
 
 
 @pytest.mark.parametrize("force", [0, 3])
-def test_tree_verify_m64_kernel(force):
-    pb = workloads.tree_verify(batch=4, n_draft=40, kv_lo=60, kv_hi=700)
+@pytest.mark.parametrize("page_size,kernel", [(16, "prefill_m128"), (2, "prefill_m64")])
+def test_tree_verify_wide_trees(force, page_size, kernel):
+    """40 draft nodes x GQA 4 = 160 packed rows: the tcgen05 kernel with the
+    mask ANDed per element, or the mma.sync M = 64 kernel at page size 2."""
+    pb = workloads.tree_verify(batch=4, n_draft=40, kv_lo=60, kv_hi=700, page_size=page_size)
     out, lse, kern, mask, mi = run_masked(pb, True, -1, force)
-    assert kern == "prefill_m64"
+    assert kern == kernel
     toks, heads = sample(pb, 2000, 9)
-    check(pb, out, lse, True, -1, mask, mi, toks, heads, what="tree m64")
+    check(pb, out, lse, True, -1, mask, mi, toks, heads, what="tree %s" % kernel)
+
+
+@pytest.mark.parametrize("causal,wl", [(False, -1), (True, 50), (False, 70)])
+def test_random_masks_on_tcgen05(causal, wl):
+    """Random bit masks over requests of 40..300 packed rows on the tcgen05
+    kernel, every row; includes rows whose mask keeps no key."""
+    rng = np.random.default_rng(777 + wl)
+    ql = rng.integers(10, 76, size=5)
+    kl = ql + rng.integers(0, 400, size=5)
+    pb = workloads.make_paged_batch(ql, kl, 8, 2, 128, 16, "bf16", 778 + wl)
+    masks = [rng.random((int(a), int(b))) < 0.6 for a, b in zip(ql, kl)]
+    masks[0][3, :] = False  # a row with no kept key
+    pb.extra["masks"] = masks
+    packed, mi = workloads.pack_masks(masks)
+    pb.extra["mask"], pb.extra["mask_indptr"] = torch.from_numpy(packed), torch.from_numpy(mi)
+    out, lse, kern, mask, mi = run_masked(pb, causal, wl, 0)
+    assert kern == "prefill_m128"
+    check(pb, out, lse, causal, wl, mask, mi, what="random masks tcgen05")
 
 
 def test_random_masks_with_empty_rows():

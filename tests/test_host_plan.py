@@ -299,8 +299,8 @@ def test_workspace_bytes_grows_with_chunks():
 
 def test_schedule_balances_the_persistent_grid():
     """Items are laid out so CTA c runs positions c, c + grid, ...: the
-    longest-first assignment keeps every CTA's share of keys within a few
-    percent of the mean on the batch-decode workload."""
+    balanced spans keep every CTA's share of keys within a few percent of
+    the mean on the batch-decode workload."""
     pb = workloads.batch_decode()
     p = _plan()
     p.plan(None, pb.kv_indptr, pb.last_page_len, 16, 32, 8, 128, q_len_per_req=1)
@@ -311,7 +311,7 @@ def test_schedule_balances_the_persistent_grid():
     load = np.zeros(G)
     for i, it in enumerate(items):
         if it[0] >= 0:
-            load[i % G] += max(0, min(int(it[4]), kv[it[0]]) - int(it[3])) + 64
+            load[i % G] += max(0, min(int(it[4]), kv[it[0]]) - int(it[3])) + 32
     assert load.max() / load.mean() < 1.03
 
 
@@ -339,6 +339,72 @@ def test_long_context_split_is_balanced():
         assert load.sum() == 8 * 8 * 32768  # every key of every unit, once
         assert load.max() / load.mean() < 1.05
         _check_cover(p, pb, causal, -1, 0)
+
+
+def _span_costs(info, rows_of):
+    """Per-CTA cost of a short-query plan: (keys + 32) x rows per item, the
+    span scheduler's own cost model."""
+    items, G = info["items"], info["grid"]
+    cost = np.zeros(G)
+    for i, it in enumerate(items):
+        if it[0] >= 0:
+            cost[i % G] += (int(it[4]) - int(it[3]) + 32) * rows_of(it)
+    return cost
+
+
+@pytest.mark.parametrize("which", ["verify", "tree", "decode"])
+def test_short_query_spans_are_balanced(which):
+    """Split short-query plans cut the keys of all tiles, end to end, into one
+    span per bundle of kv-head CTAs: every CTA's cost is within a few percent
+    of the mean, the kv heads of a piece run side by side, and the work list
+    stays an exact cover."""
+    p = _plan()
+    if which == "verify":
+        pb = workloads.speculative_verify(batch=32)
+        p.plan(None, pb.kv_indptr, pb.last_page_len, 16, 32, 8, 128, q_len_per_req=4)
+    elif which == "tree":
+        pb = workloads.tree_verify(batch=32)
+        p.plan_masked(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, 16, 32, 8, 128,
+                      pb.extra["mask_indptr"].numpy(), causal=True)
+    else:
+        pb = workloads.batch_decode()
+        p.plan(None, pb.kv_indptr, pb.last_page_len, 16, 32, 8, 128, q_len_per_req=1)
+    info = p.info(with_arrays=True)
+    assert info["kernel_name"] == "decode" and info["max_chunks"] > 1
+    cost = _span_costs(info, lambda it: info["tile_rows"])
+    used = cost[cost > 0]
+    assert len(used) == info["grid"]
+    assert used.max() / used.mean() < 1.03
+    items, G = info["items"], info["grid"]
+    for i in range(0, len(items), 8):  # a bundle: the 8 kv heads of one piece
+        blk = items[i:i + 8]
+        if blk[0][0] >= 0:
+            assert [int(x[1]) for x in blk] == list(range(8))
+            assert len({(int(x[0]), int(x[3]), int(x[4])) for x in blk}) == 1
+    # far fewer item ends than fixed chunks: at most 5 items per CTA
+    per_cta = np.bincount(np.nonzero(info["items"][:, 0] >= 0)[0] % info["grid"])
+    assert per_cta.max() <= 5
+    _check_cover(p, pb, True, -1, 0)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_short_query_spans_terminate_and_cover(seed):
+    """Random short-query batches (1 to 300 requests, 1 to 20000 keys, one
+    to eight query rows) plan quickly and exactly cover their keys."""
+    import time
+    rng = np.random.default_rng(9100 + seed)
+    hk = int(rng.choice([1, 2, 4, 8]))
+    g = int(rng.choice([1, 2, 4, 8]))
+    B = int(rng.choice([1, 2, 5, 17, 64, 300]))
+    q = int(rng.choice([1, 2, 4, 8]))
+    hi = int(rng.choice([40, 700, 5000, 20000]))
+    kl = [max(q, int(x)) for x in rng.integers(1, hi + 1, size=B)]
+    pb = _meta_batch([q] * B, kl, g * hk, hk, 16)
+    p = _plan()
+    t0 = time.perf_counter()
+    p.plan(None, pb.kv_indptr, pb.last_page_len, 16, g * hk, hk, 128, q_len_per_req=q)
+    assert time.perf_counter() - t0 < 2.0
+    _check_cover(p, pb, True, -1, 0)
 
 
 # ----------------------------------------------------------- ragged prefill
@@ -410,10 +476,15 @@ def test_masked_plan_refusals_and_kernel_choice():
     with pytest.raises(fi.FiError) as e:
         p.plan_masked(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, 16, 32, 8, 128, short)
     assert _status(e) == "FI_ERR_INVALID_ARG"
-    # more than 64 packed rows: the mma.sync M = 64 kernel, never the tcgen05 one
+    # more than 32 packed rows: the tcgen05 kernel reads the mask too; at a
+    # page size it cannot tile (2), the mma.sync M = 64 kernel
     pb2 = workloads.tree_verify(batch=2, n_draft=40, kv_lo=100, kv_hi=200)
     p.plan_masked(pb2.qo_indptr, pb2.kv_indptr, pb2.last_page_len, 16, 32, 8, 128,
                   pb2.extra["mask_indptr"].numpy())
+    assert p.info()["kernel_name"] == "prefill_m128"
+    pb3 = workloads.tree_verify(batch=2, n_draft=40, kv_lo=100, kv_hi=200, page_size=2)
+    p.plan_masked(pb3.qo_indptr, pb3.kv_indptr, pb3.last_page_len, 2, 32, 8, 128,
+                  pb3.extra["mask_indptr"].numpy())
     assert p.info()["kernel_name"] == "prefill_m64"
 
 

@@ -1,13 +1,14 @@
 """Pins for the chain speculative-sampling oracle, against things other than
 itself: numpy's searchsorted for the inverse-CDF draw, the special cases the
-acceptance rule fixes, and the defining property of speculative sampling
+acceptance rule fixes, closed forms of the draw margin and the residual
+fallback, and the defining property of speculative sampling
 (Leviathan et al. 2023, Theorem 1): with the draft token drawn from q, the
 first emitted token is distributed exactly as the target p.
 """
 import numpy as np
 import pytest
 
-from oracle.speculative import (accept_draft, chain_speculative_sampling, residual,
+from oracle.speculative import (accept_draft, chain_speculative_sampling, draw_margin, residual,
                                 sample_inverse_cdf)
 import workloads
 
@@ -98,3 +99,52 @@ def test_generator_shapes_and_rows_are_distributions():
     np.testing.assert_allclose(d["target_probs"].double().sum(-1).numpy(), 1.0, atol=1e-5)
     np.testing.assert_allclose(d["draft_probs"].double().sum(-1).numpy(), 1.0, atol=1e-5)
     assert int(d["draft_ids"].max()) < 50
+
+
+def test_draw_margin_closed_forms():
+    """Weights [1, 1, 2] have cumulative fractions 0.25, 0.5, 1: the margin of
+    u is its distance to the nearest of them (an off-by-one cumsum or a
+    missing normalisation moves these values)."""
+    w = [1.0, 1.0, 2.0]
+    assert draw_margin(w, 0.25) == 0.0
+    assert abs(draw_margin(w, 0.3) - 0.05) < 1e-15
+    assert abs(draw_margin(w, 0.45) - 0.05) < 1e-15
+    assert abs(draw_margin(w, 0.8) - 0.2) < 1e-15
+    assert abs(draw_margin(w, 0.0) - 0.25) < 1e-15
+    assert draw_margin([0.0, 0.0], 0.5) == np.inf  # no mass: no boundary
+
+
+def test_draw_margin_zero_only_on_a_boundary():
+    """Brute force: the margin is zero exactly where the inverse-CDF draw
+    switches token, and a draw with margin m does not change for any u'
+    within m of u."""
+    rng = np.random.default_rng(5)
+    w = rng.random(9) + 0.05
+    us = np.linspace(0.0, 0.999, 400)
+    for u in us:
+        m = draw_margin(w, u)
+        t = sample_inverse_cdf(w, u)
+        for du in (-0.9 * m, 0.9 * m):
+            uu = min(max(u + du, 0.0), 0.999999)
+            if m > 1e-12:
+                assert sample_inverse_cdf(w, uu) == t
+
+
+def test_residual_falls_back_to_the_target_when_all_zero():
+    """q >= p everywhere (here q == p): max(0, p - q) has no mass, so the draw
+    uses p itself; otherwise the residual is max(0, p - q) elementwise."""
+    p = np.array([0.1, 0.6, 0.3], np.float32)
+    assert np.array_equal(residual(p, p), p)
+    q = np.array([0.5, 0.5, 0.0], np.float32)
+    r = residual(p, q)
+    assert np.array_equal(r, np.array([0.0, np.float32(0.6) - np.float32(0.5), 0.3], np.float32))
+    # a full chain through the fallback: draft = target, u_accept above 1 so
+    # the first draft is rejected; the draw must then follow p_0 (one-hot)
+    V = 5
+    tp = np.zeros((1, 2, V), np.float32)
+    tp[0, :, 3] = 1.0
+    dp = tp[:, :1].copy()
+    toks, acc, pos = chain_speculative_sampling(dp, np.array([[3]]), tp,
+                                                np.array([[1.5]], np.float32),
+                                                np.array([0.4], np.float32))
+    assert acc[0] == 0 and pos[0] == 0 and toks[0, 0] == 3 and toks[0, 1] == -1
