@@ -15,7 +15,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfi.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["abi.cc", "decode.cu", "prefill_mma.cu", "prefill_tc.cu", "merge.cu", "noalloc.cu",
+SOURCES = ["abi.cc", "decode.cu", "decode_pair.cu", "prefill_mma.cu", "prefill_tc.cu", "merge.cu", "noalloc.cu",
            "tma_map.cu", "sampling.cu", "check.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

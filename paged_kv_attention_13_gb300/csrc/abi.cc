@@ -244,9 +244,8 @@ namespace {
 // rows (one tile) on its tensor-core consumer when the group and page size allow, and
 // decode on its CUDA-core consumer otherwise (groups 1, 2, 4).
 // Requests of up to kShortRowsMax packed rows go to the short-query kernel
-// too, in 16-row tiles: each tile reads the request's K/V once, and at two
-// tiles that beats the mma.sync M = 64 kernel's single pass (measured on 8-node
-// tree verify at GQA 4: 32 rows per request).
+// too: 17 to 32 rows in one 32-row tile of its pair consumer (two M tiles,
+// one read of the keys).
 constexpr int64_t kShortRowsMax = 32;
 
 int choose_kernel(int32_t q_len_per_req, int32_t g, int64_t max_rows_per_req, int32_t d,
@@ -277,7 +276,8 @@ int tile_rows_of(int kernel, int g, int64_t max_rows_per_req, int32_t d, int32_t
       // tensor-core consumer: one row half (8 rows) when every request fits,
       // else two; CUDA-core consumer: the G heads of one token
       if (!fi::decode_mma_supports(d, page_size, g)) return g;
-      return (max_rows_per_req <= 8 && g <= 8) ? (8 / g) * g : (16 / g) * g;
+      if (max_rows_per_req <= 8 && g <= 8) return (8 / g) * g;
+      return max_rows_per_req <= 16 ? (16 / g) * g : (32 / g) * g;
     case fi::kPrefillM16: return (16 / g) * g;
     case fi::kPrefillM64: return (64 / g) * g;
     case fi::kPrefillM128: return 2 * ((128 / g) * g);  // two 128-row Q tiles

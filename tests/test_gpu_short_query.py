@@ -1,6 +1,7 @@
-"""The short-query kernel (every request of at most 16 packed rows) against
-the oracle: GQA groups 1..16, decode, verify, ragged short prefill, masks,
-split-KV with several query rows per work item, and run-to-run determinism.
+"""The short-query kernel (every request of at most 32 packed rows) against
+the oracle: GQA groups 1..16, decode, verify, ragged short prefill, the
+32-row pair consumer, split-KV with several query rows per work item, and
+run-to-run determinism.
 """
 import numpy as np
 import pytest
@@ -67,13 +68,47 @@ def test_runs_are_bitwise_reproducible():
 
 @pytest.mark.parametrize("force", [0, 4])
 @pytest.mark.parametrize("window_left", [-1, 6])
-def test_verify_32_rows_in_two_tiles(force, window_left):
-    """8 draft rows at GQA 4: 32 packed rows, two 16-row tiles per request."""
+def test_verify_32_rows_in_one_tile(force, window_left):
+    """8 draft rows at GQA 4: 32 packed rows in one tile of the pair
+    consumer (two M tiles over complementary key halves)."""
     kv = [8, 11, 300, 1200, 77]
     pb = workloads.make_paged_batch([8] * len(kv), kv, 32, 8, 128, 16, "bf16", 61)
     out, lse, plan = run_gpu(pb, True, window_left, mode="verify", force_kv_chunks=force,
                              q_len_per_req=8)
     info = plan.info()
-    assert info["kernel_name"] == "decode" and info["tile_rows"] == 16
+    assert info["kernel_name"] == "decode" and info["tile_rows"] == 32
     assert_close(pb, out, lse, True, window_left, what="verify 32 rows f=%d wl=%d" % (
         force, window_left))
+
+
+@pytest.mark.parametrize("hq,hk,qlen", [(8, 8, 20), (16, 8, 9), (32, 8, 5), (64, 8, 3),
+                                         (32, 2, 2), (16, 16, 32)])
+@pytest.mark.parametrize("head_dim,dtype", [(128, "bf16"), (64, "f16")])
+@pytest.mark.parametrize("force", [0, 3])
+def test_pair_consumer_groups(hq, hk, qlen, head_dim, dtype, force):
+    """17 to 32 packed rows for every group (1, 2, 4, 8, 16), both head
+    dims and dtypes, split or not: rows past the request's own (a 20-row
+    tile of group 1, an 18-row tile of group 2) stay unwritten padding."""
+    kv = [qlen, qlen + 5, 130, 999, 64]
+    pb = workloads.make_paged_batch([qlen] * len(kv), kv, hq, hk, head_dim, 16, dtype,
+                                    300 + hq + qlen + head_dim)
+    out, lse, plan = run_gpu(pb, True, -1, mode="verify", force_kv_chunks=force,
+                             q_len_per_req=qlen)
+    info = plan.info()
+    g = hq // hk
+    assert info["kernel_name"] == "decode" and info["tile_rows"] == (32 // g) * g
+    assert_close(pb, out, lse, True, -1, what="pair g=%d q=%d d=%d f=%d" % (g, qlen, head_dim,
+                                                                                force))
+
+
+def test_pair_consumer_mixed_rows_and_window():
+    """Ragged short prefill mixing 1..32 packed rows (GQA 4: 1..8 query rows)
+    with a window: tiles of the pair consumer with fewer live rows than 32."""
+    q_lens = [8, 5, 1, 7, 0, 6]
+    kv_lens = [8, 40, 300, 2100, 10, 6]
+    pb = workloads.make_paged_batch(q_lens, kv_lens, 16, 4, 128, 16, "bf16", 91)
+    for causal, wl in ((True, -1), (False, 33), (True, 7)):
+        out, lse, plan = run_gpu(pb, causal, wl, mode="prefill")
+        info = plan.info()
+        assert info["kernel_name"] == "decode" and info["tile_rows"] == 32
+        assert_close(pb, out, lse, causal, wl, what="pair mixed causal=%s wl=%d" % (causal, wl))
