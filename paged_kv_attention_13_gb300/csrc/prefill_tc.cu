@@ -287,13 +287,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // 128-column score row: 128 x 112 + 256 x 192 = 63488 <= 384 x 168 launched.
   if (warp < 4) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // Lane 0 owns the barriers; for each K or V tile every lane fetches one
-    // page index (up to 8 pages per tile) and issues that page's boxes. K and
-    // V stages are released separately (K after the S products, V after the
-    // P V products), and K is issued one tile ahead of V.
-    int gk = 0, gv = 0, qc = 0;
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------ producers
+    // Warp 0 loads the Q tiles and the K tiles, warp 2 the V tiles, each at
+    // its own pace: a V stage is released only after its P V product, long
+    // after the K stage of the same tile, and one warp issuing both waited
+    // on V slots while K slots stood free (split items of the long-context
+    // batch streamed at 0.7 of the HBM rate). Lane 0 owns the warp's
+    // barriers; for each tile every lane fetches one page index (up to 8
+    // pages per tile) and issues that page's boxes.
+    const int which_w = warp == 0 ? 0 : 1;
+    int gcnt = 0, qc = 0;
     // stage (which, st) at bit 2 * which + st: armed at least once, and the
     // parity of its latest arming (bit masks, so they stay in registers)
     uint32_t armed = 0, apar = 0;
@@ -353,7 +357,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return (t < G.n_tiles && pg < n_pages && lane < tiles_per_batch * npg) ? __ldg(pages + pg) : 0;
       };
       int idx_cur = fetch(0), idx_nxt = fetch(1);
-      if (lane == 0) {
+      if (which_w == 0 && lane == 0) {
         if (qc > 0 && !mbar_wait(BAR(B_QEMPTY), (qc - 1) & 1, ctl)) ok = false;
         if (ok) {
           mbar_expect_tx(BAR(B_QFULL), (hasB ? 2u : 1u) * uint32_t(tr) * uint32_t(D) * 2u);
@@ -368,30 +372,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ++qc;
-      bool has_prev = false;
-      int page_prev = 0, nvalid_prev = 0;
-      for (int step = 0; step <= G.n_tiles && ok; ++step) {
-        bool has = false;
-        int page = 0, nvalid = 0;
-        if (step < G.n_tiles) {
-          const int bt = step / tiles_per_batch, k = step % tiles_per_batch;
-          if (k == 0 && bt > 0) {  // move to the next batch, prefetch the one after
-            idx_cur = idx_nxt;
-            idx_nxt = fetch(bt + 1);
-          }
-          has = lane < npg && page_of(G.t_start + step * 128 + lane * kv_box_rows) < n_pages;
-          page = __shfl_sync(0xffffffffu, idx_cur, (k * npg + lane) & 31);
-          nvalid = __popc(__ballot_sync(0xffffffffu, has));
-          ok = load(0, G, step, gk, has, page, nvalid);
-          ++gk;
+      for (int step = 0; step < G.n_tiles && ok; ++step) {
+        const int bt = step / tiles_per_batch, k = step % tiles_per_batch;
+        if (k == 0 && bt > 0) {  // move to the next batch, prefetch the one after
+          idx_cur = idx_nxt;
+          idx_nxt = fetch(bt + 1);
         }
-        if (ok && step >= 1) {
-          ok = load(1, G, step - 1, gv, has_prev, page_prev, nvalid_prev);
-          ++gv;
-        }
-        has_prev = has;
-        page_prev = page;
-        nvalid_prev = nvalid;
+        const bool has = lane < npg && page_of(G.t_start + step * 128 + lane * kv_box_rows) < n_pages;
+        const int page = __shfl_sync(0xffffffffu, idx_cur, (k * npg + lane) & 31);
+        const int nvalid = __popc(__ballot_sync(0xffffffffu, has));
+        ok = load(which_w, G, step, gcnt, has, page, nvalid);
+        ++gcnt;
       }
     }
     // before exit: every copy this warp started has landed (these waits
