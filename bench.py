@@ -380,23 +380,44 @@ class Runner:
         return pipe_ms, serial_ms, in_bytes + meta, res_bytes, brk
 
 
-def traffic_from_profile(kernel_file, name):
-    """Per-launch DRAM bytes from the committed ncu summary, if the kernel
-    source is unchanged since it was taken (else None)."""
+# the sources each profiled kernel is built from (their digest is recorded
+# with the profile; a profile of other sources is not reported)
+KERNEL_SOURCES = {
+    "decode": ["decode_kernel.cuh", "decode.cu", "tma.cuh", "common.cuh", "fi_internal.h"],
+    "prefill_tc": ["prefill_tc.cu", "tma.cuh", "common.cuh", "fi_internal.h"],
+}
+
+
+def source_digest(kernel):
+    """First 16 hex digits of the SHA-256 of the kernel's sources, in order."""
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(ROOT, "paged_kv_attention_13_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profile_record(kernel, name):
+    """The key: value lines of a committed ncu summary under profiles/, if the
+    kernel's sources are unchanged since it was taken (else None)."""
     path = os.path.join(ROOT, "profiles", name)
-    src = os.path.join(ROOT, "paged_kv_attention_13_gb300", "csrc", kernel_file)
-    if not os.path.exists(path) or not os.path.exists(src):
+    if not os.path.exists(path):
         return None
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     vals = {}
     for line in open(path):
         if ":" in line:
             k, v = line.split(":", 1)
             vals[k.strip()] = v.strip()
-    if vals.get("source_sha256_16") != digest:
+    if vals.get("source_sha256_16") != source_digest(kernel):
         return None
+    return vals
+
+
+def traffic_from_profile(kernel, name):
+    """Per-launch DRAM bytes from the committed ncu summary (None when the
+    kernel changed since)."""
+    vals = profile_record(kernel, name)
     try:
-        return float(vals["dram_bytes_per_launch"])
+        return float(vals["dram_bytes_per_launch"]) if vals else None
     except (KeyError, ValueError):
         return None
 
@@ -476,7 +497,7 @@ def run_ours(args):
     e2e_ms, e2e_serial_ms, h2d, d2h, e2e_brk = r.time_e2e(max(5, args.steps), 3)
     e2e_value = world * r.bytes / (e2e_ms * 1e-3) / 1e9
     achieved = r.bytes / (ms_step * 1e-3) / 1e9
-    traffic = traffic_from_profile("decode.cu", "decode_tma_kernel_batch64.txt")
+    traffic = traffic_from_profile("decode", "decode_tma_kernel_batch64.txt")
     roof = {"bound": "hbm", "kernel": "decode_tma_kernel (+ split-KV merge, timed together)",
             "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
@@ -588,7 +609,7 @@ def other_workloads(args, dev, ws, hbm_peak, bf16_peak):
         gbs = r.bytes / (ms * 1e-3) / 1e9
         ent = {"ms": round(ms, 4), "TFLOPS": round(tf, 2), "GB/s": round(gbs, 1),
                "kernel": r.info["kernel_name"], "items": r.info["num_items"],
-               "chunks": r.info["max_chunks"]}
+               "chunks": r.info["max_chunks"], "bytes_per_launch": int(r.bytes)}
         if graph:
             ent["replay"] = "CUDA graph (planned once, captured, replayed)"
         if bound == "tensor":
@@ -608,6 +629,20 @@ def other_workloads(args, dev, ws, hbm_peak, bf16_peak):
         pb = workloads.batch_prefill(page_size=P)
         one("prefill_p%d_causal" % P, pb, True, -1, "prefill", bound="tensor")
         if P == 16:
+            # the ncu capture of this launch (its tensor-pipe share and DRAM
+            # traffic), when the kernel is the one that was captured
+            rec = profile_record("prefill_tc", "prefill_tc_kernel_prefill_b16_causal.txt")
+            if rec:
+                ent = res["prefill_p16_causal"]
+                prof = {"source": "profiles/prefill_tc_kernel_prefill_b16_causal.txt"}
+                for k in ("tensor_pipe_active_pct", "dram_bytes_per_launch",
+                          "duration_us_under_ncu"):
+                    if k in rec:
+                        prof[k] = float(rec[k])
+                if "dram_bytes_per_launch" in prof:
+                    prof["traffic_over_algorithmic"] = round(
+                        prof["dram_bytes_per_launch"] / ent["bytes_per_launch"], 3)
+                ent["profile"] = prof
             one("prefill_p16_noncausal", pb, False, -1, "prefill", bound="tensor")
             one("prefill_p16_causal_wl127", pb, True, 127, "prefill")
     pb = workloads.batch_prefill_hd64()

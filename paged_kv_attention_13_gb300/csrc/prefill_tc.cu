@@ -42,8 +42,13 @@ namespace {
 constexpr int kTcThreads = 384;  // 4 control warps + 2 softmax warpgroups
 constexpr int kBlk = 128 * 128;  // 128 rows x 128 bytes: one 64-column swizzled block
 
+// K and V stages (a third V stage, 32 KB more shared memory, measured no
+// faster on the long-context split prefill once K and V have their own
+// producer warps)
+constexpr int kNK = 2, kNV = 2;
+
 // Shared-memory layout for head_dim D (64 or 128): a tile is 128 rows of D
-// 16-bit columns, D / 64 swizzled blocks; Q tiles A and B, two K and two V
+// 16-bit columns, D / 64 swizzled blocks; Q tiles A and B, the K and V
 // stages, the barriers, and the rows handed between the warpgroups.
 template <int D>
 struct TcLayout {
@@ -51,16 +56,16 @@ struct TcLayout {
   static constexpr int kTile = kH * kBlk;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kTile;
-  static constexpr int kOffV = kOffK + 2 * kTile;
-  static constexpr int kOffBar = kOffV + 2 * kTile;
+  static constexpr int kOffV = kOffK + kNK * kTile;
+  static constexpr int kOffBar = kOffV + kNV * kTile;
   static constexpr int kOffMl = kOffBar + 256;
   static constexpr int kSmem = kOffMl + 1024 + 1024;  // + alignment slack
 };
 
 // barrier slots
-constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 4, B_VFULL = 6, B_VEMPTY = 8,
-              B_SFULL = 10, B_PFULL = 12, B_ODONE = 14, B_OFREE = 16, B_FINAL = 18,
-              B_MLFULL = 19, B_MLFREE = 20, N_BARS = 21;
+constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 4, B_VFULL = 6, B_VEMPTY = 9,
+              B_SFULL = 12, B_PFULL = 14, B_ODONE = 16, B_OFREE = 18, B_FINAL = 20,
+              B_MLFULL = 21, B_MLFREE = 22, N_BARS = 23;
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -250,11 +255,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(BAR(B_QFULL), 1);
     mbar_init(BAR(B_QEMPTY), 1);
+    for (int s = 0; s < kNV; ++s) {
+      mbar_init(BAR(B_VFULL + s), 1);
+      mbar_init(BAR(B_VEMPTY + s), 1);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(BAR(B_KFULL + s), 1);
       mbar_init(BAR(B_KEMPTY + s), 1);
-      mbar_init(BAR(B_VFULL + s), 1);
-      mbar_init(BAR(B_VEMPTY + s), 1);
       mbar_init(BAR(B_SFULL + s), 1);
       mbar_init(BAR(B_PFULL + s), 128);
       mbar_init(BAR(B_ODONE + s), 1);
@@ -268,7 +275,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init_fence();
   }
   // K/V stages start zeroed so rows no copy has written yet hold finite values
-  for (int i = threadIdx.x; i < (4 * kTile) / 16; i += kTcThreads)
+  for (int i = threadIdx.x; i < ((kNK + kNV) * kTile) / 16; i += kTcThreads)
     reinterpret_cast<uint4*>(smem + kOffK)[i] = make_uint4(0, 0, 0, 0);
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   if (warp == 1) {
@@ -314,17 +321,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // lane holds in `page` (valid when `has`)
     auto load = [&](int which, const ItemGeom& G, int t, int cntr, bool has, int page,
                     int nvalid) {
-      const int st = cntr & 1;
+      const int ns = which ? kNV : kNK;
+      const int st = cntr % ns, fill = cntr / ns;  // the stage's fill-th use
       const int t0 = G.t_start + t * 128;
       const int full = which ? B_VFULL : B_KFULL, empty = which ? B_VEMPTY : B_KEMPTY;
       bool okl = true;
       if (lane == 0) {
-        if (cntr >= 2 && !mbar_wait(BAR(empty + st), ((cntr >> 1) - 1) & 1, ctl)) okl = false;
+        if (fill >= 1 && !mbar_wait(BAR(empty + st), (fill - 1) & 1, ctl)) okl = false;
         if (okl) {
           mbar_expect_tx(BAR(full + st), uint32_t(nvalid) * uint32_t(kv_box_rows) * uint32_t(D) * 2u);
           const uint32_t bit = 1u << (2 * which + st);
           armed |= bit;
-          apar = ((cntr >> 1) & 1) ? (apar | bit) : (apar & ~bit);
+          apar = (fill & 1) ? (apar | bit) : (apar & ~bit);
         }
       }
       okl = __shfl_sync(0xffffffffu, okl, 0);
@@ -391,7 +399,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       volatile WaitCtl drain = {0, 0, kWaitLimitNs};
       if (q_armed) mbar_wait(BAR(B_QFULL), q_par, &drain);
       for (int which = 0; which < 2; ++which)
-        for (int s = 0; s < 2; ++s)
+        for (int s = 0; s < (which ? kNV : kNK); ++s)
           if ((armed >> (2 * which + s)) & 1)
             mbar_wait(BAR((which ? B_VFULL : B_KFULL) + s), (apar >> (2 * which + s)) & 1, &drain);
       if (drain.abort) ctl->abort = 1;  // an expired drain wait is reported too
@@ -454,16 +462,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!ok) break;
           if (n == 2) tc_commit(BAR(B_QEMPTY));
           for (int j = 0; j < n && ok; ++j) {
-            const int xw = j & 1, jx = j >> 1, g1 = gt + j, st = g1 & 1;
+            const int xw = j & 1, jx = j >> 1, g1 = gt + j, st = g1 & 1, sv = g1 % kNV;
             const int itc_x = xw ? itc1 : itc0, cnt_x = xw ? cnt1 : cnt0;
             if (jx == 0 && itc_x > 0 &&
                 !mbar_wait(BAR(B_OFREE + xw), (itc_x - 1) & 1, ctl)) { ok = false; break; }
             if (!mbar_wait(BAR(B_PFULL + xw), (cnt_x + jx) & 1, ctl)) { ok = false; break; }
-            if (!mbar_wait(BAR(B_VFULL + st), (g1 >> 1) & 1, ctl)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_VFULL + sv), (g1 / kNV) & 1, ctl)) { ok = false; break; }
             tc_fence_after();
-            issue_pv(xw, st, jx > 0);
+            issue_pv(xw, sv, jx > 0);
             if (j >= n - 2) tc_commit(BAR(B_ODONE + xw));  // the warpgroup's last tile
-            tc_commit(BAR(B_VEMPTY + st));
+            tc_commit(BAR(B_VEMPTY + sv));
             if (j + 2 < n) {  // tile j + 2 reuses tile j's K stage
               if (!mbar_wait(BAR(B_KFULL + st), ((g1 + 2) >> 1) & 1, ctl)) { ok = false; break; }
               tc_fence_after();
@@ -487,15 +495,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_commit(BAR(B_KEMPTY + (gt & 1)));
         if (n == 1) tc_commit(BAR(B_QEMPTY));
         for (int j = 0; j < n && ok; ++j) {
-          const int g1 = gt + j, st = g1 & 1, st1 = (g1 + 1) & 1;
+          const int g1 = gt + j, sv = g1 % kNV, st1 = (g1 + 1) & 1;
           // ---- tile A
           if (j == 0 && itc0 > 0 && !mbar_wait(BAR(B_OFREE), (itc0 - 1) & 1, ctl)) { ok = false; break; }
           if (!mbar_wait(BAR(B_PFULL), (cnt0 + j) & 1, ctl)) { ok = false; break; }
-          if (!mbar_wait(BAR(B_VFULL + st), (g1 >> 1) & 1, ctl)) { ok = false; break; }
+          if (!mbar_wait(BAR(B_VFULL + sv), (g1 / kNV) & 1, ctl)) { ok = false; break; }
           tc_fence_after();
-          issue_pv(0, st, j > 0);
+          issue_pv(0, sv, j > 0);
           if (j == n - 1) tc_commit(BAR(B_ODONE));
-          if (!hasB) tc_commit(BAR(B_VEMPTY + st));
+          if (!hasB) tc_commit(BAR(B_VEMPTY + sv));
           if (j + 1 < n) {
             if (!mbar_wait(BAR(B_KFULL + st1), ((g1 + 1) >> 1) & 1, ctl)) { ok = false; break; }
             tc_fence_after();
@@ -510,8 +518,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (j == 0 && itc1 > 0 && !mbar_wait(BAR(B_OFREE + 1), (itc1 - 1) & 1, ctl)) { ok = false; break; }
             if (!mbar_wait(BAR(B_PFULL + 1), (cnt1 + j) & 1, ctl)) { ok = false; break; }
             tc_fence_after();
-            issue_pv(1, st, j > 0);
-            tc_commit(BAR(B_VEMPTY + st));
+            issue_pv(1, sv, j > 0);
+            tc_commit(BAR(B_VEMPTY + sv));
             if (j == n - 1) tc_commit(BAR(B_ODONE + 1));
             if (j + 1 < n) {
               issue_s(1, st1, 1);
@@ -602,7 +610,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float m_run = neg_inf(), l_run = 0.f;
       for (int jj = 0; jj < nt; ++jj) {
         const int j = split ? 2 * jj + x : jj;
-        const int g1 = gt + j, st = g1 & 1;
+        const int g1 = gt + j;
         const int t0 = G.t_start + j * 128;
         if (!wwait(BAR(B_SFULL + x), (cnt + jj) & 1)) { ok = false; break; }
         tc_fence_after();
@@ -742,11 +750,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool zeroed = false;
         if ((x == 0 || split) && t0 + 128 > G.lk) {  // the tile's first (or only) reader
           // rows of V past the request's last key may hold anything: zero them
-          if (!wwait(BAR(B_VFULL + st), (g1 >> 1) & 1)) { ok = false; break; }
+          if (!wwait(BAR(B_VFULL + g1 % kNV), (g1 / kNV) & 1)) { ok = false; break; }
           if (t0 + r >= G.lk) {
 #pragma unroll
             for (int h = 0; h < kH; ++h) {
-              uint4* row = reinterpret_cast<uint4*>(smem + kOffV + st * kTile + h * kBlk + r * 128);
+              uint4* row = reinterpret_cast<uint4*>(smem + kOffV + (g1 % kNV) * kTile + h * kBlk +
+                                                    r * 128);
 #pragma unroll
               for (int q = 0; q < 8; ++q) row[q] = make_uint4(0, 0, 0, 0);
             }
