@@ -404,7 +404,7 @@ def profile_record(kernel, name):
         return None
     vals = {}
     for line in open(path):
-        if ":" in line:
+        if ":" in line and not line.lstrip().startswith("#"):
             k, v = line.split(":", 1)
             vals[k.strip()] = v.strip()
     if vals.get("source_sha256_16") != source_digest(kernel):
