@@ -42,10 +42,11 @@ namespace {
 constexpr int kTcThreads = 384;  // 4 control warps + 2 softmax warpgroups
 constexpr int kBlk = 128 * 128;  // 128 rows x 128 bytes: one 64-column swizzled block
 
-// K and V stages (a third V stage, 32 KB more shared memory, measured no
-// faster on the long-context split prefill once K and V have their own
-// producer warps)
+// K and V stages (a third V or a third K stage, 32 KB more shared memory,
+// measured no faster on the long-context split prefill once K and V have
+// their own producer warps)
 constexpr int kNK = 2, kNV = 2;
+static_assert(kNK <= 4 && kNV <= 4, "a producer's stage bits");
 
 // Shared-memory layout for head_dim D (64 or 128): a tile is 128 rows of D
 // 16-bit columns, D / 64 swizzled blocks; Q tiles A and B, the K and V
@@ -63,9 +64,12 @@ struct TcLayout {
 };
 
 // barrier slots
-constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 4, B_VFULL = 6, B_VEMPTY = 9,
-              B_SFULL = 12, B_PFULL = 14, B_ODONE = 16, B_OFREE = 18, B_FINAL = 20,
-              B_MLFULL = 21, B_MLFREE = 22, N_BARS = 23;
+constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = B_KFULL + kNK,
+              B_VFULL = B_KEMPTY + kNK, B_VEMPTY = B_VFULL + kNV, B_SFULL = B_VEMPTY + kNV,
+              B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2, B_OFREE = B_ODONE + 2,
+              B_FINAL = B_OFREE + 2, B_MLFULL = B_FINAL + 1, B_MLFREE = B_MLFULL + 1,
+              N_BARS = B_MLFREE + 1;
+static_assert(8 * N_BARS + 8 + 16 <= 256, "barriers, the TMEM slot and the wait control fit");
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -259,9 +263,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(BAR(B_VFULL + s), 1);
       mbar_init(BAR(B_VEMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kNK; ++s) {
       mbar_init(BAR(B_KFULL + s), 1);
       mbar_init(BAR(B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(BAR(B_SFULL + s), 1);
       mbar_init(BAR(B_PFULL + s), 128);
       mbar_init(BAR(B_ODONE + s), 1);
@@ -305,7 +311,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // pages per tile) and issues that page's boxes.
     const int which_w = warp == 0 ? 0 : 1;
     int gcnt = 0, qc = 0;
-    // stage (which, st) at bit 2 * which + st: armed at least once, and the
+    // stage (which, st) at bit 4 * which + st: armed at least once, and the
     // parity of its latest arming (bit masks, so they stay in registers)
     uint32_t armed = 0, apar = 0;
     bool q_armed = false;
@@ -330,7 +336,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (fill >= 1 && !mbar_wait(BAR(empty + st), (fill - 1) & 1, ctl)) okl = false;
         if (okl) {
           mbar_expect_tx(BAR(full + st), uint32_t(nvalid) * uint32_t(kv_box_rows) * uint32_t(D) * 2u);
-          const uint32_t bit = 1u << (2 * which + st);
+          const uint32_t bit = 1u << (4 * which + st);
           armed |= bit;
           apar = (fill & 1) ? (apar | bit) : (apar & ~bit);
         }
@@ -400,8 +406,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (q_armed) mbar_wait(BAR(B_QFULL), q_par, &drain);
       for (int which = 0; which < 2; ++which)
         for (int s = 0; s < (which ? kNV : kNK); ++s)
-          if ((armed >> (2 * which + s)) & 1)
-            mbar_wait(BAR((which ? B_VFULL : B_KFULL) + s), (apar >> (2 * which + s)) & 1, &drain);
+          if ((armed >> (4 * which + s)) & 1)
+            mbar_wait(BAR((which ? B_VFULL : B_KFULL) + s), (apar >> (4 * which + s)) & 1, &drain);
       if (drain.abort) ctl->abort = 1;  // an expired drain wait is reported too
     }
     __syncwarp();
@@ -454,15 +460,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // split item: key tile j goes to warpgroup j & 1, both on Q tile A
           for (int j0 = 0; j0 < 2 && ok; ++j0) {
             const int g0 = gt + j0;
-            if (!mbar_wait(BAR(B_KFULL + (g0 & 1)), (g0 >> 1) & 1, ctl)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_KFULL + g0 % kNK), (g0 / kNK) & 1, ctl)) { ok = false; break; }
             tc_fence_after();
-            issue_s(j0, g0 & 1, 0);
-            tc_commit(BAR(B_KEMPTY + (g0 & 1)));
+            issue_s(j0, g0 % kNK, 0);
+            tc_commit(BAR(B_KEMPTY + g0 % kNK));
           }
           if (!ok) break;
           if (n == 2) tc_commit(BAR(B_QEMPTY));
           for (int j = 0; j < n && ok; ++j) {
-            const int xw = j & 1, jx = j >> 1, g1 = gt + j, st = g1 & 1, sv = g1 % kNV;
+            const int xw = j & 1, jx = j >> 1, g1 = gt + j, sv = g1 % kNV;
             const int itc_x = xw ? itc1 : itc0, cnt_x = xw ? cnt1 : cnt0;
             if (jx == 0 && itc_x > 0 &&
                 !mbar_wait(BAR(B_OFREE + xw), (itc_x - 1) & 1, ctl)) { ok = false; break; }
@@ -472,11 +478,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             issue_pv(xw, sv, jx > 0);
             if (j >= n - 2) tc_commit(BAR(B_ODONE + xw));  // the warpgroup's last tile
             tc_commit(BAR(B_VEMPTY + sv));
-            if (j + 2 < n) {  // tile j + 2 reuses tile j's K stage
-              if (!mbar_wait(BAR(B_KFULL + st), ((g1 + 2) >> 1) & 1, ctl)) { ok = false; break; }
+            if (j + 2 < n) {  // tile j + 2, on this warpgroup's S columns
+              const int sk = (g1 + 2) % kNK;
+              if (!mbar_wait(BAR(B_KFULL + sk), ((g1 + 2) / kNK) & 1, ctl)) { ok = false; break; }
               tc_fence_after();
-              issue_s(xw, st, 0);
-              tc_commit(BAR(B_KEMPTY + st));
+              issue_s(xw, sk, 0);
+              tc_commit(BAR(B_KEMPTY + sk));
               if (j + 2 == n - 1) tc_commit(BAR(B_QEMPTY));
             }
           }
@@ -488,14 +495,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ++itc1;
           continue;
         }
-        if (!mbar_wait(BAR(B_KFULL + (gt & 1)), (gt >> 1) & 1, ctl)) { ok = false; break; }
+        if (!mbar_wait(BAR(B_KFULL + gt % kNK), (gt / kNK) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        issue_s(0, gt & 1, 0);
-        if (hasB) issue_s(1, gt & 1, 1);
-        tc_commit(BAR(B_KEMPTY + (gt & 1)));
+        issue_s(0, gt % kNK, 0);
+        if (hasB) issue_s(1, gt % kNK, 1);
+        tc_commit(BAR(B_KEMPTY + gt % kNK));
         if (n == 1) tc_commit(BAR(B_QEMPTY));
         for (int j = 0; j < n && ok; ++j) {
-          const int g1 = gt + j, sv = g1 % kNV, st1 = (g1 + 1) & 1;
+          const int g1 = gt + j, sv = g1 % kNV, st1 = (g1 + 1) % kNK;
           // ---- tile A
           if (j == 0 && itc0 > 0 && !mbar_wait(BAR(B_OFREE), (itc0 - 1) & 1, ctl)) { ok = false; break; }
           if (!mbar_wait(BAR(B_PFULL), (cnt0 + j) & 1, ctl)) { ok = false; break; }
@@ -505,7 +512,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (j == n - 1) tc_commit(BAR(B_ODONE));
           if (!hasB) tc_commit(BAR(B_VEMPTY + sv));
           if (j + 1 < n) {
-            if (!mbar_wait(BAR(B_KFULL + st1), ((g1 + 1) >> 1) & 1, ctl)) { ok = false; break; }
+            if (!mbar_wait(BAR(B_KFULL + st1), ((g1 + 1) / kNK) & 1, ctl)) { ok = false; break; }
             tc_fence_after();
             issue_s(0, st1, 0);
             if (!hasB) {
