@@ -578,22 +578,28 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
   int32_t max_chunks = 1;
   int64_t G = 0;  // the grid
 
-  // Balanced spans (short-query kernel, when the plan splits keys): the live
-  // keys of all tiles, laid end to end, are cut into one contiguous span per
-  // bundle of Hk CTAs (one CTA per kv head), every span of about the same
-  // cost, (keys + kSpanItemKeys) x rows per piece. A bundle takes the rest of the
+  // Balanced spans (when the plan splits keys): the live keys of all tiles,
+  // laid end to end, are cut into one contiguous span per bundle of Hk CTAs
+  // (one CTA per kv head), every span of about the same cost,
+  // (keys + kSpanItemKeys) x rows per piece. A bundle takes the rest of the
   // tile it starts in and as much of the next ones as its share allows, so
   // the CTAs end at about the same time: a longest-first schedule of
   // fixed-length chunks left 5% of the CTA time idle on the batch-32 verify
-  // (and fewer, longer items cost fewer item ends). Cuts fall on multiples of
-  // 64 keys (whole stages) and no piece is shorter than kMinPiece keys.
+  // (and fewer, longer items cost fewer item ends and fewer partial states).
+  // Cuts fall on multiples of kCut keys and no piece is shorter than
+  // kMinPiece keys.
   auto schedule_spans = [&]() -> bool {
-    constexpr int64_t kMinPiece = 64;
-    // An item's fixed cost in keys: a per-item timeline of the batch-32
-    // verify and batch-64 decode runs (item end times against their keys)
-    // put it near zero once the producer runs ahead across items; 32 keys
-    // (half a stage) keeps pieces from being cut for nothing.
-    constexpr int64_t kSpanItemKeys = 32;
+    // Cut granularity (a stage of the short-query kernel, a key tile of the
+    // tcgen05 kernel), the shortest piece, and an item's fixed cost in keys.
+    // Short-query kernel: a per-item timeline of the batch-32 verify and
+    // batch-64 decode runs (item end times against their keys) put the fixed
+    // cost near zero once the producer runs ahead across items; 32 keys keep
+    // pieces from being cut for nothing. tcgen05 kernel: an item reloads its
+    // Q tile and writes a 64 KB partial state, about 128 keys' worth.
+    const bool tc = ns.kernel == fi::kPrefillM128;
+    const int64_t kCut = tc ? 128 : 64;
+    const int64_t kMinPiece = tc ? 256 : 64;
+    const int64_t kSpanItemKeys = tc ? 128 : 32;
     if (grid_cap % hk != 0) return false;
     const int64_t B = grid_cap / hk;
     if (B < 2) return false;
@@ -605,7 +611,7 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
     trial.reserve(tiles.size() + size_t(B));
     // One walk: every bundle takes up to `share` of cost from its own start
     // (a piece that starts costs kSpanItemKeys x rows on top of its keys); cuts
-    // round to multiples of 64 keys, a remainder shorter than kMinPiece keys
+    // round to multiples of kCut keys, a remainder shorter than kMinPiece keys
     // stays with its piece, and a bundle with room for less than kMinPiece
     // keys ends there. Returns the bundles used, or B + 1 once it needs more.
     // share >= (kSpanItemKeys + 2 kMinPiece) x the largest rows, so a fresh
@@ -631,7 +637,7 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
             room = share;
             continue;
           }
-          int64_t cut = (pos + int64_t(fit) + 32) / 64 * 64;
+          int64_t cut = (pos + int64_t(fit) + kCut / 2) / kCut * kCut;
           cut = std::max<int64_t>(cut, pos + kMinPiece);
           out.push_back({int32_t(bundle), int32_t(ti), int32_t(pos), int32_t(cut)});
           pos = cut;
@@ -702,8 +708,8 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
     G = g_spans;
     return true;
   };
-  const bool spans = ns.kernel == fi::kDecode && force_kv_chunks == 0 && chunk_len > 0 &&
-                     schedule_spans();
+  const bool spans = (ns.kernel == fi::kDecode || ns.kernel == fi::kPrefillM128) &&
+                     force_kv_chunks == 0 && chunk_len > 0 && schedule_spans();
   if (!spans) {
     // Items are made per (tile, chunk) group - one per kv head, all of the same
     // cost - and the groups are sorted by cost, longest first.
