@@ -633,19 +633,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         auto mask_chunk = [&](auto cc) {
           constexpr int c = decltype(cc)::value;
-          // the custom mask's bits of these 32 keys: bit qi * Lk + key of
-          // the request's segment (bits past it read as 0; keys past Lk are
-          // masked by jmax anyway)
-          uint32_t bits = ~0u;
+          // the keys of this chunk the row keeps, as a bit mask: those in
+          // [jmin, jmax], ANDed with the custom mask's bits (bit qi * Lk +
+          // key of the request's segment; bits past it read as 0, and keys
+          // past Lk are outside jmax anyway). A warp whose rows keep the whole
+          // chunk skips the per-element pass.
+          const int base = t0 + c * 32;
+          const int lo = max(jmin - base, 0), hi = min(jmax - base, 31);
+          uint32_t keep = lo > hi ? 0u : ((0xFFFFFFFFu >> (31 - (hi - lo))) << lo);
           if constexpr (MASKED)
-            bits = custom_mask_word(p.custom_mask + mbase, int64_t(G.lq) * G.lk,
-                                    int64_t(qi) * G.lk + t0 + c * 32);
+            keep &= custom_mask_word(p.custom_mask + mbase, int64_t(G.lq) * G.lk,
+                                     int64_t(qi) * G.lk + base);
+          if (__all_sync(0xffffffffu, keep == 0xFFFFFFFFu)) return;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int key = t0 + c * 32 + e;
-            if (key < jmin || key > jmax || !((bits >> e) & 1u))
-              sv[c][e] = __float_as_uint(neg_inf());
-          }
+          for (int e = 0; e < 32; ++e)
+            if (!(keep & (1u << e))) sv[c][e] = __float_as_uint(neg_inf());
         };
         auto exp_chunk = [&](auto cc, float2 nmu2) {
           constexpr int c = decltype(cc)::value;
