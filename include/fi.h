@@ -243,9 +243,11 @@ fi_status fi_batch_decode_paged(fi_plan_t plan, const fi_tensor* q, const fi_ten
  *                Lq_b * Lk_b bits (query row i, key j at bit i * Lk_b + j,
  *                least significant bit of each byte first), so
  *                mask_indptr[b+1] - mask_indptr[b] >= ceil(Lq_b * Lk_b / 8).
- * Masked plans run on the short-query kernel (at most 32 packed rows per
- * request, in 16-row tiles) or on the mma.sync kernels. FI_ERR_INVALID_ARG for a segment
- * shorter than its request's bits or a decreasing mask_indptr.
+ * Masked plans run on the same kernels as unmasked ones: the short-query
+ * kernel (at most 32 packed rows per request), the tcgen05 kernel (more rows,
+ * page sizes that are multiples of 8) or the mma.sync kernels (other page
+ * sizes). FI_ERR_INVALID_ARG for a segment shorter than its request's bits or
+ * a decreasing mask_indptr.
  *
  * fi_batch_prefill_paged_masked: as fi_batch_prefill_paged, plus
  *   custom_mask  device FI_U8 [>= mask_indptr[batch]] bytes, contiguous.

@@ -1,6 +1,6 @@
 // Short-query attention kernels (decode, speculative verify, and any request
-// of at most 32 packed rows, in 16-row tiles: query row x head of the GQA
-// group), against the paged KV. Bandwidth-bound: every K/V byte is read
+// of at most 32 packed rows, in one tile of 8, 16 or 32 rows: query row x
+// head of the GQA group), against the paged KV. Bandwidth-bound: every K/V byte is read
 // exactly once, the online softmax is kept in fp32.
 //
 // Work item = (request tile, kv head, key chunk). One producer warp streams
