@@ -724,6 +724,7 @@ PROFILE_CASES = {
     "prefill_b4_causal": (lambda: workloads.batch_prefill(page_size=16, batch=4), True, -1, "prefill"),
     "prefill_p1024_causal": (lambda: workloads.batch_prefill(page_size=1024), True, -1, "prefill"),
     "prefill_p16_noncausal": (lambda: workloads.batch_prefill(page_size=16), False, -1, "prefill"),
+    "prefill_p16_causal_wl127": (lambda: workloads.batch_prefill(page_size=16), True, 127, "prefill"),
     "prefill_hd64_f16_causal": (lambda: workloads.batch_prefill_hd64(), True, -1, "prefill"),
     "prefill_p48_causal": (lambda: workloads.batch_prefill(page_size=48), True, -1, "prefill"),
     "longctx_causal": (lambda: workloads.long_context(), True, -1, "prefill"),
