@@ -728,6 +728,7 @@ PROFILE_CASES = {
     "prefill_hd64_f16_causal": (lambda: workloads.batch_prefill_hd64(), True, -1, "prefill"),
     "prefill_p48_causal": (lambda: workloads.batch_prefill(page_size=48), True, -1, "prefill"),
     "longctx_causal": (lambda: workloads.long_context(), True, -1, "prefill"),
+    "longctx_causal_wl127": (lambda: workloads.long_context(), True, 127, "prefill"),
     "ragged_prefill_causal": (lambda: workloads.ragged_prefill(), True, -1, "ragged"),
     "tree_verify_b32": (lambda: workloads.tree_verify(batch=32), True, -1, "masked"),
     "spec_sampling_b64": None,  # the sampling step (spec_sampling_entry)

@@ -163,7 +163,7 @@ struct ItemGeom {
 
 __device__ __forceinline__ ItemGeom item_geom(const WorkItem& it, const int32_t* qo_indptr,
                                               const int32_t* kv_len, int g, int tile_rows,
-                                              int causal, int wl) {
+                                              int causal, int wl, int align) {
   ItemGeom G;
   G.b = it.b; G.hk = it.kv_head; G.row0 = it.row0;
   G.token0 = qo_indptr[it.b];
@@ -176,7 +176,11 @@ __device__ __forceinline__ ItemGeom item_geom(const WorkItem& it, const int32_t*
   const int lo_t = wl >= 0 ? max(0, G.lk - G.lq + G.i0 - wl) : 0;
   G.kv_lo = max(it.kv_begin, lo_t);
   G.kv_hi = min(it.kv_end, hi_t);
-  G.t_start = (G.kv_lo / 128) * 128;
+  // the first key tile starts on the TMA box boundary at or below the first
+  // live key (a box never crosses a page), not on a multiple of 128, so it
+  // holds at most align - 1 keys before the first live one: a sliding window
+  // of 127 keys over 64 query tokens then takes 2 tiles, not 2 or 3
+  G.t_start = (G.kv_lo / align) * align;
   G.n_tiles = G.kv_lo < G.kv_hi ? (G.kv_hi - G.t_start + 127) / 128 : 0;
   G.chunk = it.chunk; G.num_chunks = it.num_chunks; G.partial_base = it.partial_base;
   G.kv_start = 0;
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       if (items[w].b < 0) continue;  // schedule padding
-      ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
+      ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl, kv_box_rows);
       if (G.n_tiles == 0) continue;
       G.kv_start = kv_indptr[G.b];
       const bool hasB = G.n_rows > tr;
@@ -451,7 +455,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
         if (items[w].b < 0) continue;  // schedule padding
-      const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
+      const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl, kv_box_rows);
         if (G.n_tiles == 0) continue;
         const bool hasB = G.n_rows > tr;
         const int n = G.n_tiles;
@@ -575,7 +579,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       if (items[w].b < 0) continue;  // schedule padding
-      const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl);
+      const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl, kv_box_rows);
       const bool hasB = G.n_rows > tr;
       const int n = G.n_tiles;
       const bool split = !hasB && n >= 2;
