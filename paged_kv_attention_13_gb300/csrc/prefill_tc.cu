@@ -187,6 +187,14 @@ __device__ __forceinline__ ItemGeom item_geom(const WorkItem& it, const int32_t*
   return G;
 }
 
+// Bring a 3-D box of a tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // 16 packed columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
@@ -401,6 +409,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int nvalid = __popc(__ballot_sync(0xffffffffu, has));
         ok = load(which_w, G, step, gcnt, has, page, nvalid);
         ++gcnt;
+      }
+      // once this item's K tiles are issued, the Q tiles of the CTA's next
+      // item go to L2, so their copy into shared memory, which waits for this
+      // item's last S product, is an L2 read rather than an HBM one
+      if (which_w == 0 && lane == 0 && ok) {
+        for (int w2 = w + gridDim.x; w2 < n_items; w2 += gridDim.x) {
+          if (items[w2].b < 0) continue;
+          const ItemGeom G2 =
+              item_geom(items[w2], qo_indptr, kv_len, g, tile_rows, causal, wl, kv_box_rows);
+          if (G2.n_tiles == 0) continue;
+          for (int x = 0; x < (G2.n_rows > tr ? 2 : 1); ++x)
+            for (int h = 0; h < kH; ++h)
+              tma_prefetch_3d(&tq, h * 64, G2.hk * g, G2.token0 + G2.i0 + x * (tr / g));
+          break;
+        }
       }
     }
     // before exit: every copy this warp started has landed (these waits
