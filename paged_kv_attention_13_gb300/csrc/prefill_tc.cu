@@ -158,17 +158,28 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool b_mn_major, int
 struct ItemGeom {
   int b, hk, token0, lq, lk, n_rows, i0, kv_lo, kv_hi, t_start, n_tiles;
   int chunk, num_chunks, partial_base, row0;
-  int kv_start;  // ragged cache: the request's first row (set by the producer)
+  int kv_start;   // the request's first page-table entry (ragged cache: first K/V row)
+  int mask_base;  // first byte of the request's custom mask
 };
 
-__device__ __forceinline__ ItemGeom item_geom(const WorkItem& it, const int32_t* qo_indptr,
-                                              const int32_t* kv_len, int g, int tile_rows,
+// A work item in four 16-byte loads issued together: it carries its
+// request's metadata, so nothing else is read before its geometry is known.
+__device__ __forceinline__ WorkItem load_item(const WorkItem* items, int w) {
+  WorkItem it;
+  const int4* src = reinterpret_cast<const int4*>(items + w);
+  int4* dst = reinterpret_cast<int4*>(&it);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[i] = __ldg(src + i);
+  return it;
+}
+
+__device__ __forceinline__ ItemGeom item_geom(const WorkItem& it, int g, int tile_rows,
                                               int causal, int wl, int align) {
   ItemGeom G;
   G.b = it.b; G.hk = it.kv_head; G.row0 = it.row0;
-  G.token0 = qo_indptr[it.b];
-  G.lq = qo_indptr[it.b + 1] - G.token0;
-  G.lk = kv_len[it.b];
+  G.token0 = it.tok0;
+  G.lq = it.lq;
+  G.lk = it.lk;
   G.n_rows = min(tile_rows, G.lq * g - it.row0);
   G.i0 = it.row0 / g;
   const int i1 = (it.row0 + G.n_rows) / g - 1;
@@ -183,7 +194,8 @@ __device__ __forceinline__ ItemGeom item_geom(const WorkItem& it, const int32_t*
   G.t_start = (G.kv_lo / align) * align;
   G.n_tiles = G.kv_lo < G.kv_hi ? (G.kv_hi - G.t_start + 127) / 128 : 0;
   G.chunk = it.chunk; G.num_chunks = it.num_chunks; G.partial_base = it.partial_base;
-  G.kv_start = 0;
+  G.kv_start = it.kv_start;
+  G.mask_base = it.mask_base;
   return G;
 }
 
@@ -255,12 +267,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const WsHeader* hdr = static_cast<const WsHeader*>(p.ws);
   const int n_items = hdr->n_items;
   const WorkItem* items = ws_ptr<const WorkItem>(p.ws, hdr->off_items);
-  const int32_t* qo_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_qo_indptr);
-  const int32_t* kv_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_kv_indptr);
-  const int32_t* kv_len = ws_ptr<const int32_t>(p.ws, hdr->off_kv_len);
   float* tmp_lse = ws_ptr<float>(p.ws, hdr->off_tmp_lse);
   float* tmp_o = ws_ptr<float>(p.ws, hdr->off_tmp_o);
-  const int32_t* mask_indptr = ws_ptr<const int32_t>(p.ws, hdr->off_mask_indptr);
   const int g = hdr->group;
   const int causal = hdr->causal;
   const int wl = hdr->window_left;
@@ -366,14 +374,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       return okl;
     };
+    WorkItem nit{};
+    nit.b = -1;
+    if (int(blockIdx.x) < n_items) nit = load_item(items, blockIdx.x);
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      if (items[w].b < 0) continue;  // schedule padding
-      ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl, kv_box_rows);
+      const WorkItem it = nit;  // this item, loaded one item ahead
+      if (w + int(gridDim.x) < n_items) nit = load_item(items, w + gridDim.x);
+      if (it.b < 0) continue;  // schedule padding
+      const ItemGeom G = item_geom(it, g, tile_rows, causal, wl, kv_box_rows);
       if (G.n_tiles == 0) continue;
-      G.kv_start = kv_indptr[G.b];
       const bool hasB = G.n_rows > tr;
-      const int32_t* pages = p.ragged ? nullptr : p.kv_indices + kv_indptr[G.b];
-      const int n_pages = kv_indptr[G.b + 1] - kv_indptr[G.b];  // ragged: rows, > 0 when n_tiles > 0
+      const int32_t* pages = p.ragged ? nullptr : p.kv_indices + G.kv_start;
+      // the request's pages (every page but the last is full); ragged: rows
+      const int n_pages = p.ragged ? G.lk : (G.lk + p.page_size - 1) / p.page_size;
       // page index of lane L for batch bt: tile bt * tiles_per_batch + L / npg,
       // its page L % npg (0 when past the request)
       auto fetch = [&](int bt) {
@@ -415,9 +428,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // item's last S product, is an L2 read rather than an HBM one
       if (which_w == 0 && lane == 0 && ok) {
         for (int w2 = w + gridDim.x; w2 < n_items; w2 += gridDim.x) {
-          if (items[w2].b < 0) continue;
-          const ItemGeom G2 =
-              item_geom(items[w2], qo_indptr, kv_len, g, tile_rows, causal, wl, kv_box_rows);
+          const WorkItem it2 = load_item(items, w2);
+          if (it2.b < 0) continue;
+          const ItemGeom G2 = item_geom(it2, g, tile_rows, causal, wl, kv_box_rows);
           if (G2.n_tiles == 0) continue;
           for (int x = 0; x < (G2.n_rows > tr ? 2 : 1); ++x)
             for (int h = 0; h < kH; ++h)
@@ -476,9 +489,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       };
       int gt = 0, qc = 0, cnt0 = 0, cnt1 = 0, itc0 = 0, itc1 = 0;
       bool ok = true;
+      WorkItem nit{};
+      nit.b = -1;
+      if (int(blockIdx.x) < n_items) nit = load_item(items, blockIdx.x);
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        if (items[w].b < 0) continue;  // schedule padding
-      const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl, kv_box_rows);
+        const WorkItem it = nit;  // this item, loaded one item ahead
+        if (w + int(gridDim.x) < n_items) nit = load_item(items, w + gridDim.x);
+        if (it.b < 0) continue;  // schedule padding
+        const ItemGeom G = item_geom(it, g, tile_rows, causal, wl, kv_box_rows);
         if (G.n_tiles == 0) continue;
         const bool hasB = G.n_rows > tr;
         const int n = G.n_tiles;
@@ -601,8 +619,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int gt = 0, cnt = 0, itc = 0, itc_b = 0, nsplit = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      if (items[w].b < 0) continue;  // schedule padding
-      const ItemGeom G = item_geom(items[w], qo_indptr, kv_len, g, tile_rows, causal, wl, kv_box_rows);
+      const WorkItem it = load_item(items, w);
+      if (it.b < 0) continue;  // schedule padding
+      const ItemGeom G = item_geom(it, g, tile_rows, causal, wl, kv_box_rows);
       const bool hasB = G.n_rows > tr;
       const int n = G.n_tiles;
       const bool split = !hasB && n >= 2;
@@ -617,7 +636,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool direct = G.chunk < 0;
       const int slot = direct ? 0 : G.partial_base + (qi - G.i0) * G.num_chunks + G.chunk;
       // custom (tree) mask: request b's bits start on byte mbase (-1: none)
-      const int mbase = MASKED ? mask_indptr[G.b] : -1;
+      const int mbase = MASKED ? G.mask_base : -1;
       if (!active) {
         if (n == 0 && row_ok) {  // no live key: o = 0, lse = -inf
           if (direct) {
