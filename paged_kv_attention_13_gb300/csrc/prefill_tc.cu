@@ -317,9 +317,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   // Register split: the control warpgroup (producer, MMA issuer, two idle
   // warps) gives registers to the two softmax warpgroups, which hold a whole
-  // 128-column score row: 128 x 112 + 256 x 192 = 63488 <= 384 x 168 launched.
+  // 128-column score row: 128 x 104 + 256 x 200 = 64512 = 384 x 168 launched.
+  // The compiler allocates each side to its own limit; at 192 the softmax
+  // spilled to local memory.
   if (warp < 4) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------ producers
     // Warp 0 loads the Q tiles and the K tiles, warp 2 the V tiles, each at
@@ -597,7 +599,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
     // ------------------------------------------------------------ softmax + epilogue
     const int x = (warp - 4) >> 2;         // Q tile of this warpgroup
     const int sw = warp & 3;               // TMEM lane quadrant
