@@ -60,7 +60,10 @@ struct TcLayout {
   static constexpr int kOffV = kOffK + kNK * kTile;
   static constexpr int kOffBar = kOffV + kNV * kTile;
   static constexpr int kOffMl = kOffBar + 256;
-  static constexpr int kSmem = kOffMl + 1024 + 1024;  // + alignment slack
+  // per softmax warp, 32 rows x 128 bytes: output rows pass through it so the
+  // stores to global memory cover whole 128-byte lines
+  static constexpr int kOffStage = kOffMl + 1024;
+  static constexpr int kSmem = kOffStage + 8 * 4096 + 1024;  // + alignment slack
 };
 
 // barrier slots
@@ -248,7 +251,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   using T = typename DT::T;
   using L = TcLayout<D>;
   constexpr int kH = L::kH, kTile = L::kTile, kOffQ = L::kOffQ, kOffK = L::kOffK,
-                kOffV = L::kOffV, kOffBar = L::kOffBar, kOffMl = L::kOffMl;
+                kOffV = L::kOffV, kOffBar = L::kOffBar, kOffMl = L::kOffMl,
+                kOffStage = L::kOffStage;
   // the page table failed the index check: the whole CTA leaves before any
   // barrier, tensor-memory allocation or copy
   if (static_cast<const WsHeader*>(p.ws)->index_error) return;
@@ -861,6 +865,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (split && !wwait(BAR(B_ODONE + 1), itc_b & 1)) { ok = false; break; }
       tc_fence_after();
       const uint32_t tOb = tmem + lane_addr + 384u;  // O of warpgroup B
+      // The rows leave through this warp's staging buffer: a thread writes
+      // its row's 128-byte blocks there (16-byte pieces in XOR-swizzled
+      // order, so neither side has bank conflicts), then each store
+      // instruction sends four rows' blocks, 8 lanes per block. A thread
+      // storing its own row wrote 16-byte pieces of 32 rows per instruction.
+      uint8_t* stg = smem + kOffStage + (warp - 4) * 4096;
+      char* my_dst = nullptr;  // this thread's output row (none past the tile)
+      if (row_ok)
+        my_dst = direct ? reinterpret_cast<char*>(static_cast<T*>(p.out) + (int64_t(tok) * Hq + head) * D)
+                        : reinterpret_cast<char*>(tmp_o + (int64_t(slot) * Hq + head) * D);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
@@ -877,24 +891,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * fa);
         }
-        if (row_ok) {
-          if (direct) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) +
-                                                  (int64_t(tok) * Hq + head) * D + c * 32);
+        // this chunk's 16-byte pieces q of the row's 128-byte block: the
+        // 16-bit output packs two chunks per block, fp32 partials one
+        if (direct) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              dst[q] = make_uint4(
-                  DT::pack(__uint_as_float(ov[8 * q + 0]), __uint_as_float(ov[8 * q + 1])),
-                  DT::pack(__uint_as_float(ov[8 * q + 2]), __uint_as_float(ov[8 * q + 3])),
-                  DT::pack(__uint_as_float(ov[8 * q + 4]), __uint_as_float(ov[8 * q + 5])),
-                  DT::pack(__uint_as_float(ov[8 * q + 6]), __uint_as_float(ov[8 * q + 7])));
-          } else {
-            float4* dst = reinterpret_cast<float4*>(tmp_o + (int64_t(slot) * Hq + head) * D + c * 32);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(__uint_as_float(ov[4 * q]), __uint_as_float(ov[4 * q + 1]),
-                                   __uint_as_float(ov[4 * q + 2]), __uint_as_float(ov[4 * q + 3]));
+          for (int i = 0; i < 4; ++i) {
+            const int q = (c & 1) * 4 + i;
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((q ^ (lane & 7)) << 4)) = make_uint4(
+                DT::pack(__uint_as_float(ov[8 * i + 0]), __uint_as_float(ov[8 * i + 1])),
+                DT::pack(__uint_as_float(ov[8 * i + 2]), __uint_as_float(ov[8 * i + 3])),
+                DT::pack(__uint_as_float(ov[8 * i + 4]), __uint_as_float(ov[8 * i + 5])),
+                DT::pack(__uint_as_float(ov[8 * i + 6]), __uint_as_float(ov[8 * i + 7])));
           }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+                make_uint4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
+        }
+        if (!direct || (c & 1)) {
+          __syncwarp();
+          const int blk = direct ? (c >> 1) : c;  // the 128-byte block of each row
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int row = k * 4 + (lane >> 3), q = lane & 7;
+            char* dst = reinterpret_cast<char*>(
+                __shfl_sync(0xffffffffu, reinterpret_cast<long long>(my_dst), row));
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + row * 128 + ((q ^ (row & 7)) << 4));
+            if (dst) *reinterpret_cast<uint4*>(dst + blk * 128 + q * 16) = v;
+          }
+          __syncwarp();
         }
       }
       tc_fence_before();
