@@ -315,6 +315,45 @@ def test_schedule_balances_the_persistent_grid():
     assert load.max() / load.mean() < 1.03
 
 
+def _tc_step_loads(info, pb, causal, page_size):
+    """Per-CTA time of a tcgen05 prefill plan in tile steps: each item pays its
+    128-key tiles (counted from the K/V box boundary at or below its first live
+    key) once per 128-row Q tile, plus 2 steps for its start and epilogue."""
+    items, G = info["items"], info["grid"]
+    g = pb.num_qo_heads // pb.num_kv_heads
+    qo = pb.qo_indptr.numpy()
+    kv = np.array(pb.kv_lens)
+    box = int(np.gcd(page_size, 128))
+    load = np.zeros(G)
+    for i, it in enumerate(items):
+        b, row0, kb, ke = int(it[0]), int(it[2]), int(it[3]), int(it[4])
+        if b < 0:
+            continue
+        lq, lk = int(qo[b + 1] - qo[b]), int(kv[b])
+        rows = min(info["tile_rows"], lq * g - row0)
+        i1 = (row0 + rows) // g - 1
+        hi = min(ke, min(lk, i1 + lk - lq + 1) if causal else lk)
+        lo = kb
+        n_kt = (hi - lo // box * box + 127) // 128 if hi > lo else 0
+        load[i % G] += n_kt * (2 if rows > 128 else 1) + 2
+    return load
+
+
+@pytest.mark.parametrize("causal,page", [(True, 16), (False, 16), (True, 1024)])
+def test_tcgen05_prefill_schedule_is_balanced(causal, page):
+    """The unsplit batch-16 prefill on the tcgen05 kernel: items dealt longest
+    first by their tile steps leave no CTA more than 2% above the mean (a
+    schedule by live keys x rows left the longest 4% above it)."""
+    pb = workloads.batch_prefill(page_size=page)
+    p = _plan()
+    p.plan(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, page, 32, 8, 128, causal=causal)
+    info = p.info(with_arrays=True)
+    assert info["kernel_name"] == "prefill_m128" and info["max_chunks"] == 1
+    load = _tc_step_loads(info, pb, causal, page)
+    assert load.max() / load.mean() < 1.02
+    _check_cover(p, pb, causal, -1, 0)
+
+
 def _cta_loads(info, kv_lens):
     items, G = info["items"], info["grid"]
     load = np.zeros(G)
