@@ -601,11 +601,18 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
     const int64_t kCut = tc ? 128 : 64;
     const int64_t kMinPiece = tc ? 256 : 64;
     const int64_t kSpanItemKeys = tc ? 128 : 32;
+    // A piece's rows as the kernel pays them: the tcgen05 kernel computes a
+    // whole 128-row Q tile whatever its live rows (a request's last tile of 46
+    // rows costs half a two-tile piece, not a fifth); the short-query kernel
+    // pays by rows.
+    auto wrows = [&](const Tile& t) -> double {
+      return tc ? (t.rows > 128 ? 256.0 : 128.0) : double(t.rows);
+    };
     if (grid_cap % hk != 0) return false;
     const int64_t B = grid_cap / hk;
     if (B < 2) return false;
     double total = 0;
-    for (const Tile& t : tiles) total += double(t.hi - t.lo + kSpanItemKeys) * double(t.rows);
+    for (const Tile& t : tiles) total += double(t.hi - t.lo + kSpanItemKeys) * wrows(t);
     struct Piece { int32_t bundle, tile, kb, ke; };
     std::vector<Piece> pieces, trial;
     pieces.reserve(tiles.size() + size_t(B));
@@ -623,7 +630,7 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
       double room = share;
       for (size_t ti = 0; ti < tiles.size() && bundle < B; ++ti) {
         const Tile& t = tiles[ti];
-        const double rows = double(t.rows);
+        const double rows = wrows(t);
         int64_t pos = t.lo;
         for (;;) {
           const double fit = room / rows - double(kSpanItemKeys);  // keys a piece here may take
@@ -651,9 +658,9 @@ fi_status build_plan(const fi_plan_s& P, const int32_t* qo_indptr_h, const int32
     };
     // the smallest share whose walk fits the B bundles (bisection; each walk
     // is tiles + bundles steps)
-    int64_t max_rows = 1;
-    for (const Tile& t : tiles) max_rows = std::max<int64_t>(max_rows, t.rows);
-    double lo_s = std::max(total / double(B), double(kSpanItemKeys + 2 * kMinPiece) * double(max_rows));
+    double max_rows = 1;
+    for (const Tile& t : tiles) max_rows = std::max(max_rows, wrows(t));
+    double lo_s = std::max(total / double(B), double(kSpanItemKeys + 2 * kMinPiece) * max_rows);
     double hi_s = 2.0 * lo_s;
     for (int iter = 0; iter < 24; ++iter) {
       const double mid = 0.5 * (lo_s + hi_s);
