@@ -354,6 +354,22 @@ def test_tcgen05_prefill_schedule_is_balanced(causal, page):
     _check_cover(p, pb, causal, -1, 0)
 
 
+def test_tcgen05_split_plan_weighs_q_tiles():
+    """The head_dim-64 prefill (4 q / 2 kv heads) is split into spans: a
+    request's last, partial Q tile is weighed as the whole 128-row tile the
+    kernel computes, so no CTA carries more than 10% above the mean in tile
+    steps (weighing it by its live rows left one 23% above)."""
+    pb = workloads.batch_prefill_hd64()
+    p = _plan()
+    p.plan(pb.qo_indptr, pb.kv_indptr, pb.last_page_len, 16, 4, 2, 64, causal=True,
+           dtype=torch.float16)
+    info = p.info(with_arrays=True)
+    assert info["kernel_name"] == "prefill_m128" and info["max_chunks"] > 1
+    load = _tc_step_loads(info, pb, True, 16)
+    assert load.max() / load.mean() < 1.10
+    _check_cover(p, pb, True, -1, 0)
+
+
 def _cta_loads(info, kv_lens):
     items, G = info["items"], info["grid"]
     load = np.zeros(G)
