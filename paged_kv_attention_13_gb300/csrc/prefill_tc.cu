@@ -4,24 +4,27 @@
 //
 // A work item is two 128-row Q tiles (packed rows: query row x head in the
 // GQA group, all heads of one kv head) against a range of 128-key tiles,
-// head_dim 128, bf16 or fp16 in, fp32 accumulate. Both Q tiles use every K/V
-// tile staged in shared memory.
+// head_dim 64 or 128, bf16 or fp16 in, fp32 accumulate. Both Q tiles use every
+// K/V tile staged in shared memory. An item carries its request's metadata.
 //
 // Roles inside one CTA (384 threads, one CTA per SM, persistent over the work
 // items of the plan):
-//   warp 0      TMA producer: the two Q tiles (3-D map over [tokens, heads,
-//               dim]) and, per key tile, one box per page of K and of V (4-D
-//               maps over [pages, slot, kv head, dim]) straight from the
-//               paged cache; two K and two V stages, released separately;
+//   warp 0      TMA producer of the two Q tiles (3-D map over [tokens, heads,
+//               dim]) and, per key tile, one box per page of K (4-D map over
+//               [pages, slot, kv head, dim]) straight from the paged cache;
+//               it also prefetches the next item's Q tiles into L2;
+//   warp 2      TMA producer of V, the same way, at its own pace (two K and
+//               two V stages, released separately);
 //   warp 1      MMA issuer (one thread): S_x = Q_x K^T into TMEM, then
 //               O_x += P_x V with P_x read from TMEM, alternating the tiles so
 //               the tensor core works on one tile while the other's softmax
-//               runs;
+//               runs; warp 3 only gives up its registers;
 //   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: a thread owns
 //               one row (its TMEM lane), masks boundary tiles, keeps the
 //               running max / sum in registers, rescales O in TMEM only when
 //               the max grows by more than 2^8, writes P over its S columns,
-//               and runs the epilogue.
+//               and runs the epilogue, whose output rows pass through a
+//               per-warp shared-memory staging buffer.
 // Every mbarrier wait is bounded in time; on expiry the CTA records an error
 // in the workspace header, stops issuing work, waits for its own copies and
 // MMAs in flight, frees its tensor memory and exits.
