@@ -337,9 +337,10 @@ fi_status fi_chain_speculative_sampling(const fi_tensor* draft_probs,
                                         fi_tensor* emitted_num, void* stream);
 
 /* Copy a plan's host metadata out (any pointer may be NULL):
- *   items [num_items * 8] int32: per work item {request, kv_head, first packed
- *         row, packed rows, kv_begin, kv_end, chunk (-1 = written directly),
- *         partial base};
+ *   items [num_items * 8] int32: per work item {request (-1 = schedule
+ *         padding), kv_head, first packed row, kv_begin, kv_end, chunk (-1 =
+ *         written directly), chunks of the item's row tile, partial base};
+ *         the items sit in per-CTA order: CTA c runs positions c, c + grid, ...;
  *   merge_indptr [total_rows + 1]: partial slots of each query token. */
 fi_status fi_plan_get_info(fi_plan_t plan, fi_plan_info* info, int32_t* items,
                            int32_t items_capacity, int32_t* merge_indptr,
